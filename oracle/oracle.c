@@ -1,0 +1,205 @@
+/*
+ * CPU oracle for the packed-int4 integer GEMMs.  TEST INFRASTRUCTURE ONLY:
+ * tests, the smoke check and the benchmark's CPU-baseline leg call it; the
+ * library never does.  It shares no code with the CUDA path.
+ *
+ * What it computes (the plain definition, nothing reordered or blocked):
+ *
+ *   C[m,n] = sum_{k<K} a[m,k] * b[n,k]                         (NT product)
+ *
+ * with a, b the logical signed integers, accumulated in int64 and narrowed
+ * to int32 after checking the no-overflow bound |C| <= K*max|a|*max|b|.
+ *   - "[CUDA] Support int4 T.gemm" (tilelang PR #2063),
+ *     examples/gemm_int4/example_tilelang_gemm_int4.py, matmul_nt_int4:
+ *     A (M,K) int4, B (N,K) int4, C (M,N) int32, gemm with transpose_B.
+ *   - "[Example] add w4a8 gemm kernel" (tilelang PR #815), review of
+ *     ref_program: A int8 times the unpacked int4 B, taken in integers.
+ *   - TileLang tutorial low_precision_gemm.py, matmul_int4 (int4 inputs,
+ *     int32 accumulator).
+ *
+ * Packing (tutorial low_precision_gemm.py, pack_int4): byte j of a packed row
+ * holds logical element 2j in its low nibble and element 2j+1 in its high
+ * nibble, each masked to 4 bits.
+ *
+ * Unpacking ("[Example] add w4a8 gemm kernel", reviewer's vectorised
+ * torch_convert): the nibble at position pos (0 = low, 1 = high) is
+ * (byte >> 4*pos) & 0xF, read as a 4-bit two's-complement number, i.e. minus
+ * 16 when it is 8 or more.
+ *
+ * Every function here is pinned by the CPU tests (closed forms, brute force,
+ * numpy int64 matmul, round trips, hand-computed bytes).
+ *
+ * ORACLE_MUTANT (compile-time, tests only): plants one known mistake so that
+ * the pin suite can show it catches it.  Never defined in a normal build.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <pthread.h>
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+/* Signed value of nibble `pos` (0 = low = even k, 1 = high = odd k). */
+int oracle_nibble(uint8_t byte, int pos)
+{
+#if ORACLE_MUTANT == 1 /* planted: nibble order swapped */
+    pos = 1 - pos;
+#endif
+    int v = (byte >> (4 * pos)) & 0xF;
+#if ORACLE_MUTANT == 2 /* planted: no sign extension */
+    return v;
+#else
+    return v >= 8 ? v - 16 : v;
+#endif
+}
+
+/* logical [rows, K] int8 -> packed [rows, K/2] bytes.  K must be even. */
+void oracle_pack_int4(const int8_t *logical, uint8_t *packed, int64_t rows, int64_t K)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < K / 2; ++j) {
+            int lo = logical[r * K + 2 * j] & 0xF;
+            int hi = logical[r * K + 2 * j + 1] & 0xF;
+            packed[r * (K / 2) + j] = (uint8_t)(lo | (hi << 4));
+        }
+    }
+}
+
+/* packed [rows, K/2] -> logical [rows, K] int8 in [-8, 7]. */
+void oracle_unpack_int4(const uint8_t *packed, int8_t *logical, int64_t rows, int64_t K)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t k = 0; k < K; ++k)
+            logical[r * K + k] = (int8_t)oracle_nibble(packed[r * (K / 2) + k / 2], (int)(k % 2));
+}
+
+/* One output element, int64 accumulation over the full K. */
+static int64_t dot_i64(const int8_t *a_row, const int8_t *b_row, int64_t K)
+{
+    int64_t s = 0;
+#if ORACLE_MUTANT == 4 /* planted: last k dropped */
+    K -= 1;
+#endif
+    for (int64_t k = 0; k < K; ++k) {
+#if ORACLE_MUTANT == 5 /* planted: sign of one product flipped (k == 1) */
+        if (k == 1) { s -= (int64_t)a_row[k] * (int64_t)b_row[k]; continue; }
+#endif
+        s += (int64_t)a_row[k] * (int64_t)b_row[k];
+    }
+    return s;
+}
+
+struct job {
+    const int8_t *a;  /* [M, K] logical */
+    const int8_t *b;  /* [N, K] logical */
+    int32_t *c;       /* [M, N] */
+    int64_t M, N, K, bound;
+    int64_t m_begin, m_end;
+    int violated;
+};
+
+static void *run_rows(void *arg)
+{
+    struct job *j = (struct job *)arg;
+    for (int64_t m = j->m_begin; m < j->m_end; ++m) {
+        for (int64_t n = 0; n < j->N; ++n) {
+#if ORACLE_MUTANT == 3 /* planted: operands transposed (b indexed by m) */
+            int64_t s = dot_i64(j->a + m * j->K, j->b + (m % j->N) * j->K, j->K);
+#else
+            int64_t s = dot_i64(j->a + m * j->K, j->b + n * j->K, j->K);
+#endif
+            if (s > j->bound || s < -j->bound) j->violated = 1;
+            j->c[m * j->N + n] = (int32_t)s;
+        }
+    }
+    return NULL;
+}
+
+/* C = A . B^T over logical int8 rows, `nthreads` threads over m.
+ * `amax`, `bmax` are the largest magnitudes the operands may take (8 for int4,
+ * 128 for int8); the bound checked is K*amax*bmax.  Returns 0, or 4 if the
+ * bound was exceeded (inputs outside the stated ranges), or -1 on a thread
+ * error. */
+static int gemm_logical(const int8_t *a, const int8_t *b, int32_t *c, int64_t M, int64_t N,
+                        int64_t K, int64_t amax, int64_t bmax, int nthreads)
+{
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > M) nthreads = (int)(M > 0 ? M : 1);
+    struct job *jobs = (struct job *)calloc((size_t)nthreads, sizeof(struct job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tids) { free(jobs); free(tids); return -1; }
+    int rc = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = (struct job){a, b, c, M, N, K, K * amax * bmax,
+                               M * t / nthreads, M * (t + 1) / nthreads, 0};
+        if (pthread_create(&tids[t], NULL, run_rows, &jobs[t]) != 0) {
+            run_rows(&jobs[t]);
+            tids[t] = 0;
+        }
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        if (tids[t]) pthread_join(tids[t], NULL);
+        if (jobs[t].violated) rc = 4;
+    }
+    free(jobs);
+    free(tids);
+    return rc;
+}
+
+/* int4 x int4: Ap [M, K/2], Bp [N, K/2] packed; C [M, N] int32. */
+int oracle_i4i4_gemm(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int64_t M, int64_t N,
+                     int64_t K, int nthreads)
+{
+    int8_t *a = (int8_t *)malloc((size_t)(M * K));
+    int8_t *b = (int8_t *)malloc((size_t)(N * K));
+    if (!a || !b) { free(a); free(b); return -1; }
+    oracle_unpack_int4(Ap, a, M, K);
+    oracle_unpack_int4(Bp, b, N, K);
+    int rc = gemm_logical(a, b, C, M, N, K, 8, 8, nthreads);
+    free(a);
+    free(b);
+    return rc;
+}
+
+/* W4A8: A [M, K] int8 activations, Bp [N, K/2] packed int4 weights. */
+int oracle_w4a8_gemm(const int8_t *A, const uint8_t *Bp, int32_t *C, int64_t M, int64_t N,
+                     int64_t K, int nthreads)
+{
+    int8_t *b = (int8_t *)malloc((size_t)(N * K));
+    if (!b) return -1;
+    oracle_unpack_int4(Bp, b, N, K);
+    int rc = gemm_logical(A, b, C, M, N, K, 128, 8, nthreads);
+    free(b);
+    return rc;
+}
+
+/* Single elements, for sampled checks at sizes too large for the full loop.
+ * `ms`, `ns` list `count` (m, n) pairs; out[i] receives C[ms[i], ns[i]]. */
+void oracle_i4i4_entries(const uint8_t *Ap, const uint8_t *Bp, int64_t K, const int64_t *ms,
+                         const int64_t *ns, int64_t count, int64_t *out)
+{
+    int8_t *a = (int8_t *)malloc((size_t)K);
+    int8_t *b = (int8_t *)malloc((size_t)K);
+    if (!a || !b) { free(a); free(b); return; }
+    for (int64_t i = 0; i < count; ++i) {
+        oracle_unpack_int4(Ap + ms[i] * (K / 2), a, 1, K);
+        oracle_unpack_int4(Bp + ns[i] * (K / 2), b, 1, K);
+        out[i] = dot_i64(a, b, K);
+    }
+    free(a);
+    free(b);
+}
+
+void oracle_w4a8_entries(const int8_t *A, const uint8_t *Bp, int64_t K, const int64_t *ms,
+                         const int64_t *ns, int64_t count, int64_t *out)
+{
+    int8_t *b = (int8_t *)malloc((size_t)K);
+    if (!b) return;
+    for (int64_t i = 0; i < count; ++i) {
+        oracle_unpack_int4(Bp + ns[i] * (K / 2), b, 1, K);
+        out[i] = dot_i64(A + ms[i] * K, b, K);
+    }
+    free(b);
+}

@@ -1,0 +1,277 @@
+"""Pins for the CPU oracle: checks against facts fixed outside the oracle itself.
+
+Each check compares the oracle with something it does not compute itself:
+hand-worked bytes and products (tests/golden), an independent sign-extension
+method (shift left, arithmetic shift right, as in the W4A8 page's
+_tir_u8_to_i4_to_i8), Python-integer brute force, numpy int64 matmul, closed
+forms and invariants.  The last test builds the oracle with planted mistakes
+and shows that each one fails at least one pin.
+"""
+
+import os
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_pairs():
+    rows = []
+    with open(os.path.join(GOLDEN, "pack_int4_bytes.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            e, o, h = line.split()
+            rows.append((int(e), int(o), int(h, 16)))
+    return rows
+
+
+def _read_tiny():
+    A, B, C = [], [], []
+    with open(os.path.join(GOLDEN, "tiny_gemm.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            tag, *vals = line.split()
+            {"A": A, "B": B, "C": C}[tag].append([int(v) for v in vals])
+    return (np.array(A, dtype=np.int8), np.array(B, dtype=np.int8), np.array(C, dtype=np.int64))
+
+
+def _shift_sign_extend(n4: int) -> int:
+    """Sign-extend a 4-bit field by the shift method (place it in the high
+    nibble of a byte, read the byte as signed, arithmetic-shift right by 4)."""
+    return int.from_bytes(bytes([(n4 << 4) & 0xFF]), "little", signed=True) >> 4
+
+
+def _np_unpack(packed: np.ndarray) -> np.ndarray:
+    """Independent numpy unpack by the shift method, natural k order."""
+    p = packed.view(np.int8)
+    lo = np.left_shift(p, 4) >> 4          # int8 arithmetic shifts
+    hi = p >> 4
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.int8)
+    out[..., 0::2] = lo
+    out[..., 1::2] = hi
+    return out
+
+
+def _brute(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    M, K = a.shape
+    N = b.shape[0]
+    C = np.zeros((M, N), dtype=np.int64)
+    for m in range(M):
+        for n in range(N):
+            C[m, n] = sum(int(a[m, k]) * int(b[n, k]) for k in range(K))
+    return C
+
+
+# --------------------------------------------------------------------------
+# The pin suite, as a list of named checks returning True when they hold.
+# --------------------------------------------------------------------------
+
+def check_nibbles(o):
+    for byte in range(256):
+        if o.nibble(byte, 0) != _shift_sign_extend(byte & 0xF):
+            return False
+        if o.nibble(byte, 1) != _shift_sign_extend(byte >> 4):
+            return False
+    return True
+
+
+def check_roundtrip(o):
+    vals = np.array(list(itertools.product(range(-8, 8), repeat=2)), dtype=np.int8)  # 256 x 2
+    packed = o.pack_int4(vals)
+    if packed.shape != (256, 1):
+        return False
+    if not np.array_equal(o.unpack_int4(packed), vals):
+        return False
+    # every byte value occurs exactly once, and the nibbles reassemble the byte:
+    # (lo mod 16) + 16 * (hi mod 16) == byte
+    if sorted(packed[:, 0].tolist()) != list(range(256)):
+        return False
+    lohi = o.unpack_int4(np.arange(256, dtype=np.uint8).reshape(256, 1)).astype(np.int64)
+    if lohi.min() < -8 or lohi.max() > 7:
+        return False
+    return bool(np.all((lohi[:, 0] % 16) + 16 * (lohi[:, 1] % 16) == np.arange(256)))
+
+
+def check_golden_bytes(o):
+    pairs = _read_pairs()
+    logical = np.array([[e, od] for e, od, _ in pairs], dtype=np.int8)
+    want = np.array([[h] for _, _, h in pairs], dtype=np.uint8)
+    return np.array_equal(o.pack_int4(logical), want) and np.array_equal(o.unpack_int4(want), logical)
+
+
+def check_tiny_golden(o):
+    A, B, C = _read_tiny()
+    K = A.shape[1]
+    got = o.i4i4_gemm(o.pack_int4(A), o.pack_int4(B), K, threads=1)
+    got2 = o.w4a8_gemm(A, o.pack_int4(B), K, threads=1)
+    return np.array_equal(got, C) and np.array_equal(got2, C)
+
+
+def check_brute_force(o):
+    rng = np.random.default_rng(7)
+    for (M, N, K) in [(1, 1, 2), (2, 3, 4), (3, 2, 6), (4, 4, 8), (3, 1, 8)]:
+        a4 = rng.integers(-8, 8, (M, K), dtype=np.int8)
+        a8 = rng.integers(-128, 128, (M, K), dtype=np.int8)
+        b = rng.integers(-8, 8, (N, K), dtype=np.int8)
+        bp = o.pack_int4(b)
+        if not np.array_equal(o.i4i4_gemm(o.pack_int4(a4), bp, K, threads=2), _brute(a4, b)):
+            return False
+        if not np.array_equal(o.w4a8_gemm(a8, bp, K, threads=2), _brute(a8, b)):
+            return False
+    return True
+
+
+def check_numpy_matmul(o):
+    for idx, (M, N, K) in enumerate([(64, 96, 128), (37, 53, 64)]):
+        a4 = si.int4_values(100 + idx, (M, K))
+        a8 = si.int8_values(200 + idx, (M, K))
+        b = si.int4_values(300 + idx, (N, K))
+        ap, bp = o.pack_int4(a4), o.pack_int4(b)
+        a4n, bn = _np_unpack(ap), _np_unpack(bp)
+        if not (np.array_equal(a4n, a4) and np.array_equal(bn, b)):
+            return False
+        want4 = a4n.astype(np.int64) @ bn.astype(np.int64).T
+        want8 = a8.astype(np.int64) @ bn.astype(np.int64).T
+        if not np.array_equal(o.i4i4_gemm(ap, bp, K), want4):
+            return False
+        if not np.array_equal(o.w4a8_gemm(a8, bp, K), want8):
+            return False
+    return True
+
+
+def check_closed_forms(o):
+    M, N, K = 5, 7, 16
+    b = si.int4_values(11, (N, K))
+    bp = o.pack_int4(b)
+    ones = np.ones((M, K), dtype=np.int8)
+    # all-ones A gives the row sums of B, in every row
+    rs = b.astype(np.int64).sum(axis=1)
+    if not np.array_equal(o.i4i4_gemm(o.pack_int4(ones), bp, K), np.tile(rs, (M, 1))):
+        return False
+    if not np.array_equal(o.w4a8_gemm(ones, bp, K), np.tile(rs, (M, 1))):
+        return False
+    # identity-like B (b[n,k] = 1 iff k == n) returns A's columns
+    a = si.int4_values(12, (M, K))
+    eye = np.zeros((N, K), dtype=np.int8)
+    eye[np.arange(N), np.arange(N)] = 1
+    if not np.array_equal(o.i4i4_gemm(o.pack_int4(a), o.pack_int4(eye), K), a[:, :N]):
+        return False
+    a8 = si.int8_values(13, (M, K))
+    if not np.array_equal(o.w4a8_gemm(a8, o.pack_int4(eye), K), a8[:, :N]):
+        return False
+    # extremes: the no-overflow bound is attained
+    m8 = np.full((M, K), -8, dtype=np.int8)
+    n8 = np.full((N, K), -8, dtype=np.int8)
+    if not np.all(o.i4i4_gemm(o.pack_int4(m8), o.pack_int4(n8), K) == 64 * K):
+        return False
+    if not np.all(o.w4a8_gemm(np.full((M, K), -128, np.int8), o.pack_int4(n8), K) == 1024 * K):
+        return False
+    if not np.all(o.i4i4_gemm(o.pack_int4(np.full((M, K), 7, np.int8)), o.pack_int4(n8), K) == -56 * K):
+        return False
+    # alternating signs against a constant row give zero
+    alt = np.tile(np.array([3, -3], dtype=np.int8), (M, K // 2))
+    if not np.all(o.i4i4_gemm(o.pack_int4(alt), o.pack_int4(np.full((N, K), 5, np.int8)), K) == 0):
+        return False
+    return True
+
+
+def check_k_permutation(o):
+    M, N, K = 6, 5, 32
+    a = si.int4_values(21, (M, K))
+    a8 = si.int8_values(22, (M, K))
+    b = si.int4_values(23, (N, K))
+    perm = np.random.default_rng(3).permutation(K)
+    base4 = o.i4i4_gemm(o.pack_int4(a), o.pack_int4(b), K)
+    base8 = o.w4a8_gemm(a8, o.pack_int4(b), K)
+    p4 = o.i4i4_gemm(o.pack_int4(np.ascontiguousarray(a[:, perm])),
+                     o.pack_int4(np.ascontiguousarray(b[:, perm])), K)
+    p8 = o.w4a8_gemm(np.ascontiguousarray(a8[:, perm]), o.pack_int4(np.ascontiguousarray(b[:, perm])), K)
+    return np.array_equal(base4, p4) and np.array_equal(base8, p8)
+
+
+def check_entries(o):
+    M, N, K = 9, 11, 64
+    a = si.int4_values(31, (M, K))
+    a8 = si.int8_values(32, (M, K))
+    b = si.int4_values(33, (N, K))
+    ap, bp = o.pack_int4(a), o.pack_int4(b)
+    full4 = o.i4i4_gemm(ap, bp, K)
+    full8 = o.w4a8_gemm(a8, bp, K)
+    ms = np.array([0, 3, 8, 8, 5])
+    ns = np.array([0, 10, 2, 10, 7])
+    return (np.array_equal(o.i4i4_entries(ap, bp, K, ms, ns), full4[ms, ns])
+            and np.array_equal(o.w4a8_entries(a8, bp, K, ms, ns), full8[ms, ns]))
+
+
+PINS = [check_nibbles, check_roundtrip, check_golden_bytes, check_tiny_golden, check_brute_force,
+        check_numpy_matmul, check_closed_forms, check_k_permutation, check_entries]
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.Oracle()
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
+def test_pin(orc, pin):
+    assert pin(orc)
+
+
+def test_pack_shape_pin(orc):
+    # tutorial low_precision_gemm.py main(): a (1024, 1024) logical tensor packs to (1024, 512)
+    logical = si.int4_values(5, (1024, 1024))
+    assert orc.pack_int4(logical).shape == (1024, 512)
+
+
+def test_pack_rejects_odd_last_dim(orc):
+    with pytest.raises(ValueError):
+        orc.pack_int4(np.zeros((3, 5), dtype=np.int8))
+
+
+def test_pack_masks_out_of_range(orc):
+    # values outside [-8, 7] are masked to 4 bits (two's-complement wrap), no error
+    got = orc.pack_int4(np.array([[9, -9]], dtype=np.int8))
+    assert got[0, 0] == ((9 & 0xF) | ((-9 & 0xF) << 4))
+
+
+def test_generator_ranges_and_determinism():
+    x4 = si.int4_values(si.workload_seed(1, 0), (256, 256))
+    x8 = si.int8_values(si.workload_seed(3, 0), (64, 4096))
+    assert x4.min() == -8 and x4.max() == 7
+    assert x8.min() == -128 and x8.max() == 127
+    assert np.array_equal(x4, si.int4_values(si.workload_seed(1, 0), (256, 256)))
+    # both nibbles of packed bytes take all 16 values (unlike a low-nibble-only draw)
+    assert len(np.unique(x4[:, 1::2])) == 16
+    # chunked generation equals one-shot generation
+    s = si.splitmix64(42, 10)
+    assert np.array_equal(np.concatenate([si.splitmix64(42, 4), si.splitmix64(42, 6, start=4)]), s)
+
+
+def test_splitmix64_reference_value():
+    # SplitMix64 with state 0: the first output is 0xE220A8397B1DCDAF (value
+    # widely published with Vigna's splitmix64.c for seed 0).
+    assert int(si.splitmix64(0, 1)[0]) == 0xE220A8397B1DCDAF
+
+
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5])
+def test_planted_mistakes_are_caught(tmp_path, mutant):
+    path = oracle.build(str(tmp_path / f"liboracle_m{mutant}.so"), mutant=mutant)
+    bad = oracle.Oracle(oracle.load(path))
+    failed = []
+    for pin in PINS:
+        try:
+            ok = pin(bad)
+        except Exception:
+            ok = False
+        if not ok:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {mutant} passed every pin"
