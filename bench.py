@@ -1,0 +1,324 @@
+"""Benchmark: exact integer GEMM throughput (TOPS = 2*M*N*K / s) on GB300.
+
+One step is one GEMM call of the chosen workload through the C-ABI (host plan
++ TMA loads + unpack + tcgen05 MMA + epilogue, and the split-K reduction when
+the plan splits K).  Inputs are seeded synthetic operands resident in HBM
+before timing; L2 is flushed (a 256 MB write, outside the timed events)
+before every step.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+--impl reference times the CPU oracle (plain C, int64 accumulation) on the
+host cores, each step a bounded row sample of the same workload.
+Under torchrun every rank runs an independent replica (the GEMM is not
+sharded: "replicas only"); value = all ranks' ops / the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "int4/W4A8 GEMM TOPS (2*M*N*K/s)"
+UNIT = "TOPS"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+E4M3_PER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        out = {}
+        for k in FALLBACK_PEAKS:
+            v = d.get(k)
+            if isinstance(v, dict):
+                v = v.get("value")
+            out[k] = float(v) if v is not None else None
+        if all(out[k] for k in ("hbm_gbs", "bf16_tflops")):
+            return out, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_bytes(variant, M, N, K):
+    a = M * K if variant == "w4a8" else M * K // 2
+    return a + N * K // 2 + 4 * M * N
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_sample_time(orc, variant, a, b, K, rows, threads):
+    """Run the oracle on the first `rows` rows of A; returns seconds."""
+    t0 = time.perf_counter()
+    if variant == "i4i4":
+        orc.i4i4_gemm(orc.pack_int4(a[:rows]), orc.pack_int4(b), K, threads=threads)
+    else:
+        orc.w4a8_gemm(np.ascontiguousarray(a[:rows]), orc.pack_int4(b), K, threads=threads)
+    return time.perf_counter() - t0
+
+
+def calibrate_rows(orc, variant, a, b, K, threads, target_s):
+    M = a.shape[0]
+    rows = max(1, min(M, threads))
+    t = oracle_sample_time(orc, variant, a, b, K, rows, threads)
+    if t < target_s / 8 and rows < M:
+        rows = int(min(M, max(rows + 1, rows * target_s / max(t, 1e-3))))
+        rows = max(threads, (rows // threads) * threads) if rows >= threads else rows
+        rows = min(rows, M)
+    return rows
+
+
+def run_reference(args, variant, M, N, K, a, b, rank, world):
+    import oracle
+    if rank != 0:
+        return
+    orc = oracle.Oracle()
+    threads = os.cpu_count() or 1
+    step_target = max(0.5, min(4.0, 150.0 / max(1, args.steps + args.warmup)))
+    rows = calibrate_rows(orc, variant, a, b, K, threads, step_target)
+    for _ in range(args.warmup):
+        oracle_sample_time(orc, variant, a, b, K, rows, threads)
+    times = [oracle_sample_time(orc, variant, a, b, K, rows, threads) for _ in range(args.steps)]
+    ops = 2.0 * rows * N * K
+    total = sum(times)
+    value = ops * args.steps / total / 1e12
+    sample = f"rows 0..{rows - 1} of A against all {N} rows of B, K={K} (each step)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
+        "data": "synthetic (SplitMix64-seeded, uniform)",
+        "config": {"workload": args.workload, "variant": variant, "M": M, "N": N, "K": K},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
+    import torch
+    import precision_integer_gemm_gb300 as pig
+
+    pig.build_library()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    stream = torch.cuda.current_stream()
+
+    # operands resident in HBM: logical -> packed by the library's pack kernel
+    a_dev = torch.from_numpy(a).cuda()
+    b_dev = torch.from_numpy(b).cuda()
+    bp = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
+    pig.pack_int4(b_dev, bp, N, K)
+    if variant == "i4i4":
+        a_in = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+        pig.pack_int4(a_dev, a_in, M, K)
+        gemm = pig.i4i4_gemm
+    else:
+        a_in = a_dev
+        gemm = pig.w4a8_gemm
+    del b_dev
+    C = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+
+    def step():
+        gemm(a_in, bp, C, M, N, K, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    if pig.igemm_last_status(stream) != 0:
+        raise RuntimeError("device status after warm-up is not ok")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    if pig.igemm_last_status(stream) != 0:
+        raise RuntimeError("device status after the timed region is not ok")
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_s = sum(kernel_ms) / 1e3
+    if dist is not None:
+        t = torch.tensor([total_s], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+
+    ops = 2.0 * M * N * K
+    value = ops * args.steps * world / total_s / 1e12
+    avg_launch_s = total_s / args.steps
+
+    # end to end through the public API with pinned host buffers
+    e2e_steps = max(1, min(args.steps, 5))
+    a_host = (a_in.cpu() if variant == "i4i4" else torch.from_numpy(a)).pin_memory()
+    bp_host = bp.cpu().pin_memory()
+    c_host = torch.empty((M, N), dtype=torch.int32).pin_memory()
+    a_e, bp_e = torch.empty_like(a_in), torch.empty_like(bp)
+    C_e = torch.empty_like(C)
+    e_s = torch.cuda.Event(enable_timing=True)
+    e_e = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e_s.record(stream)
+    for _ in range(e2e_steps):
+        a_e.copy_(a_host, non_blocking=True)
+        bp_e.copy_(bp_host, non_blocking=True)
+        gemm(a_e, bp_e, C_e, M, N, K, stream)
+        c_host.copy_(C_e, non_blocking=True)
+    e_e.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = e_s.elapsed_time(e_e) / 1e3
+    e2e_value = ops * e2e_steps * world / e2e_s / 1e12  # replicas run concurrently
+    if not torch.equal(C_e, C):
+        raise RuntimeError("end-to-end result differs from the device-resident result")
+
+    peaks, peak_src = load_peaks()
+    nbytes = workload_bytes(variant, M, N, K)
+    if args.workload.startswith("w4a8_decode"):
+        achieved = nbytes / avg_launch_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "algorithmic_bytes_per_launch": nbytes, "peak_source": peak_src}
+    else:
+        peak = E4M3_PER_BF16 * peaks["bf16_tflops"]
+        achieved = ops / avg_launch_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None, "algorithmic_ops_per_launch": ops,
+                "peak_source": f"{peak_src} bf16 x {E4M3_PER_BF16} (e4m3 MMA)",
+                "mma_macs_per_op": 1 if variant == "i4i4" else 2}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int4" if variant == "i4i4" else "int8xint4",
+        "data": "synthetic (SplitMix64-seeded, uniform)",
+        "config": {"workload": args.workload, "variant": variant, "M": M, "N": N, "K": K,
+                   "l2": "flushed before every step (256 MB write, outside the timed events)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "wall_ms_per_step": 1e3 * wall / args.steps,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": UNIT,
+                "h2d_bytes_per_step": int(a_in.numel() * a_in.element_size() + bp.numel()),
+                "d2h_bytes_per_step": int(C.numel() * 4)},
+        "roofline": roof,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        orc = oracle.Oracle()
+        threads = os.cpu_count() or 1
+        rows = calibrate_rows(orc, variant, a, b, K, threads, args.cpu_seconds)
+        t = oracle_sample_time(orc, variant, a, b, K, rows, threads)
+        line["cpu_baseline"] = {"value": 2.0 * rows * N * K / t / 1e12, "unit": UNIT, "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"rows 0..{rows - 1} of A against all {N} rows of B, K={K}; {t:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="i4i4_8192", choices=sorted(si.WORKLOADS))
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = p.parse_args()
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    variant, M, N, K, a, b = si.workload_operands(args.workload)
+
+    if args.impl == "reference":
+        run_reference(args, variant, M, N, K, a, b, rank, world)
+        return
+
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    try:
+        run_ours(args, variant, M, N, K, a, b, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

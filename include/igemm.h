@@ -1,0 +1,121 @@
+/*
+ * igemm.h — exact integer GEMM on packed int4 operands for NVIDIA GB300 (sm_103a).
+ *
+ * C-ABI of libigemm.so.  All entry points are asynchronous on `stream` and
+ * return an igemm_status synchronously: argument errors are reported before
+ * anything is enqueued, and nothing is launched when the return value is not
+ * IGEMM_OK.  Every pointer argument is caller-owned device memory (global
+ * memory of the current device); the library allocates and frees nothing.
+ * Device-side problems (a pipeline wait that exceeded the watchdog limit) are
+ * reported later by igemm_last_status().
+ *
+ * Operand formats
+ *   Packed int4 matrix [rows, K/2] bytes, row-major: byte j of a row holds
+ *   element 2j in its low nibble and element 2j+1 in its high nibble, each a
+ *   4-bit two's-complement value in [-8, 7] (TileLang tutorial page
+ *   low_precision_gemm.py, pack_int4; "[Example] add w4a8 gemm kernel",
+ *   tilelang PR #815, _tir_u8_to_i4_to_i8: pos 0 = low nibble).
+ *   C is [M, N] int32, row-major; every element is overwritten.
+ *
+ * Shape and alignment rules (violations are returned, never launched)
+ *   M, N, K >= 0; M == 0 or N == 0 is an empty product (no work, IGEMM_OK);
+ *   K == 0 with M, N > 0 sets C to zero.
+ *   K % 32 == 0 (a packed row is a whole number of 16-byte units, the TMA
+ *   row-pitch rule) else IGEMM_UNSUPPORTED_SHAPE.
+ *   K <= 65536 else IGEMM_OVERFLOW_BOUND: the accumulation is exact only up to
+ *   this depth (the int32 result itself would fit far beyond it).
+ *   Every non-empty operand base address and C must be 16-byte aligned, else
+ *   IGEMM_MISALIGNED.
+ */
+#ifndef IGEMM_H
+#define IGEMM_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define IGEMM_API __attribute__((visibility("default")))
+#else
+#define IGEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum igemm_status {
+    IGEMM_OK = 0,
+    IGEMM_INVALID_ARGUMENT = 1,  /* null pointer for a non-empty operand, negative size */
+    IGEMM_UNSUPPORTED_SHAPE = 2, /* K % 32 != 0 (GEMM); odd K (pack_int4) */
+    IGEMM_MISALIGNED = 3,        /* a base address is not 16-byte aligned */
+    IGEMM_OVERFLOW_BOUND = 4,    /* K above the exact-accumulation bound (65536) */
+    IGEMM_CUDA_ERROR = 5,        /* tensor-map encoding, memset or launch failed */
+    IGEMM_DEVICE_TIMEOUT = 6     /* a kernel's bounded wait expired (see igemm_last_status) */
+} igemm_status;
+
+/*
+ * int4 x int4 GEMM:  C[m,n] = sum_k a[m,k] * b[n,k], exact, int32.
+ * Defined by "[CUDA] Support int4 T.gemm" (tilelang PR #2063),
+ * examples/gemm_int4/example_tilelang_gemm_int4.py, matmul_nt_int4: A (M,K)
+ * int4, B (N,K) int4, C (M,N) int32, T.gemm(A_shared, B_shared, C_local,
+ * transpose_B=True); same contract as matmul_int4 of the tutorial page
+ * low_precision_gemm.py.
+ *   Ap  [M, K/2] packed int4 (device), read only
+ *   Bp  [N, K/2] packed int4 (device), read only
+ *   C   [M, N] int32 (device), written
+ * Returns IGEMM_OK once the work is enqueued on `stream`.
+ */
+IGEMM_API int i4i4_gemm(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);
+
+/*
+ * W4A8 GEMM:  C[m,n] = sum_k a[m,k] * b[n,k], a int8, b int4, exact, int32.
+ * Defined by "[Example] add w4a8 gemm kernel" (tilelang PR #815): int8
+ * activations times int4 weights sign-extended in the kernel
+ * (_tir_u8_to_i4_to_i8), checked against an integer matmul (reviewed
+ * ref_program).  The page's kernel returns C transposed; this entry point
+ * returns C[M, N].
+ *   A   [M, K] int8 activations (device), read only
+ *   Bp  [N, K/2] packed int4 weights (device), read only
+ *   C   [M, N] int32 (device), written
+ */
+IGEMM_API int w4a8_gemm(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);
+
+/*
+ * Pack logical int4 values two per byte (TileLang tutorial page
+ * low_precision_gemm.py, pack_int4): packed[r, j] = (logical[r, 2j] & 0xF) |
+ * ((logical[r, 2j+1] & 0xF) << 4).  Values outside [-8, 7] are masked to four
+ * bits (two's-complement wrap), as on the page; this is not an error.
+ *   logical [rows, K] int8 (device), read only
+ *   packed  [rows, K/2] bytes (device), written
+ * K must be even (IGEMM_UNSUPPORTED_SHAPE otherwise, the page's ValueError);
+ * rows == 0 or K == 0 is a no-op.  Any alignment is accepted.
+ */
+IGEMM_API int pack_int4(const int8_t *logical, uint8_t *packed, int64_t rows, int64_t K, cudaStream_t stream);
+
+/* Static, human-readable text for an igemm_status value. */
+IGEMM_API const char *igemm_strerror(int code);
+
+/*
+ * Synchronizes `stream`, then returns and clears the device status word of
+ * the current device: IGEMM_OK, or IGEMM_DEVICE_TIMEOUT when some kernel of
+ * this library had a pipeline wait exceed the watchdog limit (that kernel then
+ * stopped early and its C is not valid).  IGEMM_CUDA_ERROR if the
+ * synchronization itself failed.  The limit is 2 s per wait, or
+ * IGEMM_WATCHDOG_MS milliseconds from the environment (read once).
+ */
+IGEMM_API int igemm_last_status(cudaStream_t stream);
+
+/*
+ * Self-test of the watchdog: enqueues one single-CTA kernel whose wait can
+ * never be satisfied (an mbarrier nobody arrives at) with a limit of
+ * `limit_us` microseconds.  The kernel gives up, records IGEMM_DEVICE_TIMEOUT
+ * in the status word and exits normally; igemm_last_status() then returns it.
+ * No GPU fault or hang is involved.  limit_us must be in [1, 1000000].
+ */
+IGEMM_API int igemm_watchdog_selftest(uint32_t limit_us, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IGEMM_H */

@@ -1,0 +1,122 @@
+"""Python binding of libigemm.so (exact int4 x int4 and W4A8 GEMM on sm_103a).
+
+Argument marshalling only: each function passes device pointers, sizes and
+the CUDA stream to the C entry point of the same name (include/igemm.h) and
+raises IgemmError when it returns a non-zero status.  All work runs in the
+library's CUDA kernels; if the shared library is missing, loading fails with
+an error instead of falling back to anything else.
+
+Tensors are torch CUDA tensors (or raw integer device addresses).  `stream`
+defaults to torch's current stream on the current device.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH, build as build_library
+
+__all__ = [
+    "IgemmError", "load", "i4i4_gemm", "w4a8_gemm", "pack_int4", "igemm_strerror",
+    "igemm_last_status", "igemm_watchdog_selftest", "EXPORTED_SYMBOLS", "LIB_PATH", "build_library",
+]
+
+EXPORTED_SYMBOLS = ("i4i4_gemm", "w4a8_gemm", "pack_int4", "igemm_strerror", "igemm_last_status",
+                    "igemm_watchdog_selftest")
+
+IGEMM_OK = 0
+IGEMM_INVALID_ARGUMENT = 1
+IGEMM_UNSUPPORTED_SHAPE = 2
+IGEMM_MISALIGNED = 3
+IGEMM_OVERFLOW_BOUND = 4
+IGEMM_CUDA_ERROR = 5
+IGEMM_DEVICE_TIMEOUT = 6
+
+_lib = None
+
+
+class IgemmError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {igemm_strerror(code)} (status {code})")
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libigemm.so (the in-tree build); raises if it has not been built."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise OSError(f"{LIB_PATH} is missing: build it with precision_integer_gemm_gb300.build_library()")
+        _lib = _bind(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    p = ctypes.c_void_p
+    i = ctypes.c_int
+    i64 = ctypes.c_int64
+    lib.i4i4_gemm.argtypes = [p, p, p, i, i, i, p]
+    lib.i4i4_gemm.restype = i
+    lib.w4a8_gemm.argtypes = [p, p, p, i, i, i, p]
+    lib.w4a8_gemm.restype = i
+    lib.pack_int4.argtypes = [p, p, i64, i64, p]
+    lib.pack_int4.restype = i
+    lib.igemm_strerror.argtypes = [i]
+    lib.igemm_strerror.restype = ctypes.c_char_p
+    lib.igemm_last_status.argtypes = [p]
+    lib.igemm_last_status.restype = i
+    lib.igemm_watchdog_selftest.argtypes = [ctypes.c_uint32, p]
+    lib.igemm_watchdog_selftest.restype = i
+    return lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(code: int, where: str) -> None:
+    if code != IGEMM_OK:
+        raise IgemmError(code, where)
+
+
+def i4i4_gemm(Ap, Bp, C, M: int, N: int, K: int, stream=None) -> None:
+    """C[M,N] (int32) = A . B^T for packed int4 Ap [M,K/2] and Bp [N,K/2]."""
+    _check(load().i4i4_gemm(_ptr(Ap), _ptr(Bp), _ptr(C), M, N, K, _stream(stream)), "i4i4_gemm")
+
+
+def w4a8_gemm(A, Bp, C, M: int, N: int, K: int, stream=None) -> None:
+    """C[M,N] (int32) = A . B^T for int8 A [M,K] and packed int4 Bp [N,K/2]."""
+    _check(load().w4a8_gemm(_ptr(A), _ptr(Bp), _ptr(C), M, N, K, _stream(stream)), "w4a8_gemm")
+
+
+def pack_int4(logical, packed, rows: int, K: int, stream=None) -> None:
+    """packed [rows,K/2] = two int4 values per byte of logical [rows,K] (low nibble = even k)."""
+    _check(load().pack_int4(_ptr(logical), _ptr(packed), rows, K, _stream(stream)), "pack_int4")
+
+
+def igemm_strerror(code: int) -> str:
+    return load().igemm_strerror(code).decode()
+
+
+def igemm_last_status(stream=None) -> int:
+    return int(load().igemm_last_status(_stream(stream)))
+
+
+def igemm_watchdog_selftest(limit_us: int, stream=None) -> None:
+    _check(load().igemm_watchdog_selftest(limit_us, _stream(stream)), "igemm_watchdog_selftest")

@@ -1,0 +1,241 @@
+// C-ABI entry points of libigemm.so (declared in include/igemm.h): argument
+// validation, tensor maps, the device status word, pack_int4 and the
+// watchdog self-test.  The GEMM kernels live in gemm_kernel.cuh.
+#include <cstdint>
+#include <cstdlib>
+#include <cudaTypedefs.h>
+#include "launch.cuh"
+#include "igemm.h"
+
+namespace igemm {
+
+// Device status word: 0, or the first error a kernel recorded (a timed-out
+// wait).  Read and cleared by igemm_last_status().
+__device__ int g_status_word = 0;
+
+int *device_status_word()
+{
+    static int *cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!cache[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<int *>(p);
+    }
+    return cache[dev];
+}
+
+unsigned long long watchdog_limit_ns()
+{
+    static unsigned long long limit = [] {
+        const char *s = std::getenv("IGEMM_WATCHDOG_MS");
+        long long ms = s ? std::atoll(s) : 0;
+        if (ms <= 0) ms = 2000;
+        return static_cast<unsigned long long>(ms) * 1000000ull;
+    }();
+    return limit;
+}
+
+int sm_count()
+{
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+int make_map_u8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t row_bytes, uint32_t box_rows,
+                uint32_t box_bytes)
+{
+    auto fn = encode_tiled();
+    if (!fn) return kCudaError;
+    const cuuint64_t dims[2] = {row_bytes, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_bytes, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? kOk : kCudaError;
+}
+
+Launch plan_launch(int p_tiles, int q_tiles, int kb_total, int64_t c_bytes, int64_t operand_bytes)
+{
+    const int sms = sm_count();
+    const int64_t tiles = int64_t(p_tiles) * q_tiles;
+    int best = 1;
+    double best_eff = 0.0;
+    const bool may_split = tiles < sms || c_bytes * 4 <= operand_bytes;
+    const int max_split = may_split ? (kb_total / 2 > 1 ? kb_total / 2 : 1) : 1;
+    for (int s = 1; s <= 16 && s <= max_split; ++s) {
+        const int64_t ctas = tiles * s;
+        const int64_t waves = (ctas + sms - 1) / sms;
+        const double eff = double(ctas) / double(waves * sms);
+        if (eff > best_eff + 0.03) {  // a split must buy a clear improvement
+            best_eff = eff;
+            best = s;
+        }
+    }
+    Launch l;
+    l.kb_per_split = (kb_total + best - 1) / best;
+    l.split = (kb_total + l.kb_per_split - 1) / l.kb_per_split;  // no empty split
+    l.grid = dim3(p_tiles, q_tiles, l.split);
+    return l;
+}
+
+// ---------------------------------------------------------------- pack_int4
+// Output byte j is built from logical elements 2j and 2j+1 of the flat
+// row-major array (rows are contiguous and K is even, so the flat view and
+// the per-row view agree).  16-byte units go through the vector path.
+__global__ void pack_int4_kernel(const int8_t *__restrict__ logical, uint8_t *__restrict__ packed, int64_t n_out,
+                                 int64_t n_vec)
+{
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    const int64_t t0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (int64_t u = t0; u < n_vec; u += stride) {
+        const uint4 a = reinterpret_cast<const uint4 *>(logical)[2 * u];
+        const uint4 b = reinterpret_cast<const uint4 *>(logical)[2 * u + 1];
+        const uint32_t x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t ev = __byte_perm(x[2 * j], x[2 * j + 1], 0x6420);
+            const uint32_t od = __byte_perm(x[2 * j], x[2 * j + 1], 0x7531);
+            o[j] = (ev & 0x0F0F0F0Fu) | ((od & 0x0F0F0F0Fu) << 4);
+        }
+        reinterpret_cast<uint4 *>(packed)[u] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    for (int64_t j = n_vec * 16 + t0; j < n_out; j += stride) {
+        packed[j] = static_cast<uint8_t>((logical[2 * j] & 0xF) | ((logical[2 * j + 1] & 0xF) << 4));
+    }
+}
+
+// ---------------------------------------------------------------- watchdog self-test
+__global__ void watchdog_selftest_kernel(int *status, unsigned long long limit_ns)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const Watchdog wd{&abort_flag, status, limit_ns};
+        wait_bounded(&bar, 0, wd);  // nothing ever arrives: returns false after limit_ns
+    }
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace igemm
+
+using namespace igemm;
+
+static int gemm_common_checks(const void *a, const void *b, int32_t *C, int M, int N, int K, cudaStream_t stream,
+                              bool *done)
+{
+    *done = true;
+    if (M < 0 || N < 0 || K < 0) return kInvalidArgument;
+    if (M == 0 || N == 0) return kOk;
+    if (!C) return kInvalidArgument;
+    if (K % 32 != 0) return kUnsupportedShape;
+    if (K > kMaxK) return kOverflowBound;
+    if (!aligned16(C)) return kMisaligned;
+    if (K == 0) {
+        return cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 4, stream) == cudaSuccess ? kOk : kCudaError;
+    }
+    if (!a || !b) return kInvalidArgument;
+    if (!aligned16(a) || !aligned16(b)) return kMisaligned;
+    *done = false;
+    return kOk;
+}
+
+extern "C" int i4i4_gemm(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K,
+                         cudaStream_t stream)
+{
+    bool done;
+    const int rc = gemm_common_checks(Ap, Bp, C, M, N, K, stream, &done);
+    if (done) return rc;
+    return launch_i4i4(Ap, Bp, C, M, N, K, stream);
+}
+
+extern "C" int w4a8_gemm(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K,
+                         cudaStream_t stream)
+{
+    bool done;
+    const int rc = gemm_common_checks(A, Bp, C, M, N, K, stream, &done);
+    if (done) return rc;
+    return launch_w4a8(A, Bp, C, M, N, K, stream);
+}
+
+extern "C" int pack_int4(const int8_t *logical, uint8_t *packed, int64_t rows, int64_t K, cudaStream_t stream)
+{
+    if (rows < 0 || K < 0) return kInvalidArgument;
+    if (K % 2 != 0) return kUnsupportedShape;
+    if (rows == 0 || K == 0) return kOk;
+    if (!logical || !packed) return kInvalidArgument;
+    const int64_t n_out = rows * (K / 2);
+    const int64_t n_vec = (aligned16(logical) && aligned16(packed)) ? n_out / 16 : 0;
+    const int64_t work = n_vec > 0 ? n_vec : n_out;
+    int64_t blocks = (work + 255) / 256;
+    const int64_t cap = int64_t(sm_count()) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    pack_int4_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(logical, packed, n_out, n_vec);
+    return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
+}
+
+extern "C" const char *igemm_strerror(int code)
+{
+    switch (code) {
+    case kOk: return "ok";
+    case kInvalidArgument: return "invalid argument (null pointer for a non-empty operand, or a negative size)";
+    case kUnsupportedShape: return "unsupported shape (GEMM: K must be a multiple of 32; pack_int4: K must be even)";
+    case kMisaligned: return "misaligned pointer (operand and C base addresses must be 16-byte aligned)";
+    case kOverflowBound: return "K above the exact-accumulation bound (65536)";
+    case kCudaError: return "CUDA error (tensor-map encoding, memset, launch or synchronization failed)";
+    case kDeviceTimeout: return "device timeout (a kernel's bounded pipeline wait expired; its output is not valid)";
+    default: return "unknown igemm status";
+    }
+}
+
+extern "C" int igemm_last_status(cudaStream_t stream)
+{
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return kCudaError;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return kCudaError;
+    const int zero = 0;
+    if (v != 0 && cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return kCudaError;
+    return v;
+}
+
+extern "C" int igemm_watchdog_selftest(uint32_t limit_us, cudaStream_t stream)
+{
+    if (limit_us < 1 || limit_us > 1000000) return kInvalidArgument;
+    int *status = device_status_word();
+    if (!status) return kCudaError;
+    watchdog_selftest_kernel<<<1, 32, 0, stream>>>(status, static_cast<unsigned long long>(limit_us) * 1000ull);
+    return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
+}

@@ -1,0 +1,94 @@
+"""Host-side checks of the C-ABI library that need no GPU.
+
+The library must build for sm_103a, load, export every entry point that
+include/igemm.h declares, and reject bad arguments synchronously (these paths
+return before any CUDA call, so they run on a machine without a GPU).
+"""
+
+import os
+import re
+
+import pytest
+
+import precision_integer_gemm_gb300 as pig
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "igemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pig.build_library()
+    return pig.load()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    return re.findall(r"IGEMM_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_python_names():
+    assert sorted(header_functions()) == sorted(pig.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+    # nothing else leaks out of the library besides the declared entry points
+    out = os.popen(f"nm -D --defined-only {pig.LIB_PATH}").read()
+    ours = {line.split()[-1] for line in out.splitlines()
+            if " T " in line and re.match(r"^(i4i4|w4a8|pack|igemm)", line.split()[-1])}
+    assert ours == set(header_functions())
+
+
+def test_strerror_covers_every_status(lib):
+    texts = {pig.igemm_strerror(c) for c in range(7)}
+    assert len(texts) == 7
+    assert "unknown" in pig.igemm_strerror(99)
+
+
+FAKE = 0x10000  # a 16-byte-aligned address that is never dereferenced here
+
+
+@pytest.mark.parametrize("fn", ["i4i4_gemm", "w4a8_gemm"])
+def test_gemm_argument_validation(lib, fn):
+    f = getattr(lib, fn)
+    # negative sizes
+    assert f(FAKE, FAKE, FAKE, -1, 8, 32, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert f(FAKE, FAKE, FAKE, 8, -1, 32, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert f(FAKE, FAKE, FAKE, 8, 8, -32, None) == pig.IGEMM_INVALID_ARGUMENT
+    # empty products are no-ops, even with null pointers
+    assert f(None, None, None, 0, 8, 32, None) == pig.IGEMM_OK
+    assert f(None, None, None, 8, 0, 32, None) == pig.IGEMM_OK
+    # null C / operands for a non-empty product
+    assert f(FAKE, FAKE, None, 8, 8, 32, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert f(None, FAKE, FAKE, 8, 8, 32, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert f(FAKE, None, FAKE, 8, 8, 32, None) == pig.IGEMM_INVALID_ARGUMENT
+    # K must be a multiple of 32 and at most 65536
+    for k in (2, 16, 48, 1000):
+        assert f(FAKE, FAKE, FAKE, 8, 8, k, None) == pig.IGEMM_UNSUPPORTED_SHAPE
+    assert f(FAKE, FAKE, FAKE, 8, 8, 65536 + 32, None) == pig.IGEMM_OVERFLOW_BOUND
+    # 16-byte alignment of every base address
+    assert f(FAKE, FAKE, FAKE + 4, 8, 8, 32, None) == pig.IGEMM_MISALIGNED
+    assert f(FAKE + 1, FAKE, FAKE, 8, 8, 32, None) == pig.IGEMM_MISALIGNED
+    assert f(FAKE, FAKE + 8, FAKE, 8, 8, 32, None) == pig.IGEMM_MISALIGNED
+
+
+def test_pack_argument_validation(lib):
+    assert lib.pack_int4(FAKE, FAKE, -1, 8, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert lib.pack_int4(FAKE, FAKE, 4, -2, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert lib.pack_int4(FAKE, FAKE, 4, 7, None) == pig.IGEMM_UNSUPPORTED_SHAPE
+    assert lib.pack_int4(None, None, 0, 8, None) == pig.IGEMM_OK
+    assert lib.pack_int4(None, None, 4, 0, None) == pig.IGEMM_OK
+    assert lib.pack_int4(None, FAKE, 4, 8, None) == pig.IGEMM_INVALID_ARGUMENT
+
+
+def test_watchdog_selftest_argument_validation(lib):
+    assert lib.igemm_watchdog_selftest(0, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert lib.igemm_watchdog_selftest(2_000_000, None) == pig.IGEMM_INVALID_ARGUMENT
+
+
+def test_python_binding_raises_with_status(lib):
+    with pytest.raises(pig.IgemmError) as e:
+        pig.i4i4_gemm(FAKE, FAKE, FAKE, 8, 8, 40, stream=0)
+    assert e.value.code == pig.IGEMM_UNSUPPORTED_SHAPE

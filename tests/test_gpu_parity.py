@@ -1,0 +1,250 @@
+"""GPU parity: the CUDA path against the CPU oracle, bit for bit.
+
+Inputs are seeded logical values (seeded_inputs); each side packs them on its
+own (the library's pack_int4 kernel on the GPU, the oracle's packer on the
+CPU) and the packed bytes are compared too.  Small and medium shapes are
+compared element by element over the whole C; the full-size workloads are
+compared on sampled elements that the oracle computes one by one, in the same
+launch configuration the benchmark times (the same entry points).
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import precision_integer_gemm_gb300 as pig  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.Oracle()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    pig.build_library()
+    return pig.load()
+
+
+def dev(x: np.ndarray):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def gpu_pack(logical: np.ndarray):
+    rows, k = logical.shape
+    lt = dev(logical)
+    out = torch.empty((rows, k // 2), dtype=torch.uint8, device="cuda")
+    pig.pack_int4(lt, out, rows, k)
+    return out
+
+
+def run_i4i4(a: np.ndarray, b: np.ndarray, orc):
+    """GPU int4 x int4 of logical a [M,K], b [N,K]; returns (C_gpu, Ap_cpu, Bp_cpu)."""
+    M, K = a.shape
+    N = b.shape[0]
+    ap_g, bp_g = gpu_pack(a), gpu_pack(b)
+    ap_c, bp_c = orc.pack_int4(a), orc.pack_int4(b)
+    assert np.array_equal(ap_g.cpu().numpy(), ap_c) and np.array_equal(bp_g.cpu().numpy(), bp_c)
+    C = torch.full((M, N), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+    pig.i4i4_gemm(ap_g, bp_g, C, M, N, K)
+    assert pig.igemm_last_status() == 0
+    return C.cpu().numpy(), ap_c, bp_c
+
+
+def run_w4a8(a: np.ndarray, b: np.ndarray, orc):
+    M, K = a.shape
+    N = b.shape[0]
+    bp_g = gpu_pack(b)
+    bp_c = orc.pack_int4(b)
+    assert np.array_equal(bp_g.cpu().numpy(), bp_c)
+    C = torch.full((M, N), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+    pig.w4a8_gemm(dev(a), bp_g, C, M, N, K)
+    assert pig.igemm_last_status() == 0
+    return C.cpu().numpy(), bp_c
+
+
+# ---------------------------------------------------------------- pack_int4
+
+def test_pack_all_nibble_pairs(orc):
+    vals = np.array([[e, o] for e in range(-8, 8) for o in range(-8, 8)], dtype=np.int8)
+    assert np.array_equal(gpu_pack(vals).cpu().numpy(), orc.pack_int4(vals))
+
+
+@pytest.mark.parametrize("rows,k", [(1, 2), (3, 30), (7, 64), (129, 96), (1000, 1024), (33, 4098)])
+def test_pack_random_and_out_of_range(orc, rows, k):
+    x = si.int8_values(77 + rows, (rows, k))  # full int8 range: exercises the 4-bit wrap
+    assert np.array_equal(gpu_pack(x).cpu().numpy(), orc.pack_int4(x))
+
+
+def test_pack_unaligned_pointers_take_the_scalar_path(orc):
+    x = si.int4_values(5, (16, 64))
+    buf = torch.zeros(16 * 64 + 3, dtype=torch.int8, device="cuda")
+    buf[3:] = dev(x).view(-1)
+    out = torch.zeros(16 * 32 + 1, dtype=torch.uint8, device="cuda")
+    pig.pack_int4(buf.data_ptr() + 3, out.data_ptr() + 1, 16, 64)
+    assert np.array_equal(out[1:].cpu().numpy().reshape(16, 32), orc.pack_int4(x))
+
+
+# ---------------------------------------------------------------- whole-C parity
+
+SMALL_I4I4 = [(256, 256, 256), (1, 1, 32), (1, 300, 96), (129, 257, 160), (300, 72, 384), (128, 256, 128),
+              (77, 513, 1024), (1024, 1024, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", SMALL_I4I4)
+def test_i4i4_matches_oracle(orc, M, N, K):
+    a = si.int4_values(1000 + M, (M, K))
+    b = si.int4_values(2000 + N, (N, K))
+    C, ap, bp = run_i4i4(a, b, orc)
+    assert np.array_equal(C, orc.i4i4_gemm(ap, bp, K))
+
+
+SMALL_W4A8 = [(1, 1, 32), (5, 300, 1024), (16, 256, 256), (17, 130, 512), (32, 1000, 2048), (33, 129, 160),
+              (128, 128, 128), (300, 257, 384), (520, 640, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", SMALL_W4A8)
+def test_w4a8_matches_oracle(orc, M, N, K):
+    a = si.int8_values(3000 + M, (M, K))
+    b = si.int4_values(4000 + N, (N, K))
+    C, bp = run_w4a8(a, b, orc)
+    assert np.array_equal(C, orc.w4a8_gemm(a, bp, K))
+
+
+def test_configured_small_workloads(orc):
+    for name in ("i4i4_256", "i4i4_1024"):
+        variant, M, N, K, a, b = si.workload_operands(name)
+        C, ap, bp = run_i4i4(a, b, orc)
+        assert np.array_equal(C, orc.i4i4_gemm(ap, bp, K)), name
+
+
+def test_decode_workload_whole_c(orc):
+    variant, M, N, K, a, b = si.workload_operands("w4a8_decode_16x28672x8192")
+    C, bp = run_w4a8(a, b, orc)
+    assert np.array_equal(C, orc.w4a8_gemm(a, bp, K))
+
+
+# ---------------------------------------------------------------- extremes and exactness bound
+
+@pytest.mark.parametrize("K", [32, 8192, 65536])
+@pytest.mark.parametrize("av,bv", [(-8, -8), (7, 7), (-8, 7), (7, -8)])
+def test_i4i4_extreme_constants(orc, K, av, bv):
+    M, N = 130, 260
+    a = np.full((M, K), av, dtype=np.int8)
+    b = np.full((N, K), bv, dtype=np.int8)
+    C, _, _ = run_i4i4(a, b, orc)
+    assert np.all(C == av * bv * K)
+
+
+@pytest.mark.parametrize("K", [32, 8192, 65536])
+@pytest.mark.parametrize("av,bv", [(-128, -8), (127, 7), (-128, 7), (127, -8), (0, -8)])
+def test_w4a8_extreme_constants(orc, K, av, bv):
+    for M in (16, 130):
+        N = 260
+        a = np.full((M, K), av, dtype=np.int8)
+        b = np.full((N, K), bv, dtype=np.int8)
+        C, _ = run_w4a8(a, b, orc)
+        assert np.all(C == av * bv * K), (M, K, av, bv)
+
+
+def test_adversarial_partial_sums(orc):
+    # a long run of maximal products followed by +/-1 terms: any lost low bit
+    # in a large accumulator shows up
+    K = 65536
+    M, N = 128, 256
+    a = np.full((M, K), 7, dtype=np.int8)
+    b = np.full((N, K), 7, dtype=np.int8)
+    a[:, K // 2:] = np.where(np.arange(K // 2) % 3 == 0, 1, -1)
+    b[:, K // 2:] = 1
+    a[::2, -5:] = -8
+    C, ap, bp = run_i4i4(a, b, orc)
+    ms = np.arange(M).repeat(2)
+    ns = np.tile([0, N - 1], M)
+    assert np.array_equal(C[ms, ns], orc.i4i4_entries(ap, bp, K, ms, ns))
+    a8 = np.full((M, K), 127, dtype=np.int8)
+    a8[:, K // 2:] = np.where(np.arange(K // 2) % 3 == 0, -128, 1)
+    C8, bp8 = run_w4a8(a8, b, orc)
+    assert np.array_equal(C8[ms, ns], orc.w4a8_entries(a8, bp8, K, ms, ns))
+
+
+# ---------------------------------------------------------------- full-size workloads, sampled
+
+def sample_indices(M, N, count, seed):
+    rng = np.random.default_rng(seed)
+    ms = list(rng.integers(0, M, count))
+    ns = list(rng.integers(0, N, count))
+    # tile corners and the ragged edges
+    for m in sorted({0, min(127, M - 1), min(128, M - 1), M - 1, max(0, M - 33)}):
+        for n in sorted({0, min(255, N - 1), min(256, N - 1), N - 1, max(0, N - 129)}):
+            ms.append(m)
+            ns.append(n)
+    return np.array(ms, dtype=np.int64), np.array(ns, dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", ["i4i4_8192", "w4a8_4096", "w4a8_ragged_4000x12288x5120"])
+def test_full_size_workload_sampled(orc, name):
+    variant, M, N, K, a, b = si.workload_operands(name)
+    ms, ns = sample_indices(M, N, 4000, seed=len(name))
+    if variant == "i4i4":
+        C, ap, bp = run_i4i4(a, b, orc)
+        want = orc.i4i4_entries(ap, bp, K, ms, ns)
+    else:
+        C, bp = run_w4a8(a, b, orc)
+        want = orc.w4a8_entries(a, bp, K, ms, ns)
+    assert np.array_equal(C[ms, ns].astype(np.int64), want)
+    # every element was written (the fill pattern is outside the reachable range)
+    assert not np.any(C == 0x5A5A5A5A)
+    # property at any size: |C| within the no-overflow bound
+    bound = K * (64 if variant == "i4i4" else 1024)
+    assert int(np.abs(C.astype(np.int64)).max()) <= bound
+
+
+# ---------------------------------------------------------------- determinism, edges, watchdog
+
+def test_split_path_is_deterministic(orc):
+    variant, M, N, K, a, b = si.workload_operands("w4a8_decode_16x28672x8192")
+    bp = gpu_pack(b)
+    at = dev(a)
+    outs = []
+    for _ in range(3):
+        C = torch.empty((M, N), dtype=torch.int32, device="cuda")
+        pig.w4a8_gemm(at, bp, C, M, N, K)
+        outs.append(C.cpu().numpy())
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def test_empty_and_zero_k():
+    C = torch.full((4, 4), 7, dtype=torch.int32, device="cuda")
+    pig.i4i4_gemm(None, None, C, 0, 4, 64)
+    pig.w4a8_gemm(None, None, C, 4, 0, 64)
+    torch.cuda.synchronize()
+    assert bool((C == 7).all())
+    pig.i4i4_gemm(None, None, C, 4, 4, 0)
+    torch.cuda.synchronize()
+    assert bool((C == 0).all())
+
+
+def test_misaligned_device_pointers_are_rejected():
+    a = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    C = torch.zeros(64, dtype=torch.int32, device="cuda")
+    with pytest.raises(pig.IgemmError) as e:
+        pig.i4i4_gemm(a.data_ptr() + 1, a.data_ptr(), C, 4, 4, 64)
+    assert e.value.code == pig.IGEMM_MISALIGNED
+
+
+def test_watchdog_times_out_without_fault(orc):
+    assert pig.igemm_last_status() == 0
+    pig.igemm_watchdog_selftest(2000)  # 2 ms
+    assert pig.igemm_last_status() == pig.IGEMM_DEVICE_TIMEOUT
+    assert pig.igemm_last_status() == 0  # cleared
+    # the context is still usable
+    a = si.int4_values(9, (64, 128))
+    b = si.int4_values(10, (64, 128))
+    C, ap, bp = run_i4i4(a, b, orc)
+    assert np.array_equal(C, orc.i4i4_gemm(ap, bp, 128))
