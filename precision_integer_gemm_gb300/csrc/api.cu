@@ -64,43 +64,47 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled()
     return fn;
 }
 
-int make_map_u8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t row_bytes, uint32_t box_rows,
-                uint32_t box_bytes)
+int make_map(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t rows, uint64_t cols,
+             uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swizzle)
 {
     auto fn = encode_tiled();
     if (!fn) return kCudaError;
-    const cuuint64_t dims[2] = {row_bytes, rows};
-    const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {box_bytes, box_rows};
+    const uint64_t esize = dtype == CU_TENSOR_MAP_DATA_TYPE_INT32 ? 4 : 1;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * esize};
+    const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? kOk : kCudaError;
 }
 
-Launch plan_launch(int p_tiles, int q_tiles, int kb_total, int64_t c_bytes, int64_t operand_bytes)
+Plan plan_units(int tiles, int kb_total, int64_t c_bytes, int64_t operand_bytes)
 {
     const int sms = sm_count();
-    const int64_t tiles = int64_t(p_tiles) * q_tiles;
-    int best = 1;
-    double best_eff = 0.0;
     const bool may_split = tiles < sms || c_bytes * 4 <= operand_bytes;
-    const int max_split = may_split ? (kb_total / 2 > 1 ? kb_total / 2 : 1) : 1;
-    for (int s = 1; s <= 16 && s <= max_split; ++s) {
-        const int64_t ctas = tiles * s;
-        const int64_t waves = (ctas + sms - 1) / sms;
-        const double eff = double(ctas) / double(waves * sms);
-        if (eff > best_eff + 0.03) {  // a split must buy a clear improvement
-            best_eff = eff;
-            best = s;
+    int best = 1;
+    int64_t best_cost = -1;
+    for (int s = 1; s <= 16; ++s) {
+        if (s > 1 && (!may_split || kb_total / s < 2)) break;
+        const int kbps = (kb_total + s - 1) / s;
+        const int splits = (kb_total + kbps - 1) / kbps;  // no empty split
+        const int64_t units = int64_t(tiles) * splits;
+        const int64_t ctas = units < sms ? units : sms;
+        // the busiest CTA runs ceil(units / ctas) units of kbps blocks, plus a
+        // fixed per-unit cost (pipeline fill, epilogue) of about 2 blocks
+        const int64_t cost = ((units + ctas - 1) / ctas) * (kbps + 2);
+        if (best_cost < 0 || cost * 100 < best_cost * 97) {  // a split must buy > 3%
+            best_cost = cost;
+            best = splits;
         }
     }
-    Launch l;
-    l.kb_per_split = (kb_total + best - 1) / best;
-    l.split = (kb_total + l.kb_per_split - 1) / l.kb_per_split;  // no empty split
-    l.grid = dim3(p_tiles, q_tiles, l.split);
-    return l;
+    Plan p;
+    p.kb_per_split = (kb_total + best - 1) / best;
+    p.split = (kb_total + p.kb_per_split - 1) / p.kb_per_split;
+    const int64_t units = int64_t(tiles) * p.split;
+    p.ctas = static_cast<int>(units < sms ? units : sms);
+    return p;
 }
 
 // ---------------------------------------------------------------- pack_int4

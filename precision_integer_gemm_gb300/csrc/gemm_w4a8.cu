@@ -1,25 +1,38 @@
 // W4A8 -> int32: A [M, K] int8 activations, B [N, K/2] packed int4 weights.
-// Swap-AB: P (MMA M side) = the weights B, 128 rows per tile; Q (MMA N side) =
-// QA activation rows, split into high and low code rows (2*QA MMA columns).
-// Skinny activation counts (M <= 32, decode) take QA = 16 with a deeper TMA
-// ring; larger M take QA = 128.
+// Swap-AB: the MMA A side is the weights (128 rows per tile, codes in TMEM);
+// the B side is QA activation rows split into high and low code rows (2*QA
+// MMA columns, shared memory).  Skinny activation counts (M <= 32, decode)
+// take QA = 16 with a deep TMA ring; larger M take QA = 128.
 #include "launch.cuh"
 
 namespace igemm {
 
+using CfgW4A8 = KernelCfg<true, 128, 4, 2, 8>;
+using CfgW4A8Skinny = KernelCfg<true, 16, 12, 4, 2>;
+
+template <class Cfg>
+static int run_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
+{
+    CUtensorMap mapA, mapB, mapC = {};
+    if (make_map(&mapA, CU_TENSOR_MAP_DATA_TYPE_UINT8, Bp, N, K / 2, kPRows, kBK / 2,
+                 CU_TENSOR_MAP_SWIZZLE_64B) != kOk)
+        return kCudaError;
+    if (make_map(&mapB, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, M, K, Cfg::QA, kBK, CU_TENSOR_MAP_SWIZZLE_128B) != kOk)
+        return kCudaError;
+    const bool tma_store = (N % 4) == 0;
+    if (tma_store && make_map(&mapC, CU_TENSOR_MAP_DATA_TYPE_INT32, C, M, N, Cfg::kStageRows, 32,
+                              CU_TENSOR_MAP_SWIZZLE_NONE) != kOk)
+        return kCudaError;
+    const int p_tiles = (N + kPRows - 1) / kPRows;
+    const int q_tiles = (M + Cfg::QA - 1) / Cfg::QA;
+    const int64_t operand_bytes = int64_t(M) * K + int64_t(N) * (K / 2);
+    return launch_gemm<Cfg>(mapA, mapB, mapC, tma_store, C, M, N, K, p_tiles, q_tiles, operand_bytes, stream);
+}
+
 int launch_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
 {
-    CUtensorMap mapP, mapQ;
-    if (make_map_u8(&mapP, Bp, N, K / 2, kPRows, kBK / 2) != kOk) return kCudaError;
-    const int64_t operand_bytes = int64_t(M) * K + int64_t(N) * (K / 2);
-    if (M <= 32) {
-        constexpr int QA = 16;
-        if (make_map_u8(&mapQ, A, M, K, QA, kBK) != kOk) return kCudaError;
-        return launch_gemm<true, QA, 8, 4>(mapP, mapQ, C, M, N, K, N, M, operand_bytes, stream);
-    }
-    constexpr int QA = 128;
-    if (make_map_u8(&mapQ, A, M, K, QA, kBK) != kOk) return kCudaError;
-    return launch_gemm<true, QA, 4, 2>(mapP, mapQ, C, M, N, K, N, M, operand_bytes, stream);
+    if (M <= 32) return run_w4a8<CfgW4A8Skinny>(A, Bp, C, M, N, K, stream);
+    return run_w4a8<CfgW4A8>(A, Bp, C, M, N, K, stream);
 }
 
 }  // namespace igemm

@@ -17,10 +17,10 @@ enum Status : int {
     kDeviceTimeout = 6,
 };
 
-// One 2-D tiled tensor map over a row-major byte matrix [rows, row_bytes],
-// box [box_rows, box_bytes], no swizzle, out-of-bounds elements read as zero.
-int make_map_u8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t row_bytes, uint32_t box_rows,
-                uint32_t box_bytes);
+// 2-D tiled tensor map over a row-major matrix [rows, cols] of `dtype`
+// (UINT8 or INT32), box [box_rows, box_cols]; out-of-bounds reads are zero.
+int make_map(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t rows, uint64_t cols,
+             uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swizzle);
 
 // Device status word of the current device (address of a file-scope
 // __device__ int, fetched once per device).
@@ -28,28 +28,30 @@ int *device_status_word();
 unsigned long long watchdog_limit_ns();
 int sm_count();
 
-struct Launch {
-    dim3 grid;
+struct Plan {
     int split;
     int kb_per_split;
+    int ctas;
 };
 
-// Split-K plan: k blocks are split over grid z when the tile count alone
-// leaves SMs idle (tiles < SMs) or the last wave badly filled, and C is small
-// next to the operands (the split path zeroes C and adds with red.add).
-Launch plan_launch(int p_tiles, int q_tiles, int kb_total, int64_t c_bytes, int64_t operand_bytes);
+// Persistent launch plan: `ctas` CTAs (at most one per SM) walk the work
+// units (tile, k split).  K is split only when C is small next to the
+// operands (the split path zeroes C and reduce-adds partial tiles), choosing
+// the split that minimises the largest number of k blocks any CTA runs.
+Plan plan_units(int tiles, int kb_total, int64_t c_bytes, int64_t operand_bytes);
 
-template <bool kW4A8, int QA, int SP, int SO>
-int launch_gemm(const CUtensorMap &mapP, const CUtensorMap &mapQ, int32_t *C, int M, int N, int K, int p_rows,
-                int q_rows, int64_t operand_bytes, cudaStream_t stream)
+template <class Cfg>
+int launch_gemm(const CUtensorMap &mapA, const CUtensorMap &mapB, const CUtensorMap &mapC, bool tma_store,
+                int32_t *C, int M, int N, int K, int p_tiles, int q_tiles, int64_t operand_bytes,
+                cudaStream_t stream)
 {
-    using L = SmemLayout<kW4A8, QA, SP, SO>;
-    auto kernel = igemm_tc_kernel<kW4A8, QA, SP, SO>;
+    auto kernel = igemm_tc_kernel<Cfg>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return kCudaError;
     static bool attr_set[64] = {};
     if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes) != cudaSuccess)
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) !=
+            cudaSuccess)
             return kCudaError;
         attr_set[dev] = true;
     }
@@ -58,18 +60,20 @@ int launch_gemm(const CUtensorMap &mapP, const CUtensorMap &mapQ, int32_t *C, in
     prm.M = M;
     prm.N = N;
     prm.K = K;
+    prm.p_tiles = p_tiles;
+    prm.q_tiles = q_tiles;
     prm.kb_total = (K + kBK - 1) / kBK;
-    const int p_tiles = (p_rows + kPRows - 1) / kPRows;
-    const int q_tiles = (q_rows + QA - 1) / QA;
-    const Launch plan = plan_launch(p_tiles, q_tiles, prm.kb_total, int64_t(M) * N * 4, operand_bytes);
+    const Plan plan = plan_units(p_tiles * q_tiles, prm.kb_total, int64_t(M) * N * 4, operand_bytes);
     prm.kb_per_split = plan.kb_per_split;
     prm.split = plan.split;
+    prm.num_units = p_tiles * q_tiles * plan.split;
+    prm.tma_store = tma_store ? 1 : 0;
     prm.status = device_status_word();
     prm.limit_ns = watchdog_limit_ns();
     if (!prm.status) return kCudaError;
     if (plan.split > 1 && cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 4, stream) != cudaSuccess)
         return kCudaError;
-    kernel<<<plan.grid, kThreads, L::kBytes, stream>>>(mapP, mapQ, prm);
+    kernel<<<plan.ctas, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mapA, mapB, mapC, prm);
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
 }
 
