@@ -87,7 +87,8 @@ Plan plan_units(int tiles, int kb_total, int64_t c_bytes, int64_t operand_bytes)
     int64_t best_cost = -1;
     for (int s = 1; s <= 16; ++s) {
         if (s > 1 && (!may_split || kb_total / s < 2)) break;
-        const int kbps = (kb_total + s - 1) / s;
+        // splits cover an even number of k blocks (a packed stage holds two)
+        const int kbps = ((kb_total + s - 1) / s + 1) & ~1;
         const int splits = (kb_total + kbps - 1) / kbps;  // no empty split
         const int64_t units = int64_t(tiles) * splits;
         const int64_t ctas = units < sms ? units : sms;
@@ -100,7 +101,7 @@ Plan plan_units(int tiles, int kb_total, int64_t c_bytes, int64_t operand_bytes)
         }
     }
     Plan p;
-    p.kb_per_split = (kb_total + best - 1) / best;
+    p.kb_per_split = best == 1 ? kb_total : (((kb_total + best - 1) / best + 1) & ~1);
     p.split = (kb_total + p.kb_per_split - 1) / p.kb_per_split;
     const int64_t units = int64_t(tiles) * p.split;
     p.ctas = static_cast<int>(units < sms ? units : sms);

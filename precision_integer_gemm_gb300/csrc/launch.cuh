@@ -41,9 +41,9 @@ struct Plan {
 Plan plan_units(int tiles, int kb_total, int64_t c_bytes, int64_t operand_bytes);
 
 template <class Cfg>
-int launch_gemm(const CUtensorMap &mapA, const CUtensorMap &mapB, const CUtensorMap &mapC, bool tma_store,
-                int32_t *C, int M, int N, int K, int p_tiles, int q_tiles, int64_t operand_bytes,
-                cudaStream_t stream)
+int launch_gemm(const CUtensorMap &mapA, const CUtensorMap &mapB, const CUtensorMap &mapC32,
+                const CUtensorMap &mapC31, bool tma_store, int32_t *C, int M, int N, int K, int p_tiles, int q_tiles,
+                int64_t operand_bytes, cudaStream_t stream)
 {
     auto kernel = igemm_tc_kernel<Cfg>;
     int dev = 0;
@@ -73,7 +73,7 @@ int launch_gemm(const CUtensorMap &mapA, const CUtensorMap &mapB, const CUtensor
     if (!prm.status) return kCudaError;
     if (plan.split > 1 && cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 4, stream) != cudaSuccess)
         return kCudaError;
-    kernel<<<plan.ctas, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mapA, mapB, mapC, prm);
+    kernel<<<plan.ctas, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mapA, mapB, mapC32, mapC31, prm);
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
 }
 
