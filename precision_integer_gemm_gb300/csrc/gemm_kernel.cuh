@@ -42,7 +42,7 @@
 //                     -> bulk tensor store (reduce-add for split K) into C
 //   warps 4-7         A unpack, set 0 (packed row -> 32 code words -> tcgen05.st)
 //   warp 8            TMEM allocation + MMA issue (one thread)
-//   warp 9            TMA producer of the packed stages
+//   warp 9            TMA producer of the packed stages (several issuing lanes)
 //   warps 10..10+NB-1 B unpack: packed / int8 stage -> swizzled e4m3 codes
 //   next 4 warps      A unpack, set 1 (when two sets share the k blocks)
 // Every wait is bounded (ptx.cuh wait_bounded).
@@ -93,6 +93,7 @@ struct KernelCfg {
     static constexpr int kACol0 = kAccBufs * kAccCols;  // first column of the A ring
     static_assert(kACol0 + kAStages * kAStageCols <= kTmemCols, "TMEM budget");
     static_assert(kQRows % 16 == 0 && kQRows <= 256, "MMA N");
+    static_assert(QA % 8 == 0, "B unpack maps eight rows to a quarter warp");
     static_assert(kAStages % kASets == 0, "each A set owns every kASets-th ring stage");
     static_assert(!(kW4A8 && kOnesRow), "W4A8 takes its B-side sums from the B unpack");
     static constexpr int kWarpA0 = 4, kWarpMma = 8, kWarpTma = 9, kWarpB0 = 10, kWarpA1 = 10 + NB;
@@ -132,6 +133,9 @@ struct KernelCfg {
     // arrivals on sum_full: every A-unpack warp, and the B-unpack warps when they
     // supply the B-side sums
     static constexpr int kSumArrivals = 4 * kASets + (kOnesRow ? 0 : NB);
+    // producer lanes (each owns the ring slots congruent to its lane)
+    static constexpr int kIssuers = SP % 4 == 0 ? 4 : SP % 3 == 0 ? 3 : SP % 2 == 0 ? 2 : 1;
+    static_assert(SP <= 32, "ring slot masks");
 };
 
 // Index and phase of a ring of n stages.
@@ -276,13 +280,17 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 
     if (warp == Cfg::kWarpTma) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
+        // kIssuers lanes issue the loads, lane l those of the ring slots
+        // l, l + kIssuers, ...: one thread alone completes only about one
+        // stage per microsecond, so several threads keep the copies flowing.
+        if (lane < Cfg::kIssuers) {
             Ring rp;
-            uint32_t issued = 0;
+            uint32_t issued_mask = 0, last_phase = 0;  // per ring slot
             bool ok = true;
             for (int u = blockIdx.x; ok && u < prm.num_units; u += gridDim.x) {
                 const Unit x = unit_of<Cfg>(prm, u);
                 for (int i = 0; i < x.nkb; i += 2, rp.next(SP)) {
+                    if (rp.idx % Cfg::kIssuers != lane) continue;
                     if (!wait_bounded(&empty_p[rp.idx], rp.phase ^ 1u, wd)) {
                         ok = false;
                         break;
@@ -297,12 +305,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     } else {
                         tma_load_2d(pkB + rp.idx * Cfg::kPkB, &mapB, &full_p[rp.idx], kb * (kBK / 2), x.q0);
                     }
-                    ++issued;
+                    issued_mask |= 1u << rp.idx;
+                    last_phase = (last_phase & ~(1u << rp.idx)) | (rp.phase << rp.idx);
                 }
             }
-            // never leave with copies in flight: the last min(SP, issued) stages
-            for (uint32_t j = issued > (uint32_t)SP ? issued - SP : 0; j < issued; ++j)
-                wait_drain(&full_p[j % SP], (j / SP) & 1, prm.limit_ns);
+            // never leave with copies in flight: the last load of each own slot
+#pragma unroll
+            for (int s = 0; s < SP; ++s)
+                if ((issued_mask >> s) & 1u) wait_drain(&full_p[s], (last_phase >> s) & 1u, prm.limit_ns);
         }
     } else if (warp == Cfg::kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
@@ -339,12 +349,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         const int t = threadIdx.x - 32 * Cfg::kWarpB0;  // 0 .. 32*NB-1
         // per-thread shared-memory offsets are the same in every stage.  Item j
         // of k block h: int4 x int4 reads 16-byte chunk 4h + c of packed row r;
-        // W4A8 reads 16-byte chunks 2c, 2c + 1 of int8 row r in box h.
+        // W4A8 reads 16-byte chunks 2c, 2c + 1 of int8 row r in box h.  Eight
+        // consecutive lanes take eight consecutive rows and the same c, so each
+        // quarter warp of a 16-byte access touches eight distinct swizzled
+        // chunks (no bank conflicts); the four c of a row sit 8 lanes apart.
         uint32_t src_off[Cfg::kQIter][2][2], dst_off[Cfg::kQIter][2];
 #pragma unroll
         for (int j = 0; j < Cfg::kQIter; ++j) {
             const int item = t + 32 * NB * j;
-            const int r = item >> 2, c = item & 3;
+            const int r = ((item >> 5) << 3) | (item & 7), c = (item >> 3) & 3;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 if constexpr (Cfg::kW4A8) {
@@ -466,15 +479,17 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             }
             if (!ok) break;
             if constexpr (Cfg::kW4A8) {
-                // activation row sums of this unit: lanes 4r..4r+3 hold the four parts of row r
+                // activation row sums of this unit: lanes l, l + 8, l + 16, l + 24
+                // hold the four parts of one row
                 if (!warp_wait(&sum_empty[rs.idx], rs.phase ^ 1u, wd)) break;
 #pragma unroll
                 for (int j = 0; j < Cfg::kQIter; ++j) {
                     int v = rsum[j];
-                    v += __shfl_xor_sync(0xffffffffu, v, 1);
-                    v += __shfl_xor_sync(0xffffffffu, v, 2);
+                    v += __shfl_xor_sync(0xffffffffu, v, 8);
+                    v += __shfl_xor_sync(0xffffffffu, v, 16);
                     const int item = t + 32 * NB * j;
-                    if ((t & 3) == 0 && item < Cfg::kQItems) sumQ[rs.idx * Cfg::kSumQ + (item >> 2)] = -8 * v;
+                    const int r = ((item >> 5) << 3) | (item & 7);
+                    if (lane < 8 && item < Cfg::kQItems) sumQ[rs.idx * Cfg::kSumQ + r] = -8 * v;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sum_full[rs.idx]);
