@@ -1,17 +1,55 @@
 // int4 x int4 -> int32: A [M, K/2] and B [N, K/2] packed (low nibble = even k).
-// MMA A side = A (127 data rows + the row of ones per tile, codes in TMEM), B
-// side = B (192 rows per tile, codes in shared memory), two accumulators so
-// the epilogue of a tile overlaps the next tile's MMAs.  C leaves through
-// bulk tensor stores (boxes of 32 rows, 31 for the last quadrant of a tile).
+//
+// Two paths.  Shapes with M and N of at least 256 take the prepared-codes path:
+// one pass turns A and B into code rows and row sums (prep.cu), then
+// igemm_ss_kernel runs a TMA -> tcgen05.mma pipeline on 128 x 256 tiles with
+// both operands in shared memory.  Smaller shapes, where that pass would cost
+// more than it saves, take igemm_tc_kernel, which unpacks every tile in the
+// kernel: MMA A side = A (127 data rows + a row of ones per tile, codes in
+// TMEM), B side = B (192 rows per tile, codes in shared memory).
 #include "launch.cuh"
 
 namespace igemm {
 
 //                      W4A8   QA  SP  SO  NB  A stages  A sets  ones row  staging
 using CfgI4I4 = KernelCfg<false, 192, 3, 3, 8, 4, 1, true, 1>;
+//                    W4A8   BN  stages
+using CfgI4I4Ss = SsCfg<false, 256, 4>;
+
+static bool use_codes_i4i4(int M, int N) { return M >= 256 && N >= 256; }
+
+static int run_i4i4_codes(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
+{
+    using Cfg = CfgI4I4Ss;
+    CodesLayout lay;
+    codes_layout(M, N, N, K, &lay);
+    void *ws = nullptr;
+    if (workspace_alloc(&ws, lay.total, stream) != kOk) return kCudaError;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    uint8_t *a_codes = base + lay.p_codes, *b_codes = base + lay.q_codes;
+    int32_t *a_sums = reinterpret_cast<int32_t *>(base + lay.p_sums);
+    int32_t *b_sums = reinterpret_cast<int32_t *>(base + lay.q_sums);
+    int rc = launch_prep(Ap, M, Bp, N, false, K, a_codes, b_codes, a_sums, b_sums, stream);
+    CUtensorMap mapP, mapQ, mapC = {};
+    if (rc == kOk)
+        rc = make_map(&mapP, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, M, K, Cfg::kPRows, Cfg::kBK,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc == kOk)
+        rc = make_map(&mapQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_codes, N, K, Cfg::QA, Cfg::kBK,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    const bool tma_store = (N % 4) == 0;
+    if (rc == kOk && tma_store)
+        rc = make_map(&mapC, CU_TENSOR_MAP_DATA_TYPE_INT32, C, M, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc == kOk)
+        rc = launch_ss<Cfg>(mapP, mapQ, mapC, tma_store, C, M, N, K, a_sums, b_sums, M, N,
+                            (int64_t(M) + N) * K, stream);
+    const int rf = workspace_free(ws, stream);
+    return rc != kOk ? rc : rf;
+}
 
 int launch_i4i4(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
 {
+    if (use_codes_i4i4(M, N)) return run_i4i4_codes(Ap, Bp, C, M, N, K, stream);
     using Cfg = CfgI4I4;
     CUtensorMap mapA, mapB, mapC32 = {}, mapC31 = {};
     // packed stages carry two k blocks: boxes of 128 bytes (256 k) per row

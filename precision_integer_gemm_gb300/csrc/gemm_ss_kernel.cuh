@@ -1,0 +1,393 @@
+// The integer GEMM on prepared operand codes: both MMA operands come from
+// shared memory as e4m3 code bytes that a preparation pass (prep.cu) wrote to
+// global memory once per call, so the main loop is a plain TMA -> tcgen05.mma
+// pipeline with no per-tile unpacking.
+//
+// What is computed is the same exact C[M,N] = A[M,K] . B[N,K]^T of
+// "[CUDA] Support int4 T.gemm" (tilelang PR #2063, matmul_nt_int4) and of the
+// W4A8 kernel of "[Example] add w4a8 gemm kernel" (tilelang PR #815); the code
+// arithmetic is the one of gemm_kernel.cuh:
+//   int4 value v -> code u = v + 8;  int8 value a -> a + 128 = 16 h + l.
+//   int4 x int4:  C = S - 8 sum uA - 8 sum uB + 64 K
+//   W4A8:         C = 16 S_h + S_l - 8 sum a - 128 sum ub
+// with S the MMA's sum of code products and the row sums written by the
+// preparation pass.  Codes past K are zero (TMA fill): they add nothing to S,
+// and the row sums and the K term count the real k only.
+//
+// Tiles: the MMA M side ("P") is 128 code rows of the int4 operand (A for
+// int4 x int4; the weights for W4A8, swap-AB); the N side ("Q") is BN code
+// rows: BN rows of B (int4 x int4), or QA = BN/2 activation rows as a block of
+// QA high-part rows followed by QA low-part rows (W4A8).  One pipeline stage
+// is one 128-k block of both, 128-byte swizzled K-major.
+//
+// Warp roles (persistent CTAs, one per SM, work units = (tile, k split)):
+//   warps 0-3   epilogue: TMEM -> registers -> int32 -> shared staging ->
+//               bulk tensor store (reduce-add for split K) into C
+//   warp 4      TMEM allocation + MMA issue (one thread)
+//   warp 5      TMA producer (several lanes, each owning every kIssuers-th
+//               stage: one thread completes only about one stage per
+//               microsecond)
+// Every wait is bounded (ptx.cuh wait_bounded).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include "ptx.cuh"
+
+namespace igemm {
+
+template <bool W4A8, int BN_, int ST_>
+struct SsCfg {
+    static constexpr bool kW4A8 = W4A8;
+    static constexpr int kQRows = BN_;                 // MMA N
+    static constexpr int QA = W4A8 ? BN_ / 2 : BN_;    // Q source rows per tile
+    static constexpr int ST = ST_;                     // pipeline stages
+    static constexpr int kBK = 128;                    // k per stage
+    static constexpr int kPRows = 128;                 // MMA M
+    static constexpr int kIssuers = ST % 4 == 0 ? 4 : ST % 3 == 0 ? 3 : ST % 2 == 0 ? 2 : 1;
+    static constexpr int kAccCols = kQRows;
+    static constexpr int kAccBufs = 2 * kAccCols <= 512 ? 2 : 1;
+    static constexpr int kTmemCols = kAccBufs * kAccCols <= 128 ? 128 : kAccBufs * kAccCols <= 256 ? 256 : 512;
+    static constexpr int kStageA = kPRows * kBK;
+    static constexpr int kStageB = kQRows * kBK;
+    static constexpr int kStage = kStageA + kStageB;
+    static constexpr int kStageRows = W4A8 ? (QA < 32 ? QA : 32) : 32;  // C staging box rows
+    static constexpr int kCStage = 32 * 32 * 4;
+    static constexpr int kOffStages = 0;
+    static constexpr int kOffCStage = kOffStages + ST * kStage;
+    static constexpr int kOffBars = kOffCStage + 4 * kCStage;
+    static constexpr int kNumBars = 2 * ST + 4 + 1;
+    static constexpr int kOffMisc = ((kOffBars + 8 * kNumBars + 127) / 128) * 128;
+    static constexpr int kSmemBytes = kOffMisc + 128 + 1024;  // + alignment slack
+    static constexpr int kThreads = 6 * 32;
+    static_assert(kQRows % 16 == 0 && kQRows <= 256, "MMA N");
+    static_assert(!W4A8 || QA % 8 == 0, "high and low blocks start on 1024-byte boundaries");
+    static_assert(kStageB % 1024 == 0 && kStage % 1024 == 0, "1024-byte aligned stages");
+    static_assert(kAccBufs * kAccCols <= 512, "TMEM budget");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(ST <= 32, "stage masks");
+};
+
+struct SsParams {
+    int32_t *C;           // [M, N] row-major
+    int M, N, K;
+    const int32_t *sumP;  // per P row: sum of its codes (int4 x int4: uA; W4A8: ub)
+    const int32_t *sumQ;  // per Q row: int4 x int4: sum uB; W4A8: sum a (signed)
+    int p_rows, q_rows;   // rows of the P and Q operands
+    int p_tiles, q_tiles;
+    int kb_total, kb_per_split, split, num_units;
+    int tma_store;
+    int *status;
+    unsigned long long limit_ns;
+};
+
+struct SsUnit {
+    int p0, q0, kb0, nkb;
+};
+
+template <class Cfg>
+__device__ __forceinline__ SsUnit ss_unit(const SsParams &prm, int u)
+{
+    const int tile = u / prm.split;
+    const int s = u - tile * prm.split;
+    const int pt = tile % prm.p_tiles;
+    const int qt = tile / prm.p_tiles;
+    SsUnit x;
+    x.p0 = pt * Cfg::kPRows;
+    x.q0 = qt * Cfg::QA;
+    x.kb0 = s * prm.kb_per_split;
+    x.nkb = min(prm.kb_total - x.kb0, prm.kb_per_split);
+    return x;
+}
+
+__device__ __forceinline__ void ss_wait_drain(uint64_t *bar, uint32_t parity, unsigned long long limit_ns)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < limit_ns) {
+    }
+}
+
+__device__ __forceinline__ bool ss_warp_wait(uint64_t *bar, uint32_t parity, const Watchdog &wd)
+{
+    const bool ok = wait_bounded(bar, parity, wd);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Integer S from an accumulator word holding S * 2^-18 exactly; the magic form
+// (S < 2^22) leaves 0x4B400000 + S in the bits.
+__device__ __forceinline__ uint32_t ss_magic(uint32_t bits)
+{
+    return __float_as_uint(fmaf(__uint_as_float(bits), 262144.0f, 12582912.0f));
+}
+constexpr uint32_t kSsMagic = 0x4B400000u;
+__device__ __forceinline__ int ss_exact(uint32_t bits) { return __float2int_rn(__uint_as_float(bits) * 262144.0f); }
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
+    igemm_ss_kernel(const __grid_constant__ CUtensorMap mapP, const __grid_constant__ CUtensorMap mapQ,
+                    const __grid_constant__ CUtensorMap mapC, const SsParams prm)
+{
+    constexpr int ST = Cfg::ST, QA = Cfg::QA;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint8_t *stages = smem + Cfg::kOffStages;
+    uint8_t *cstage = smem + Cfg::kOffCStage;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBars);
+    uint64_t *full = bars;              // [ST] stage landed (1 arrival + tx)
+    uint64_t *empty = full + ST;        // [ST] stage consumed (MMA commit)
+    uint64_t *acc_full = empty + ST;    // [2] accumulator complete (commit)
+    uint64_t *acc_empty = acc_full + 2; // [2] accumulator drained (4 epilogue warps)
+    uint64_t *mma_drain = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);
+        }
+        mbar_init(mma_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_map(&mapP);
+        tma_prefetch_map(&mapQ);
+        if (prm.tma_store) tma_prefetch_map(&mapC);
+    }
+    if (warp == 4) {
+        tmem_alloc(tmem_slot, Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Watchdog wd{abort_flag, prm.status, prm.limit_ns};
+
+    if (warp == 5) {
+        // ------------------------------------------------------------ producer
+        if (lane < Cfg::kIssuers) {
+            uint32_t g = 0;  // stages (k blocks) over all units of this CTA
+            uint32_t issued_mask = 0, last_phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < prm.num_units; u += gridDim.x) {
+                const SsUnit x = ss_unit<Cfg>(prm, u);
+                for (int i = 0; i < x.nkb; ++i, ++g) {
+                    const int s = static_cast<int>(g % ST);
+                    if (s % Cfg::kIssuers != lane) continue;
+                    const uint32_t ph = (g / ST) & 1u;
+                    if (!wait_bounded(&empty[s], ph ^ 1u, wd)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *st = stages + s * Cfg::kStage;
+                    const int kx = (x.kb0 + i) * Cfg::kBK;
+                    mbar_arrive_expect_tx(&full[s], Cfg::kStage);
+                    tma_load_2d(st, &mapP, &full[s], kx, x.p0);
+                    if constexpr (Cfg::kW4A8) {
+                        // high-part rows q0.., low-part rows M + q0.. (the code planes are stacked)
+                        tma_load_2d(st + Cfg::kStageA, &mapQ, &full[s], kx, x.q0);
+                        tma_load_2d(st + Cfg::kStageA + QA * Cfg::kBK, &mapQ, &full[s], kx, prm.q_rows + x.q0);
+                    } else {
+                        tma_load_2d(st + Cfg::kStageA, &mapQ, &full[s], kx, x.q0);
+                    }
+                    issued_mask |= 1u << s;
+                    last_phase = (last_phase & ~(1u << s)) | (ph << s);
+                }
+            }
+            // never leave with copies in flight: the last load of each own stage
+#pragma unroll 1
+            for (int s = 0; s < ST; ++s)
+                if ((issued_mask >> s) & 1u) ss_wait_drain(&full[s], (last_phase >> s) & 1u, prm.limit_ns);
+        }
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_e4m3_f32(Cfg::kPRows, Cfg::kQRows);
+            uint32_t g = 0, nacc = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < prm.num_units; u += gridDim.x, ++nacc) {
+                const SsUnit x = ss_unit<Cfg>(prm, u);
+                const uint32_t ab = nacc % Cfg::kAccBufs;
+                const uint32_t aph = (nacc / Cfg::kAccBufs) & 1u;
+                const uint32_t d_tmem = tmem + ab * Cfg::kAccCols;
+                if (!wait_bounded(&acc_empty[ab], aph ^ 1u, wd)) break;
+                tc_fence_after();
+                for (int i = 0; i < x.nkb; ++i, ++g) {
+                    const int s = static_cast<int>(g % ST);
+                    if (!wait_bounded(&full[s], (g / ST) & 1u, wd)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(stages + s * Cfg::kStage);
+                    const uint32_t b_base = a_base + Cfg::kStageA;
+#pragma unroll
+                    for (int kk = 0; kk < Cfg::kBK / 32; ++kk)
+                        mma_f8f6f4(d_tmem, sdesc_kmajor_sw128(a_base + 32 * kk), sdesc_kmajor_sw128(b_base + 32 * kk),
+                                   idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&empty[s]);
+                }
+                if (ok) mma_commit(&acc_full[ab]);
+            }
+            mma_commit(mma_drain);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 0-3)
+        const int quad = warp;
+        const int p = quad * 32 + lane;
+        const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        uint8_t *stg = cstage + quad * Cfg::kCStage;
+        const bool reduce = prm.split > 1;
+        uint32_t nacc = 0;
+        for (int u = blockIdx.x; u < prm.num_units; u += gridDim.x, ++nacc) {
+            const SsUnit x = ss_unit<Cfg>(prm, u);
+            const uint32_t ab = nacc % Cfg::kAccBufs;
+            if (!ss_warp_wait(&acc_full[ab], (nacc / Cfg::kAccBufs) & 1u, wd)) break;
+            tc_fence_after();
+            const uint32_t tacc = trow + ab * Cfg::kAccCols;
+            const bool magic = x.nkb * Cfg::kBK <= 16384;  // every code sum below 2^22
+            const bool first = x.kb0 == 0;                  // the split that adds the row-sum terms
+            const int prow = min(x.p0 + p, prm.p_rows - 1);
+            const int sp = first ? __ldg(prm.sumP + prow) : 0;
+            if constexpr (!Cfg::kW4A8) {
+                // C[m, n] = S - 8 sum uA[m] - 8 sum uB[n] + 64 K   (first split adds the terms)
+                const int m = x.p0 + p;
+                const uint32_t rowterm = static_cast<uint32_t>(first ? 64 * prm.K - 8 * sp : 0) -
+                                         (magic ? kSsMagic : 0u);
+#pragma unroll 1
+                for (int c0 = 0; c0 < Cfg::kQRows; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tacc + c0, v);
+                    tmem_ld_wait();
+                    const int n0 = x.q0 + c0;
+                    // -8 sum uB of the chunk's 32 columns (the sums array is padded
+                    // past the last row, so whole chunks are readable)
+                    const int4 *sq = reinterpret_cast<const int4 *>(prm.sumQ + n0);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int4 q = first ? __ldg(sq + j) : make_int4(0, 0, 0, 0);
+                        const int qq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = 4 * j + e;
+                            v[i] = (magic ? ss_magic(v[i]) : static_cast<uint32_t>(ss_exact(v[i]))) + rowterm +
+                                   static_cast<uint32_t>(-8 * qq[e]);
+                        }
+                    }
+                    if (prm.tma_store) {
+                        if (lane == 0) bulk_wait_group_read<0>();
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<uint4 *>(stg + ((lane * 128) + ((((j ^ lane) & 7)) << 4))) =
+                                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        const int y = x.p0 + quad * 32;
+                        if (lane == 0 && y < prm.M && n0 < prm.N) {
+                            if (reduce)
+                                tma_reduce_add_2d(&mapC, stg, n0, y);
+                            else
+                                tma_store_2d(&mapC, stg, n0, y);
+                            bulk_commit_group();
+                        }
+                    } else if (m < prm.M) {
+                        int32_t *crow = prm.C + static_cast<int64_t>(m) * prm.N;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            if (n0 + i < prm.N) {
+                                if (reduce)
+                                    atomicAdd(crow + n0 + i, static_cast<int>(v[i]));
+                                else
+                                    crow[n0 + i] = static_cast<int>(v[i]);
+                            }
+                        }
+                    }
+                }
+            } else {
+                // C[m, n] for n = this thread's weight row, m = q0 + j, staged as [m][n] boxes:
+                // C = 16 S_h + S_l - 8 sum a[m] - 128 sum ub[n]
+                const int n = x.p0 + p;
+                const uint32_t colterm = static_cast<uint32_t>(-128 * sp) - (magic ? 17u * kSsMagic : 0u);
+                constexpr int kChunk = Cfg::kStageRows;
+                int *sbi = reinterpret_cast<int *>(stg);
+#pragma unroll 1
+                for (int j0 = 0; j0 < QA; j0 += kChunk) {
+                    if (prm.tma_store) {
+                        if (lane == 0) bulk_wait_group_read<0>();
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int h = 0; h < kChunk; h += 16) {
+                        uint32_t vh[16], vl[16];
+                        tmem_ld_32x32b_x16(tacc + j0 + h, vh);
+                        tmem_ld_32x32b_x16(tacc + QA + j0 + h, vl);
+                        tmem_ld_wait();
+                        const int4 *sq = reinterpret_cast<const int4 *>(prm.sumQ + x.q0 + j0 + h);
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int4 q = first ? __ldg(sq + jj) : make_int4(0, 0, 0, 0);
+                            const int qq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int i = 4 * jj + e;
+                                uint32_t val;
+                                if (magic)
+                                    val = 16u * ss_magic(vh[i]) + ss_magic(vl[i]);
+                                else
+                                    val = static_cast<uint32_t>(16 * ss_exact(vh[i]) + ss_exact(vl[i]));
+                                val += colterm + static_cast<uint32_t>(-8 * qq[e]);
+                                if (prm.tma_store) {
+                                    sbi[(h + i) * 32 + lane] = static_cast<int>(val);
+                                } else {
+                                    const int m = x.q0 + j0 + h + i;
+                                    if (n < prm.N && m < prm.M) {
+                                        int32_t *cp = prm.C + static_cast<int64_t>(m) * prm.N + n;
+                                        if (reduce)
+                                            atomicAdd(cp, static_cast<int>(val));
+                                        else
+                                            *cp = static_cast<int>(val);
+                                    }
+                                }
+                            }
+                        }
+                    }
+                    if (prm.tma_store) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        const int m0 = x.q0 + j0, nx = x.p0 + quad * 32;
+                        if (lane == 0 && m0 < prm.M && nx < prm.N) {
+                            if (reduce)
+                                tma_reduce_add_2d(&mapC, stg, nx, m0);
+                            else
+                                tma_store_2d(&mapC, stg, nx, m0);
+                            bulk_commit_group();
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[ab]);
+        }
+        if (lane == 0) bulk_wait_group_all();
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        if (lane == 0) ss_wait_drain(mma_drain, 0, prm.limit_ns);  // every MMA of this CTA is done
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, Cfg::kTmemCols);
+    }
+}
+
+}  // namespace igemm

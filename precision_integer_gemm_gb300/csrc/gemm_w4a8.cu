@@ -1,4 +1,9 @@
 // W4A8 -> int32: A [M, K] int8 activations, B [N, K/2] packed int4 weights.
+//
+// M > 32 and N >= 256 take the prepared-codes path: one pass writes weight
+// code rows, activation high/low code planes and the row sums (prep.cu), then
+// igemm_ss_kernel multiplies 128 weight rows by 128 activation rows (256 code
+// rows) per tile from shared memory.  The rest takes igemm_tc_kernel below.
 // Swap-AB: the MMA A side is the weights (128 rows per tile, codes in TMEM);
 // the B side is QA activation rows split into high and low code rows (2*QA
 // MMA columns, shared memory).  Larger M take QA = 96 (N = 192, two
@@ -12,6 +17,39 @@ namespace igemm {
 //                         W4A8  QA  SP  SO  NB  A stages  A sets  ones row  staging
 using CfgW4A8 = KernelCfg<true, 96, 3, 3, 8, 4, 1, false, 1>;
 using CfgW4A8Skinny = KernelCfg<true, 16, 8, 4, 2, 8, 2, false, 1>;
+//                    W4A8  BN  stages
+using CfgW4A8Ss = SsCfg<true, 256, 4>;
+
+static int run_w4a8_codes(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
+{
+    using Cfg = CfgW4A8Ss;
+    CodesLayout lay;
+    codes_layout(N, 2 * M, M, K, &lay);
+    void *ws = nullptr;
+    if (workspace_alloc(&ws, lay.total, stream) != kOk) return kCudaError;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    uint8_t *w_codes = base + lay.p_codes, *a_codes = base + lay.q_codes;
+    int32_t *w_sums = reinterpret_cast<int32_t *>(base + lay.p_sums);
+    int32_t *a_sums = reinterpret_cast<int32_t *>(base + lay.q_sums);
+    int rc = launch_prep(Bp, N, reinterpret_cast<const uint8_t *>(A), M, true, K, w_codes, a_codes, w_sums, a_sums,
+                         stream);
+    CUtensorMap mapP, mapQ, mapC = {};
+    if (rc == kOk)
+        rc = make_map(&mapP, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_codes, N, K, Cfg::kPRows, Cfg::kBK,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    // the high-code plane (rows 0..M-1) and the low-code plane (rows M..2M-1)
+    if (rc == kOk)
+        rc = make_map(&mapQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, 2 * uint64_t(M), K, Cfg::QA, Cfg::kBK,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    const bool tma_store = (N % 4) == 0;
+    if (rc == kOk && tma_store)
+        rc = make_map(&mapC, CU_TENSOR_MAP_DATA_TYPE_INT32, C, M, N, Cfg::kStageRows, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc == kOk)
+        rc = launch_ss<Cfg>(mapP, mapQ, mapC, tma_store, C, M, N, K, w_sums, a_sums, N, M,
+                            int64_t(N) * K + 2 * int64_t(M) * K, stream);
+    const int rf = workspace_free(ws, stream);
+    return rc != kOk ? rc : rf;
+}
 
 template <class Cfg>
 static int run_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
@@ -37,6 +75,7 @@ static int run_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N
 int launch_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
 {
     if (M <= 32) return run_w4a8<CfgW4A8Skinny>(A, Bp, C, M, N, K, stream);
+    if (N >= 256) return run_w4a8_codes(A, Bp, C, M, N, K, stream);
     return run_w4a8<CfgW4A8>(A, Bp, C, M, N, K, stream);
 }
 

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include "gemm_kernel.cuh"
+#include "gemm_ss_kernel.cuh"
 
 namespace igemm {
 
@@ -74,6 +75,65 @@ int launch_gemm(const CUtensorMap &mapA, const CUtensorMap &mapB, const CUtensor
     if (plan.split > 1 && cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 4, stream) != cudaSuccess)
         return kCudaError;
     kernel<<<plan.ctas, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mapA, mapB, mapC32, mapC31, prm);
+    return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
+}
+
+// ---------------------------------------------------------------- prepared-codes path
+// Byte offsets of the parts of a prepared-codes workspace (all 256-aligned).
+struct CodesLayout {
+    size_t p_codes, q_codes, p_sums, q_sums, total;
+};
+// p_rows code rows of P, q_code_rows code rows of Q (2 * q_rows for int8 Q),
+// q_rows sums of Q; returns the total size.
+size_t codes_layout(int p_rows, int q_code_rows, int q_rows, int K, CodesLayout *lay);
+
+// Codes and row sums of P (packed int4) and Q (packed int4, or int8 when
+// q_int8: high-code plane then low-code plane).
+int launch_prep(const uint8_t *P, int p_rows, const uint8_t *Q, int q_rows, bool q_int8, int K, uint8_t *p_codes,
+                uint8_t *q_codes, int32_t *p_sums, int32_t *q_sums, cudaStream_t stream);
+
+// Stream-ordered workspace from the library's own per-device pool.
+int workspace_alloc(void **p, size_t bytes, cudaStream_t stream);
+int workspace_free(void *p, cudaStream_t stream);
+
+template <class Cfg>
+int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMap &mapC, bool tma_store, int32_t *C,
+              int M, int N, int K, const int32_t *sumP, const int32_t *sumQ, int p_rows, int q_rows,
+              int64_t operand_bytes, cudaStream_t stream)
+{
+    auto kernel = igemm_ss_kernel<Cfg>;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return kCudaError;
+    static bool attr_set[64] = {};
+    if (dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) !=
+            cudaSuccess)
+            return kCudaError;
+        attr_set[dev] = true;
+    }
+    SsParams prm{};
+    prm.C = C;
+    prm.M = M;
+    prm.N = N;
+    prm.K = K;
+    prm.sumP = sumP;
+    prm.sumQ = sumQ;
+    prm.p_rows = p_rows;
+    prm.q_rows = q_rows;
+    prm.p_tiles = (p_rows + Cfg::kPRows - 1) / Cfg::kPRows;
+    prm.q_tiles = (q_rows + Cfg::QA - 1) / Cfg::QA;
+    prm.kb_total = (K + Cfg::kBK - 1) / Cfg::kBK;
+    const Plan plan = plan_units(prm.p_tiles * prm.q_tiles, prm.kb_total, int64_t(M) * N * 4, operand_bytes);
+    prm.kb_per_split = plan.kb_per_split;
+    prm.split = plan.split;
+    prm.num_units = prm.p_tiles * prm.q_tiles * plan.split;
+    prm.tma_store = tma_store ? 1 : 0;
+    prm.status = device_status_word();
+    prm.limit_ns = watchdog_limit_ns();
+    if (!prm.status) return kCudaError;
+    if (plan.split > 1 && cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 4, stream) != cudaSuccess)
+        return kCudaError;
+    kernel<<<plan.ctas, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mapP, mapQ, mapC, prm);
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
 }
 

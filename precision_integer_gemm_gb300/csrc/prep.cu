@@ -1,0 +1,156 @@
+// Operand preparation for the prepared-codes GEMM path (gemm_ss_kernel.cuh):
+// each operand row becomes a row of e4m3 code bytes in natural k order plus
+// the row's code sum, once per call, and a stream-ordered workspace holds
+// them.
+//
+//   packed int4 row [K/2] (low nibble = even k, the packing of the TileLang
+//   tutorial's pack_int4)  ->  codes u = v + 8 in [0, 15], sum of u
+//   int8 row [K] (W4A8 activations, "[Example] add w4a8 gemm kernel")
+//       ->  high codes h = (a + 128) >> 4 and low codes l = a & 15 (two planes),
+//           and the signed sum of a
+#include <cstdint>
+#include <mutex>
+#include "launch.cuh"
+
+namespace igemm {
+
+// Two 16-byte outputs (32 codes in k order) from 16 packed bytes (32 nibbles).
+__device__ __forceinline__ void int4_codes(uint4 w, uint4 &o0, uint4 &o1, int &sum)
+{
+    const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = (x[i] & 0x0F0F0F0Fu) ^ 0x08080808u;         // k = 8i + 0, 2, 4, 6
+        const uint32_t hi = ((x[i] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;  // k = 8i + 1, 3, 5, 7
+        o[2 * i] = __byte_perm(lo, hi, 0x5140);
+        o[2 * i + 1] = __byte_perm(lo, hi, 0x7362);
+        sum = __dp4a(static_cast<int>(lo), 0x01010101, sum);
+        sum = __dp4a(static_cast<int>(hi), 0x01010101, sum);
+    }
+    o0 = make_uint4(o[0], o[1], o[2], o[3]);
+    o1 = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+__device__ __forceinline__ int block_sum(int v, int *red)
+{
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    int t = 0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += red[w];
+    return t;
+}
+
+// One CTA per row: rows [0, p_rows) of the packed int4 operand P, then rows
+// [p_rows, p_rows + q_rows) of Q (packed int4, or int8 when kQInt8).
+template <bool kQInt8>
+__global__ void __launch_bounds__(256) prep_codes_kernel(const uint8_t *__restrict__ P, int p_rows,
+                                                         const uint8_t *__restrict__ Q, int q_rows, int K,
+                                                         uint8_t *__restrict__ p_codes, uint8_t *__restrict__ q_codes,
+                                                         int32_t *__restrict__ p_sums, int32_t *__restrict__ q_sums)
+{
+    __shared__ int red[8];
+    const int row = blockIdx.x;
+    int sum = 0;
+    const bool is_p = row < p_rows;
+    const int r = is_p ? row : row - p_rows;
+    if (is_p || !kQInt8) {
+        const uint4 *src = reinterpret_cast<const uint4 *>((is_p ? P : Q) + static_cast<size_t>(r) * (K / 2));
+        uint4 *dst = reinterpret_cast<uint4 *>((is_p ? p_codes : q_codes) + static_cast<size_t>(r) * K);
+        for (int c = threadIdx.x; c < K / 32; c += blockDim.x) {
+            uint4 o0, o1;
+            int4_codes(src[c], o0, o1, sum);
+            dst[2 * c] = o0;
+            dst[2 * c + 1] = o1;
+        }
+    } else {
+        const uint4 *src = reinterpret_cast<const uint4 *>(Q + static_cast<size_t>(r) * K);
+        uint4 *dh = reinterpret_cast<uint4 *>(q_codes + static_cast<size_t>(r) * K);
+        uint4 *dl = reinterpret_cast<uint4 *>(q_codes + (static_cast<size_t>(q_rows) + r) * K);
+        for (int c = threadIdx.x; c < K / 16; c += blockDim.x) {
+            const uint4 w = src[c];
+            const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+            uint32_t h[4], l[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                // (a + 128) >> 4 = ((a >> 4) & 15) ^ 8 ;  (a + 128) & 15 = a & 15
+                h[i] = ((x[i] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+                l[i] = x[i] & 0x0F0F0F0Fu;
+                sum = __dp4a(static_cast<int>(x[i]), 0x01010101, sum);
+            }
+            dh[c] = make_uint4(h[0], h[1], h[2], h[3]);
+            dl[c] = make_uint4(l[0], l[1], l[2], l[3]);
+        }
+    }
+    const int t = block_sum(sum, red);
+    if (threadIdx.x == 0) (is_p ? p_sums : q_sums)[r] = t;
+}
+
+int launch_prep(const uint8_t *P, int p_rows, const uint8_t *Q, int q_rows, bool q_int8, int K, uint8_t *p_codes,
+                uint8_t *q_codes, int32_t *p_sums, int32_t *q_sums, cudaStream_t stream)
+{
+    const unsigned grid = static_cast<unsigned>(p_rows) + static_cast<unsigned>(q_rows);
+    if (q_int8)
+        prep_codes_kernel<true><<<grid, 256, 0, stream>>>(P, p_rows, Q, q_rows, K, p_codes, q_codes, p_sums, q_sums);
+    else
+        prep_codes_kernel<false><<<grid, 256, 0, stream>>>(P, p_rows, Q, q_rows, K, p_codes, q_codes, p_sums, q_sums);
+    return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
+}
+
+// ---------------------------------------------------------------- workspace
+// A memory pool per device that keeps what it has reserved (release threshold
+// = all), so that after the first call of a given size the stream-ordered
+// allocation costs no driver round trip.
+static cudaMemPool_t workspace_pool(int dev)
+{
+    static std::mutex mu;
+    static cudaMemPool_t pools[64] = {};
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!pools[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+        uint64_t keep = ~uint64_t(0);
+        if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return nullptr;
+        }
+        pools[dev] = pool;
+    }
+    return pools[dev];
+}
+
+int workspace_alloc(void **p, size_t bytes, cudaStream_t stream)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return kCudaError;
+    cudaMemPool_t pool = workspace_pool(dev);
+    if (!pool) return kCudaError;
+    return cudaMallocFromPoolAsync(p, bytes, pool, stream) == cudaSuccess ? kOk : kCudaError;
+}
+
+int workspace_free(void *p, cudaStream_t stream)
+{
+    return cudaFreeAsync(p, stream) == cudaSuccess ? kOk : kCudaError;
+}
+
+size_t codes_layout(int p_rows, int q_code_rows, int q_rows, int K, CodesLayout *lay)
+{
+    auto up = [](size_t v) { return (v + 255) & ~size_t(255); };
+    lay->p_codes = 0;
+    lay->q_codes = up(static_cast<size_t>(p_rows) * K);
+    lay->p_sums = lay->q_codes + up(static_cast<size_t>(q_code_rows) * K);
+    // sums are padded by a tile and a chunk: the epilogue reads whole 32-entry chunks
+    lay->q_sums = lay->p_sums + up(4 * (static_cast<size_t>(p_rows) + 512));
+    lay->total = lay->q_sums + up(4 * (static_cast<size_t>(q_rows) + 512));
+    return lay->total;
+}
+
+}  // namespace igemm

@@ -117,6 +117,32 @@ def test_w4a8_matches_oracle(orc, M, N, K):
     assert np.array_equal(C, orc.w4a8_gemm(a, bp, K))
 
 
+# Shapes of the prepared-codes path (int4 x int4: M, N >= 256; W4A8: M > 32,
+# N >= 256): K below one 128-k block, K tails, ragged M and N, N % 4 != 0
+# (direct stores instead of bulk tensor stores) and a split K.
+CODES_I4I4 = [(256, 256, 32), (300, 520, 96), (257, 300, 8224), (1000, 777, 2080), (256, 258, 128),
+              (256, 256, 65536)]
+
+
+@pytest.mark.parametrize("M,N,K", CODES_I4I4)
+def test_i4i4_prepared_codes_path(orc, M, N, K):
+    a = si.int4_values(5000 + M + K, (M, K))
+    b = si.int4_values(6000 + N + K, (N, K))
+    C, ap, bp = run_i4i4(a, b, orc)
+    assert np.array_equal(C, orc.i4i4_gemm(ap, bp, K))
+
+
+CODES_W4A8 = [(33, 256, 32), (130, 300, 4160), (1000, 258, 1056), (64, 512, 65536), (129, 1024, 384)]
+
+
+@pytest.mark.parametrize("M,N,K", CODES_W4A8)
+def test_w4a8_prepared_codes_path(orc, M, N, K):
+    a = si.int8_values(7000 + M + K, (M, K))
+    b = si.int4_values(8000 + N + K, (N, K))
+    C, bp = run_w4a8(a, b, orc)
+    assert np.array_equal(C, orc.w4a8_gemm(a, bp, K))
+
+
 def test_configured_small_workloads(orc):
     for name in ("i4i4_256", "i4i4_1024"):
         variant, M, N, K, a, b = si.workload_operands(name)
