@@ -58,7 +58,8 @@ typedef enum igemm_status {
     IGEMM_MISALIGNED = 3,        /* a base address is not 16-byte aligned */
     IGEMM_OVERFLOW_BOUND = 4,    /* K above the exact-accumulation bound (65536) */
     IGEMM_CUDA_ERROR = 5,        /* tensor-map encoding, memset or launch failed */
-    IGEMM_DEVICE_TIMEOUT = 6     /* a kernel's bounded wait expired (see igemm_last_status) */
+    IGEMM_DEVICE_TIMEOUT = 6,    /* a kernel's bounded wait expired (see igemm_last_status) */
+    IGEMM_WORKSPACE_LIMIT = 7    /* i4i4_gemm_noalloc: the problem needs more than its fixed workspace */
 } igemm_status;
 
 /*
@@ -74,6 +75,32 @@ typedef enum igemm_status {
  * Returns IGEMM_OK once the work is enqueued on `stream`.
  */
 IGEMM_API int i4i4_gemm(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);
+
+/*
+ * int4 x int4 GEMM that allocates nothing: the same result as i4i4_gemm, for
+ * callers that may not allocate device memory during a call (for example
+ * code running where a memory allocation would block on other work, or
+ * whose memory budget is fixed up front).  None of the pages describes such
+ * an entry point; it is an addition of this library.
+ *
+ * Its workspace is a fixed array of 32 MiB (IGEMM_NOALLOC_WORKSPACE_BYTES)
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.  It always takes the prepared-codes path, which needs
+ * (M + N) * K bytes plus about 4 * (M + N + 1024) bytes of row sums; larger
+ * problems return IGEMM_WORKSPACE_LIMIT before anything is enqueued.  The
+ * call makes no cudaMalloc, cudaFree or pool allocation.
+ *
+ * The first call on each device looks up the device address of the array
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the one array and each call
+ * rewrites what it reads, so results never depend on an earlier call; but
+ * calls whose work overlaps on the GPU (on different streams, or from
+ * different threads without ordering) race on the array and give wrong
+ * results.  Arguments and the other rules are those of i4i4_gemm.
+ */
+#define IGEMM_NOALLOC_WORKSPACE_BYTES (32u << 20)
+IGEMM_API int i4i4_gemm_noalloc(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K,
+                                cudaStream_t stream);
 
 /*
  * W4A8 GEMM:  C[m,n] = sum_k a[m,k] * b[n,k], a int8, b int4, exact, int32.

@@ -18,11 +18,11 @@ import os
 from .build import LIB_PATH, build as build_library
 
 __all__ = [
-    "IgemmError", "load", "i4i4_gemm", "w4a8_gemm", "pack_int4", "igemm_strerror",
+    "IgemmError", "load", "i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "pack_int4", "igemm_strerror",
     "igemm_last_status", "igemm_watchdog_selftest", "EXPORTED_SYMBOLS", "LIB_PATH", "build_library",
 ]
 
-EXPORTED_SYMBOLS = ("i4i4_gemm", "w4a8_gemm", "pack_int4", "igemm_strerror", "igemm_last_status",
+EXPORTED_SYMBOLS = ("i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "pack_int4", "igemm_strerror", "igemm_last_status",
                     "igemm_watchdog_selftest")
 
 IGEMM_OK = 0
@@ -32,6 +32,8 @@ IGEMM_MISALIGNED = 3
 IGEMM_OVERFLOW_BOUND = 4
 IGEMM_CUDA_ERROR = 5
 IGEMM_DEVICE_TIMEOUT = 6
+IGEMM_WORKSPACE_LIMIT = 7
+NOALLOC_WORKSPACE_BYTES = 32 << 20
 
 _lib = None
 
@@ -60,6 +62,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     i64 = ctypes.c_int64
     lib.i4i4_gemm.argtypes = [p, p, p, i, i, i, p]
     lib.i4i4_gemm.restype = i
+    lib.i4i4_gemm_noalloc.argtypes = [p, p, p, i, i, i, p]
+    lib.i4i4_gemm_noalloc.restype = i
     lib.w4a8_gemm.argtypes = [p, p, p, i, i, i, p]
     lib.w4a8_gemm.restype = i
     lib.pack_int4.argtypes = [p, p, i64, i64, p]
@@ -98,6 +102,14 @@ def _check(code: int, where: str) -> None:
 def i4i4_gemm(Ap, Bp, C, M: int, N: int, K: int, stream=None) -> None:
     """C[M,N] (int32) = A . B^T for packed int4 Ap [M,K/2] and Bp [N,K/2]."""
     _check(load().i4i4_gemm(_ptr(Ap), _ptr(Bp), _ptr(C), M, N, K, _stream(stream)), "i4i4_gemm")
+
+
+def i4i4_gemm_noalloc(Ap, Bp, C, M: int, N: int, K: int, stream=None) -> None:
+    """Same as i4i4_gemm, with the library's fixed 32 MiB device workspace
+    instead of allocated memory (for callers that cannot allocate during a
+    call); larger problems raise with IGEMM_WORKSPACE_LIMIT.  Calls that
+    overlap on the GPU share that workspace and race."""
+    _check(load().i4i4_gemm_noalloc(_ptr(Ap), _ptr(Bp), _ptr(C), M, N, K, _stream(stream)), "i4i4_gemm_noalloc")
 
 
 def w4a8_gemm(A, Bp, C, M: int, N: int, K: int, stream=None) -> None:

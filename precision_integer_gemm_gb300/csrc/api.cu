@@ -195,6 +195,15 @@ extern "C" int w4a8_gemm(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, 
     return launch_w4a8(A, Bp, C, M, N, K, stream);
 }
 
+extern "C" int i4i4_gemm_noalloc(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K,
+                                 cudaStream_t stream)
+{
+    bool done;
+    const int rc = gemm_common_checks(Ap, Bp, C, M, N, K, stream, &done);
+    if (done) return rc;
+    return launch_i4i4_noalloc(Ap, Bp, C, M, N, K, stream);
+}
+
 extern "C" int pack_int4(const int8_t *logical, uint8_t *packed, int64_t rows, int64_t K, cudaStream_t stream)
 {
     if (rows < 0 || K < 0) return kInvalidArgument;
@@ -222,6 +231,9 @@ extern "C" const char *igemm_strerror(int code)
     case kOverflowBound: return "K above the exact-accumulation bound (65536)";
     case kCudaError: return "CUDA error (tensor-map encoding, memset, launch or synchronization failed)";
     case kDeviceTimeout: return "device timeout (a kernel's bounded pipeline wait expired; its output is not valid)";
+    case kWorkspaceLimit:
+        return "problem too large for the fixed 32 MiB workspace of i4i4_gemm_noalloc ((M + N) * K bytes of codes "
+               "plus row sums); use i4i4_gemm";
     default: return "unknown igemm status";
     }
 }

@@ -7,6 +7,7 @@
 // more than it saves, take igemm_tc_kernel, which unpacks every tile in the
 // kernel: MMA A side = A (127 data rows + a row of ones per tile, codes in
 // TMEM), B side = B (192 rows per tile, codes in shared memory).
+#include <mutex>
 #include "launch.cuh"
 
 namespace igemm {
@@ -69,6 +70,63 @@ int launch_i4i4(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, 
     const int64_t operand_bytes = (int64_t(M) + N) * (K / 2);
     return launch_gemm<Cfg>(mapA, mapB, mapC32, mapC31, tma_store, C, M, N, K, p_tiles, q_tiles, operand_bytes,
                             stream);
+}
+
+// ---------------------------------------------------------------- allocation-free variant
+// i4i4_gemm_noalloc runs the prepared-codes path with its workspace in this
+// fixed device array instead of memory from the pool: for callers that must
+// not allocate during a call.  Every GPU that loads the library holds the
+// array until the process exits; every call shares it.
+static __device__ __align__(256) uint8_t g_noalloc_workspace[kNoAllocWorkspaceBytes];
+
+// Device address of the array on the current device.  Host code cannot use
+// the array's name as a device pointer (in host code it names a host-side
+// stand-in), so the address is looked up once per device, with that device
+// current, and cached.
+static int noalloc_workspace(uint8_t **out)
+{
+    static std::mutex mu;
+    static uint8_t *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kCudaError;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || !p) return kCudaError;
+        addr[dev] = static_cast<uint8_t *>(p);
+    }
+    *out = addr[dev];
+    return kOk;
+}
+
+int launch_i4i4_noalloc(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
+{
+    using Cfg = CfgI4I4Ss;
+    CodesLayout lay;
+    if (codes_layout(M, N, N, K, &lay) > kNoAllocWorkspaceBytes) return kWorkspaceLimit;
+    uint8_t *base = nullptr;
+    int rc = noalloc_workspace(&base);
+    if (rc != kOk) return rc;
+    uint8_t *a_codes = base + lay.p_codes, *b_codes = base + lay.q_codes;
+    int32_t *a_sums = reinterpret_cast<int32_t *>(base + lay.p_sums);
+    int32_t *b_sums = reinterpret_cast<int32_t *>(base + lay.q_sums);
+    // the preparation pass rewrites every code row and row sum the GEMM reads,
+    // so nothing left in the array by an earlier call is used
+    rc = launch_prep(Ap, M, Bp, N, false, K, a_codes, b_codes, a_sums, b_sums, stream);
+    CUtensorMap mapP, mapQ, mapC = {};
+    if (rc == kOk)
+        rc = make_map(&mapP, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, M, K, Cfg::kPRows, Cfg::kBK,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc == kOk)
+        rc = make_map(&mapQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_codes, N, K, Cfg::QA, Cfg::kBK,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    const bool tma_store = (N % 4) == 0;
+    if (rc == kOk && tma_store)
+        rc = make_map(&mapC, CU_TENSOR_MAP_DATA_TYPE_INT32, C, M, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc == kOk)
+        rc = launch_ss<Cfg>(mapP, mapQ, mapC, tma_store, C, M, N, K, a_sums, b_sums, M, N,
+                            (int64_t(M) + N) * K, stream);
+    return rc;
 }
 
 }  // namespace igemm

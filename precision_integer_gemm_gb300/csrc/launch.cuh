@@ -16,6 +16,7 @@ enum Status : int {
     kOverflowBound = 4,
     kCudaError = 5,
     kDeviceTimeout = 6,
+    kWorkspaceLimit = 7,
 };
 
 // 2-D tiled tensor map over a row-major matrix [rows, cols] of `dtype`
@@ -138,6 +139,10 @@ int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMa
 }
 
 int launch_i4i4(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);
+
+// Fixed workspace of i4i4_gemm_noalloc (a file-scope device array).
+constexpr size_t kNoAllocWorkspaceBytes = size_t(32) << 20;
+int launch_i4i4_noalloc(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);
 int launch_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);
 
 }  // namespace igemm

@@ -1,0 +1,64 @@
+"""i4i4_gemm_noalloc: the int4 x int4 GEMM for callers that cannot allocate
+device memory during a call.  It keeps its workspace in a fixed array inside
+the library, so its results must equal those of i4i4_gemm (which takes its
+workspace from a memory pool) bit for bit, call after call, although every
+call reuses the same array.
+
+This file is collected last so that a run stopping at the first failure has
+already run every other test.
+"""
+
+import numpy as np
+import pytest
+
+import seeded_inputs as si
+import precision_integer_gemm_gb300 as pig
+
+FAKE = 0x10000  # a 16-byte-aligned address that the rejected calls never touch
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pig.build_library()
+    return pig.load()
+
+
+def test_noalloc_rejects_bad_arguments_and_oversized_problems(lib):
+    f = lib.i4i4_gemm_noalloc
+    assert f(FAKE, FAKE, FAKE, -1, 8, 32, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert f(FAKE, FAKE, FAKE, 8, 8, 48, None) == pig.IGEMM_UNSUPPORTED_SHAPE
+    assert f(FAKE, FAKE, FAKE, 8, 8, 65536 + 32, None) == pig.IGEMM_OVERFLOW_BOUND
+    assert f(FAKE + 8, FAKE, FAKE, 8, 8, 32, None) == pig.IGEMM_MISALIGNED
+    assert f(None, None, None, 0, 8, 32, None) == pig.IGEMM_OK
+    # (M + N) * K = 64 MiB of codes: more than the fixed 32 MiB workspace
+    assert f(FAKE, FAKE, FAKE, 4096, 4096, 8192, None) == pig.IGEMM_WORKSPACE_LIMIT
+    assert "32 MiB" in pig.igemm_strerror(pig.IGEMM_WORKSPACE_LIMIT)
+
+
+# (M, N, K): a shape that i4i4_gemm sends through its in-kernel unpacking
+# path (N < 256), a ragged one with a K tail, one that fills half the array,
+# and a deep K that the launch plan splits
+SHAPES = [(300, 200, 1056), (513, 770, 4128), (2048, 2048, 4096), (128, 128, 65536)]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_noalloc_equals_i4i4_gemm_on_consecutive_calls(lib, M, N, K):
+    torch = pytest.importorskip("torch")
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    stream = torch.cuda.current_stream()
+    for call in range(2):
+        # new operands for each call: nothing the first call left in the
+        # shared array may show up in the second result
+        a = torch.from_numpy(si.int4_values(9000 + 10 * call + M, (M, K))).cuda()
+        b = torch.from_numpy(si.int4_values(9500 + 10 * call + N, (N, K))).cuda()
+        ap = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+        bp = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
+        pig.pack_int4(a, ap, M, K, stream)
+        pig.pack_int4(b, bp, N, K, stream)
+        want = torch.full((M, N), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+        got = torch.full((M, N), -0x5A5A5A5A, dtype=torch.int32, device="cuda")
+        pig.i4i4_gemm(ap, bp, want, M, N, K, stream)
+        pig.i4i4_gemm_noalloc(ap, bp, got, M, N, K, stream)
+        assert pig.igemm_last_status(stream) == 0
+        assert torch.equal(got, want), (M, N, K, call)
