@@ -127,6 +127,14 @@ IGEMM_API int w4a8_gemm(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, i
  */
 IGEMM_API int pack_int4(const int8_t *logical, uint8_t *packed, int64_t rows, int64_t K, cudaStream_t stream);
 
+/*
+ * Number of kernels this library has launched in this process so far (all
+ * devices and streams; a launch counts when it was enqueued).  One GEMM call
+ * launches one kernel, or two on the prepared-codes path (the preparation
+ * pass and the GEMM); a split K adds a memset, which is not a kernel.
+ */
+IGEMM_API uint64_t igemm_kernels_launched(void);
+
 /* Static, human-readable text for an igemm_status value. */
 IGEMM_API const char *igemm_strerror(int code);
 

@@ -19,11 +19,11 @@ from .build import LIB_PATH, build as build_library
 
 __all__ = [
     "IgemmError", "load", "i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "pack_int4", "igemm_strerror",
-    "igemm_last_status", "igemm_watchdog_selftest", "EXPORTED_SYMBOLS", "LIB_PATH", "build_library",
+    "igemm_last_status", "igemm_watchdog_selftest", "igemm_kernels_launched", "EXPORTED_SYMBOLS", "LIB_PATH", "build_library",
 ]
 
 EXPORTED_SYMBOLS = ("i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "pack_int4", "igemm_strerror", "igemm_last_status",
-                    "igemm_watchdog_selftest")
+                    "igemm_watchdog_selftest", "igemm_kernels_launched")
 
 IGEMM_OK = 0
 IGEMM_INVALID_ARGUMENT = 1
@@ -72,6 +72,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.igemm_strerror.restype = ctypes.c_char_p
     lib.igemm_last_status.argtypes = [p]
     lib.igemm_last_status.restype = i
+    lib.igemm_kernels_launched.argtypes = []
+    lib.igemm_kernels_launched.restype = ctypes.c_uint64
     lib.igemm_watchdog_selftest.argtypes = [ctypes.c_uint32, p]
     lib.igemm_watchdog_selftest.restype = i
     return lib
@@ -128,6 +130,11 @@ def igemm_strerror(code: int) -> str:
 
 def igemm_last_status(stream=None) -> int:
     return int(load().igemm_last_status(_stream(stream)))
+
+
+def igemm_kernels_launched() -> int:
+    """Kernels this library has enqueued in this process so far."""
+    return int(load().igemm_kernels_launched())
 
 
 def igemm_watchdog_selftest(limit_us: int, stream=None) -> None:

@@ -1,6 +1,7 @@
 // C-ABI entry points of libigemm.so (declared in include/igemm.h): argument
 // validation, tensor maps, the device status word, pack_int4 and the
 // watchdog self-test.  The GEMM kernels live in gemm_kernel.cuh.
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <cudaTypedefs.h>
@@ -12,6 +13,10 @@ namespace igemm {
 // Device status word: 0, or the first error a kernel recorded (a timed-out
 // wait).  Read and cleared by igemm_last_status().
 __device__ int g_status_word = 0;
+
+static std::atomic<unsigned long long> g_launches{0};
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 int *device_status_word()
 {
@@ -218,6 +223,7 @@ extern "C" int pack_int4(const int8_t *logical, uint8_t *packed, int64_t rows, i
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     pack_int4_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(logical, packed, n_out, n_vec);
+    note_launch();
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
 }
 
@@ -238,6 +244,8 @@ extern "C" const char *igemm_strerror(int code)
     }
 }
 
+extern "C" uint64_t igemm_kernels_launched(void) { return g_launches.load(std::memory_order_relaxed); }
+
 extern "C" int igemm_last_status(cudaStream_t stream)
 {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return kCudaError;
@@ -254,5 +262,6 @@ extern "C" int igemm_watchdog_selftest(uint32_t limit_us, cudaStream_t stream)
     int *status = device_status_word();
     if (!status) return kCudaError;
     watchdog_selftest_kernel<<<1, 32, 0, stream>>>(status, static_cast<unsigned long long>(limit_us) * 1000ull);
+    note_launch();
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
 }

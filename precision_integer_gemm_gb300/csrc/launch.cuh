@@ -27,6 +27,8 @@ int make_map(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint
 // Device status word of the current device (address of a file-scope
 // __device__ int, fetched once per device).
 int *device_status_word();
+// Counts one kernel launch of this library (igemm_kernels_launched).
+void note_launch();
 unsigned long long watchdog_limit_ns();
 int sm_count();
 
@@ -76,6 +78,7 @@ int launch_gemm(const CUtensorMap &mapA, const CUtensorMap &mapB, const CUtensor
     if (plan.split > 1 && cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 4, stream) != cudaSuccess)
         return kCudaError;
     kernel<<<plan.ctas, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mapA, mapB, mapC32, mapC31, prm);
+    note_launch();
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
 }
 
@@ -135,6 +138,7 @@ int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMa
     if (plan.split > 1 && cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 4, stream) != cudaSuccess)
         return kCudaError;
     kernel<<<plan.ctas, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mapP, mapQ, mapC, prm);
+    note_launch();
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
 }
 

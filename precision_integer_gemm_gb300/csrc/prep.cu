@@ -97,6 +97,7 @@ int launch_prep(const uint8_t *P, int p_rows, const uint8_t *Q, int q_rows, bool
         prep_codes_kernel<true><<<grid, 256, 0, stream>>>(P, p_rows, Q, q_rows, K, p_codes, q_codes, p_sums, q_sums);
     else
         prep_codes_kernel<false><<<grid, 256, 0, stream>>>(P, p_rows, Q, q_rows, K, p_codes, q_codes, p_sums, q_sums);
+    note_launch();
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
 }
 

@@ -245,6 +245,24 @@ def test_split_path_is_deterministic(orc):
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
 
 
+def test_kernel_launch_counter():
+    # the prepared-codes path launches the preparation pass and the GEMM, the
+    # in-kernel unpacking path one kernel; rejected and empty calls none
+    a = torch.zeros((512, 64), dtype=torch.uint8, device="cuda")
+    C = torch.empty((512, 512), dtype=torch.int32, device="cuda")
+    n0 = pig.igemm_kernels_launched()
+    pig.i4i4_gemm(a, a, C, 512, 512, 128)
+    n1 = pig.igemm_kernels_launched()
+    pig.i4i4_gemm(a, a, C, 100, 100, 128)
+    n2 = pig.igemm_kernels_launched()
+    pig.i4i4_gemm(None, None, C, 0, 4, 64)
+    with pytest.raises(pig.IgemmError):
+        pig.i4i4_gemm(a, a, C, 4, 4, 48)
+    n3 = pig.igemm_kernels_launched()
+    torch.cuda.synchronize()
+    assert (n1 - n0, n2 - n1, n3 - n2) == (2, 1, 0)
+
+
 def test_empty_and_zero_k():
     C = torch.full((4, 4), 7, dtype=torch.int32, device="cuda")
     pig.i4i4_gemm(None, None, C, 0, 4, 64)
