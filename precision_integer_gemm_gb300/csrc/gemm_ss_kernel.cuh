@@ -74,6 +74,7 @@ struct SsParams {
     const int32_t *sumQ;  // per Q row: int4 x int4: sum uB; W4A8: sum a (signed)
     int p_rows, q_rows;   // rows of the P and Q operands
     int p_tiles, q_tiles;
+    int group_p;          // tiles run in groups of group_p P tiles (P tile fastest)
     int kb_total, kb_per_split, split, num_units;
     int tma_store;
     int *status;
@@ -89,8 +90,17 @@ __device__ __forceinline__ SsUnit ss_unit(const SsParams &prm, int u)
 {
     const int tile = u / prm.split;
     const int s = u - tile * prm.split;
-    const int pt = tile % prm.p_tiles;
-    const int qt = tile / prm.p_tiles;
+    // Grouped order: group_p P tiles times every Q tile, P fastest.  The CTAs
+    // of one wave share a few Q tiles through L2 and the group's P tiles
+    // stay in L2 for the whole group, so each operand comes from DRAM about
+    // once per group instead of once per wave.
+    const int per_group = prm.group_p * prm.q_tiles;
+    const int grp = tile / per_group;
+    const int first = grp * prm.group_p;
+    const int gsize = min(prm.p_tiles - first, prm.group_p);
+    const int r = tile - grp * per_group;
+    const int pt = first + r % gsize;
+    const int qt = r / gsize;
     SsUnit x;
     x.p0 = pt * Cfg::kPRows;
     x.q0 = qt * Cfg::QA;
@@ -172,6 +182,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     if (warp == 5) {
         // ------------------------------------------------------------ producer
         if (lane < Cfg::kIssuers) {
+            // P tiles are reused by the whole group: keep them in L2 (an
+            // evict-first hint on the Q tiles, which one wave shares, measured
+            // slower: the CTAs of a wave do not read a Q tile at the same time)
+            const uint64_t keep = l2_policy_evict_last();
             uint32_t g = 0;  // stages (k blocks) over all units of this CTA
             uint32_t issued_mask = 0, last_phase = 0;
             bool ok = true;
@@ -188,7 +202,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     uint8_t *st = stages + s * Cfg::kStage;
                     const int kx = (x.kb0 + i) * Cfg::kBK;
                     mbar_arrive_expect_tx(&full[s], Cfg::kStage);
-                    tma_load_2d(st, &mapP, &full[s], kx, x.p0);
+                    tma_load_2d_hint(st, &mapP, &full[s], kx, x.p0, keep);
                     if constexpr (Cfg::kW4A8) {
                         // high-part rows q0.., low-part rows M + q0.. (the code planes are stacked)
                         tma_load_2d(st + Cfg::kStageA, &mapQ, &full[s], kx, x.q0);
@@ -244,6 +258,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         uint8_t *stg = cstage + quad * Cfg::kCStage;
         const bool reduce = prm.split > 1;
+        const uint64_t out_policy = l2_policy_evict_first();  // C is not read again
         uint32_t nacc = 0;
         for (int u = blockIdx.x; u < prm.num_units; u += gridDim.x, ++nacc) {
             const SsUnit x = ss_unit<Cfg>(prm, u);
@@ -292,9 +307,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                         const int y = x.p0 + quad * 32;
                         if (lane == 0 && y < prm.M && n0 < prm.N) {
                             if (reduce)
-                                tma_reduce_add_2d(&mapC, stg, n0, y);
+                                tma_reduce_add_2d_hint(&mapC, stg, n0, y, out_policy);
                             else
-                                tma_store_2d(&mapC, stg, n0, y);
+                                tma_store_2d_hint(&mapC, stg, n0, y, out_policy);
                             bulk_commit_group();
                         }
                     } else if (m < prm.M) {
@@ -364,9 +379,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                         const int m0 = x.q0 + j0, nx = x.p0 + quad * 32;
                         if (lane == 0 && m0 < prm.M && nx < prm.N) {
                             if (reduce)
-                                tma_reduce_add_2d(&mapC, stg, nx, m0);
+                                tma_reduce_add_2d_hint(&mapC, stg, nx, m0, out_policy);
                             else
-                                tma_store_2d(&mapC, stg, nx, m0);
+                                tma_store_2d_hint(&mapC, stg, nx, m0, out_policy);
                             bulk_commit_group();
                         }
                     }

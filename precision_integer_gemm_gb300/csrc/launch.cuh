@@ -1,5 +1,6 @@
 // Host-side launch plumbing shared by the GEMM translation units.
 #pragma once
+#include <algorithm>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -126,6 +127,10 @@ int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMa
     prm.q_rows = q_rows;
     prm.p_tiles = (p_rows + Cfg::kPRows - 1) / Cfg::kPRows;
     prm.q_tiles = (q_rows + Cfg::QA - 1) / Cfg::QA;
+    // a group's P tiles (kGroupBytes of codes) stay in L2 while it runs
+    constexpr int64_t kGroupBytes = int64_t(32) << 20;
+    const int64_t p_tile_bytes = int64_t(Cfg::kPRows) * K;
+    prm.group_p = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(prm.p_tiles, kGroupBytes / p_tile_bytes)));
     prm.kb_total = (K + Cfg::kBK - 1) / Cfg::kBK;
     const Plan plan = plan_units(prm.p_tiles * prm.q_tiles, prm.kb_total, int64_t(M) * N * 4, operand_bytes);
     prm.kb_per_split = plan.kb_per_split;
