@@ -84,9 +84,9 @@ int make_map(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint
     return r == CUDA_SUCCESS ? kOk : kCudaError;
 }
 
-Plan plan_units(int tiles, int kb_total, int64_t c_bytes, int64_t operand_bytes)
+Plan plan_units(int tiles, int kb_total, int64_t c_bytes, int64_t operand_bytes, int workers)
 {
-    const int sms = sm_count();
+    const int sms = workers > 0 ? workers : sm_count();
     const bool may_split = tiles < sms || c_bytes * 4 <= operand_bytes;
     int best = 1;
     int64_t best_cost = -1;

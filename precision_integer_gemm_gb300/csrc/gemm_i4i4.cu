@@ -15,7 +15,7 @@ namespace igemm {
 //                      W4A8   QA  SP  SO  NB  A stages  A sets  ones row  staging
 using CfgI4I4 = KernelCfg<false, 192, 3, 3, 8, 4, 1, true, 1>;
 //                    W4A8   BN  stages
-using CfgI4I4Ss = SsCfg<false, 256, 4>;
+using CfgI4I4Ss = SsCfg<false, 256, 4, 2>;
 
 static bool use_codes_i4i4(int M, int N) { return M >= 256 && N >= 256; }
 
@@ -36,7 +36,7 @@ static int run_i4i4_codes(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int 
         rc = make_map(&mapP, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, M, K, Cfg::kPRows, Cfg::kBK,
                       CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc == kOk)
-        rc = make_map(&mapQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_codes, N, K, Cfg::QA, Cfg::kBK,
+        rc = make_map(&mapQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_codes, N, K, Cfg::kQBoxRows, Cfg::kBK,
                       CU_TENSOR_MAP_SWIZZLE_128B);
     const bool tma_store = (N % 4) == 0;
     if (rc == kOk && tma_store)
@@ -118,7 +118,7 @@ int launch_i4i4_noalloc(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M,
         rc = make_map(&mapP, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, M, K, Cfg::kPRows, Cfg::kBK,
                       CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc == kOk)
-        rc = make_map(&mapQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_codes, N, K, Cfg::QA, Cfg::kBK,
+        rc = make_map(&mapQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_codes, N, K, Cfg::kQBoxRows, Cfg::kBK,
                       CU_TENSOR_MAP_SWIZZLE_128B);
     const bool tma_store = (N % 4) == 0;
     if (rc == kOk && tma_store)

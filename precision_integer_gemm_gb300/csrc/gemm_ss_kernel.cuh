@@ -20,6 +20,12 @@
 // QA high-part rows followed by QA low-part rows (W4A8).  One pipeline stage
 // is one 128-k block of both, 128-byte swizzled K-major.
 //
+// Clusters (CL = 2): the two CTAs of a cluster take P tiles 2i and 2i + 1 of
+// the same Q tile and k range.  Each loads its own P tile and one half of the
+// Q tile, multicast into both CTAs' stage, so the Q tile leaves L2 once for
+// two MMAs.  A stage is free again only when both CTAs' MMAs have read it:
+// every MMA commit arrives on the empty barrier of both CTAs.
+//
 // Warp roles (persistent CTAs, one per SM, work units = (tile, k split)):
 //   warps 0-3   epilogue: TMEM -> registers -> int32 -> shared staging ->
 //               bulk tensor store (reduce-add for split K) into C
@@ -35,12 +41,16 @@
 
 namespace igemm {
 
-template <bool W4A8, int BN_, int ST_>
+template <bool W4A8, int BN_, int ST_, int CL_ = 1>
 struct SsCfg {
     static constexpr bool kW4A8 = W4A8;
     static constexpr int kQRows = BN_;                 // MMA N
     static constexpr int QA = W4A8 ? BN_ / 2 : BN_;    // Q source rows per tile
     static constexpr int ST = ST_;                     // pipeline stages
+    static constexpr int CL = CL_;                     // CTAs per cluster sharing the Q tile
+    // rows of the Q box one CTA loads: int4 x int4 splits the Q tile by rows;
+    // W4A8 with CL = 2 gives the high-code block to one CTA, the low to the other
+    static constexpr int kQBoxRows = W4A8 ? QA : QA / CL;
     static constexpr int kBK = 128;                    // k per stage
     static constexpr int kPRows = 128;                 // MMA M
     static constexpr int kIssuers = ST % 4 == 0 ? 4 : ST % 3 == 0 ? 3 : ST % 2 == 0 ? 2 : 1;
@@ -65,6 +75,8 @@ struct SsCfg {
     static_assert(kAccBufs * kAccCols <= 512, "TMEM budget");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
     static_assert(ST <= 32, "stage masks");
+    static_assert(CL == 1 || CL == 2, "cluster size");
+    static_assert(W4A8 || kQBoxRows % 8 == 0, "Q half tiles start on 1024-byte boundaries");
 };
 
 struct SsParams {
@@ -74,7 +86,7 @@ struct SsParams {
     const int32_t *sumQ;  // per Q row: int4 x int4: sum uB; W4A8: sum a (signed)
     int p_rows, q_rows;   // rows of the P and Q operands
     int p_tiles, q_tiles;
-    int group_p;          // tiles run in groups of group_p P tiles (P tile fastest)
+    int group_p;          // tiles run in groups of group_p P-tile slots (slot fastest)
     int kb_total, kb_per_split, split, num_units;
     int tma_store;
     int *status;
@@ -85,9 +97,11 @@ struct SsUnit {
     int p0, q0, kb0, nkb;
 };
 
+// Unit u of the cluster; a P-tile slot holds Cfg::CL P tiles, one per CTA rank.
 template <class Cfg>
-__device__ __forceinline__ SsUnit ss_unit(const SsParams &prm, int u)
+__device__ __forceinline__ SsUnit ss_unit(const SsParams &prm, int u, int rank)
 {
+    const int p_slots = (prm.p_tiles + Cfg::CL - 1) / Cfg::CL;
     const int tile = u / prm.split;
     const int s = u - tile * prm.split;
     // Grouped order: group_p P tiles times every Q tile, P fastest.  The CTAs
@@ -97,9 +111,9 @@ __device__ __forceinline__ SsUnit ss_unit(const SsParams &prm, int u)
     const int per_group = prm.group_p * prm.q_tiles;
     const int grp = tile / per_group;
     const int first = grp * prm.group_p;
-    const int gsize = min(prm.p_tiles - first, prm.group_p);
+    const int gsize = min(p_slots - first, prm.group_p);
     const int r = tile - grp * per_group;
-    const int pt = first + r % gsize;
+    const int pt = (first + r % gsize) * Cfg::CL + rank;  // may pass the last P tile (all rows out of range)
     const int qt = r / gsize;
     SsUnit x;
     x.p0 = pt * Cfg::kPRows;
@@ -152,11 +166,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int rank = Cfg::CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int cid = blockIdx.x / Cfg::CL;       // cluster index
+    const int ncl = gridDim.x / Cfg::CL;        // clusters
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], Cfg::CL);  // one MMA commit per CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -176,6 +193,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the peer's barriers are initialised before anything reaches them
+    if constexpr (Cfg::CL > 1) cluster_sync_all();
     const uint32_t tmem = *tmem_slot;
     const Watchdog wd{abort_flag, prm.status, prm.limit_ns};
 
@@ -189,8 +208,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             uint32_t g = 0;  // stages (k blocks) over all units of this CTA
             uint32_t issued_mask = 0, last_phase = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < prm.num_units; u += gridDim.x) {
-                const SsUnit x = ss_unit<Cfg>(prm, u);
+            for (int u = cid; ok && u < prm.num_units; u += ncl) {
+                const SsUnit x = ss_unit<Cfg>(prm, u, rank);
                 for (int i = 0; i < x.nkb; ++i, ++g) {
                     const int s = static_cast<int>(g % ST);
                     if (s % Cfg::kIssuers != lane) continue;
@@ -203,7 +222,18 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     const int kx = (x.kb0 + i) * Cfg::kBK;
                     mbar_arrive_expect_tx(&full[s], Cfg::kStage);
                     tma_load_2d_hint(st, &mapP, &full[s], kx, x.p0, keep);
-                    if constexpr (Cfg::kW4A8) {
+                    if constexpr (Cfg::CL > 1) {
+                        // this CTA's share of the Q tile, into both CTAs' stage
+                        int qy, qoff;
+                        if constexpr (Cfg::kW4A8) {
+                            qy = rank == 0 ? x.q0 : prm.q_rows + x.q0;
+                            qoff = rank * QA * Cfg::kBK;
+                        } else {
+                            qy = x.q0 + rank * Cfg::kQBoxRows;
+                            qoff = rank * Cfg::kQBoxRows * Cfg::kBK;
+                        }
+                        tma_load_2d_multicast(st + Cfg::kStageA + qoff, &mapQ, &full[s], kx, qy, 0x3);
+                    } else if constexpr (Cfg::kW4A8) {
                         // high-part rows q0.., low-part rows M + q0.. (the code planes are stacked)
                         tma_load_2d(st + Cfg::kStageA, &mapQ, &full[s], kx, x.q0);
                         tma_load_2d(st + Cfg::kStageA + QA * Cfg::kBK, &mapQ, &full[s], kx, prm.q_rows + x.q0);
@@ -218,6 +248,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 #pragma unroll 1
             for (int s = 0; s < ST; ++s)
                 if ((issued_mask >> s) & 1u) ss_wait_drain(&full[s], (last_phase >> s) & 1u, prm.limit_ns);
+            if constexpr (Cfg::CL > 1) {
+                // ... and no commit of the peer's MMA still on its way to this
+                // CTA's barriers: wait for the release of each own stage's last load
+#pragma unroll 1
+                for (int s = 0; s < ST; ++s)
+                    if ((issued_mask >> s) & 1u) ss_wait_drain(&empty[s], (last_phase >> s) & 1u, prm.limit_ns);
+            }
         }
     } else if (warp == 4) {
         // ------------------------------------------------------------ MMA issuer
@@ -225,8 +262,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             constexpr uint32_t idesc = idesc_e4m3_f32(Cfg::kPRows, Cfg::kQRows);
             uint32_t g = 0, nacc = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < prm.num_units; u += gridDim.x, ++nacc) {
-                const SsUnit x = ss_unit<Cfg>(prm, u);
+            for (int u = cid; ok && u < prm.num_units; u += ncl, ++nacc) {
+                const SsUnit x = ss_unit<Cfg>(prm, u, rank);
                 const uint32_t ab = nacc % Cfg::kAccBufs;
                 const uint32_t aph = (nacc / Cfg::kAccBufs) & 1u;
                 const uint32_t d_tmem = tmem + ab * Cfg::kAccCols;
@@ -245,7 +282,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     for (int kk = 0; kk < Cfg::kBK / 32; ++kk)
                         mma_f8f6f4(d_tmem, sdesc_kmajor_sw128(a_base + 32 * kk), sdesc_kmajor_sw128(b_base + 32 * kk),
                                    idesc, (i > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&empty[s]);
+                    if constexpr (Cfg::CL > 1)
+                        mma_commit_multicast(&empty[s], 0x3);
+                    else
+                        mma_commit(&empty[s]);
                 }
                 if (ok) mma_commit(&acc_full[ab]);
             }
@@ -260,8 +300,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         const bool reduce = prm.split > 1;
         const uint64_t out_policy = l2_policy_evict_first();  // C is not read again
         uint32_t nacc = 0;
-        for (int u = blockIdx.x; u < prm.num_units; u += gridDim.x, ++nacc) {
-            const SsUnit x = ss_unit<Cfg>(prm, u);
+        for (int u = cid; u < prm.num_units; u += ncl, ++nacc) {
+            const SsUnit x = ss_unit<Cfg>(prm, u, rank);
             const uint32_t ab = nacc % Cfg::kAccBufs;
             if (!ss_warp_wait(&acc_full[ab], (nacc / Cfg::kAccBufs) & 1u, wd)) break;
             tc_fence_after();
@@ -400,6 +440,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     if (warp == 4) {
         if (lane == 0) ss_wait_drain(mma_drain, 0, prm.limit_ns);  // every MMA of this CTA is done
         __syncwarp();
+    }
+    // neither CTA of a cluster leaves while the other may still reach it
+    if constexpr (Cfg::CL > 1) cluster_sync_all();
+    if (warp == 4) {
         tc_fence_after();
         tmem_dealloc(tmem, Cfg::kTmemCols);
     }

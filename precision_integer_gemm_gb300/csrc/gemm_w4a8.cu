@@ -18,7 +18,7 @@ namespace igemm {
 using CfgW4A8 = KernelCfg<true, 96, 3, 3, 8, 4, 1, false, 1>;
 using CfgW4A8Skinny = KernelCfg<true, 16, 8, 4, 2, 8, 2, false, 1>;
 //                    W4A8  BN  stages
-using CfgW4A8Ss = SsCfg<true, 256, 4>;
+using CfgW4A8Ss = SsCfg<true, 256, 4, 2>;
 
 static int run_w4a8_codes(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
 {
@@ -39,7 +39,7 @@ static int run_w4a8_codes(const int8_t *A, const uint8_t *Bp, int32_t *C, int M,
                       CU_TENSOR_MAP_SWIZZLE_128B);
     // the high-code plane (rows 0..M-1) and the low-code plane (rows M..2M-1)
     if (rc == kOk)
-        rc = make_map(&mapQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, 2 * uint64_t(M), K, Cfg::QA, Cfg::kBK,
+        rc = make_map(&mapQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, 2 * uint64_t(M), K, Cfg::kQBoxRows, Cfg::kBK,
                       CU_TENSOR_MAP_SWIZZLE_128B);
     const bool tma_store = (N % 4) == 0;
     if (rc == kOk && tma_store)

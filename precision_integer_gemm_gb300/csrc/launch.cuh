@@ -43,7 +43,8 @@ struct Plan {
 // units (tile, k split).  K is split only when C is small next to the
 // operands (the split path zeroes C and reduce-adds partial tiles), choosing
 // the split that minimises the largest number of k blocks any CTA runs.
-Plan plan_units(int tiles, int kb_total, int64_t c_bytes, int64_t operand_bytes);
+// `workers`: units that run at once (0: one per SM).
+Plan plan_units(int tiles, int kb_total, int64_t c_bytes, int64_t operand_bytes, int workers = 0);
 
 template <class Cfg>
 int launch_gemm(const CUtensorMap &mapA, const CUtensorMap &mapB, const CUtensorMap &mapC32,
@@ -101,6 +102,37 @@ int launch_prep(const uint8_t *P, int p_rows, const uint8_t *Q, int q_rows, bool
 int workspace_alloc(void **p, size_t bytes, cudaStream_t stream);
 int workspace_free(void *p, cudaStream_t stream);
 
+// CTAs of kernel `k` (clusters of `cl`) that can be resident at once: one per
+// SM for single CTAs; for clusters, what the GPC layout admits, asked once.
+template <class Cfg, class Kernel>
+int ss_resident_ctas(Kernel k)
+{
+    if constexpr (Cfg::CL == 1) {
+        return sm_count();
+    } else {
+        static int cache[64] = {};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+        if (!cache[dev]) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = Cfg::CL;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(Cfg::CL * sm_count(), 1, 1);
+            cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+            cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, k, &cfg) != cudaSuccess || clusters <= 0) return 0;
+            cache[dev] = clusters * Cfg::CL;
+        }
+        return cache[dev];
+    }
+}
+
 template <class Cfg>
 int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMap &mapC, bool tma_store, int32_t *C,
               int M, int N, int K, const int32_t *sumP, const int32_t *sumQ, int p_rows, int q_rows,
@@ -116,6 +148,8 @@ int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMa
             return kCudaError;
         attr_set[dev] = true;
     }
+    const int resident = ss_resident_ctas<Cfg>(kernel);
+    if (resident < Cfg::CL) return kCudaError;
     SsParams prm{};
     prm.C = C;
     prm.M = M;
@@ -127,22 +161,42 @@ int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMa
     prm.q_rows = q_rows;
     prm.p_tiles = (p_rows + Cfg::kPRows - 1) / Cfg::kPRows;
     prm.q_tiles = (q_rows + Cfg::QA - 1) / Cfg::QA;
+    const int p_slots = (prm.p_tiles + Cfg::CL - 1) / Cfg::CL;
     // a group's P tiles (kGroupBytes of codes) stay in L2 while it runs
     constexpr int64_t kGroupBytes = int64_t(32) << 20;
-    const int64_t p_tile_bytes = int64_t(Cfg::kPRows) * K;
-    prm.group_p = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(prm.p_tiles, kGroupBytes / p_tile_bytes)));
+    const int64_t slot_bytes = int64_t(Cfg::CL) * Cfg::kPRows * K;
+    prm.group_p = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(p_slots, kGroupBytes / slot_bytes)));
     prm.kb_total = (K + Cfg::kBK - 1) / Cfg::kBK;
-    const Plan plan = plan_units(prm.p_tiles * prm.q_tiles, prm.kb_total, int64_t(M) * N * 4, operand_bytes);
+    // the split plan counts cluster units against the clusters that fit at once
+    Plan plan = plan_units(p_slots * prm.q_tiles, prm.kb_total, int64_t(M) * N * 4, operand_bytes,
+                           resident / Cfg::CL);
     prm.kb_per_split = plan.kb_per_split;
     prm.split = plan.split;
-    prm.num_units = prm.p_tiles * prm.q_tiles * plan.split;
+    prm.num_units = p_slots * prm.q_tiles * plan.split;
     prm.tma_store = tma_store ? 1 : 0;
     prm.status = device_status_word();
     prm.limit_ns = watchdog_limit_ns();
     if (!prm.status) return kCudaError;
     if (plan.split > 1 && cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 4, stream) != cudaSuccess)
         return kCudaError;
-    kernel<<<plan.ctas, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mapP, mapQ, mapC, prm);
+    const int clusters = std::min(prm.num_units, resident / Cfg::CL);
+    if constexpr (Cfg::CL == 1) {
+        kernel<<<clusters, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mapP, mapQ, mapC, prm);
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = Cfg::CL;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(Cfg::CL * clusters, 1, 1);
+        cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kernel, mapP, mapQ, mapC, prm) != cudaSuccess) return kCudaError;
+    }
     note_launch();
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
 }
