@@ -135,6 +135,18 @@ IGEMM_API int pack_int4(const int8_t *logical, uint8_t *packed, int64_t rows, in
  */
 IGEMM_API uint64_t igemm_kernels_launched(void);
 
+/*
+ * Measurement hook: arms two caller-created CUDA events for the next GEMM call
+ * (i4i4_gemm, i4i4_gemm_noalloc or w4a8_gemm) made by this host thread.  That
+ * call records `start` on its stream right before it launches its GEMM kernel
+ * and `stop` right after, so cudaEventElapsedTime(start, stop) is that
+ * kernel's duration alone (without the preparation pass of the
+ * prepared-codes path).  Calls that launch no GEMM kernel (empty shapes,
+ * argument errors) leave the events armed.  IGEMM_INVALID_ARGUMENT for a null
+ * event.
+ */
+IGEMM_API int igemm_time_next_gemm(cudaEvent_t start, cudaEvent_t stop);
+
 /* Static, human-readable text for an igemm_status value. */
 IGEMM_API const char *igemm_strerror(int code);
 

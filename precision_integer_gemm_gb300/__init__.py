@@ -19,11 +19,13 @@ from .build import LIB_PATH, build as build_library
 
 __all__ = [
     "IgemmError", "load", "i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "pack_int4", "igemm_strerror",
-    "igemm_last_status", "igemm_watchdog_selftest", "igemm_kernels_launched", "EXPORTED_SYMBOLS", "LIB_PATH", "build_library",
+    "igemm_last_status", "igemm_watchdog_selftest", "igemm_kernels_launched", "igemm_time_next_gemm",
+    "EXPORTED_SYMBOLS", "LIB_PATH", "build_library",
 ]
 
 EXPORTED_SYMBOLS = ("i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "pack_int4", "igemm_strerror", "igemm_last_status",
-                    "igemm_watchdog_selftest", "igemm_kernels_launched")
+                    "igemm_watchdog_selftest", "igemm_kernels_launched",
+                    "igemm_time_next_gemm")
 
 IGEMM_OK = 0
 IGEMM_INVALID_ARGUMENT = 1
@@ -72,6 +74,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.igemm_strerror.restype = ctypes.c_char_p
     lib.igemm_last_status.argtypes = [p]
     lib.igemm_last_status.restype = i
+    lib.igemm_time_next_gemm.argtypes = [p, p]
+    lib.igemm_time_next_gemm.restype = i
     lib.igemm_kernels_launched.argtypes = []
     lib.igemm_kernels_launched.restype = ctypes.c_uint64
     lib.igemm_watchdog_selftest.argtypes = [ctypes.c_uint32, p]
@@ -130,6 +134,14 @@ def igemm_strerror(code: int) -> str:
 
 def igemm_last_status(stream=None) -> int:
     return int(load().igemm_last_status(_stream(stream)))
+
+
+def igemm_time_next_gemm(start, stop) -> None:
+    """Arm two CUDA events (torch.cuda.Event with timing, already recorded
+    once so that they exist, or raw handles) around the GEMM kernel of this
+    thread's next GEMM call."""
+    h = [e if isinstance(e, int) else e.cuda_event for e in (start, stop)]
+    _check(load().igemm_time_next_gemm(h[0], h[1]), "igemm_time_next_gemm")
 
 
 def igemm_kernels_launched() -> int:

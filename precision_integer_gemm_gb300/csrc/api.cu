@@ -18,6 +18,15 @@ static std::atomic<unsigned long long> g_launches{0};
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+static thread_local GemmEvents t_gemm_events = {nullptr, nullptr};
+
+GemmEvents take_gemm_events()
+{
+    const GemmEvents e = t_gemm_events;
+    t_gemm_events = {nullptr, nullptr};
+    return e;
+}
+
 int *device_status_word()
 {
     static int *cache[64] = {};
@@ -242,6 +251,13 @@ extern "C" const char *igemm_strerror(int code)
                "plus row sums); use i4i4_gemm";
     default: return "unknown igemm status";
     }
+}
+
+extern "C" int igemm_time_next_gemm(cudaEvent_t start, cudaEvent_t stop)
+{
+    if (!start || !stop) return kInvalidArgument;
+    t_gemm_events = {start, stop};
+    return kOk;
 }
 
 extern "C" uint64_t igemm_kernels_launched(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -13,7 +13,7 @@
 namespace igemm {
 
 //                      W4A8   QA  SP  SO  NB  A stages  A sets  ones row  staging
-using CfgI4I4 = KernelCfg<false, 192, 3, 3, 8, 4, 1, true, 1>;
+using CfgI4I4 = KernelCfg<false, 192, 2, 4, 8, 4, 1, true, 1>;
 //                    W4A8   BN  stages
 using CfgI4I4Ss = SsCfg<false, 256, 4, 2>;
 

@@ -94,7 +94,8 @@ struct KernelCfg {
     static_assert(kACol0 + kAStages * kAStageCols <= kTmemCols, "TMEM budget");
     static_assert(kQRows % 16 == 0 && kQRows <= 256, "MMA N");
     static_assert(QA % 8 == 0, "B unpack maps eight rows to a quarter warp");
-    static_assert(kAStages % kASets == 0, "each A set owns every kASets-th ring stage");
+    static_assert(kAStages % 2 == 0 && SO % 2 == 0, "code rings hold whole packed stages (two k blocks)");
+    static_assert((kAStages / 2) % kASets == 0, "each A set owns every kASets-th TMEM pair");
     static_assert(!(kW4A8 && kOnesRow), "W4A8 takes its B-side sums from the B unpack");
     static constexpr int kWarpA0 = 4, kWarpMma = 8, kWarpTma = 9, kWarpB0 = 10, kWarpA1 = 10 + NB;
     static constexpr int kThreads = 32 * (kWarpB0 + NB + 4 * (kASets - 1));
@@ -118,7 +119,11 @@ struct KernelCfg {
     static constexpr int kOffPkB = kOffPkA + SP * kPkA;
     static constexpr int kOffStage = ((kOffPkB + SP * kPkB + 1023) / 1024) * 1024;
     static constexpr int kOffBars = kOffStage + 4 * kStageBufs * kStage;
-    static constexpr int kNumBars = 2 * SP + 2 * kAStages + 2 * SO + 2 + 2 + 4 + 1;
+    // the A and B code rings hand over one packed stage (two k blocks) per
+    // barrier round trip: kAPairs TMEM pairs, kBPairs shared-memory pairs
+    static constexpr int kAPairs = kAStages / 2;
+    static constexpr int kBPairs = SO / 2;
+    static constexpr int kNumBars = 2 * SP + 2 * kAPairs + 2 * kBPairs + 2 + 2 + 4 + 1;
     static constexpr int kOffMisc = ((kOffBars + 8 * kNumBars + 127) / 128) * 128;
     static constexpr int kOffSumP = kOffMisc + 128;                  // [2 units][kASets][128]
     static constexpr int kOffSumQ = kOffSumP + 2 * kASets * 4 * kPRows;  // [2][kSumQ], 16-byte loads
@@ -210,7 +215,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     const GemmParams prm)
 {
     constexpr int SP = Cfg::SP, SO = Cfg::SO, QA = Cfg::QA, NB = Cfg::NB;
-    constexpr int AST = Cfg::kAStages, ASETS = Cfg::kASets;
+    constexpr int ASETS = Cfg::kASets;
+    constexpr int APR = Cfg::kAPairs, BPR = Cfg::kBPairs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t *opB = smem + Cfg::kOffOpB;
@@ -220,11 +226,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBars);
     uint64_t *full_p = bars;                  // TMA landed (1 + tx)
     uint64_t *empty_p = full_p + SP;          // packed stage read (4 A warps of one set + NB B warps)
-    uint64_t *a_full = empty_p + SP;          // A codes in TMEM (4)
-    uint64_t *a_empty = a_full + AST;         // A codes consumed (commit)
-    uint64_t *b_full = a_empty + AST;         // B codes in smem (NB)
-    uint64_t *b_empty = b_full + SO;          // B codes consumed (commit)
-    uint64_t *acc_full = b_empty + SO;        // [2] accumulator complete (commit)
+    uint64_t *a_full = empty_p + SP;          // [kAPairs] A codes of a packed stage in TMEM (4)
+    uint64_t *a_empty = a_full + APR;         // [kAPairs] consumed (commit)
+    uint64_t *b_full = a_empty + APR;         // [kBPairs] B codes of a packed stage in smem (NB)
+    uint64_t *b_empty = b_full + BPR;         // [kBPairs] consumed (commit)
+    uint64_t *acc_full = b_empty + BPR;       // [2] accumulator complete (commit)
     uint64_t *acc_empty = acc_full + 2;       // [2] accumulator drained (4 epilogue warps)
     uint64_t *sum_full = acc_empty + 2;       // [2] row sums of a unit written
     uint64_t *sum_empty = sum_full + 2;       // [2] row sums of a unit read (4 epilogue warps)
@@ -242,11 +248,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             mbar_init(&full_p[s], 1);
             mbar_init(&empty_p[s], 4 + NB);
         }
-        for (int s = 0; s < AST; ++s) {
+        for (int s = 0; s < APR; ++s) {
             mbar_init(&a_full[s], 4);
             mbar_init(&a_empty[s], 1);
         }
-        for (int s = 0; s < SO; ++s) {
+        for (int s = 0; s < BPR; ++s) {
             mbar_init(&b_full[s], NB);
             mbar_init(&b_empty[s], 1);
         }
@@ -318,6 +324,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_e4m3_f32(kPRows, Cfg::kQRows);
+            const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(opB));
             Ring ra, rb, racc;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < prm.num_units; u += gridDim.x, racc.next(Cfg::kAccBufs)) {
@@ -325,18 +332,32 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 const uint32_t d_tmem = tmem + racc.idx * Cfg::kAccCols;
                 if (!wait_bounded(&acc_empty[racc.idx], racc.phase ^ 1u, wd)) break;
                 tc_fence_after();
-                for (int i = 0; i < x.nkb; ++i, ra.next(AST), rb.next(SO)) {
+                // one packed stage (k blocks i, i + 1) per barrier round trip
+                for (int i = 0; i < x.nkb; i += 2, ra.next(APR), rb.next(BPR)) {
                     if (!wait_bounded(&a_full[ra.idx], ra.phase, wd) || !wait_bounded(&b_full[rb.idx], rb.phase, wd)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_col = tmem + Cfg::kACol0 + ra.idx * kAStageCols;
-                    const uint32_t b_base = smem_u32(opB + rb.idx * Cfg::kOpB);
+                    // descriptors differ from the ring base's only in the start-address
+                    // field (address >> 4, no carry below 256 KB of shared memory)
+                    const uint32_t a0 = tmem + Cfg::kACol0 + 2 * ra.idx * kAStageCols;
+                    const uint64_t b0 = bdesc0 + static_cast<uint64_t>((2 * rb.idx * Cfg::kOpB) >> 4);
+                    const uint32_t acc0 = i > 0 ? 1u : 0u;
+                    if (x.nkb - i >= 2) {
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 32; ++kk)
-                        mma_f8f6f4_tmem_a(d_tmem, a_col + 8 * kk, sdesc_kmajor_sw128(b_base + 32 * kk), idesc,
-                                          (i > 0 || kk > 0) ? 1u : 0u);
+                        for (int q = 0; q < 2 * (kBK / 32); ++q) {
+                            const int h = q / (kBK / 32), kk = q % (kBK / 32);
+                            mma_f8f6f4_tmem_a(d_tmem, a0 + h * kAStageCols + 8 * kk,
+                                              b0 + static_cast<uint64_t>(h * (Cfg::kOpB >> 4) + 2 * kk), idesc,
+                                              q > 0 ? 1u : acc0);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 32; ++kk)
+                            mma_f8f6f4_tmem_a(d_tmem, a0 + 8 * kk, b0 + static_cast<uint64_t>(2 * kk), idesc,
+                                              kk > 0 ? 1u : acc0);
+                    }
                     mma_commit(&a_empty[ra.idx]);
                     mma_commit(&b_empty[rb.idx]);
                 }
@@ -396,14 +417,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     fence_proxy_async_smem();  // reads done before the TMA refills the stage
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty_p[rp.idx]);
+                    if (!warp_wait(&b_empty[rb.idx], rb.phase ^ 1u, wd)) {
+                        ok = false;
+                        break;
+                    }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         if (h >= nk) break;
-                        if (!warp_wait(&b_empty[rb.idx], rb.phase ^ 1u, wd)) {
-                            ok = false;
-                            break;
-                        }
-                        uint8_t *dst = opB + rb.idx * Cfg::kOpB;
+                        uint8_t *dst = opB + (2 * rb.idx + h) * Cfg::kOpB;
 #pragma unroll
                         for (int j = 0; j < Cfg::kQIter; ++j) {
                             if (t + 32 * NB * j < Cfg::kQItems) {
@@ -414,11 +435,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                                     make_uint4(nib_lo(q.z), nib_hi(q.z), nib_lo(q.w), nib_hi(q.w));
                             }
                         }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&b_full[rb.idx]);
-                        rb.next(SO);
                     }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&b_full[rb.idx]);
+                    rb.next(BPR);
                 } else {
                     uint4 xa[2][Cfg::kQIter], xb[2][Cfg::kQIter];
 #pragma unroll
@@ -432,14 +453,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     fence_proxy_async_smem();  // reads done before the TMA refills the stage
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty_p[rp.idx]);
+                    if (!warp_wait(&b_empty[rb.idx], rb.phase ^ 1u, wd)) {
+                        ok = false;
+                        break;
+                    }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         if (h >= nk) break;
-                        if (!warp_wait(&b_empty[rb.idx], rb.phase ^ 1u, wd)) {
-                            ok = false;
-                            break;
-                        }
-                        uint8_t *dst = opB + rb.idx * Cfg::kOpB;
+                        uint8_t *dst = opB + (2 * rb.idx + h) * Cfg::kOpB;
 #pragma unroll
                         for (int j = 0; j < Cfg::kQIter; ++j) {
                             if (t + 32 * NB * j < Cfg::kQItems) {
@@ -469,11 +490,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                                                od[3] & 0x0F0F0F0Fu);
                             }
                         }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&b_full[rb.idx]);
-                        rb.next(SO);
                     }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&b_full[rb.idx]);
+                    rb.next(BPR);
                 }
                 if (!ok) break;
             }
@@ -515,8 +536,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             for (int i = 0; i < x.nkb; i += 2, ++gs, rp.next(SP)) {
                 const int nk = min(2, x.nkb - i);
                 if (ASETS > 1 && static_cast<int>(gs % ASETS) != set) {
-                    ra.next(AST);
-                    if (nk == 2) ra.next(AST);
+                    ra.next(APR);
                     continue;
                 }
                 if (!warp_wait(&full_p[rp.idx], rp.phase, wd)) {
@@ -535,6 +555,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty_p[rp.idx]);
+                if (!warp_wait(&a_empty[ra.idx], ra.phase ^ 1u, wd)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();  // the MMAs that read this TMEM pair are done
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     if (h >= nk) break;
@@ -563,19 +588,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j) code[j] = kOnes;
                     }
-                    if (!warp_wait(&a_empty[ra.idx], ra.phase ^ 1u, wd)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();  // the MMAs that read this ring stage are done
-                    tmem_st_32x32b_x32(trow + ra.idx * kAStageCols, code);
+                    tmem_st_32x32b_x32(trow + (2 * ra.idx + h) * kAStageCols, code);
                     tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&a_full[ra.idx]);
-                    ra.next(AST);
                 }
-                if (!ok) break;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[ra.idx]);
+                ra.next(APR);
             }
             if (!ok) break;
             if (!warp_wait(&sum_empty[rs.idx], rs.phase ^ 1u, wd)) break;

@@ -15,7 +15,7 @@
 namespace igemm {
 
 //                         W4A8  QA  SP  SO  NB  A stages  A sets  ones row  staging
-using CfgW4A8 = KernelCfg<true, 96, 3, 3, 8, 4, 1, false, 1>;
+using CfgW4A8 = KernelCfg<true, 96, 2, 4, 8, 4, 1, false, 1>;
 using CfgW4A8Skinny = KernelCfg<true, 16, 8, 4, 2, 8, 2, false, 1>;
 //                    W4A8  BN  stages
 using CfgW4A8Ss = SsCfg<true, 256, 4, 2>;

@@ -30,6 +30,13 @@ int make_map(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint
 int *device_status_word();
 // Counts one kernel launch of this library (igemm_kernels_launched).
 void note_launch();
+// Events armed by igemm_time_next_gemm (null when none): recorded on the
+// stream right before and right after the next GEMM kernel launch of this
+// thread, then disarmed.
+struct GemmEvents {
+    cudaEvent_t start, stop;
+};
+GemmEvents take_gemm_events();
 unsigned long long watchdog_limit_ns();
 int sm_count();
 
@@ -79,8 +86,11 @@ int launch_gemm(const CUtensorMap &mapA, const CUtensorMap &mapB, const CUtensor
     if (!prm.status) return kCudaError;
     if (plan.split > 1 && cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 4, stream) != cudaSuccess)
         return kCudaError;
+    const GemmEvents ev = take_gemm_events();
+    if (ev.start && cudaEventRecord(ev.start, stream) != cudaSuccess) return kCudaError;
     kernel<<<plan.ctas, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mapA, mapB, mapC32, mapC31, prm);
     note_launch();
+    if (ev.stop && cudaEventRecord(ev.stop, stream) != cudaSuccess) return kCudaError;
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
 }
 
@@ -180,6 +190,8 @@ int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMa
     if (plan.split > 1 && cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 4, stream) != cudaSuccess)
         return kCudaError;
     const int clusters = std::min(prm.num_units, resident / Cfg::CL);
+    const GemmEvents ev = take_gemm_events();
+    if (ev.start && cudaEventRecord(ev.start, stream) != cudaSuccess) return kCudaError;
     if constexpr (Cfg::CL == 1) {
         kernel<<<clusters, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mapP, mapQ, mapC, prm);
     } else {
@@ -198,6 +210,7 @@ int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMa
         if (cudaLaunchKernelEx(&cfg, kernel, mapP, mapQ, mapC, prm) != cudaSuccess) return kCudaError;
     }
     note_launch();
+    if (ev.stop && cudaEventRecord(ev.stop, stream) != cudaSuccess) return kCudaError;
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
 }
 

@@ -263,6 +263,26 @@ def test_kernel_launch_counter():
     assert (n1 - n0, n2 - n1, n3 - n2) == (2, 1, 0)
 
 
+def test_gemm_kernel_timing_hook():
+    # the armed events bracket the GEMM kernel of the next call only
+    a = torch.zeros((512, 64), dtype=torch.uint8, device="cuda")
+    C = torch.empty((512, 512), dtype=torch.int32, device="cuda")
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for ev in (s0, s1):
+        ev.record()
+    torch.cuda.synchronize()
+    pig.igemm_time_next_gemm(s0, s1)
+    pig.i4i4_gemm(a, a, C, 512, 512, 128)
+    torch.cuda.synchronize()
+    first = s0.elapsed_time(s1)
+    assert first > 0.0
+    pig.i4i4_gemm(a, a, C, 512, 512, 128)  # not armed: the events keep their times
+    torch.cuda.synchronize()
+    assert s0.elapsed_time(s1) == first
+    with pytest.raises(pig.IgemmError):
+        pig.igemm_time_next_gemm(0, 0)
+
+
 def test_empty_and_zero_k():
     C = torch.full((4, 4), 7, dtype=torch.int32, device="cuda")
     pig.i4i4_gemm(None, None, C, 0, 4, 64)
