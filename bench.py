@@ -85,6 +85,8 @@ def recorded_traffic(workload):
 
 
 def workload_bytes(variant, M, N, K):
+    if variant == "fp8":
+        return (M + N) * K + 4 * M * N
     a = M * K if variant == "w4a8" else M * K // 2
     return a + N * K // 2 + 4 * M * N
 
@@ -153,7 +155,9 @@ class ClockSampler:
 def oracle_sample_time(orc, variant, a, b, K, rows, threads):
     """Run the oracle on the first `rows` rows of A; returns seconds."""
     t0 = time.perf_counter()
-    if variant == "i4i4":
+    if variant == "fp8":
+        orc.fp8_gemm(np.ascontiguousarray(a[:rows]), b, K, threads=threads)
+    elif variant == "i4i4":
         orc.i4i4_gemm(orc.pack_int4(a[:rows]), orc.pack_int4(b), K, threads=threads)
     else:
         orc.w4a8_gemm(np.ascontiguousarray(a[:rows]), orc.pack_int4(b), K, threads=threads)
@@ -210,9 +214,15 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
     # operands resident in HBM: logical -> packed by the library's pack kernel
     a_dev = torch.from_numpy(a).cuda()
     b_dev = torch.from_numpy(b).cuda()
-    bp = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
-    pig.pack_int4(b_dev, bp, N, K)
-    if variant == "i4i4":
+    if variant == "fp8":
+        bp = b_dev  # E4M3 bytes as they are
+    else:
+        bp = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
+        pig.pack_int4(b_dev, bp, N, K)
+    if variant == "fp8":
+        a_in = a_dev
+        gemm = pig.fp8_gemm
+    elif variant == "i4i4":
         a_in = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
         pig.pack_int4(a_dev, a_in, M, K)
         gemm = pig.i4i4_gemm
@@ -220,7 +230,7 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
         a_in = a_dev
         gemm = pig.w4a8_gemm
     del b_dev
-    C = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    C = torch.empty((M, N), dtype=torch.float32 if variant == "fp8" else torch.int32, device="cuda")
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     torch.cuda.synchronize()
 
@@ -278,7 +288,7 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
     e2e_steps = max(1, min(args.steps, 5))
     a_host = (a_in.cpu() if variant == "i4i4" else torch.from_numpy(a)).pin_memory()
     bp_host = bp.cpu().pin_memory()
-    c_host = torch.empty((M, N), dtype=torch.int32).pin_memory()
+    c_host = torch.empty((M, N), dtype=C.dtype).pin_memory()
     a_e, bp_e = torch.empty_like(a_in), torch.empty_like(bp)
     C_e = torch.empty_like(C)
     e_s = torch.cuda.Event(enable_timing=True)
@@ -313,12 +323,13 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
                 "frac": achieved / peak, "traffic": traffic, "kernel": "igemm_ss_kernel",
                 "kernel_ms": 1e3 * gemm_kernel_s, "algorithmic_ops_per_launch": ops,
                 "peak_source": f"{peak_src} bf16 burst x {E4M3_PER_BF16} (nominal e4m3/bf16 ratio)",
-                "mma_macs_per_op": 1 if variant == "i4i4" else 2}
+                "mma_macs_per_op": 2 if variant == "w4a8" else 1}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int4" if variant == "i4i4" else "int8xint4",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {"i4i4": "int4", "w4a8": "int8xint4", "fp8": "e4m3 (float32 accumulate)"}[variant],
         "data": "synthetic (SplitMix64-seeded, uniform)",
         "config": {"workload": args.workload, "variant": variant, "M": M, "N": N, "K": K,
                    "l2": "flushed before every step (256 MB write, outside the timed events)",

@@ -28,8 +28,8 @@
  * Shape and alignment rules (violations are returned, never launched)
  *   M, N, K >= 0; M == 0 or N == 0 is an empty product (no work, IGEMM_OK);
  *   K == 0 with M, N > 0 sets C to zero.
- *   K % 32 == 0 (a packed row is a whole number of 16-byte units, the TMA
- *   row-pitch rule) else IGEMM_UNSUPPORTED_SHAPE.
+ *   K % 32 == 0 for the integer GEMMs (a packed row is a whole number of
+ *   16-byte units, the TMA row-pitch rule) else IGEMM_UNSUPPORTED_SHAPE.
  *   K <= 65536 else IGEMM_OVERFLOW_BOUND: the accumulation is exact only up to
  *   this depth (the int32 result itself would fit far beyond it).
  *   Every non-empty operand base address and C must be 16-byte aligned, else
@@ -116,6 +116,24 @@ IGEMM_API int i4i4_gemm_noalloc(const uint8_t *Ap, const uint8_t *Bp, int32_t *C
 IGEMM_API int w4a8_gemm(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);
 
 /*
+ * fp8 GEMM:  C[m,n] = sum_k a[m,k] * b[n,k] for E4M3 operands, accumulated in
+ * float32 (TileLang tutorial page low_precision_gemm.py, gemm_fp8: A (M,K) and
+ * B (N,K) in an fp8 dtype, float32 accumulator, C = A . B^T).  The page writes C
+ * in the operands' fp8 dtype; this entry point returns the float32
+ * accumulator itself (rounding it to fp8 is the caller's choice).
+ *   A   [M, K] E4M3 bytes (device), read only
+ *   B   [N, K] E4M3 bytes (device), read only
+ *   C   [M, N] float32 (device), written
+ * K % 16 == 0 (IGEMM_UNSUPPORTED_SHAPE otherwise; the TMA row pitch).  The
+ * order of the float32 additions is not specified: when the launch splits K
+ * (few output tiles, deep K) the partial sums meet through atomic adds, so the
+ * last bits can differ from call to call.  Other rules as for i4i4_gemm
+ * (K == 0 zeroes C, 16-byte alignment, empty shapes are no-ops); there is no
+ * K limit.
+ */
+IGEMM_API int fp8_gemm(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, cudaStream_t stream);
+
+/*
  * Pack logical int4 values two per byte (TileLang tutorial page
  * low_precision_gemm.py, pack_int4): packed[r, j] = (logical[r, 2j] & 0xF) |
  * ((logical[r, 2j+1] & 0xF) << 4).  Values outside [-8, 7] are masked to four
@@ -146,6 +164,19 @@ IGEMM_API uint64_t igemm_kernels_launched(void);
  * event.
  */
 IGEMM_API int igemm_time_next_gemm(cudaEvent_t start, cudaEvent_t stop);
+
+/*
+ * Unpack int4 values to int8, the inverse of pack_int4: logical[r, 2j + p] is
+ * nibble p (p = 0: low) of packed[r, j], sign-extended from 4 bits, so every
+ * value lies in [-8, 7].  This is the conversion the W4A8 page applies to the
+ * weights inside its kernel ("[Example] add w4a8 gemm kernel", tilelang PR
+ * #815, _tir_u8_to_i4_to_i8: pos 0 = low nibble), as a standalone pass.
+ *   packed  [rows, K/2] bytes (device), read only
+ *   logical [rows, K] int8 (device), written
+ * K must be even (IGEMM_UNSUPPORTED_SHAPE otherwise); rows == 0 or K == 0 is a
+ * no-op.  Any alignment is accepted.
+ */
+IGEMM_API int unpack_int4(const uint8_t *packed, int8_t *logical, int64_t rows, int64_t K, cudaStream_t stream);
 
 /* Static, human-readable text for an igemm_status value. */
 IGEMM_API const char *igemm_strerror(int code);

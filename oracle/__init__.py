@@ -52,6 +52,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.argtypes = [p, p, p, i64, i64, i64, ctypes.c_int]
         fn.restype = ctypes.c_int
+    lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_value.restype = ctypes.c_double
+    lib.oracle_fp8_gemm.argtypes = [p, p, p, p, i64, i64, i64, ctypes.c_int]
+    lib.oracle_fp8_gemm.restype = ctypes.c_int
     for name in ("oracle_i4i4_entries", "oracle_w4a8_entries"):
         fn = getattr(lib, name)
         fn.argtypes = [p, p, i64, p, p, i64, p]
@@ -148,3 +152,23 @@ class Oracle:
         out = np.empty(ms.shape[0], dtype=np.int64)
         self.lib.oracle_w4a8_entries(_ptr(A), _ptr(Bp), K, _ptr(ms), _ptr(ns), ms.shape[0], _ptr(out))
         return out
+
+    def e4m3_value(self, codes: np.ndarray) -> np.ndarray:
+        """float64 value of each E4M3 byte (NaN for S.1111.111)."""
+        codes = np.asarray(codes, dtype=np.uint8)
+        table = np.array([self.lib.oracle_e4m3_value(c) for c in range(256)], dtype=np.float64)
+        return table[codes]
+
+    def fp8_gemm(self, A: np.ndarray, B: np.ndarray, K: int, threads: int | None = None):
+        """(C, Cabs): C = A . B^T of E4M3 bytes A [M,K], B [N,K] in float64, and the
+        sum of the products' magnitudes per element (the scale of any rounding)."""
+        A = np.ascontiguousarray(A).view(np.uint8)
+        B = np.ascontiguousarray(B).view(np.uint8)
+        M, N = A.shape[0], B.shape[0]
+        assert A.shape[1] == K and B.shape[1] == K
+        C = np.empty((M, N), dtype=np.float64)
+        Cabs = np.empty((M, N), dtype=np.float64)
+        rc = self.lib.oracle_fp8_gemm(_ptr(A), _ptr(B), _ptr(C), _ptr(Cabs), M, N, K, threads or default_threads())
+        if rc:
+            raise RuntimeError(f"oracle_fp8_gemm failed ({rc})")
+        return C, Cabs

@@ -203,3 +203,83 @@ void oracle_w4a8_entries(const int8_t *A, const uint8_t *Bp, int64_t K, const in
     }
     free(b);
 }
+
+/* ---------------------------------------------------------------- fp8 GEMM
+ * TileLang tutorial low_precision_gemm.py, gemm_fp8: A (M,K) and B (N,K) in an
+ * fp8 dtype, C = A . B^T accumulated in float32 (accum_dtype).  The oracle
+ * takes the plain definition in double: every fp8 value is exact in double and
+ * so is every product; the sum of K products is kept in double next to the sum
+ * of their magnitudes, which bounds the rounding of any float32 accumulation
+ * order.
+ *
+ * E4M3 ("fn" variant of the OCP 8-bit floating point formats): 1 sign bit, 4
+ * exponent bits with bias 7, 3 mantissa bits; exponent 0 holds the subnormals
+ * m/8 * 2^-6; S.1111.111 is NaN; there are no infinities (largest finite 448).
+ */
+double oracle_e4m3_value(uint8_t byte)
+{
+    int s = byte >> 7, e = (byte >> 3) & 15, m = byte & 7;
+    if (e == 15 && m == 7) return 0.0 / 0.0;
+#if ORACLE_MUTANT == 6 /* planted: exponent bias 8 instead of 7 */
+    double v = e == 0 ? (m / 8.0) / 128.0 : (1.0 + m / 8.0) * (double)(1u << e) / 256.0;
+#else
+    double v = e == 0 ? (m / 8.0) / 64.0 : (1.0 + m / 8.0) * (double)(1u << e) / 128.0;
+#endif
+    return s ? -v : v;
+}
+
+struct fjob {
+    const double *a, *b;
+    double *c, *cabs;
+    int64_t N, K, m_begin, m_end;
+};
+
+static void *run_rows_f(void *arg)
+{
+    struct fjob *j = (struct fjob *)arg;
+    for (int64_t m = j->m_begin; m < j->m_end; ++m) {
+        for (int64_t n = 0; n < j->N; ++n) {
+            const double *ar = j->a + m * j->K, *br = j->b + n * j->K;
+            double s = 0.0, sa = 0.0;
+            for (int64_t k = 0; k < j->K; ++k) {
+                const double p = ar[k] * br[k];
+                s += p;
+                sa += p < 0 ? -p : p;
+            }
+            j->c[m * j->N + n] = s;
+            j->cabs[m * j->N + n] = sa;
+        }
+    }
+    return NULL;
+}
+
+/* A [M, K], B [N, K] e4m3 bytes; C [M, N] = sum_k a*b and Cabs = sum_k |a*b| in
+ * double.  Returns 0, or -1 on an allocation error. */
+int oracle_fp8_gemm(const uint8_t *A, const uint8_t *B, double *C, double *Cabs, int64_t M, int64_t N,
+                    int64_t K, int nthreads)
+{
+    double *a = (double *)malloc(sizeof(double) * (size_t)(M * K));
+    double *b = (double *)malloc(sizeof(double) * (size_t)(N * K));
+    if (!a || !b) { free(a); free(b); return -1; }
+    for (int64_t i = 0; i < M * K; ++i) a[i] = oracle_e4m3_value(A[i]);
+    for (int64_t i = 0; i < N * K; ++i) b[i] = oracle_e4m3_value(B[i]);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > M) nthreads = (int)(M > 0 ? M : 1);
+    struct fjob *jobs = (struct fjob *)calloc((size_t)nthreads, sizeof(struct fjob));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tids) { free(a); free(b); free(jobs); free(tids); return -1; }
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = (struct fjob){a, b, C, Cabs, N, K, M * t / nthreads, M * (t + 1) / nthreads};
+        if (pthread_create(&tids[t], NULL, run_rows_f, &jobs[t]) != 0) {
+            run_rows_f(&jobs[t]);
+            tids[t] = 0;
+        }
+    }
+    for (int t = 0; t < nthreads; ++t)
+        if (tids[t]) pthread_join(tids[t], NULL);
+    free(jobs);
+    free(tids);
+    free(a);
+    free(b);
+    return 0;
+}

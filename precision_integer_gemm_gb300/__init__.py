@@ -18,12 +18,13 @@ import os
 from .build import LIB_PATH, build as build_library
 
 __all__ = [
-    "IgemmError", "load", "i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "pack_int4", "igemm_strerror",
+    "IgemmError", "load", "i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "fp8_gemm", "pack_int4", "unpack_int4",
+    "igemm_strerror",
     "igemm_last_status", "igemm_watchdog_selftest", "igemm_kernels_launched", "igemm_time_next_gemm",
     "EXPORTED_SYMBOLS", "LIB_PATH", "build_library",
 ]
 
-EXPORTED_SYMBOLS = ("i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "pack_int4", "igemm_strerror", "igemm_last_status",
+EXPORTED_SYMBOLS = ("i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "fp8_gemm", "pack_int4", "unpack_int4", "igemm_strerror", "igemm_last_status",
                     "igemm_watchdog_selftest", "igemm_kernels_launched",
                     "igemm_time_next_gemm")
 
@@ -66,10 +67,14 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.i4i4_gemm.restype = i
     lib.i4i4_gemm_noalloc.argtypes = [p, p, p, i, i, i, p]
     lib.i4i4_gemm_noalloc.restype = i
+    lib.fp8_gemm.argtypes = [p, p, p, i, i, i, p]
+    lib.fp8_gemm.restype = i
     lib.w4a8_gemm.argtypes = [p, p, p, i, i, i, p]
     lib.w4a8_gemm.restype = i
     lib.pack_int4.argtypes = [p, p, i64, i64, p]
     lib.pack_int4.restype = i
+    lib.unpack_int4.argtypes = [p, p, i64, i64, p]
+    lib.unpack_int4.restype = i
     lib.igemm_strerror.argtypes = [i]
     lib.igemm_strerror.restype = ctypes.c_char_p
     lib.igemm_last_status.argtypes = [p]
@@ -123,9 +128,19 @@ def w4a8_gemm(A, Bp, C, M: int, N: int, K: int, stream=None) -> None:
     _check(load().w4a8_gemm(_ptr(A), _ptr(Bp), _ptr(C), M, N, K, _stream(stream)), "w4a8_gemm")
 
 
+def fp8_gemm(A, B, C, M: int, N: int, K: int, stream=None) -> None:
+    """C[M,N] (float32) = A . B^T for E4M3 byte matrices A [M,K] and B [N,K]."""
+    _check(load().fp8_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(stream)), "fp8_gemm")
+
+
 def pack_int4(logical, packed, rows: int, K: int, stream=None) -> None:
     """packed [rows,K/2] = two int4 values per byte of logical [rows,K] (low nibble = even k)."""
     _check(load().pack_int4(_ptr(logical), _ptr(packed), rows, K, _stream(stream)), "pack_int4")
+
+
+def unpack_int4(packed, logical, rows: int, K: int, stream=None) -> None:
+    """logical [rows,K] int8 = the sign-extended nibbles of packed [rows,K/2] (low nibble = even k)."""
+    _check(load().unpack_int4(_ptr(packed), _ptr(logical), rows, K, _stream(stream)), "unpack_int4")
 
 
 def igemm_strerror(code: int) -> str:

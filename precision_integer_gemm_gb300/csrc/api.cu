@@ -83,7 +83,7 @@ int make_map(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint
 {
     auto fn = encode_tiled();
     if (!fn) return kCudaError;
-    const uint64_t esize = dtype == CU_TENSOR_MAP_DATA_TYPE_INT32 ? 4 : 1;
+    const uint64_t esize = (dtype == CU_TENSOR_MAP_DATA_TYPE_INT32 || dtype == CU_TENSOR_MAP_DATA_TYPE_FLOAT32) ? 4 : 1;
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * esize};
     const cuuint32_t box[2] = {box_cols, box_rows};
@@ -146,6 +146,40 @@ __global__ void pack_int4_kernel(const int8_t *__restrict__ logical, uint8_t *__
     }
     for (int64_t j = n_vec * 16 + t0; j < n_out; j += stride) {
         packed[j] = static_cast<uint8_t>((logical[2 * j] & 0xF) | ((logical[2 * j + 1] & 0xF) << 4));
+    }
+}
+
+// ---------------------------------------------------------------- unpack_int4
+// Inverse of pack_int4: nibble p of byte j -> logical element 2j + p, sign
+// extended from 4 to 8 bits.  16 packed bytes (32 values) per vector step.
+__device__ __forceinline__ uint32_t sext_nibbles(uint32_t n)  // four nibbles in the low halves of four bytes
+{
+    return __vsub4(n ^ 0x08080808u, 0x08080808u);  // (n ^ 8) - 8 per byte, no borrow between bytes
+}
+
+__global__ void unpack_int4_kernel(const uint8_t *__restrict__ packed, int8_t *__restrict__ logical, int64_t n_in,
+                                   int64_t n_vec)
+{
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    const int64_t t0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (int64_t u = t0; u < n_vec; u += stride) {
+        const uint4 p = reinterpret_cast<const uint4 *>(packed)[u];
+        const uint32_t x[4] = {p.x, p.y, p.z, p.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t lo = sext_nibbles(x[j] & 0x0F0F0F0Fu);         // even elements
+            const uint32_t hi = sext_nibbles((x[j] >> 4) & 0x0F0F0F0Fu);  // odd elements
+            o[2 * j] = __byte_perm(lo, hi, 0x5140);
+            o[2 * j + 1] = __byte_perm(lo, hi, 0x7362);
+        }
+        reinterpret_cast<uint4 *>(logical)[2 * u] = make_uint4(o[0], o[1], o[2], o[3]);
+        reinterpret_cast<uint4 *>(logical)[2 * u + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+    for (int64_t j = n_vec * 16 + t0; j < n_in; j += stride) {
+        const int b = packed[j];
+        logical[2 * j] = static_cast<int8_t>(((b & 0xF) ^ 8) - 8);
+        logical[2 * j + 1] = static_cast<int8_t>((((b >> 4) & 0xF) ^ 8) - 8);
     }
 }
 
@@ -218,6 +252,19 @@ extern "C" int i4i4_gemm_noalloc(const uint8_t *Ap, const uint8_t *Bp, int32_t *
     return launch_i4i4_noalloc(Ap, Bp, C, M, N, K, stream);
 }
 
+extern "C" int fp8_gemm(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, cudaStream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0) return kInvalidArgument;
+    if (M == 0 || N == 0) return kOk;
+    if (!C) return kInvalidArgument;
+    if (K % 16 != 0) return kUnsupportedShape;
+    if (!aligned16(C)) return kMisaligned;
+    if (K == 0) return cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 4, stream) == cudaSuccess ? kOk : kCudaError;
+    if (!A || !B) return kInvalidArgument;
+    if (!aligned16(A) || !aligned16(B)) return kMisaligned;
+    return launch_fp8(A, B, C, M, N, K, stream);
+}
+
 extern "C" int pack_int4(const int8_t *logical, uint8_t *packed, int64_t rows, int64_t K, cudaStream_t stream)
 {
     if (rows < 0 || K < 0) return kInvalidArgument;
@@ -236,12 +283,32 @@ extern "C" int pack_int4(const int8_t *logical, uint8_t *packed, int64_t rows, i
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
 }
 
+extern "C" int unpack_int4(const uint8_t *packed, int8_t *logical, int64_t rows, int64_t K, cudaStream_t stream)
+{
+    if (rows < 0 || K < 0) return kInvalidArgument;
+    if (K % 2 != 0) return kUnsupportedShape;
+    if (rows == 0 || K == 0) return kOk;
+    if (!packed || !logical) return kInvalidArgument;
+    const int64_t n_in = rows * (K / 2);
+    const int64_t n_vec = (aligned16(logical) && aligned16(packed)) ? n_in / 16 : 0;
+    const int64_t work = n_vec > 0 ? n_vec : n_in;
+    int64_t blocks = (work + 255) / 256;
+    const int64_t cap = int64_t(sm_count()) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    unpack_int4_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(packed, logical, n_in, n_vec);
+    note_launch();
+    return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
+}
+
 extern "C" const char *igemm_strerror(int code)
 {
     switch (code) {
     case kOk: return "ok";
     case kInvalidArgument: return "invalid argument (null pointer for a non-empty operand, or a negative size)";
-    case kUnsupportedShape: return "unsupported shape (GEMM: K must be a multiple of 32; pack_int4: K must be even)";
+    case kUnsupportedShape:
+        return "unsupported shape (integer GEMMs: K must be a multiple of 32; fp8_gemm: of 16; pack_int4 and "
+               "unpack_int4: K must be even)";
     case kMisaligned: return "misaligned pointer (operand and C base addresses must be 16-byte aligned)";
     case kOverflowBound: return "K above the exact-accumulation bound (65536)";
     case kCudaError: return "CUDA error (tensor-map encoding, memset, launch or synchronization failed)";

@@ -41,9 +41,11 @@
 
 namespace igemm {
 
-template <bool W4A8, int BN_, int ST_, int CL_ = 1>
+template <bool W4A8, int BN_, int ST_, int CL_ = 1, bool FLOAT_ = false>
 struct SsCfg {
     static constexpr bool kW4A8 = W4A8;
+    // kFloat: plain e4m3 operands (the fp8 GEMM), C = the float32 accumulator
+    static constexpr bool kFloat = FLOAT_;
     static constexpr int kQRows = BN_;                 // MMA N
     static constexpr int QA = W4A8 ? BN_ / 2 : BN_;    // Q source rows per tile
     static constexpr int ST = ST_;                     // pipeline stages
@@ -76,6 +78,7 @@ struct SsCfg {
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
     static_assert(ST <= 32, "stage masks");
     static_assert(CL == 1 || CL == 2, "cluster size");
+    static_assert(!(FLOAT_ && W4A8), "the fp8 GEMM uses the int4 x int4 tile layout");
     static_assert(W4A8 || kQBoxRows % 8 == 0, "Q half tiles start on 1024-byte boundaries");
 };
 
@@ -309,7 +312,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const bool magic = x.nkb * Cfg::kBK <= 16384;  // every code sum below 2^22
             const bool first = x.kb0 == 0;                  // the split that adds the row-sum terms
             const int prow = min(x.p0 + p, prm.p_rows - 1);
-            const int sp = first ? __ldg(prm.sumP + prow) : 0;
+            int sp = 0;
+            if constexpr (!Cfg::kFloat) sp = first ? __ldg(prm.sumP + prow) : 0;
             if constexpr (!Cfg::kW4A8) {
                 // C[m, n] = S - 8 sum uA[m] - 8 sum uB[n] + 64 K   (first split adds the terms)
                 const int m = x.p0 + p;
@@ -321,20 +325,22 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     tmem_ld_32x32b_x32(tacc + c0, v);
                     tmem_ld_wait();
                     const int n0 = x.q0 + c0;
-                    // -8 sum uB of the chunk's 32 columns (the sums array is padded
-                    // past the last row, so whole chunks are readable)
-                    const int4 *sq = reinterpret_cast<const int4 *>(prm.sumQ + n0);
+                    if constexpr (!Cfg::kFloat) {
+                        // -8 sum uB of the chunk's 32 columns (the sums array is padded
+                        // past the last row, so whole chunks are readable)
+                        const int4 *sq = reinterpret_cast<const int4 *>(prm.sumQ + n0);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int4 q = first ? __ldg(sq + j) : make_int4(0, 0, 0, 0);
-                        const int qq[4] = {q.x, q.y, q.z, q.w};
+                        for (int j = 0; j < 8; ++j) {
+                            const int4 q = first ? __ldg(sq + j) : make_int4(0, 0, 0, 0);
+                            const int qq[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int i = 4 * j + e;
-                            v[i] = (magic ? ss_magic(v[i]) : static_cast<uint32_t>(ss_exact(v[i]))) + rowterm +
-                                   static_cast<uint32_t>(-8 * qq[e]);
+                            for (int e = 0; e < 4; ++e) {
+                                const int i = 4 * j + e;
+                                v[i] = (magic ? ss_magic(v[i]) : static_cast<uint32_t>(ss_exact(v[i]))) + rowterm +
+                                       static_cast<uint32_t>(-8 * qq[e]);
+                            }
                         }
-                    }
+                    }  // else: v holds the float32 sums, stored as they are
                     if (prm.tma_store) {
                         if (lane == 0) bulk_wait_group_read<0>();
                         __syncwarp();
@@ -357,7 +363,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             if (n0 + i < prm.N) {
-                                if (reduce)
+                                if (Cfg::kFloat && reduce)
+                                    atomicAdd(reinterpret_cast<float *>(crow) + n0 + i, __uint_as_float(v[i]));
+                                else if (reduce)
                                     atomicAdd(crow + n0 + i, static_cast<int>(v[i]));
                                 else
                                     crow[n0 + i] = static_cast<int>(v[i]);

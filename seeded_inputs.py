@@ -68,6 +68,19 @@ def int8_values(seed: int, shape) -> np.ndarray:
     return out.reshape(shape)
 
 
+def e4m3_bytes(seed: int, shape) -> np.ndarray:
+    """E4M3 bytes uniform over the 254 finite codes, as uint8: the top byte
+    modulo 254 is x in [0, 253], and x >= 0x7F moves up by one, which skips
+    the NaN code 0x7F and ends at 0xFE (0xFF, the other NaN, never occurs)."""
+    n = int(np.prod(shape, dtype=np.int64))
+    out = np.empty(n, dtype=np.uint8)
+    for s in range(0, n, _CHUNK):
+        e = min(n, s + _CHUNK)
+        x = (splitmix64(seed, e - s, start=s) >> np.uint64(56)).astype(np.int64) % 254
+        out[s:e] = np.where(x >= 0x7F, x + 1, x).astype(np.uint8)
+    return out.reshape(shape)
+
+
 def workload_seed(index: int, operand: int) -> int:
     """Seed of operand 0 (A) or 1 (B) of workload ``index``."""
     return 0x1A2B0000 + 16 * index + operand
@@ -82,11 +95,16 @@ WORKLOADS = {
     "w4a8_decode_16x28672x8192": ("w4a8", 16, 28672, 8192, 4),
     "i4i4_8192": ("i4i4", 8192, 8192, 8192, 5),
     "w4a8_ragged_4000x12288x5120": ("w4a8", 4000, 12288, 5120, 6),
+    # the tutorial's fp8 GEMM (a "next" row): E4M3 operands, float32 C
+    "fp8_8192": ("fp8", 8192, 8192, 8192, 7),
 }
 
 
 def logical_operands(variant: str, M: int, N: int, K: int, index: int):
-    """Logical (unpacked) operands: A [M,K] int8 and B [N,K] int8 (int4 range)."""
+    """Logical (unpacked) operands: A [M,K] int8 and B [N,K] int8 (int4 range);
+    for "fp8", A [M,K] and B [N,K] E4M3 bytes."""
+    if variant == "fp8":
+        return e4m3_bytes(workload_seed(index, 0), (M, K)), e4m3_bytes(workload_seed(index, 1), (N, K))
     if variant == "i4i4":
         a = int4_values(workload_seed(index, 0), (M, K))
     elif variant == "w4a8":

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(lib):
     # nothing else leaks out of the library besides the declared entry points
     out = os.popen(f"nm -D --defined-only {pig.LIB_PATH}").read()
     ours = {line.split()[-1] for line in out.splitlines()
-            if " T " in line and re.match(r"^(i4i4|w4a8|pack|igemm)", line.split()[-1])}
+            if " T " in line and re.match(r"^(i4i4|w4a8|fp8|pack|unpack|igemm)", line.split()[-1])}
     assert ours == set(header_functions())
 
 
@@ -81,6 +81,13 @@ def test_pack_argument_validation(lib):
     assert lib.pack_int4(None, None, 0, 8, None) == pig.IGEMM_OK
     assert lib.pack_int4(None, None, 4, 0, None) == pig.IGEMM_OK
     assert lib.pack_int4(None, FAKE, 4, 8, None) == pig.IGEMM_INVALID_ARGUMENT
+
+
+def test_unpack_argument_validation(lib):
+    assert lib.unpack_int4(FAKE, FAKE, -1, 4, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert lib.unpack_int4(FAKE, FAKE, 4, 3, None) == pig.IGEMM_UNSUPPORTED_SHAPE
+    assert lib.unpack_int4(None, None, 0, 4, None) == pig.IGEMM_OK
+    assert lib.unpack_int4(None, FAKE, 4, 4, None) == pig.IGEMM_INVALID_ARGUMENT
 
 
 def test_watchdog_selftest_argument_validation(lib):

@@ -91,6 +91,30 @@ def test_pack_unaligned_pointers_take_the_scalar_path(orc):
     assert np.array_equal(out[1:].cpu().numpy().reshape(16, 32), orc.pack_int4(x))
 
 
+@pytest.mark.parametrize("rows,k", [(1, 2), (3, 30), (256, 2), (129, 96), (1000, 1024), (33, 4098)])
+def test_unpack_matches_oracle(orc, rows, k):
+    rng = np.random.default_rng(rows * 7 + k)
+    packed = rng.integers(0, 256, size=(rows, k // 2), dtype=np.uint8)
+    packed.reshape(-1)[: min(256, packed.size)] = np.arange(min(256, packed.size), dtype=np.uint8)  # every byte value
+    out = torch.full((rows, k), 99, dtype=torch.int8, device="cuda")
+    pig.unpack_int4(dev(packed), out, rows, k)
+    assert np.array_equal(out.cpu().numpy(), orc.unpack_int4(packed))
+
+
+def test_unpack_inverts_pack_and_takes_unaligned_pointers(orc):
+    x = si.int4_values(77, (16, 64))
+    packed = gpu_pack(x)
+    out = torch.empty((16, 64), dtype=torch.int8, device="cuda")
+    pig.unpack_int4(packed, out, 16, 64)
+    assert np.array_equal(out.cpu().numpy(), x)
+    # unaligned base addresses take the scalar path
+    src = torch.zeros(16 * 32 + 3, dtype=torch.uint8, device="cuda")
+    src[3:] = packed.view(-1)
+    dst = torch.zeros(16 * 64 + 1, dtype=torch.int8, device="cuda")
+    pig.unpack_int4(src.data_ptr() + 3, dst.data_ptr() + 1, 16, 64)
+    assert np.array_equal(dst[1:].cpu().numpy().reshape(16, 64), x)
+
+
 # ---------------------------------------------------------------- whole-C parity
 
 SMALL_I4I4 = [(256, 256, 256), (1, 1, 32), (1, 300, 96), (129, 257, 160), (300, 72, 384), (128, 256, 128),
@@ -141,6 +165,44 @@ def test_w4a8_prepared_codes_path(orc, M, N, K):
     b = si.int4_values(8000 + N + K, (N, K))
     C, bp = run_w4a8(a, b, orc)
     assert np.array_equal(C, orc.w4a8_gemm(a, bp, K))
+
+
+# ---------------------------------------------------------------- fp8 GEMM (E4M3, float32 accumulate)
+
+def run_fp8(A: np.ndarray, B: np.ndarray):
+    M, K = A.shape
+    N = B.shape[0]
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    pig.fp8_gemm(dev(A), dev(B), C, M, N, K)
+    assert pig.igemm_last_status() == 0
+    return C.cpu().numpy().astype(np.float64)
+
+
+FP8_SHAPES = [(1, 1, 16), (128, 256, 128), (300, 520, 96), (257, 300, 4112), (1000, 777, 2048), (256, 258, 128),
+              (128, 128, 65536)]
+
+
+@pytest.mark.parametrize("M,N,K", FP8_SHAPES)
+def test_fp8_matches_oracle(orc, M, N, K):
+    A = si.e4m3_bytes(11000 + M + K, (M, K))
+    B = si.e4m3_bytes(12000 + N + K, (N, K))
+    C = run_fp8(A, B)
+    want, mag = orc.fp8_gemm(A, B, K)
+    # float32 accumulation in any order: each of the K additions rounds by at most
+    # 2^-23 of a partial sum, and every partial sum is at most sum |a*b|
+    tol = K * 2.0 ** -23 * mag + 1e-30
+    assert np.all(np.abs(C - want) <= tol), float(np.max(np.abs(C - want) / np.maximum(mag, 1e-30)))
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 4096), (130, 300, 96), (128, 128, 65536)])
+def test_fp8_integer_codes_are_exact(orc, M, N, K):
+    # bytes 0..15 are the integers 0..15 times 2^-9; every partial sum is an integer
+    # times 2^-18 below 2^24 * 2^-18, so float32 holds C exactly in any order
+    A = (si.int4_values(13000 + M, (M, K)) + 8).astype(np.uint8)
+    B = (si.int4_values(14000 + N, (N, K)) + 8).astype(np.uint8)
+    C = run_fp8(A, B)
+    want = (A.astype(np.int64) @ B.astype(np.int64).T).astype(np.float64) * 2.0 ** -18
+    assert np.array_equal(C, want)
 
 
 def test_configured_small_workloads(orc):

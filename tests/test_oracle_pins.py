@@ -212,8 +212,44 @@ def check_entries(o):
             and np.array_equal(o.w4a8_entries(a8, bp, K, ms, ns), full8[ms, ns]))
 
 
+def check_e4m3_decode(o) -> bool:
+    # every E4M3 byte against PyTorch's float8_e4m3fn (a library decoder), NaNs included,
+    # and a few values written out from the format definition
+    torch = pytest.importorskip("torch")
+    mine = o.e4m3_value(np.arange(256))
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    if not np.array_equal(np.isnan(mine), np.isnan(lib)) or not np.array_equal(mine[~np.isnan(mine)], lib[~np.isnan(lib)]):
+        return False
+    want = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0x3C: 1.5, 0x7E: 448.0, 0xB8: -1.0}
+    return all(mine[c] == v for c, v in want.items())
+
+
+def check_fp8_gemm(o) -> bool:
+    # the fp8 product against numpy's float64 matmul of the decoded values (a
+    # library routine), and the magnitude sums against a direct sum
+    rng = np.random.default_rng(5)
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    A = rng.choice(finite, size=(7, 40))
+    B = rng.choice(finite, size=(5, 40))
+    C, Cabs = o.fp8_gemm(A, B, 40)
+    a, b = o.e4m3_value(A), o.e4m3_value(B)
+    ref = a @ b.T
+    refabs = np.abs(a) @ np.abs(b).T
+    return bool(np.allclose(C, ref, rtol=1e-12, atol=1e-12 * refabs.max()) and np.allclose(Cabs, refabs, rtol=1e-12))
+
+
+def check_fp8_integer_codes(o) -> bool:
+    # bytes 0..15 are the integers 0..15 times 2^-9: the product is an exact integer times 2^-18
+    rng = np.random.default_rng(6)
+    A = rng.integers(0, 16, size=(4, 64)).astype(np.uint8)
+    B = rng.integers(0, 16, size=(3, 64)).astype(np.uint8)
+    C, _ = o.fp8_gemm(A, B, 64)
+    return bool(np.array_equal(C * 2.0 ** 18, (A.astype(np.int64) @ B.astype(np.int64).T).astype(np.float64)))
+
+
 PINS = [check_nibbles, check_roundtrip, check_golden_bytes, check_tiny_golden, check_brute_force,
-        check_numpy_matmul, check_closed_forms, check_k_permutation, check_entries]
+        check_numpy_matmul, check_closed_forms, check_k_permutation, check_entries, check_e4m3_decode,
+        check_fp8_gemm, check_fp8_integer_codes]
 
 
 @pytest.fixture(scope="module")
@@ -262,7 +298,7 @@ def test_splitmix64_reference_value():
     assert int(si.splitmix64(0, 1)[0]) == 0xE220A8397B1DCDAF
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6])
 def test_planted_mistakes_are_caught(tmp_path, mutant):
     path = oracle.build(str(tmp_path / f"liboracle_m{mutant}.so"), mutant=mutant)
     bad = oracle.Oracle(oracle.load(path))
