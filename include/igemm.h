@@ -116,6 +116,25 @@ IGEMM_API int i4i4_gemm_noalloc(const uint8_t *Ap, const uint8_t *Bp, int32_t *C
 IGEMM_API int w4a8_gemm(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);
 
 /*
+ * W4A8 GEMM with per-channel dequantisation (the "scaled epilogue" step that
+ * follows the integer product in W4A8 inference; the pages show scales only
+ * as the per-block structure of the tutorial's gemm_blockscaled):
+ *   C[m,n] = bf16_rn((float(sum_k a[m,k] * b[n,k]) * scale_a[m]) * scale_b[n])
+ * with the integer sum exact (w4a8_gemm), its conversion to float32 rounded to
+ * nearest, two float32 multiplications in that order, and round-to-nearest-even
+ * to bfloat16.
+ *   A        [M, K] int8 (device), read only
+ *   Bp       [N, K/2] packed int4 (device), read only
+ *   scale_a  [M] float32 (device), scale_b [N] float32 (device), read only
+ *   C        [M, N] bfloat16 bit patterns (device), written
+ * The int32 product is held in a workspace of M*N*4 bytes from the library's
+ * pool, then a second kernel applies the scales.  Rules as for w4a8_gemm; the
+ * scale arrays must be 16-byte aligned too.
+ */
+IGEMM_API int w4a8_gemm_scaled(const int8_t *A, const uint8_t *Bp, const float *scale_a, const float *scale_b,
+                               uint16_t *C, int M, int N, int K, cudaStream_t stream);
+
+/*
  * fp8 GEMM:  C[m,n] = sum_k a[m,k] * b[n,k] for E4M3 operands, accumulated in
  * float32 (TileLang tutorial page low_precision_gemm.py, gemm_fp8: A (M,K) and
  * B (N,K) in an fp8 dtype, float32 accumulator, C = A . B^T).  The page writes C

@@ -172,3 +172,17 @@ class Oracle:
         if rc:
             raise RuntimeError(f"oracle_fp8_gemm failed ({rc})")
         return C, Cabs
+
+    @staticmethod
+    def bf16_rne(v: np.ndarray) -> np.ndarray:
+        """float32 -> bfloat16 bit patterns, round to nearest, ties to even
+        (finite inputs): the upper 16 bits after adding 0x7FFF plus the lowest kept bit."""
+        bits = np.ascontiguousarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+        return ((bits + 0x7FFF + ((bits >> 16) & 1)) >> 16).astype(np.uint16)
+
+    def w4a8_scaled_bf16(self, C: np.ndarray, scale_a: np.ndarray, scale_b: np.ndarray) -> np.ndarray:
+        """Per-channel dequantisation of an exact int32 W4A8 product, in the float32
+        steps the library states: (float(C) * scale_a[m]) * scale_b[n], then bfloat16."""
+        v = C.astype(np.float32) * np.asarray(scale_a, dtype=np.float32)[:, None]
+        v = v * np.asarray(scale_b, dtype=np.float32)[None, :]
+        return self.bf16_rne(v)

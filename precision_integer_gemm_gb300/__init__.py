@@ -18,13 +18,14 @@ import os
 from .build import LIB_PATH, build as build_library
 
 __all__ = [
-    "IgemmError", "load", "i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "fp8_gemm", "pack_int4", "unpack_int4",
+    "IgemmError", "load", "i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "w4a8_gemm_scaled", "fp8_gemm", "pack_int4",
+    "unpack_int4",
     "igemm_strerror",
     "igemm_last_status", "igemm_watchdog_selftest", "igemm_kernels_launched", "igemm_time_next_gemm",
     "EXPORTED_SYMBOLS", "LIB_PATH", "build_library",
 ]
 
-EXPORTED_SYMBOLS = ("i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "fp8_gemm", "pack_int4", "unpack_int4", "igemm_strerror", "igemm_last_status",
+EXPORTED_SYMBOLS = ("i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "w4a8_gemm_scaled", "fp8_gemm", "pack_int4", "unpack_int4", "igemm_strerror", "igemm_last_status",
                     "igemm_watchdog_selftest", "igemm_kernels_launched",
                     "igemm_time_next_gemm")
 
@@ -67,6 +68,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.i4i4_gemm.restype = i
     lib.i4i4_gemm_noalloc.argtypes = [p, p, p, i, i, i, p]
     lib.i4i4_gemm_noalloc.restype = i
+    lib.w4a8_gemm_scaled.argtypes = [p, p, p, p, p, i, i, i, p]
+    lib.w4a8_gemm_scaled.restype = i
     lib.fp8_gemm.argtypes = [p, p, p, i, i, i, p]
     lib.fp8_gemm.restype = i
     lib.w4a8_gemm.argtypes = [p, p, p, i, i, i, p]
@@ -126,6 +129,12 @@ def i4i4_gemm_noalloc(Ap, Bp, C, M: int, N: int, K: int, stream=None) -> None:
 def w4a8_gemm(A, Bp, C, M: int, N: int, K: int, stream=None) -> None:
     """C[M,N] (int32) = A . B^T for int8 A [M,K] and packed int4 Bp [N,K/2]."""
     _check(load().w4a8_gemm(_ptr(A), _ptr(Bp), _ptr(C), M, N, K, _stream(stream)), "w4a8_gemm")
+
+
+def w4a8_gemm_scaled(A, Bp, scale_a, scale_b, C, M: int, N: int, K: int, stream=None) -> None:
+    """C[M,N] (bfloat16) = per-channel dequantised W4A8 product: bf16(float(A . B^T) * scale_a[m] * scale_b[n])."""
+    _check(load().w4a8_gemm_scaled(_ptr(A), _ptr(Bp), _ptr(scale_a), _ptr(scale_b), _ptr(C), M, N, K,
+                                   _stream(stream)), "w4a8_gemm_scaled")
 
 
 def fp8_gemm(A, B, C, M: int, N: int, K: int, stream=None) -> None:

@@ -3,6 +3,7 @@
 // watchdog self-test.  The GEMM kernels live in gemm_kernel.cuh.
 #include <atomic>
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cstdlib>
 #include <cudaTypedefs.h>
 #include "launch.cuh"
@@ -183,6 +184,44 @@ __global__ void unpack_int4_kernel(const uint8_t *__restrict__ packed, int8_t *_
     }
 }
 
+// ---------------------------------------------------------------- per-channel scaling
+// C_bf16[m, n] = bf16_rn((float(C[m, n]) * scale_a[m]) * scale_b[n]), eight
+// elements per thread step (two 16-byte loads of int32, one 16-byte store).
+__global__ void scale_to_bf16_kernel(const int32_t *__restrict__ C, const float *__restrict__ sa,
+                                     const float *__restrict__ sb, uint16_t *__restrict__ out, int M, int N)
+{
+    const int64_t total8 = (int64_t(M) * N) / 8;  // N % 8 == 0 on this path
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total8; i += stride) {
+        const int64_t e0 = 8 * i;
+        const int m = static_cast<int>(e0 / N), n0 = static_cast<int>(e0 % N);
+        const int4 c0 = reinterpret_cast<const int4 *>(C)[2 * i];
+        const int4 c1 = reinterpret_cast<const int4 *>(C)[2 * i + 1];
+        const int c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        const float a = sa[m];
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float v0 = (__int2float_rn(c[2 * j]) * a) * sb[n0 + 2 * j];
+            const float v1 = (__int2float_rn(c[2 * j + 1]) * a) * sb[n0 + 2 * j + 1];
+            o[j] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v0))) |
+                   (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v1))) << 16);
+        }
+        reinterpret_cast<uint4 *>(out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+__global__ void scale_to_bf16_scalar_kernel(const int32_t *__restrict__ C, const float *__restrict__ sa,
+                                            const float *__restrict__ sb, uint16_t *__restrict__ out, int M, int N)
+{
+    const int64_t total = int64_t(M) * N;
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total; e += stride) {
+        const int m = static_cast<int>(e / N), n = static_cast<int>(e % N);
+        out[e] = __bfloat16_as_ushort(__float2bfloat16_rn((__int2float_rn(C[e]) * sa[m]) * sb[n]));
+    }
+}
+
 // ---------------------------------------------------------------- watchdog self-test
 __global__ void watchdog_selftest_kernel(int *status, unsigned long long limit_ns)
 {
@@ -250,6 +289,41 @@ extern "C" int i4i4_gemm_noalloc(const uint8_t *Ap, const uint8_t *Bp, int32_t *
     const int rc = gemm_common_checks(Ap, Bp, C, M, N, K, stream, &done);
     if (done) return rc;
     return launch_i4i4_noalloc(Ap, Bp, C, M, N, K, stream);
+}
+
+extern "C" int w4a8_gemm_scaled(const int8_t *A, const uint8_t *Bp, const float *scale_a, const float *scale_b,
+                                uint16_t *C, int M, int N, int K, cudaStream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0) return kInvalidArgument;
+    if (M == 0 || N == 0) return kOk;
+    if (!C || !scale_a || !scale_b) return kInvalidArgument;
+    if (K % 32 != 0) return kUnsupportedShape;
+    if (K > kMaxK) return kOverflowBound;
+    if (!aligned16(C) || !aligned16(scale_a) || !aligned16(scale_b)) return kMisaligned;
+    if (K == 0) return cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 2, stream) == cudaSuccess ? kOk : kCudaError;
+    if (!A || !Bp) return kInvalidArgument;
+    if (!aligned16(A) || !aligned16(Bp)) return kMisaligned;
+    // the exact int32 product in a pool workspace, then the scaling pass
+    void *ws = nullptr;
+    if (workspace_alloc(&ws, size_t(M) * size_t(N) * 4, stream) != kOk) return kCudaError;
+    int32_t *Ci = static_cast<int32_t *>(ws);
+    int rc = launch_w4a8(A, Bp, Ci, M, N, K, stream);
+    if (rc == kOk) {
+        const int64_t work = (N % 8 == 0) ? int64_t(M) * N / 8 : int64_t(M) * N;
+        int64_t blocks = (work + 255) / 256;
+        const int64_t cap = int64_t(sm_count()) * 8;
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) blocks = 1;
+        if (N % 8 == 0)
+            scale_to_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(Ci, scale_a, scale_b, C, M, N);
+        else
+            scale_to_bf16_scalar_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(Ci, scale_a, scale_b, C, M,
+                                                                                          N);
+        note_launch();
+        if (cudaGetLastError() != cudaSuccess) rc = kCudaError;
+    }
+    const int rf = workspace_free(ws, stream);
+    return rc != kOk ? rc : rf;
 }
 
 extern "C" int fp8_gemm(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, cudaStream_t stream)

@@ -167,6 +167,23 @@ def test_w4a8_prepared_codes_path(orc, M, N, K):
     assert np.array_equal(C, orc.w4a8_gemm(a, bp, K))
 
 
+# ---------------------------------------------------------------- W4A8 with per-channel dequantisation
+
+@pytest.mark.parametrize("M,N,K", [(16, 28672, 1024), (130, 300, 512), (257, 1000, 2048), (3, 13, 64)])
+def test_w4a8_scaled_matches_oracle(orc, M, N, K):
+    a = si.int8_values(15000 + M, (M, K))
+    b = si.int4_values(16000 + N, (N, K))
+    rng = np.random.default_rng(M * 31 + N)
+    sa = (rng.standard_normal(M) * 1e-3).astype(np.float32)
+    sb = (rng.standard_normal(N) * 1e-2).astype(np.float32)
+    bp_g = gpu_pack(b)
+    C = torch.zeros((M, N), dtype=torch.int16, device="cuda")
+    pig.w4a8_gemm_scaled(dev(a), bp_g, dev(sa), dev(sb), C, M, N, K)
+    assert pig.igemm_last_status() == 0
+    want = orc.w4a8_scaled_bf16(orc.w4a8_gemm(a, orc.pack_int4(b), K), sa, sb)
+    assert np.array_equal(C.cpu().numpy().view(np.uint16), want)
+
+
 # ---------------------------------------------------------------- fp8 GEMM (E4M3, float32 accumulate)
 
 def run_fp8(A: np.ndarray, B: np.ndarray):

@@ -247,9 +247,25 @@ def check_fp8_integer_codes(o) -> bool:
     return bool(np.array_equal(C * 2.0 ** 18, (A.astype(np.int64) @ B.astype(np.int64).T).astype(np.float64)))
 
 
+def check_bf16_rounding(o) -> bool:
+    # round-to-nearest-even float32 -> bfloat16 against PyTorch's conversion (a library
+    # routine) on random values and on exact ties, and integers that bfloat16 holds exactly
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(8)
+    v = (rng.standard_normal(4096) * 10.0 ** rng.integers(-6, 7, 4096)).astype(np.float32)
+    ties = (np.arange(1, 200, dtype=np.uint32) << 16 | 0x8000).view(np.float32)  # exactly halfway
+    x = np.concatenate([v, ties, -ties])
+    lib = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    if not np.array_equal(o.bf16_rne(x), lib):
+        return False
+    ints = np.arange(-256, 257, dtype=np.int32)
+    back = (o.w4a8_scaled_bf16(ints[None, :], np.ones(1), np.ones(ints.size)).astype(np.uint32) << 16).view(np.float32)
+    return bool(np.array_equal(back.ravel(), ints.astype(np.float32)))
+
+
 PINS = [check_nibbles, check_roundtrip, check_golden_bytes, check_tiny_golden, check_brute_force,
         check_numpy_matmul, check_closed_forms, check_k_permutation, check_entries, check_e4m3_decode,
-        check_fp8_gemm, check_fp8_integer_codes]
+        check_fp8_gemm, check_fp8_integer_codes, check_bf16_rounding]
 
 
 @pytest.fixture(scope="module")
