@@ -362,6 +362,30 @@ def test_gemm_kernel_timing_hook():
         pig.igemm_time_next_gemm(0, 0)
 
 
+def test_concurrent_streams_keep_their_workspaces_apart(orc):
+    # two prepared-codes GEMMs on two streams at once: each call's workspace is
+    # allocated and released in its own stream's order, so neither sees the other's codes
+    shapes = [(512, 768, 1024), (640, 512, 2048)]
+    runs = []
+    for i, (M, N, K) in enumerate(shapes):
+        a = si.int4_values(17000 + i, (M, K))
+        b = si.int4_values(17100 + i, (N, K))
+        runs.append((M, N, K, gpu_pack(a), gpu_pack(b), orc.i4i4_gemm(orc.pack_int4(a), orc.pack_int4(b), K)))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    outs = []
+    for rep in range(3):
+        for (M, N, K, ap, bp, _), st in zip(runs, streams):
+            C = torch.empty((M, N), dtype=torch.int32, device="cuda")
+            C.record_stream(st)
+            pig.i4i4_gemm(ap, bp, C, M, N, K, st)
+            outs.append(C)
+    torch.cuda.synchronize()
+    assert pig.igemm_last_status() == 0
+    for j, C in enumerate(outs):
+        assert np.array_equal(C.cpu().numpy(), runs[j % 2][5]), j
+
+
 def test_empty_and_zero_k():
     C = torch.full((4, 4), 7, dtype=torch.int32, device="cuda")
     pig.i4i4_gemm(None, None, C, 0, 4, 64)
