@@ -123,6 +123,65 @@ Plan plan_units(int tiles, int kb_total, int64_t c_bytes, int64_t operand_bytes,
     return p;
 }
 
+SkinnyPlan plan_skinny(int n_tiles, int K, int max_slice_k, const SkinnyClusterOption *opts, int n_opts, int workers)
+{
+    constexpr int64_t kZeroingStages = 8;  // a memset of C and its launch, in packed-stage times
+    const int sms = workers > 0 ? workers : sm_count();
+    SkinnyPlan best{0, 0, 0, 1};
+    int64_t best_cost = -1;
+    // cluster kernels: exactly cs slices, summed on chip
+    for (int o = 0; o < n_opts; ++o) {
+        const int cs = opts[o].cs;
+        if (opts[o].clusters <= 0) continue;
+        const int slice = (((K + cs - 1) / cs) + 255) / 256 * 256;
+        if (slice > opts[o].max_slice_k || (K + slice - 1) / slice != cs) continue;
+        const int ncl = std::min(opts[o].clusters, n_tiles);
+        const int64_t cost = static_cast<int64_t>((n_tiles + ncl - 1) / ncl) * (slice / 256 + 1);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = SkinnyPlan{cs, slice, cs * ncl, cs};
+        }
+    }
+    // single CTAs: one slice, or slices summed into a zeroed C with atomics
+    for (int s = 1; s <= 256; ++s) {
+        const int slice = (((K + s - 1) / s) + 255) / 256 * 256;
+        if (slice > max_slice_k) continue;
+        const int S = (K + slice - 1) / slice;  // no empty slice
+        if (S != s) continue;                  // the same plan as a smaller count
+        const int per_slice = std::min(sms / S, n_tiles);
+        if (per_slice < 1) break;
+        const int64_t tiles_per_cta = (n_tiles + per_slice - 1) / per_slice;
+        const int64_t cost = tiles_per_cta * (slice / 256 + 1) + (S > 1 ? kZeroingStages : 0);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = SkinnyPlan{S, slice, per_slice * S, 1};
+        }
+    }
+    return best;
+}
+
+// Zero C, then let the dependent GEMM launch proceed (it waits for this
+// grid's writes with griddepcontrol.wait before its first access to C).
+__global__ void zero_for_dependent_kernel(int4 *__restrict__ C4, int64_t n4, int32_t *__restrict__ tail, int n_tail)
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) C4[i] = make_int4(0, 0, 0, 0);
+    if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < n_tail) tail[threadIdx.x] = 0;
+}
+
+int launch_zero_for_dependent(int32_t *C, size_t n, cudaStream_t stream)
+{
+    // C is 16-byte aligned (checked at the entry points)
+    const int64_t n4 = static_cast<int64_t>(n / 4);
+    const int n_tail = static_cast<int>(n % 4);
+    const int64_t blocks = std::min<int64_t>(std::max<int64_t>((n4 + 255) / 256, 1), 2 * sm_count());
+    zero_for_dependent_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(reinterpret_cast<int4 *>(C), n4,
+                                                                                 C + 4 * n4, n_tail);
+    note_launch();
+    return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
+}
+
 // ---------------------------------------------------------------- pack_int4
 // Output byte j is built from logical elements 2j and 2j+1 of the flat
 // row-major array (rows are contiguous and K is even, so the flat view and

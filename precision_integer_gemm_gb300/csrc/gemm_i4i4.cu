@@ -1,6 +1,8 @@
 // int4 x int4 -> int32: A [M, K/2] and B [N, K/2] packed (low nibble = even k).
 //
-// Two paths.  Shapes with M and N of at least 256 take the prepared-codes path:
+// Three paths.  M <= 32 takes igemm_skinny_kernel (gemm_skinny_kernel.cuh):
+// B's rows on the MMA A side, A's signed codes resident in shared memory per
+// k slice.  Shapes with M and N of at least 256 take the prepared-codes path:
 // one pass turns A and B into code rows and row sums (prep.cu), then
 // igemm_ss_kernel runs a TMA -> tcgen05.mma pipeline on 128 x 256 tiles with
 // both operands in shared memory.  Smaller shapes, where that pass would cost
@@ -16,6 +18,11 @@ namespace igemm {
 using CfgI4I4 = KernelCfg<false, 192, 2, 4, 8, 4, 1, true, 1>;
 //                    W4A8   BN  stages
 using CfgI4I4Ss = SsCfg<false, 256, 4, 2>;
+//                          int4 act  QA  stages  TMEM stages  unpack sets  MMA issuers  cluster
+using CfgI4I4Skinny16 = SkinnyCfg<true, 16, 8, 6, 2, 2, 1>;
+using CfgI4I4Skinny16C2 = SkinnyCfg<true, 16, 8, 6, 2, 2, 2>;
+using CfgI4I4Skinny16C4 = SkinnyCfg<true, 16, 8, 6, 2, 2, 4>;
+using CfgI4I4Skinny32 = SkinnyCfg<true, 32, 8, 6, 2, 2, 1>;
 
 static bool use_codes_i4i4(int M, int N) { return M >= 256 && N >= 256; }
 
@@ -50,6 +57,9 @@ static int run_i4i4_codes(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int 
 
 int launch_i4i4(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
 {
+    // few rows of A (decode-like): B streamed once, A's codes resident
+    if (M <= 16) return launch_skinny<CfgI4I4Skinny16, CfgI4I4Skinny16C2, CfgI4I4Skinny16C4>(Ap, Bp, C, M, N, K, stream);
+    if (M <= 32) return launch_skinny<CfgI4I4Skinny32>(Ap, Bp, C, M, N, K, stream);
     if (use_codes_i4i4(M, N)) return run_i4i4_codes(Ap, Bp, C, M, N, K, stream);
     using Cfg = CfgI4I4;
     CUtensorMap mapA, mapB, mapC32 = {}, mapC31 = {};

@@ -1,22 +1,26 @@
 // W4A8 -> int32: A [M, K] int8 activations, B [N, K/2] packed int4 weights.
 //
-// M > 32 and N >= 256 take the prepared-codes path: one pass writes weight
-// code rows, activation high/low code planes and the row sums (prep.cu), then
-// igemm_ss_kernel multiplies 128 weight rows by 128 activation rows (256 code
-// rows) per tile from shared memory.  The rest takes igemm_tc_kernel below.
-// Swap-AB: the MMA A side is the weights (128 rows per tile, codes in TMEM);
-// the B side is QA activation rows split into high and low code rows (2*QA
-// MMA columns, shared memory).  Larger M take QA = 96 (N = 192, two
-// accumulators); skinny activation counts (M <= 32, decode) take QA = 16 with
-// a deep TMA ring and two sets of A-unpack warps on alternate k blocks.  C
-// leaves through bulk tensor stores of [m][n] boxes.
+// Skinny activation counts (M <= 32, decode) take igemm_skinny_kernel
+// (gemm_skinny_kernel.cuh): split K, each CTA's slice of the activations held
+// as codes in shared memory, the weights streamed once.  M > 32 and N >= 256
+// take the prepared-codes path: one pass writes weight code rows, activation
+// high/low code planes and the row sums (prep.cu), then igemm_ss_kernel
+// multiplies 128 weight rows by 128 activation rows (256 code rows) per tile
+// from shared memory.  The rest takes igemm_tc_kernel below.  Swap-AB: the
+// MMA A side is the weights (128 rows per tile, codes in TMEM); the B side is
+// QA = 96 activation rows split into high and low code rows (N = 192, shared
+// memory).  C leaves through bulk tensor stores of [m][n] boxes.
 #include "launch.cuh"
 
 namespace igemm {
 
 //                         W4A8  QA  SP  SO  NB  A stages  A sets  ones row  staging
 using CfgW4A8 = KernelCfg<true, 96, 2, 4, 8, 4, 1, false, 1>;
-using CfgW4A8Skinny = KernelCfg<true, 16, 8, 4, 2, 8, 2, false, 1>;
+//                          int4 act  QA  stages  TMEM stages  unpack sets  MMA issuers  cluster
+using CfgW4A8Skinny16 = SkinnyCfg<false, 16, 8, 6, 2, 2, 1>;
+using CfgW4A8Skinny16C2 = SkinnyCfg<false, 16, 6, 6, 2, 2, 2>;
+using CfgW4A8Skinny16C4 = SkinnyCfg<false, 16, 8, 6, 2, 2, 4>;
+using CfgW4A8Skinny32 = SkinnyCfg<false, 32, 6, 4, 2, 2, 1>;
 //                    W4A8  BN  stages
 using CfgW4A8Ss = SsCfg<true, 256, 4, 2>;
 
@@ -74,7 +78,9 @@ static int run_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N
 
 int launch_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
 {
-    if (M <= 32) return run_w4a8<CfgW4A8Skinny>(A, Bp, C, M, N, K, stream);
+    const uint8_t *a = reinterpret_cast<const uint8_t *>(A);
+    if (M <= 16) return launch_skinny<CfgW4A8Skinny16, CfgW4A8Skinny16C2, CfgW4A8Skinny16C4>(a, Bp, C, M, N, K, stream);
+    if (M <= 32) return launch_skinny<CfgW4A8Skinny32>(a, Bp, C, M, N, K, stream);
     if (N >= 256) return run_w4a8_codes(A, Bp, C, M, N, K, stream);
     return run_w4a8<CfgW4A8>(A, Bp, C, M, N, K, stream);
 }

@@ -1,10 +1,12 @@
 // Host-side launch plumbing shared by the GEMM translation units.
 #pragma once
 #include <algorithm>
+#include <type_traits>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include "gemm_kernel.cuh"
+#include "gemm_skinny_kernel.cuh"
 #include "gemm_ss_kernel.cuh"
 
 namespace igemm {
@@ -212,6 +214,167 @@ int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMa
     note_launch();
     if (ev.stop && cudaEventRecord(ev.stop, stream) != cudaSuccess) return kCudaError;
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
+}
+
+// ---------------------------------------------------------------- skinny path
+struct SkinnyPlan {
+    int split;    // k slices
+    int slice_k;  // k per slice (multiple of 256)
+    int ctas;     // a multiple of split
+    int cs;       // > 1: the split slices run on the CTAs of clusters of cs (no zeroed C)
+};
+// A cluster kernel of the skinny path: clusters of `cs` CTAs, `clusters` of
+// which can be resident at once (0: not available), with a shared-memory
+// budget for activation slices of `max_slice_k`.
+struct SkinnyClusterOption {
+    int cs, clusters, max_slice_k;
+};
+// Split K for igemm_skinny_kernel: the choice that minimises the packed stages
+// of the busiest CTA (plus one per tile for its hand-over, plus about eight
+// for zeroing C when slices are summed with atomics), each slice's activation
+// codes fitting the kernel's shared-memory budget.
+SkinnyPlan plan_skinny(int n_tiles, int K, int max_slice_k, const SkinnyClusterOption *opts, int n_opts,
+                       int workers = 0);
+
+// Clusters of Cfg::CS CTAs of igemm_skinny_kernel<Cfg> that can be resident at
+// once (asked once per device and configuration).
+template <class Cfg>
+int skinny_max_clusters()
+{
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!cache[dev]) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = Cfg::CS;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(Cfg::CS * sm_count(), 1, 1);
+        cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, igemm_skinny_kernel<Cfg>, &cfg) != cudaSuccess || clusters <= 0)
+            return 0;
+        cache[dev] = clusters;
+    }
+    return cache[dev];
+}
+
+template <class Cfg>
+int skinny_set_smem()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return kCudaError;
+    static bool attr_set[64] = {};
+    if (dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(igemm_skinny_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::kSmemBytes) != cudaSuccess)
+            return kCudaError;
+        attr_set[dev] = true;
+    }
+    return kOk;
+}
+
+// Zeroes C [n4 int4 words] for the atomic split of igemm_skinny_kernel; lets
+// the GEMM that follows (launched with programmatic stream serialization)
+// start at once, which waits for this grid only before it touches C.
+int launch_zero_for_dependent(int32_t *C, size_t n, cudaStream_t stream);
+
+template <class Cfg>
+int launch_skinny_plan(const SkinnyPlan &plan, const uint8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K,
+                       cudaStream_t stream)
+{
+    CUtensorMap mapW;
+    if (make_map(&mapW, CU_TENSOR_MAP_DATA_TYPE_UINT8, Bp, N, K / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) != kOk)
+        return kCudaError;
+    SkinnyParams prm{};
+    prm.A = A;
+    prm.C = C;
+    prm.M = M;
+    prm.N = N;
+    prm.K = K;
+    prm.n_tiles = (N + 127) / 128;
+    prm.split = plan.split;
+    prm.slice_k = plan.slice_k;
+    prm.status = device_status_word();
+    prm.limit_ns = watchdog_limit_ns();
+    if (!prm.status) return kCudaError;
+    // slices summed with atomics need a zeroed C: a small kernel that the GEMM
+    // overlaps (its prologue, activation codes and weight stream run while C
+    // is cleared)
+    const bool zero = plan.cs == 1 && plan.split > 1;
+    if (zero && launch_zero_for_dependent(C, size_t(M) * size_t(N), stream) != kOk) return kCudaError;
+    const GemmEvents ev = take_gemm_events();
+    if (ev.start && cudaEventRecord(ev.start, stream) != cudaSuccess) return kCudaError;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if constexpr (Cfg::CS > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = Cfg::CS;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    // (with the timing events armed, the event between the two kernels keeps
+    // them apart and the GEMM's own time is measured)
+    if (zero && !ev.start) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.gridDim = dim3(plan.ctas, 1, 1);
+    cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = na ? attr : nullptr;
+    cfg.numAttrs = na;
+    if (cudaLaunchKernelEx(&cfg, igemm_skinny_kernel<Cfg>, mapW, prm) != cudaSuccess) return kCudaError;
+    note_launch();
+    if (ev.stop && cudaEventRecord(ev.stop, stream) != cudaSuccess) return kCudaError;
+    return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
+}
+
+template <class CfgC>
+int skinny_cluster_option(SkinnyClusterOption *o)
+{
+    if (skinny_set_smem<CfgC>() != kOk) return kCudaError;
+    o->cs = CfgC::CS;
+    o->max_slice_k = CfgC::kMaxSliceK;
+    o->clusters = skinny_max_clusters<CfgC>();
+    return kOk;
+}
+
+// igemm_skinny_kernel over packed int4 weights Bp [N, K/2] and activations A
+// (int8 [M, K], or packed int4 [M, K/2]), M <= Cfg::QA: the cluster kernel
+// Cfg2 (pairs) or Cfg4 (clusters of four) when its plan is the better one,
+// else Cfg (void: no cluster kernel of that size).
+template <class Cfg, class Cfg2 = void, class Cfg4 = void>
+int launch_skinny(const uint8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
+{
+    if (skinny_set_smem<Cfg>() != kOk) return kCudaError;
+    const int n_tiles = (N + 127) / 128;
+    SkinnyClusterOption opts[2] = {};
+    int n_opts = 0;
+    if constexpr (!std::is_void<Cfg2>::value) {
+        static_assert(Cfg2::CS == 2 && Cfg2::QA == Cfg::QA && Cfg2::kActI4 == Cfg::kActI4, "pair config");
+        if (skinny_cluster_option<Cfg2>(&opts[n_opts++]) != kOk) return kCudaError;
+    }
+    if constexpr (!std::is_void<Cfg4>::value) {
+        static_assert(Cfg4::CS == 4 && Cfg4::QA == Cfg::QA && Cfg4::kActI4 == Cfg::kActI4, "cluster-4 config");
+        if (skinny_cluster_option<Cfg4>(&opts[n_opts++]) != kOk) return kCudaError;
+    }
+    const SkinnyPlan plan = plan_skinny(n_tiles, K, Cfg::kMaxSliceK, opts, n_opts);
+    if (plan.ctas < 1) return kUnsupportedShape;
+    if constexpr (!std::is_void<Cfg2>::value)
+        if (plan.cs == 2) return launch_skinny_plan<Cfg2>(plan, A, Bp, C, M, N, K, stream);
+    if constexpr (!std::is_void<Cfg4>::value)
+        if (plan.cs == 4) return launch_skinny_plan<Cfg4>(plan, A, Bp, C, M, N, K, stream);
+    return launch_skinny_plan<Cfg>(plan, A, Bp, C, M, N, K, stream);
 }
 
 int launch_i4i4(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);

@@ -240,17 +240,36 @@ def test_decode_workload_whole_c(orc):
 @pytest.mark.parametrize("K", [32, 8192, 65536])
 @pytest.mark.parametrize("av,bv", [(-8, -8), (7, 7), (-8, 7), (7, -8)])
 def test_i4i4_extreme_constants(orc, K, av, bv):
-    M, N = 130, 260
-    a = np.full((M, K), av, dtype=np.int8)
-    b = np.full((N, K), bv, dtype=np.int8)
-    C, _, _ = run_i4i4(a, b, orc)
-    assert np.all(C == av * bv * K)
+    for M in (16, 32, 130):
+        N = 260
+        a = np.full((M, K), av, dtype=np.int8)
+        b = np.full((N, K), bv, dtype=np.int8)
+        C, _, _ = run_i4i4(a, b, orc)
+        assert np.all(C == av * bv * K), (M, K, av, bv)
+
+
+# Skinny path (M <= 32): split K with ragged last slices (K % 256 != 0), N
+# tails, both activation-row configurations (M <= 16, M <= 32), one and many
+# slices.
+SKINNY = [(1, 129, 8224), (7, 1000, 4128), (16, 2048, 65536), (17, 300, 2080), (32, 520, 8192), (24, 128, 256),
+          (16, 28672, 512)]
+
+
+@pytest.mark.parametrize("M,N,K", SKINNY)
+def test_skinny_path_matches_oracle(orc, M, N, K):
+    a4 = si.int4_values(6000 + M, (M, K))
+    a8 = si.int8_values(6100 + M, (M, K))
+    b = si.int4_values(6200 + N, (N, K))
+    C, ap, bp = run_i4i4(a4, b, orc)
+    assert np.array_equal(C, orc.i4i4_gemm(ap, bp, K))
+    C, bp = run_w4a8(a8, b, orc)
+    assert np.array_equal(C, orc.w4a8_gemm(a8, bp, K))
 
 
 @pytest.mark.parametrize("K", [32, 8192, 65536])
 @pytest.mark.parametrize("av,bv", [(-128, -8), (127, 7), (-128, 7), (127, -8), (0, -8)])
 def test_w4a8_extreme_constants(orc, K, av, bv):
-    for M in (16, 130):
+    for M in (16, 32, 130):
         N = 260
         a = np.full((M, K), av, dtype=np.int8)
         b = np.full((N, K), bv, dtype=np.int8)
@@ -313,15 +332,26 @@ def test_full_size_workload_sampled(orc, name):
 # ---------------------------------------------------------------- determinism, edges, watchdog
 
 def test_split_path_is_deterministic(orc):
+    # the decode shape splits K (over a cluster pair, or with atomics): five
+    # calls in a row give one result, the oracle's on sampled entries
     variant, M, N, K, a, b = si.workload_operands("w4a8_decode_16x28672x8192")
     bp = gpu_pack(b)
-    at = dev(a)
-    outs = []
-    for _ in range(3):
-        C = torch.empty((M, N), dtype=torch.int32, device="cuda")
-        pig.w4a8_gemm(at, bp, C, M, N, K)
-        outs.append(C.cpu().numpy())
-    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    a4 = si.int4_values(77, (M, K))
+    runs = [(lambda C: pig.w4a8_gemm(dev(a), bp, C, M, N, K)), (lambda C: pig.i4i4_gemm(gpu_pack(a4), bp, C, M, N, K))]
+    rng = np.random.default_rng(5)
+    ms = rng.integers(0, M, 256)
+    ns = rng.integers(0, N, 256)
+    want = [orc.w4a8_entries(a, orc.pack_int4(b), K, ms, ns), orc.i4i4_entries(orc.pack_int4(a4), orc.pack_int4(b), K, ms, ns)]
+    for run, ref in zip(runs, want):
+        outs = []
+        for _ in range(5):
+            C = torch.empty((M, N), dtype=torch.int32, device="cuda")
+            run(C)
+            assert pig.igemm_last_status() == 0
+            outs.append(C.cpu().numpy())
+        for o in outs[1:]:
+            assert np.array_equal(outs[0], o)
+        assert np.array_equal(outs[0][ms, ns].astype(np.int64), ref)
 
 
 def test_kernel_launch_counter():
@@ -338,8 +368,12 @@ def test_kernel_launch_counter():
     with pytest.raises(pig.IgemmError):
         pig.i4i4_gemm(a, a, C, 4, 4, 48)
     n3 = pig.igemm_kernels_launched()
+    # skinny path, one k slice: the GEMM alone
+    a8 = torch.zeros((16, 256), dtype=torch.int8, device="cuda")
+    pig.w4a8_gemm(a8, a[:256, :128].contiguous(), C, 16, 256, 256)
+    n4 = pig.igemm_kernels_launched()
     torch.cuda.synchronize()
-    assert (n1 - n0, n2 - n1, n3 - n2) == (2, 1, 0)
+    assert (n1 - n0, n2 - n1, n3 - n2, n4 - n3) == (2, 1, 0, 1)
 
 
 def test_gemm_kernel_timing_hook():
