@@ -50,7 +50,7 @@ static int run_i4i4_codes(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int 
         rc = make_map(&mapC, CU_TENSOR_MAP_DATA_TYPE_INT32, C, M, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc == kOk)
         rc = launch_ss<Cfg>(mapP, mapQ, mapC, tma_store, C, M, N, K, a_sums, b_sums, M, N,
-                            (int64_t(M) + N) * K, stream);
+                            (int64_t(M) + N) * K, stream, true);
     const int rf = workspace_free(ws, stream);
     return rc != kOk ? rc : rf;
 }

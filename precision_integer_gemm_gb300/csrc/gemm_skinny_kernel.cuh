@@ -261,8 +261,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     const uint32_t rank = Cfg::CS > 1 ? cluster_ctarank() : 0u;
     const int k0 = slice * prm.slice_k;
     const int nst = (min(prm.K - k0, prm.slice_k) + Cfg::kStageK - 1) / Cfg::kStageK;
+    // the first ring round is loaded by the thread that initialises the
+    // barriers, before the CTA-wide set-up (TMEM allocation, barrier)
+    const int pre = min(ST, ((prm.n_tiles - t0 + tstep - 1) / tstep) * nst);
 
-    if (threadIdx.x == 0) {
+    if (warp == Cfg::kWarpTma && lane == 0) {
         for (int s = 0; s < ST; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 4);
@@ -285,7 +288,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         *abort_flag = 0;
         for (int m = 0; m < QA; ++m) sums[m] = 0;
         fence_mbar_init();
-        tma_prefetch_map(&mapW);
+        const uint64_t stream_once = l2_policy_evict_first();
+        for (int g = 0; g < pre; ++g) {
+            const int t = t0 + (g / nst) * tstep, i = g % nst;
+            mbar_arrive_expect_tx(&full[g], Cfg::kPk);
+            tma_load_2d_hint(pk + g * Cfg::kPk, &mapW, &full[g], (k0 + i * Cfg::kStageK) / 2, t * 128, stream_once);
+        }
     }
     if (warp == Cfg::kWarpMma) {
         tmem_alloc(tmem_slot, Cfg::kTmemCols);
@@ -300,8 +308,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 
     if (warp == Cfg::kWarpTma) {
         // ------------------------------------------------------------ producer
-        // starts at once: the first weight stages load while the others build
-        // the activation codes
+        // the weight stream runs while the other warps build the activation codes
         if (lane < Cfg::kIssuers) {
             const uint64_t stream_once = l2_policy_evict_first();
             uint32_t g = 0, issued_mask = 0, last_phase = 0;
@@ -311,6 +318,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     const int s = static_cast<int>(g % ST);
                     if (s % Cfg::kIssuers != lane) continue;
                     const uint32_t ph = (g / ST) & 1u;
+                    if (static_cast<int>(g) < pre) {  // loaded before the set-up
+                        issued_mask |= 1u << s;
+                        continue;
+                    }
                     if (!wait_bounded(&empty[s], ph ^ 1u, wd)) {
                         ok = false;
                         break;

@@ -203,6 +203,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 
     if (warp == 5) {
         // ------------------------------------------------------------ producer
+        // the codes may still be being written by the grid this one was
+        // launched to overlap (no-op without such a grid)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         if (lane < Cfg::kIssuers) {
             // P tiles are reused by the whole group: keep them in L2 (an
             // evict-first hint on the Q tiles, which one wave shares, measured
@@ -296,6 +299,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue (warps 0-3)
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // the row sums, as above
         const int quad = warp;
         const int p = quad * 32 + lane;
         const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);

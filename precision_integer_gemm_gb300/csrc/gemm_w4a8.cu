@@ -50,7 +50,7 @@ static int run_w4a8_codes(const int8_t *A, const uint8_t *Bp, int32_t *C, int M,
         rc = make_map(&mapC, CU_TENSOR_MAP_DATA_TYPE_INT32, C, M, N, Cfg::kStageRows, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc == kOk)
         rc = launch_ss<Cfg>(mapP, mapQ, mapC, tma_store, C, M, N, K, w_sums, a_sums, N, M,
-                            int64_t(N) * K + 2 * int64_t(M) * K, stream);
+                            int64_t(N) * K + 2 * int64_t(M) * K, stream, true);
     const int rf = workspace_free(ws, stream);
     return rc != kOk ? rc : rf;
 }

@@ -148,7 +148,7 @@ int ss_resident_ctas(Kernel k)
 template <class Cfg>
 int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMap &mapC, bool tma_store, int32_t *C,
               int M, int N, int K, const int32_t *sumP, const int32_t *sumQ, int p_rows, int q_rows,
-              int64_t operand_bytes, cudaStream_t stream)
+              int64_t operand_bytes, cudaStream_t stream, bool after_prep = false)
 {
     auto kernel = igemm_ss_kernel<Cfg>;
     int dev = 0;
@@ -194,23 +194,30 @@ int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMa
     const int clusters = std::min(prm.num_units, resident / Cfg::CL);
     const GemmEvents ev = take_gemm_events();
     if (ev.start && cudaEventRecord(ev.start, stream) != cudaSuccess) return kCudaError;
-    if constexpr (Cfg::CL == 1) {
-        kernel<<<clusters, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mapP, mapQ, mapC, prm);
-    } else {
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = Cfg::CL;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(Cfg::CL * clusters, 1, 1);
-        cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
-        cfg.dynamicSmemBytes = Cfg::kSmemBytes;
-        cfg.stream = stream;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, kernel, mapP, mapQ, mapC, prm) != cudaSuccess) return kCudaError;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if constexpr (Cfg::CL > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = Cfg::CL;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
+    // right after the preparation pass (no memset or armed event in between):
+    // launch early; the kernel waits for the pass before it reads codes or sums
+    if (after_prep && plan.split == 1 && !ev.start) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.gridDim = dim3(Cfg::CL * clusters, 1, 1);
+    cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = na ? attr : nullptr;
+    cfg.numAttrs = na;
+    if (cudaLaunchKernelEx(&cfg, kernel, mapP, mapQ, mapC, prm) != cudaSuccess) return kCudaError;
     note_launch();
     if (ev.stop && cudaEventRecord(ev.stop, stream) != cudaSuccess) return kCudaError;
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;

@@ -53,6 +53,9 @@ __global__ void __launch_bounds__(256) prep_codes_kernel(const uint8_t *__restri
                                                          int32_t *__restrict__ p_sums, int32_t *__restrict__ q_sums)
 {
     __shared__ int red[8];
+    // the GEMM that follows may launch now; it waits for this grid before it
+    // reads any code or sum
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int row = blockIdx.x;
     int sum = 0;
     const bool is_p = row < p_rows;
