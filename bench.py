@@ -321,7 +321,7 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
     if args.workload.startswith("w4a8_decode"):
         achieved = nbytes / gemm_kernel_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "kernel": "igemm_tc_kernel",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "kernel": "igemm_skinny_kernel",
                 "kernel_ms": 1e3 * gemm_kernel_s, "algorithmic_bytes_per_launch": nbytes,
                 "peak_source": f"{peak_src} copy bandwidth"}
     else:
