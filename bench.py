@@ -3,10 +3,13 @@
 One step is one GEMM call of the chosen workload through the C-ABI (host plan
 + TMA loads + unpack + tcgen05 MMA + epilogue, and the split-K reduction when
 the plan splits K).  Inputs are seeded synthetic operands resident in HBM
-before timing; L2 is flushed (a 256 MB write, outside the timed events)
-before every step.  Prints one JSON line.
+before timing.  Between steps no step finds its operands in L2: by default
+every step reads its own copy of the operands, rotating over copies worth
+three L2 capacities; --l2 flush instead writes 256 MB before every step
+(outside the timed events).  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                  [--l2 rotate|flush]
 
 --impl reference times the CPU oracle (plain C, int64 accumulation) on the
 host cores, each step a bounded row sample of the same workload.
@@ -37,6 +40,7 @@ UNIT = "TOPS"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 E4M3_PER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 L2_FLUSH_BYTES = 256 << 20
+L2_BYTES = 129 << 20  # GB300 L2 (126.5 MiB)
 
 
 def load_peaks():
@@ -231,14 +235,33 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
         gemm = pig.w4a8_gemm
     del b_dev
     C = torch.empty((M, N), dtype=torch.float32 if variant == "fp8" else torch.int32, device="cuda")
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    # L2 between steps: either every step reads its own copy of the operands,
+    # rotating over copies worth three L2 capacities (a step's operands were last
+    # touched two or more steps ago, and all later reads evicted them), or a
+    # 256 MB write before every step
+    op_bytes = a_in.numel() * a_in.element_size() + bp.numel() * bp.element_size()
+    if args.l2 == "rotate":
+        n_copies = max(2, min(64, -(-3 * L2_BYTES // op_bytes)))
+        copies = [(a_in, bp)] + [(a_in.clone(), bp.clone()) for _ in range(n_copies - 1)]
+        flush = None
+    else:
+        n_copies = 1
+        copies = [(a_in, bp)]
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     torch.cuda.synchronize()
+    state = {"i": 0}
 
     def step():
-        gemm(a_in, bp, C, M, N, K, stream)
+        a_s, b_s = copies[state["i"] % n_copies]
+        state["i"] += 1
+        gemm(a_s, b_s, C, M, N, K, stream)
+
+    def before_step():
+        if flush is not None:
+            flush.zero_()
 
     for _ in range(args.warmup):
-        flush.zero_()
+        before_step()
         step()
     if pig.igemm_last_status(stream) != 0:
         raise RuntimeError("device status after warm-up is not ok")
@@ -260,7 +283,7 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
     launched0 = pig.igemm_kernels_launched()
     wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush.zero_()
+        before_step()
         starts[i].record(stream)
         step()
         ends[i].record(stream)
@@ -279,7 +302,7 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
     # of the timed steps: events between the kernels of a step change how
     # they overlap)
     for i in range(args.steps):
-        flush.zero_()
+        before_step()
         pig.igemm_time_next_gemm(k_starts[i], k_ends[i])
         step()
     torch.cuda.synchronize()
@@ -340,7 +363,10 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
         "dtype": {"i4i4": "int4", "w4a8": "int8xint4", "fp8": "e4m3 (float32 accumulate)"}[variant],
         "data": "synthetic (SplitMix64-seeded, uniform)",
         "config": {"workload": args.workload, "variant": variant, "M": M, "N": N, "K": K,
-                   "l2": "flushed before every step (256 MB write, outside the timed events)",
+                   "l2": (f"operands rotate over {n_copies} copies ({n_copies * op_bytes / 1e6:.0f} MB, "
+                          f"3x L2 or more): each step's operands were evicted from L2 before it; no flush"
+                          if args.l2 == "rotate" else
+                          "flushed before every step (256 MB write, outside the timed events)"),
                    "parallelism": "replicas" if world > 1 else "single"},
         "wall_ms_per_step": 1e3 * wall / args.steps,
         "gpu_launches": launched,
@@ -371,6 +397,8 @@ def main():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="i4i4_8192", choices=sorted(si.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--l2", choices=["rotate", "flush"], default="rotate",
+                   help="keep operands out of L2 between steps by rotating copies, or by a 256 MB write")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     args = p.parse_args()
     if args.warmup < 3:
