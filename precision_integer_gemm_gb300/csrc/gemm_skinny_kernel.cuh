@@ -105,6 +105,8 @@ struct SkinnyCfg {
     static constexpr int kSlots = kOwned * (CS - 1);
     static constexpr int kExchangeArrivals = 32 * kSlots;  // = 32 * (4 - kOwned) sent quadrants
     static constexpr int kIssuers = ST % 4 == 0 ? 4 : (ST <= 8 ? ST : 1);
+    // the first ring round goes out kRamp stages at a time (see the producer)
+    static constexpr int kRamp = ST < 2 ? ST : 2;
     static constexpr int kWarpU0 = 4;
     static constexpr int kWarpTma = 4 + 4 * kASets;
     static constexpr int kWarpMma = kWarpTma + 1;  // TMEM allocation; MMA issuers kWarpMma ..
@@ -261,9 +263,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     const uint32_t rank = Cfg::CS > 1 ? cluster_ctarank() : 0u;
     const int k0 = slice * prm.slice_k;
     const int nst = (min(prm.K - k0, prm.slice_k) + Cfg::kStageK - 1) / Cfg::kStageK;
-    // the first ring round is loaded by the thread that initialises the
-    // barriers, before the CTA-wide set-up (TMEM allocation, barrier)
-    const int pre = min(ST, ((prm.n_tiles - t0 + tstep - 1) / tstep) * nst);
+    // stages this CTA loads; the first kRamp are issued by the thread that
+    // initialises the barriers, before the CTA-wide set-up (TMEM allocation,
+    // barrier), the rest of the first ring round by the producer (below)
+    const int total_st = ((prm.n_tiles - t0 + tstep - 1) / tstep) * nst;
+    const int pre = min(Cfg::kRamp, total_st);
+    const int first_round = min(ST, total_st);
 
     if (warp == Cfg::kWarpTma && lane == 0) {
         for (int s = 0; s < ST; ++s) {
@@ -313,12 +318,32 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const uint64_t stream_once = l2_policy_evict_first();
             uint32_t g = 0, issued_mask = 0, last_phase = 0;
             bool ok = true;
+            // The rest of the first ring round, one stage each time the stage kRamp
+            // earlier lands.  A whole round issued at once by every CTA queues 19.5 MB
+            // at the memory controllers (decode shape) and its first stages land only
+            // after most of it; two stages in flight at first get the data flowing
+            // sooner.  No later stage is issued before this loop ends (the warp
+            // barrier), so each wait below finds its slot in its first phase.
+            if (lane == 0) {
+                for (int gr = pre; gr < first_round; ++gr) {
+                    if (!wait_bounded(&full[gr - Cfg::kRamp], 0u, wd)) {
+                        ok = false;
+                        break;
+                    }
+                    const int t = t0 + (gr / nst) * tstep, i = gr % nst;
+                    mbar_arrive_expect_tx(&full[gr], Cfg::kPk);
+                    tma_load_2d_hint(pk + gr * Cfg::kPk, &mapW, &full[gr], (k0 + i * Cfg::kStageK) / 2, t * 128,
+                                     stream_once);
+                }
+            }
+            __syncwarp((1u << Cfg::kIssuers) - 1u);
+            ok = __shfl_sync((1u << Cfg::kIssuers) - 1u, ok, 0);
             for (int t = t0; ok && t < prm.n_tiles; t += tstep) {
                 for (int i = 0; i < nst; ++i, ++g) {
                     const int s = static_cast<int>(g % ST);
                     if (s % Cfg::kIssuers != lane) continue;
                     const uint32_t ph = (g / ST) & 1u;
-                    if (static_cast<int>(g) < pre) {  // loaded before the set-up
+                    if (static_cast<int>(g) < first_round) {  // issued above, phase 0
                         issued_mask |= 1u << s;
                         continue;
                     }
