@@ -9,7 +9,8 @@ Sources of what it computes (see ``oracle.c`` for the full statement):
 "[CUDA] Support int4 T.gemm" (tilelang PR #2063) example_tilelang_gemm_int4.py
 matmul_nt_int4; "[Example] add w4a8 gemm kernel" (tilelang PR #815) review of
 torch_convert / ref_program; TileLang tutorial low_precision_gemm.py
-matmul_int4 and pack_int4.
+matmul_int4 and pack_int4, and its gemm_fp8 and gemm_blockscaled (E4M3 values
+in float64; block scales applied per block of K).
 """
 
 from __future__ import annotations
@@ -56,6 +57,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_e4m3_value.restype = ctypes.c_double
     lib.oracle_fp8_gemm.argtypes = [p, p, p, p, i64, i64, i64, ctypes.c_int]
     lib.oracle_fp8_gemm.restype = ctypes.c_int
+    lib.oracle_fp8_blockscaled.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, ctypes.c_int]
+    lib.oracle_fp8_blockscaled.restype = ctypes.c_int
     for name in ("oracle_i4i4_entries", "oracle_w4a8_entries"):
         fn = getattr(lib, name)
         fn.argtypes = [p, p, i64, p, p, i64, p]
@@ -171,6 +174,25 @@ class Oracle:
         rc = self.lib.oracle_fp8_gemm(_ptr(A), _ptr(B), _ptr(C), _ptr(Cabs), M, N, K, threads or default_threads())
         if rc:
             raise RuntimeError(f"oracle_fp8_gemm failed ({rc})")
+        return C, Cabs
+
+    def fp8_blockscaled(self, A: np.ndarray, B: np.ndarray, SFA: np.ndarray, SFB: np.ndarray, K: int,
+                        g: int = 128, threads: int | None = None):
+        """(C, Cabs): the tutorial's block-scaled fp8 GEMM in float64: scales SFA [M, KB]
+        and SFB [N, KB] (float32, KB = ceil(K/g)) applied per block of g k."""
+        A = np.ascontiguousarray(A).view(np.uint8)
+        B = np.ascontiguousarray(B).view(np.uint8)
+        SFA = np.ascontiguousarray(SFA, dtype=np.float32)
+        SFB = np.ascontiguousarray(SFB, dtype=np.float32)
+        M, N = A.shape[0], B.shape[0]
+        KB = -(-K // g)
+        assert A.shape[1] == K and B.shape[1] == K and SFA.shape == (M, KB) and SFB.shape == (N, KB)
+        C = np.empty((M, N), dtype=np.float64)
+        Cabs = np.empty((M, N), dtype=np.float64)
+        rc = self.lib.oracle_fp8_blockscaled(_ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(C), _ptr(Cabs), M, N, K, g,
+                                             threads or default_threads())
+        if rc:
+            raise RuntimeError(f"oracle_fp8_blockscaled failed ({rc})")
         return C, Cabs
 
     @staticmethod

@@ -283,3 +283,88 @@ int oracle_fp8_gemm(const uint8_t *A, const uint8_t *B, double *C, double *Cabs,
     free(b);
     return 0;
 }
+
+/*
+ * Block-scaled fp8 GEMM (the tutorial's gemm_blockscaled, low_precision_gemm.py):
+ * A [M, K], B [N, K] e4m3 bytes; SFA [M, KB], SFB [N, KB] float32 scales with
+ * KB = ceil(K / g): the scales are applied along K per block of g values,
+ *
+ *   C[m,n] = sum_{kb} SFA[m,kb] * SFB[n,kb] * sum_{k in block kb} a[m,k]*b[n,k]
+ *
+ * in double; Cabs takes the same sums of magnitudes (the scale of any rounding).
+ * Returns 0, or -1 on an allocation error.
+ */
+struct bjob {
+    const double *a, *b;
+    const float *sfa, *sfb;
+    double *c, *cabs;
+    int64_t N, K, g, KB, m_begin, m_end;
+};
+
+static void *run_rows_b(void *arg)
+{
+    struct bjob *j = (struct bjob *)arg;
+    for (int64_t m = j->m_begin; m < j->m_end; ++m) {
+        for (int64_t n = 0; n < j->N; ++n) {
+            const double *ar = j->a + m * j->K, *br = j->b + n * j->K;
+            double s = 0.0, sa = 0.0;
+            for (int64_t kb = 0; kb < j->KB; ++kb) {
+                double part = 0.0, pabs = 0.0;
+                const int64_t k1 = (kb + 1) * j->g < j->K ? (kb + 1) * j->g : j->K;
+                for (int64_t k = kb * j->g; k < k1; ++k) {
+                    const double p = ar[k] * br[k];
+                    part += p;
+                    pabs += p < 0 ? -p : p;
+                }
+#if ORACLE_MUTANT == 7 /* planted: every block takes the scales of block 0 */
+                const int64_t ks = 0;
+#else
+                const int64_t ks = kb;
+#endif
+#if ORACLE_MUTANT == 8 /* planted: SFA indexed by the B row */
+                const double sc = (double)j->sfa[(n % (j->m_end > 0 ? j->m_end : 1)) * j->KB + ks] *
+                                  (double)j->sfb[n * j->KB + ks];
+#else
+                const double sc = (double)j->sfa[m * j->KB + ks] * (double)j->sfb[n * j->KB + ks];
+#endif
+                s += sc * part;
+                sa += (sc < 0 ? -sc : sc) * pabs;
+            }
+            j->c[m * j->N + n] = s;
+            j->cabs[m * j->N + n] = sa;
+        }
+    }
+    return NULL;
+}
+
+int oracle_fp8_blockscaled(const uint8_t *A, const uint8_t *B, const float *SFA, const float *SFB, double *C,
+                           double *Cabs, int64_t M, int64_t N, int64_t K, int64_t g, int nthreads)
+{
+    if (g < 1) return -1;
+    const int64_t KB = (K + g - 1) / g;
+    double *a = (double *)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
+    double *b = (double *)malloc(sizeof(double) * (size_t)(N * K > 0 ? N * K : 1));
+    if (!a || !b) { free(a); free(b); return -1; }
+    for (int64_t i = 0; i < M * K; ++i) a[i] = oracle_e4m3_value(A[i]);
+    for (int64_t i = 0; i < N * K; ++i) b[i] = oracle_e4m3_value(B[i]);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > M) nthreads = (int)(M > 0 ? M : 1);
+    struct bjob *jobs = (struct bjob *)calloc((size_t)nthreads, sizeof(struct bjob));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tids) { free(a); free(b); free(jobs); free(tids); return -1; }
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = (struct bjob){a, b, SFA, SFB, C, Cabs, N, K, g, KB, M * t / nthreads, M * (t + 1) / nthreads};
+        if (pthread_create(&tids[t], NULL, run_rows_b, &jobs[t]) != 0) {
+            run_rows_b(&jobs[t]);
+            tids[t] = 0;
+        }
+    }
+    for (int t = 0; t < nthreads; ++t)
+        if (tids[t]) pthread_join(tids[t], NULL);
+    free(jobs);
+    free(tids);
+    free(a);
+    free(b);
+    return 0;
+}
+

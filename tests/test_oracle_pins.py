@@ -263,9 +263,47 @@ def check_bf16_rounding(o) -> bool:
     return bool(np.array_equal(back.ravel(), ints.astype(np.float32)))
 
 
+def check_blockscaled_closed_form(o) -> bool:
+    # tutorial gemm_blockscaled: scales along K per block of 128.  With every a and b
+    # equal to 1.0 (e4m3 byte 0x38) each block's partial sum is its length, so
+    # C[m,n] = sum_kb len(kb) * SFA[m,kb] * SFB[n,kb]; K = 300 gives blocks of 128,
+    # 128 and 44.  Scales differ per row, per column and per block (powers of two
+    # times small integers: every product and sum is exact in double).
+    M, N, K, g = 3, 4, 300, 128
+    KB = 3
+    lens = np.array([128.0, 128.0, 44.0])
+    sfa = np.array([[1, 2, 4], [3, -1, 0.5], [0.25, 8, -2]], dtype=np.float32)
+    sfb = np.array([[1, 1, 1], [2, 0.5, -4], [-1, 3, 0.125], [16, 0, 1]], dtype=np.float32)
+    A = np.full((M, K), 0x38, dtype=np.uint8)
+    B = np.full((N, K), 0x38, dtype=np.uint8)
+    C, Cabs = o.fp8_blockscaled(A, B, sfa, sfb, K, g)
+    want = np.array([[sum(lens[kb] * float(sfa[m, kb]) * float(sfb[n, kb]) for kb in range(KB)) for n in range(N)]
+                     for m in range(M)])
+    want_abs = np.array([[sum(lens[kb] * abs(float(sfa[m, kb]) * float(sfb[n, kb])) for kb in range(KB))
+                          for n in range(N)] for m in range(M)])
+    # a sign pattern: a = -1.0 (0xB8) on odd k flips those products
+    A2 = A.copy()
+    A2[:, 1::2] = 0xB8
+    C2, _ = o.fp8_blockscaled(A2, B, sfa, sfb, K, g)
+    return bool(np.array_equal(C, want) and np.array_equal(Cabs, want_abs) and np.all(C2 == 0.0))
+
+
+def check_blockscaled_unit_scales(o) -> bool:
+    # with every scale 1 the blocks add back up to the plain fp8 GEMM
+    rng = np.random.default_rng(9)
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    A = rng.choice(finite, size=(5, 200))
+    B = rng.choice(finite, size=(6, 200))
+    ones_a, ones_b = np.ones((5, 2), dtype=np.float32), np.ones((6, 2), dtype=np.float32)
+    C, Cabs = o.fp8_blockscaled(A, B, ones_a, ones_b, 200, 128)
+    F, Fabs = o.fp8_gemm(A, B, 200)
+    return bool(np.allclose(C, F, rtol=1e-12, atol=1e-12 * Fabs.max()) and np.allclose(Cabs, Fabs, rtol=1e-12))
+
+
 PINS = [check_nibbles, check_roundtrip, check_golden_bytes, check_tiny_golden, check_brute_force,
         check_numpy_matmul, check_closed_forms, check_k_permutation, check_entries, check_e4m3_decode,
-        check_fp8_gemm, check_fp8_integer_codes, check_bf16_rounding]
+        check_fp8_gemm, check_fp8_integer_codes, check_bf16_rounding, check_blockscaled_closed_form,
+        check_blockscaled_unit_scales]
 
 
 @pytest.fixture(scope="module")
@@ -314,7 +352,7 @@ def test_splitmix64_reference_value():
     assert int(si.splitmix64(0, 1)[0]) == 0xE220A8397B1DCDAF
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_planted_mistakes_are_caught(tmp_path, mutant):
     path = oracle.build(str(tmp_path / f"liboracle_m{mutant}.so"), mutant=mutant)
     bad = oracle.Oracle(oracle.load(path))
