@@ -91,6 +91,8 @@ def recorded_traffic(workload):
 def workload_bytes(variant, M, N, K):
     if variant == "fp8":
         return (M + N) * K + 4 * M * N
+    if variant == "fp8bs":
+        return (M + N) * K + 4 * M * N + 4 * (M + N) * (-(-K // 128))
     a = M * K if variant == "w4a8" else M * K // 2
     return a + N * K // 2 + 4 * M * N
 
@@ -156,11 +158,19 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# the block scales of the fp8bs workload (set in main)
+_SCALES = None
+
+
 def oracle_sample_time(orc, variant, a, b, K, rows, threads):
     """Run the oracle on the first `rows` rows of A; returns seconds."""
     t0 = time.perf_counter()
     if variant == "fp8":
         orc.fp8_gemm(np.ascontiguousarray(a[:rows]), b, K, threads=threads)
+    elif variant == "fp8bs":
+        sfa, sfb = _SCALES
+        orc.fp8_blockscaled(np.ascontiguousarray(a[:rows]), b, np.ascontiguousarray(sfa[:rows]), sfb, K,
+                            threads=threads)
     elif variant == "i4i4":
         orc.i4i4_gemm(orc.pack_int4(a[:rows]), orc.pack_int4(b), K, threads=threads)
     else:
@@ -218,7 +228,7 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
     # operands resident in HBM: logical -> packed by the library's pack kernel
     a_dev = torch.from_numpy(a).cuda()
     b_dev = torch.from_numpy(b).cuda()
-    if variant == "fp8":
+    if variant in ("fp8", "fp8bs"):
         bp = b_dev  # E4M3 bytes as they are
     else:
         bp = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
@@ -226,6 +236,12 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
     if variant == "fp8":
         a_in = a_dev
         gemm = pig.fp8_gemm
+    elif variant == "fp8bs":
+        a_in = a_dev
+        sfa_d, sfb_d = (torch.from_numpy(x).cuda() for x in _SCALES)
+
+        def gemm(a_, b_, c_, m_, n_, k_, st):
+            pig.fp8_blockscaled_gemm(a_, b_, sfa_d, sfb_d, c_, m_, n_, k_, st)
     elif variant == "i4i4":
         a_in = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
         pig.pack_int4(a_dev, a_in, M, K)
@@ -234,7 +250,7 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
         a_in = a_dev
         gemm = pig.w4a8_gemm
     del b_dev
-    C = torch.empty((M, N), dtype=torch.float32 if variant == "fp8" else torch.int32, device="cuda")
+    C = torch.empty((M, N), dtype=torch.float32 if variant in ("fp8", "fp8bs") else torch.int32, device="cuda")
     # L2 between steps: either every step reads its own copy of the operands,
     # rotating over copies worth three L2 capacities (a step's operands were last
     # touched two or more steps ago, and all later reads evicted them), or a
@@ -322,6 +338,8 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
     c_host = torch.empty((M, N), dtype=C.dtype).pin_memory()
     a_e, bp_e = torch.empty_like(a_in), torch.empty_like(bp)
     C_e = torch.empty_like(C)
+    # other per-step inputs (the fp8bs scales): (pinned host copy, device tensor the call reads)
+    extra_inputs = [(x.cpu().pin_memory(), x) for x in (sfa_d, sfb_d)] if variant == "fp8bs" else []
     e_s = torch.cuda.Event(enable_timing=True)
     e_e = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -329,6 +347,8 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
     for _ in range(e2e_steps):
         a_e.copy_(a_host, non_blocking=True)
         bp_e.copy_(bp_host, non_blocking=True)
+        for host, devt in extra_inputs:
+            devt.copy_(host, non_blocking=True)
         gemm(a_e, bp_e, C_e, M, N, K, stream)
         c_host.copy_(C_e, non_blocking=True)
     e_e.record(stream)
@@ -351,7 +371,8 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
         peak = E4M3_PER_BF16 * peaks["bf16_tflops"]
         achieved = ops / gemm_kernel_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": traffic, "kernel": "igemm_ss_kernel",
+                "frac": achieved / peak, "traffic": traffic,
+                "kernel": "igemm_bs_kernel" if variant == "fp8bs" else "igemm_ss_kernel",
                 "kernel_ms": 1e3 * gemm_kernel_s, "algorithmic_ops_per_launch": ops,
                 "peak_source": f"{peak_src} bf16 burst x {E4M3_PER_BF16} (nominal e4m3/bf16 ratio)",
                 "mma_macs_per_op": 2 if variant == "w4a8" else 1}
@@ -360,7 +381,8 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": {"i4i4": "int4", "w4a8": "int8xint4", "fp8": "e4m3 (float32 accumulate)"}[variant],
+        "dtype": {"i4i4": "int4", "w4a8": "int8xint4", "fp8": "e4m3 (float32 accumulate)",
+                  "fp8bs": "e4m3 with float32 block scales (float32 accumulate)"}[variant],
         "data": "synthetic (SplitMix64-seeded, uniform)",
         "config": {"workload": args.workload, "variant": variant, "M": M, "N": N, "K": K,
                    "l2": (f"operands rotate over {n_copies} copies ({n_copies * op_bytes / 1e6:.0f} MB, "
@@ -372,7 +394,8 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
         "gpu_launches": launched,
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": UNIT,
-                "h2d_bytes_per_step": int(a_in.numel() * a_in.element_size() + bp.numel()),
+                "h2d_bytes_per_step": int(a_in.numel() * a_in.element_size() + bp.numel() +
+                                          sum(d.numel() * d.element_size() for _, d in extra_inputs)),
                 "d2h_bytes_per_step": int(C.numel() * 4)},
         "roofline": roof,
     }
@@ -407,6 +430,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     variant, M, N, K, a, b = si.workload_operands(args.workload)
+    if variant == "fp8bs":
+        global _SCALES
+        _SCALES = si.block_scales(M, N, K, si.WORKLOADS[args.workload][4])
 
     if args.impl == "reference":
         run_reference(args, variant, M, N, K, a, b, rank, world)

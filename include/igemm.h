@@ -153,6 +153,29 @@ IGEMM_API int w4a8_gemm_scaled(const int8_t *A, const uint8_t *Bp, const float *
 IGEMM_API int fp8_gemm(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, cudaStream_t stream);
 
 /*
+ * Block-scaled fp8 GEMM (TileLang tutorial page low_precision_gemm.py,
+ * gemm_blockscaled: fp8 A (M,K) and B (N,K), float32 scale tensors SFA
+ * (M, ceil(K/g)) and SFB (N, ceil(K/g)) applied along K per block of g values,
+ * float32 accumulator; the page names g = 128 for sm100):
+ *   C[m,n] = sum_kb SFA[m,kb] * SFB[n,kb] * sum_{k in block kb} a[m,k] * b[n,k]
+ * with g = 128 and KB = ceil(K/128) blocks (the last one may be short).
+ *   A    [M, K] E4M3 bytes (device), read only
+ *   B    [N, K] E4M3 bytes (device), read only
+ *   SFA  [M, KB] float32 (device, row-major), read only
+ *   SFB  [N, KB] float32 (device, row-major), read only
+ *   C    [M, N] float32 (device), written
+ * Each block's partial sum comes from the tensor core (float32) and is scaled
+ * and added in float32 in block order; the order of the additions inside a
+ * block is not specified.  The scales are transposed into a workspace of
+ * 4 * KB * (M + N rounded up to 128 each) bytes from the library's pool.
+ * K % 16 == 0 (IGEMM_UNSUPPORTED_SHAPE otherwise); A, B and C 16-byte aligned,
+ * SFA and SFB 4-byte aligned (IGEMM_MISALIGNED); K == 0 zeroes C; empty shapes
+ * are no-ops.
+ */
+IGEMM_API int fp8_blockscaled_gemm(const uint8_t *A, const uint8_t *B, const float *SFA, const float *SFB, float *C,
+                                   int M, int N, int K, cudaStream_t stream);
+
+/*
  * Pack logical int4 values two per byte (TileLang tutorial page
  * low_precision_gemm.py, pack_int4): packed[r, j] = (logical[r, 2j] & 0xF) |
  * ((logical[r, 2j+1] & 0xF) << 4).  Values outside [-8, 7] are masked to four

@@ -19,13 +19,14 @@ from .build import LIB_PATH, build as build_library
 
 __all__ = [
     "IgemmError", "load", "i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "w4a8_gemm_scaled", "fp8_gemm", "pack_int4",
-    "unpack_int4",
+    "fp8_blockscaled_gemm", "unpack_int4",
     "igemm_strerror",
     "igemm_last_status", "igemm_watchdog_selftest", "igemm_kernels_launched", "igemm_time_next_gemm",
     "EXPORTED_SYMBOLS", "LIB_PATH", "build_library",
 ]
 
-EXPORTED_SYMBOLS = ("i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "w4a8_gemm_scaled", "fp8_gemm", "pack_int4", "unpack_int4", "igemm_strerror", "igemm_last_status",
+EXPORTED_SYMBOLS = ("i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "w4a8_gemm_scaled", "fp8_gemm",
+                    "fp8_blockscaled_gemm", "pack_int4", "unpack_int4", "igemm_strerror", "igemm_last_status",
                     "igemm_watchdog_selftest", "igemm_kernels_launched",
                     "igemm_time_next_gemm")
 
@@ -72,6 +73,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.w4a8_gemm_scaled.restype = i
     lib.fp8_gemm.argtypes = [p, p, p, i, i, i, p]
     lib.fp8_gemm.restype = i
+    lib.fp8_blockscaled_gemm.argtypes = [p, p, p, p, p, i, i, i, p]
+    lib.fp8_blockscaled_gemm.restype = i
     lib.w4a8_gemm.argtypes = [p, p, p, i, i, i, p]
     lib.w4a8_gemm.restype = i
     lib.pack_int4.argtypes = [p, p, i64, i64, p]
@@ -140,6 +143,13 @@ def w4a8_gemm_scaled(A, Bp, scale_a, scale_b, C, M: int, N: int, K: int, stream=
 def fp8_gemm(A, B, C, M: int, N: int, K: int, stream=None) -> None:
     """C[M,N] (float32) = A . B^T for E4M3 byte matrices A [M,K] and B [N,K]."""
     _check(load().fp8_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(stream)), "fp8_gemm")
+
+
+def fp8_blockscaled_gemm(A, B, SFA, SFB, C, M: int, N: int, K: int, stream=None) -> None:
+    """C[M,N] (float32) = sum over 128-k blocks kb of SFA[m,kb] * SFB[n,kb] * (A . B^T over the block),
+    for E4M3 byte matrices A [M,K], B [N,K] and float32 scales SFA [M,ceil(K/128)], SFB [N,ceil(K/128)]."""
+    _check(load().fp8_blockscaled_gemm(_ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(C), M, N, K, _stream(stream)),
+           "fp8_blockscaled_gemm")
 
 
 def pack_int4(logical, packed, rows: int, K: int, stream=None) -> None:

@@ -398,6 +398,22 @@ extern "C" int fp8_gemm(const uint8_t *A, const uint8_t *B, float *C, int M, int
     return launch_fp8(A, B, C, M, N, K, stream);
 }
 
+static bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+extern "C" int fp8_blockscaled_gemm(const uint8_t *A, const uint8_t *B, const float *SFA, const float *SFB, float *C,
+                                    int M, int N, int K, cudaStream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0) return kInvalidArgument;
+    if (M == 0 || N == 0) return kOk;
+    if (!C) return kInvalidArgument;
+    if (K % 16 != 0) return kUnsupportedShape;
+    if (!aligned16(C)) return kMisaligned;
+    if (K == 0) return cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 4, stream) == cudaSuccess ? kOk : kCudaError;
+    if (!A || !B || !SFA || !SFB) return kInvalidArgument;
+    if (!aligned16(A) || !aligned16(B) || !aligned4(SFA) || !aligned4(SFB)) return kMisaligned;
+    return launch_fp8_blockscaled(A, B, SFA, SFB, C, M, N, K, stream);
+}
+
 extern "C" int pack_int4(const int8_t *logical, uint8_t *packed, int64_t rows, int64_t K, cudaStream_t stream)
 {
     if (rows < 0 || K < 0) return kInvalidArgument;

@@ -1,0 +1,319 @@
+// Block-scaled fp8 GEMM: the TileLang tutorial's gemm_blockscaled
+// (low_precision_gemm.py): A [M, K] and B [N, K] E4M3, float32 scales
+// SFA [M, KB] and SFB [N, KB] with KB = ceil(K / 128), applied along K per
+// block of 128 values (the granularity the page gives for sm100), float32
+// accumulation and output:
+//
+//   C[m,n] = sum_kb SFA[m,kb] * SFB[n,kb] * sum_{k in block kb} A[m,k] * B[n,k]
+//
+// The scales are arbitrary float32 values, which the hardware block-scaled MMA
+// kinds (power-of-two UE8M0 scales per 32 values) cannot carry, so each
+// 128-k block is its own MMA sum and the scaling is done on the CUDA cores:
+//
+//  * tcgen05.mma kind::f8f6f4 (both operands in 128-byte-swizzled shared
+//    memory, TMA-loaded) writes the block's partial tile (128 x 128 float32)
+//    into one of two TMEM buffers, so the MMAs of block kb + 1 run while
+//    block kb is promoted.
+//  * Eight epilogue warps (two per TMEM lane quadrant, 64 columns each) read
+//    the partial, multiply it by SFB[n,kb] and SFA[m,kb] and add it to float32
+//    totals held in registers; after the last block they store the tile.
+//  * The scales reach the CTA through their own small ring: a preparation
+//    pass has transposed them to [KB][rows] (one 512-byte row segment per
+//    block and tile), loaded with bulk copies; the operand ring is released
+//    by the MMAs, the scale ring by the epilogue.
+//
+// Warp roles: warps 0-7 epilogue; warp 8 producer (the first kIssuers lanes
+// operand stages, the next lane scale stages); warp 9 TMEM allocation and MMA
+// issue.  Persistent
+// CTAs, tiles in groups of A tiles (A fastest) so a group's A rows stay in
+// L2.  Every wait is bounded (ptx.cuh wait_bounded).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include "ptx.cuh"
+
+namespace igemm {
+
+struct BsParams {
+    float *C;             // [M, N] row-major
+    const float *sfa_t;   // [KB][m_pad] transposed SFA
+    const float *sfb_t;   // [KB][n_pad] transposed SFB
+    int M, N, K;
+    int m_tiles, n_tiles, kb_total;
+    int m_pad, n_pad;     // multiples of 128
+    int group_m;          // A tiles per group
+    int num_tiles;
+    int *status;
+    unsigned long long limit_ns;
+};
+
+template <int ST_, int SS_>
+struct BsCfg {
+    static constexpr int ST = ST_;          // operand stages (A + B of one 128-k block)
+    static constexpr int SS = SS_;          // scale stages
+    static constexpr int kBK = 128;
+    static constexpr int kTileA = 128 * 128;  // bytes
+    static constexpr int kTileB = 128 * 128;
+    static constexpr int kStage = kTileA + kTileB;
+    static constexpr int kScaleStage = 2 * 128 * 4;  // sa[128] then sb[128]
+    static constexpr int kIssuers = ST % 4 == 0 ? 4 : ST;  // operand-stage lanes; the next lane loads scales
+    static constexpr int kWarpProd = 8, kWarpMma = 9;
+    static constexpr int kThreads = 32 * 10;
+    static constexpr int kTmemCols = 256;   // two partial buffers of 128 columns
+    static constexpr int kOffStages = 0;
+    static constexpr int kOffScales = kOffStages + ST * kStage;
+    static constexpr int kOffBars = kOffScales + SS * kScaleStage;
+    static constexpr int kNumBars = 2 * ST + 2 * SS + 4 + 1;
+    static constexpr int kOffMisc = kOffBars + 8 * kNumBars;
+    static constexpr int kSmemBytes = 1024 + kOffMisc + 64;
+    static_assert(ST % kIssuers == 0 && kIssuers < 32, "each issuing lane owns fixed stages");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ void bulk_load_1d(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bs_tile(const BsParams &prm, int u, int &m0, int &n0)
+{
+    const int per_group = prm.group_m * prm.n_tiles;
+    const int grp = u / per_group;
+    const int first = grp * prm.group_m;
+    const int gsize = min(prm.m_tiles - first, prm.group_m);
+    const int r = u - grp * per_group;
+    m0 = (first + r % gsize) * 128;
+    n0 = (r / gsize) * 128;
+}
+
+__device__ __forceinline__ bool bs_warp_wait(uint64_t *bar, uint32_t parity, const Watchdog &wd)
+{
+    const bool ok = wait_bounded(bar, parity, wd);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void bs_wait_drain(uint64_t *bar, uint32_t parity, unsigned long long limit_ns)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < limit_ns) {
+    }
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
+    igemm_bs_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                    const BsParams prm)
+{
+    constexpr int ST = Cfg::ST, SS = Cfg::SS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint8_t *stages = smem + Cfg::kOffStages;
+    float *scales = reinterpret_cast<float *>(smem + Cfg::kOffScales);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBars);
+    uint64_t *full = bars;                 // [ST] operands landed (1 + tx)
+    uint64_t *empty = full + ST;           // [ST] consumed (MMA commit)
+    uint64_t *s_full = empty + ST;         // [SS] scales landed (1 + tx)
+    uint64_t *s_empty = s_full + SS;       // [SS] read (8 epilogue warps)
+    uint64_t *p_full = s_empty + SS;       // [2] partial tile in TMEM (commit)
+    uint64_t *p_empty = p_full + 2;        // [2] partial read (8 epilogue warps)
+    uint64_t *mma_drain = p_empty + 2;     // final commit of the MMA thread
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int kbt = prm.kb_total;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < SS; ++s) {
+            mbar_init(&s_full[s], 1);
+            mbar_init(&s_empty[s], 8);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&p_full[b], 1);
+            mbar_init(&p_empty[b], 8);
+        }
+        mbar_init(mma_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_map(&mapA);
+        tma_prefetch_map(&mapB);
+    }
+    if (warp == Cfg::kWarpMma) {
+        tmem_alloc(tmem_slot, Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Watchdog wd{abort_flag, prm.status, prm.limit_ns};
+
+    if (warp == Cfg::kWarpProd) {
+        // ------------------------------------------------------------ producer
+        if (lane < Cfg::kIssuers) {
+            // operand stages: lane l issues the stages congruent to l
+            uint32_t g = 0, issued_mask = 0, last_phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < prm.num_tiles; u += gridDim.x) {
+                int m0, n0;
+                bs_tile(prm, u, m0, n0);
+                for (int kb = 0; kb < kbt; ++kb, ++g) {
+                    const int s = static_cast<int>(g % ST);
+                    if (s % Cfg::kIssuers != lane) continue;
+                    const uint32_t ph = (g / ST) & 1u;
+                    if (!wait_bounded(&empty[s], ph ^ 1u, wd)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *st = stages + s * Cfg::kStage;
+                    mbar_arrive_expect_tx(&full[s], Cfg::kStage);
+                    tma_load_2d(st, &mapA, &full[s], kb * Cfg::kBK, m0);
+                    tma_load_2d(st + Cfg::kTileA, &mapB, &full[s], kb * Cfg::kBK, n0);
+                    issued_mask |= 1u << s;
+                    last_phase = (last_phase & ~(1u << s)) | (ph << s);
+                }
+            }
+#pragma unroll 1
+            for (int s = 0; s < ST; ++s)
+                if ((issued_mask >> s) & 1u) bs_wait_drain(&full[s], (last_phase >> s) & 1u, prm.limit_ns);
+        } else if (lane == Cfg::kIssuers) {
+            // scale stages: the transposed scales are written by the preparation
+            // pass this grid may overlap
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            uint32_t g = 0, issued_mask = 0, last_phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < prm.num_tiles; u += gridDim.x) {
+                int m0, n0;
+                bs_tile(prm, u, m0, n0);
+                for (int kb = 0; kb < kbt; ++kb, ++g) {
+                    const int s = static_cast<int>(g % SS);
+                    const uint32_t ph = (g / SS) & 1u;
+                    if (!wait_bounded(&s_empty[s], ph ^ 1u, wd)) {
+                        ok = false;
+                        break;
+                    }
+                    float *dst = scales + s * (Cfg::kScaleStage / 4);
+                    mbar_arrive_expect_tx(&s_full[s], Cfg::kScaleStage);
+                    bulk_load_1d(dst, prm.sfa_t + static_cast<int64_t>(kb) * prm.m_pad + m0, 512, &s_full[s]);
+                    bulk_load_1d(dst + 128, prm.sfb_t + static_cast<int64_t>(kb) * prm.n_pad + n0, 512, &s_full[s]);
+                    issued_mask |= 1u << s;
+                    last_phase = (last_phase & ~(1u << s)) | (ph << s);
+                }
+            }
+#pragma unroll 1
+            for (int s = 0; s < SS; ++s)
+                if ((issued_mask >> s) & 1u) bs_wait_drain(&s_full[s], (last_phase >> s) & 1u, prm.limit_ns);
+        }
+    } else if (warp == Cfg::kWarpMma) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_e4m3_f32(128, 128);
+            const uint64_t desc0 = sdesc_kmajor_sw128(smem_u32(stages));
+            uint32_t g = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < prm.num_tiles; u += gridDim.x) {
+                for (int kb = 0; kb < kbt; ++kb, ++g) {
+                    const int s = static_cast<int>(g % ST);
+                    const int pb = static_cast<int>(g & 1u);
+                    if (!wait_bounded(&p_empty[pb], ((g >> 1) & 1u) ^ 1u, wd) ||
+                        !wait_bounded(&full[s], (g / ST) & 1u, wd)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a0 = desc0 + static_cast<uint64_t>((s * Cfg::kStage) >> 4);
+                    const uint64_t b0 = a0 + static_cast<uint64_t>(Cfg::kTileA >> 4);
+                    const uint32_t d_tmem = tmem + pb * 128;
+#pragma unroll
+                    for (int q = 0; q < Cfg::kBK / 32; ++q)
+                        mma_f8f6f4(d_tmem, a0 + static_cast<uint64_t>(2 * q), b0 + static_cast<uint64_t>(2 * q), idesc,
+                                   q > 0 ? 1u : 0u);
+                    mma_commit(&empty[s]);
+                    mma_commit(&p_full[pb]);
+                }
+            }
+            mma_commit(mma_drain);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 0-7)
+        const int quad = warp & 3, half = warp >> 2;
+        const int r = quad * 32 + lane;  // tile row = TMEM lane
+        const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * 64;
+        uint32_t g = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < prm.num_tiles; u += gridDim.x) {
+            int m0, n0;
+            bs_tile(prm, u, m0, n0);
+            float tot[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) tot[j] = 0.0f;
+            for (int kb = 0; kb < kbt; ++kb, ++g) {
+                const int pb = static_cast<int>(g & 1u);
+                const int ss = static_cast<int>(g % SS);
+                if (!bs_warp_wait(&p_full[pb], (g >> 1) & 1u, wd) || !bs_warp_wait(&s_full[ss], (g / SS) & 1u, wd)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t v[64];
+                tmem_ld_32x32b_x32(tbase + pb * 128, *reinterpret_cast<uint32_t(*)[32]>(v));
+                tmem_ld_32x32b_x32(tbase + pb * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_empty[pb]);  // the partial buffer may be rewritten
+                const float *sc = scales + ss * (Cfg::kScaleStage / 4);
+                const float sa = sc[r];
+                const float4 *sb4 = reinterpret_cast<const float4 *>(sc + 128 + half * 64);
+#pragma unroll
+                for (int j4 = 0; j4 < 16; ++j4) {
+                    const float4 b = sb4[j4];
+                    tot[4 * j4 + 0] = fmaf(__uint_as_float(v[4 * j4 + 0]) * b.x, sa, tot[4 * j4 + 0]);
+                    tot[4 * j4 + 1] = fmaf(__uint_as_float(v[4 * j4 + 1]) * b.y, sa, tot[4 * j4 + 1]);
+                    tot[4 * j4 + 2] = fmaf(__uint_as_float(v[4 * j4 + 2]) * b.z, sa, tot[4 * j4 + 2]);
+                    tot[4 * j4 + 3] = fmaf(__uint_as_float(v[4 * j4 + 3]) * b.w, sa, tot[4 * j4 + 3]);
+                }
+                fence_proxy_async_smem();  // generic reads before the bulk copy refills the stage
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_empty[ss]);  // the scale stage may be refilled
+            }
+            if (!ok) break;
+            const int m = m0 + r;
+            const int nb = n0 + half * 64;
+            if (m < prm.M) {
+                float *crow = prm.C + static_cast<int64_t>(m) * prm.N + nb;
+                if (nb + 64 <= prm.N && (prm.N & 3) == 0) {
+#pragma unroll
+                    for (int j4 = 0; j4 < 16; ++j4)
+                        reinterpret_cast<float4 *>(crow)[j4] =
+                            make_float4(tot[4 * j4], tot[4 * j4 + 1], tot[4 * j4 + 2], tot[4 * j4 + 3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j)
+                        if (nb + j < prm.N) crow[j] = tot[j];
+                }
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == Cfg::kWarpMma) {
+        if (lane == 0) bs_wait_drain(mma_drain, 0, prm.limit_ns);
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, Cfg::kTmemCols);
+    }
+}
+
+}  // namespace igemm

@@ -391,5 +391,7 @@ constexpr size_t kNoAllocWorkspaceBytes = size_t(32) << 20;
 int launch_i4i4_noalloc(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);
 int launch_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);
 int launch_fp8(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, cudaStream_t stream);
+int launch_fp8_blockscaled(const uint8_t *A, const uint8_t *B, const float *SFA, const float *SFB, float *C, int M,
+                           int N, int K, cudaStream_t stream);
 
 }  // namespace igemm

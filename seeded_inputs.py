@@ -81,8 +81,18 @@ def e4m3_bytes(seed: int, shape) -> np.ndarray:
     return out.reshape(shape)
 
 
+def scale_values(seed: int, shape) -> np.ndarray:
+    """Positive float32 scales (1 + u) * 2^e with u = the next 20 bits / 2^20 in
+    [0, 1) and e = the top 3 bits - 4 in [-4, 3]: magnitudes over [1/16, 16)."""
+    n = int(np.prod(shape, dtype=np.int64))
+    x = splitmix64(seed, n)
+    e = (x >> np.uint64(61)).astype(np.int64) - 4
+    u = ((x >> np.uint64(41)) & np.uint64(0xFFFFF)).astype(np.float64) / float(1 << 20)
+    return np.ldexp(1.0 + u, e).astype(np.float32).reshape(shape)
+
+
 def workload_seed(index: int, operand: int) -> int:
-    """Seed of operand 0 (A) or 1 (B) of workload ``index``."""
+    """Seed of operand 0 (A), 1 (B), 2 (scales of A) or 3 (scales of B) of workload ``index``."""
     return 0x1A2B0000 + 16 * index + operand
 
 
@@ -97,13 +107,15 @@ WORKLOADS = {
     "w4a8_ragged_4000x12288x5120": ("w4a8", 4000, 12288, 5120, 6),
     # the tutorial's fp8 GEMM (a "next" row): E4M3 operands, float32 C
     "fp8_8192": ("fp8", 8192, 8192, 8192, 7),
+    # the tutorial's block-scaled fp8 GEMM (a "next" row): plus float32 scales per 128-k block
+    "fp8bs_8192": ("fp8bs", 8192, 8192, 8192, 8),
 }
 
 
 def logical_operands(variant: str, M: int, N: int, K: int, index: int):
     """Logical (unpacked) operands: A [M,K] int8 and B [N,K] int8 (int4 range);
-    for "fp8", A [M,K] and B [N,K] E4M3 bytes."""
-    if variant == "fp8":
+    for "fp8" and "fp8bs", A [M,K] and B [N,K] E4M3 bytes."""
+    if variant in ("fp8", "fp8bs"):
         return e4m3_bytes(workload_seed(index, 0), (M, K)), e4m3_bytes(workload_seed(index, 1), (N, K))
     if variant == "i4i4":
         a = int4_values(workload_seed(index, 0), (M, K))
@@ -113,6 +125,12 @@ def logical_operands(variant: str, M: int, N: int, K: int, index: int):
         raise ValueError(f"unknown variant {variant!r}")
     b = int4_values(workload_seed(index, 1), (N, K))
     return a, b
+
+
+def block_scales(M: int, N: int, K: int, index: int, g: int = 128):
+    """SFA [M, ceil(K/g)] and SFB [N, ceil(K/g)] for the block-scaled fp8 GEMM."""
+    kb = -(-K // g)
+    return scale_values(workload_seed(index, 2), (M, kb)), scale_values(workload_seed(index, 3), (N, kb))
 
 
 def workload_operands(name: str):

@@ -83,6 +83,18 @@ def test_pack_argument_validation(lib):
     assert lib.pack_int4(None, FAKE, 4, 8, None) == pig.IGEMM_INVALID_ARGUMENT
 
 
+def test_fp8_blockscaled_argument_validation(lib):
+    f = lib.fp8_blockscaled_gemm
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 4, 16, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 24, None) == pig.IGEMM_UNSUPPORTED_SHAPE
+    assert f(None, None, None, None, None, 0, 4, 16, None) == pig.IGEMM_OK
+    assert f(None, FAKE, FAKE, FAKE, FAKE, 4, 4, 16, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert f(FAKE, FAKE, FAKE, None, FAKE, 4, 4, 16, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE + 4, 4, 4, 16, None) == pig.IGEMM_MISALIGNED
+    assert f(FAKE, FAKE, FAKE + 2, FAKE, FAKE, 4, 4, 16, None) == pig.IGEMM_MISALIGNED
+    assert f(FAKE + 8, FAKE, FAKE, FAKE, FAKE, 4, 4, 16, None) == pig.IGEMM_MISALIGNED
+
+
 def test_unpack_argument_validation(lib):
     assert lib.unpack_int4(FAKE, FAKE, -1, 4, None) == pig.IGEMM_INVALID_ARGUMENT
     assert lib.unpack_int4(FAKE, FAKE, 4, 3, None) == pig.IGEMM_UNSUPPORTED_SHAPE

@@ -211,6 +211,68 @@ def test_fp8_matches_oracle(orc, M, N, K):
     assert np.all(np.abs(C - want) <= tol), float(np.max(np.abs(C - want) / np.maximum(mag, 1e-30)))
 
 
+# Block-scaled fp8: K tails inside a 128-k block (K % 128 != 0), one block, M/N
+# tails, N % 4 != 0 (scalar stores), several tiles per CTA, deep K.
+FP8BS_SHAPES = [(128, 128, 128), (1, 1, 16), (130, 300, 304), (256, 260, 1040), (300, 520, 4096), (64, 129, 16384),
+                (1024, 1024, 2048)]
+
+
+def run_fp8bs(A, B, sfa, sfb):
+    M, K = A.shape
+    N = B.shape[0]
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    pig.fp8_blockscaled_gemm(dev(A), dev(B), dev(sfa), dev(sfb), C, M, N, K)
+    assert pig.igemm_last_status() == 0
+    return C.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("M,N,K", FP8BS_SHAPES)
+def test_fp8_blockscaled_matches_oracle(orc, M, N, K):
+    # every block's partial sum, its scaling and the running sum are float32
+    # roundings; any order of at most K + 3*KB of them stays within
+    # K * 2^-23 * sum |a*b*sfa*sfb| (the oracle's Cabs)
+    A = si.e4m3_bytes(7100 + M, (M, K))
+    B = si.e4m3_bytes(7200 + N, (N, K))
+    sfa = si.scale_values(7300 + M, (M, -(-K // 128)))
+    sfb = si.scale_values(7400 + N, (N, -(-K // 128)))
+    got = run_fp8bs(A, B, sfa, sfb)
+    want, wabs = orc.fp8_blockscaled(A, B, sfa, sfb, K)
+    tol = max(K, 16) * 2.0 ** -23 * wabs + 1e-30
+    assert np.all(np.abs(got - want) <= tol), float(np.max(np.abs(got - want) / np.maximum(wabs, 1e-30)))
+
+
+def test_fp8_blockscaled_exact_cases(orc):
+    # integer codes (bytes 0..15 are the integers times 2^-9) and power-of-two
+    # scales: every partial, product and sum is exact, so the result is
+    # bit-identical to the oracle's
+    M, N, K = 200, 300, 1024
+    rng = np.random.default_rng(11)
+    A = rng.integers(0, 16, size=(M, K)).astype(np.uint8)
+    B = rng.integers(0, 16, size=(N, K)).astype(np.uint8)
+    # scales 1, 2 or 4: every addend is a multiple of 2^-18 and the sums stay below
+    # 8 * 128 * 225 * 2^-18 * 16 = 14, where float32 still resolves 2^-18
+    sfa = np.ldexp(1.0, rng.integers(0, 3, size=(M, K // 128))).astype(np.float32)
+    sfb = np.ldexp(1.0, rng.integers(0, 3, size=(N, K // 128))).astype(np.float32)
+    got = run_fp8bs(A, B, sfa, sfb)
+    want, _ = orc.fp8_blockscaled(A, B, sfa, sfb, K)
+    assert np.array_equal(got, want)
+    # unit scales give the plain fp8 GEMM's exact result
+    ones_a, ones_b = np.ones((M, K // 128), np.float32), np.ones((N, K // 128), np.float32)
+    got1 = run_fp8bs(A, B, ones_a, ones_b)
+    want1, _ = orc.fp8_gemm(A, B, K)
+    assert np.array_equal(got1, want1)
+
+
+def test_fp8_blockscaled_full_size_sampled(orc):
+    variant, M, N, K, A, B = si.workload_operands("fp8bs_8192")
+    sfa, sfb = si.block_scales(M, N, K, si.WORKLOADS["fp8bs_8192"][4])
+    got = run_fp8bs(A, B, sfa, sfb)
+    rng = np.random.default_rng(13)
+    rows = np.unique(rng.integers(0, M, 24))
+    want, wabs = orc.fp8_blockscaled(np.ascontiguousarray(A[rows]), B, np.ascontiguousarray(sfa[rows]), sfb, K)
+    assert np.all(np.abs(got[rows] - want) <= K * 2.0 ** -23 * wabs + 1e-30)
+
+
 @pytest.mark.parametrize("M,N,K", [(256, 256, 4096), (130, 300, 96), (128, 128, 65536)])
 def test_fp8_integer_codes_are_exact(orc, M, N, K):
     # bytes 0..15 are the integers 0..15 times 2^-9; every partial sum is an integer
