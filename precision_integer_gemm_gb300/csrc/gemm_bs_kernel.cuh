@@ -12,9 +12,9 @@
 //
 //  * tcgen05.mma kind::f8f6f4 (both operands in 128-byte-swizzled shared
 //    memory, TMA-loaded) writes the block's partial tile (128 x 128 float32)
-//    into one of two TMEM buffers, so the MMAs of block kb + 1 run while
+//    into one of PB TMEM buffers, so the MMAs of the next blocks run while
 //    block kb is promoted.
-//  * Eight epilogue warps (two per TMEM lane quadrant, 64 columns each) read
+//  * Epilogue warps (EPQ per TMEM lane quadrant, 128 / EPQ columns each) read
 //    the partial, multiply it by SFB[n,kb] and SFA[m,kb] and add it to float32
 //    totals held in registers; after the last block they store the tile.
 //  * The scales reach the CTA through their own small ring: a preparation
@@ -22,11 +22,11 @@
 //    block and tile), loaded with bulk copies; the operand ring is released
 //    by the MMAs, the scale ring by the epilogue.
 //
-// Warp roles: warps 0-7 epilogue; warp 8 producer (the first kIssuers lanes
-// operand stages, the next lane scale stages); warp 9 TMEM allocation and MMA
-// issue.  Persistent
-// CTAs, tiles in groups of A tiles (A fastest) so a group's A rows stay in
-// L2.  Every wait is bounded (ptx.cuh wait_bounded).
+// Warp roles: warps 0 .. 4*EPQ-1 epilogue; then the producer (its first
+// kIssuers lanes the operand stages, the next one the scale stages); then
+// TMEM allocation and MMA issue.  Persistent CTAs, tiles in groups of A tiles
+// (A fastest) so a group's A rows stay in L2.  Every wait is bounded (ptx.cuh
+// wait_bounded).
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -47,26 +47,38 @@ struct BsParams {
     unsigned long long limit_ns;
 };
 
-template <int ST_, int SS_>
+template <int ST_, int SS_, int EPQ_ = 2, int PB_ = 4>
 struct BsCfg {
     static constexpr int ST = ST_;          // operand stages (A + B of one 128-k block)
     static constexpr int SS = SS_;          // scale stages
+    static constexpr int EPQ = EPQ_;        // epilogue warps per TMEM lane quadrant
+    static constexpr int CW = 128 / EPQ;    // partial-tile columns per epilogue warp
+    // partial-tile buffers in TMEM: the MMAs run up to PB - 1 blocks ahead of the
+    // promotion (with two, each block waited for a whole MMA -> commit -> load ->
+    // release round trip)
+    static constexpr int PB = PB_;
+    static constexpr int kEpiWarps = 4 * EPQ;
     static constexpr int kBK = 128;
     static constexpr int kTileA = 128 * 128;  // bytes
     static constexpr int kTileB = 128 * 128;
     static constexpr int kStage = kTileA + kTileB;
     static constexpr int kScaleStage = 2 * 128 * 4;  // sa[128] then sb[128]
-    static constexpr int kIssuers = ST % 4 == 0 ? 4 : ST;  // operand-stage lanes; the next lane loads scales
-    static constexpr int kWarpProd = 8, kWarpMma = 9;
-    static constexpr int kThreads = 32 * 10;
-    static constexpr int kTmemCols = 256;   // two partial buffers of 128 columns
+    static constexpr int kIssuers = ST % 4 == 0 ? 4 : ST;  // operand-stage lanes
+    // scale-stage lanes (the next ones; four measured 10 % slower than one)
+    static constexpr int kScaleIssuers = 1;
+    static_assert(SS % kScaleIssuers == 0, "each scale lane owns fixed stages");
+    static constexpr int kWarpProd = kEpiWarps, kWarpMma = kEpiWarps + 1;
+    static constexpr int kThreads = 32 * (kEpiWarps + 2);
+    static_assert(EPQ == 2 || EPQ == 4, "epilogue warps per quadrant");
+    static constexpr int kTmemCols = PB * 128 <= 256 ? 256 : 512;  // PB partial buffers of 128 columns
+    static_assert(PB == 2 || PB == 4, "partial buffers");
     static constexpr int kOffStages = 0;
     static constexpr int kOffScales = kOffStages + ST * kStage;
     static constexpr int kOffBars = kOffScales + SS * kScaleStage;
-    static constexpr int kNumBars = 2 * ST + 2 * SS + 4 + 1;
+    static constexpr int kNumBars = 2 * ST + 2 * SS + 2 * PB + 1;
     static constexpr int kOffMisc = kOffBars + 8 * kNumBars;
     static constexpr int kSmemBytes = 1024 + kOffMisc + 64;
-    static_assert(ST % kIssuers == 0 && kIssuers < 32, "each issuing lane owns fixed stages");
+    static_assert(ST % kIssuers == 0 && kIssuers + 4 <= 32, "each issuing lane owns fixed stages");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -117,10 +129,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     uint64_t *full = bars;                 // [ST] operands landed (1 + tx)
     uint64_t *empty = full + ST;           // [ST] consumed (MMA commit)
     uint64_t *s_full = empty + ST;         // [SS] scales landed (1 + tx)
-    uint64_t *s_empty = s_full + SS;       // [SS] read (8 epilogue warps)
-    uint64_t *p_full = s_empty + SS;       // [2] partial tile in TMEM (commit)
-    uint64_t *p_empty = p_full + 2;        // [2] partial read (8 epilogue warps)
-    uint64_t *mma_drain = p_empty + 2;     // final commit of the MMA thread
+    uint64_t *s_empty = s_full + SS;       // [SS] read (every epilogue warp)
+    uint64_t *p_full = s_empty + SS;       // [PB] partial tile in TMEM (commit)
+    uint64_t *p_empty = p_full + Cfg::PB;  // [PB] partial read (every epilogue warp)
+    uint64_t *mma_drain = p_empty + Cfg::PB;  // final commit of the MMA thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
 
@@ -135,11 +147,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
         for (int s = 0; s < SS; ++s) {
             mbar_init(&s_full[s], 1);
-            mbar_init(&s_empty[s], 8);
+            mbar_init(&s_empty[s], Cfg::kEpiWarps);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < Cfg::PB; ++b) {
             mbar_init(&p_full[b], 1);
-            mbar_init(&p_empty[b], 8);
+            mbar_init(&p_empty[b], Cfg::kEpiWarps);
         }
         mbar_init(mma_drain, 1);
         *abort_flag = 0;
@@ -185,10 +197,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 #pragma unroll 1
             for (int s = 0; s < ST; ++s)
                 if ((issued_mask >> s) & 1u) bs_wait_drain(&full[s], (last_phase >> s) & 1u, prm.limit_ns);
-        } else if (lane == Cfg::kIssuers) {
-            // scale stages: the transposed scales are written by the preparation
-            // pass this grid may overlap
+        } else if (lane < Cfg::kIssuers + Cfg::kScaleIssuers) {
+            // scale stages (lane j owns the stages congruent to j): the transposed
+            // scales are written by the preparation pass this grid may overlap
             asm volatile("griddepcontrol.wait;" ::: "memory");
+            const int j = lane - Cfg::kIssuers;
             uint32_t g = 0, issued_mask = 0, last_phase = 0;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < prm.num_tiles; u += gridDim.x) {
@@ -196,6 +209,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 bs_tile(prm, u, m0, n0);
                 for (int kb = 0; kb < kbt; ++kb, ++g) {
                     const int s = static_cast<int>(g % SS);
+                    if (s % Cfg::kScaleIssuers != j) continue;
                     const uint32_t ph = (g / SS) & 1u;
                     if (!wait_bounded(&s_empty[s], ph ^ 1u, wd)) {
                         ok = false;
@@ -223,8 +237,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             for (int u = blockIdx.x; ok && u < prm.num_tiles; u += gridDim.x) {
                 for (int kb = 0; kb < kbt; ++kb, ++g) {
                     const int s = static_cast<int>(g % ST);
-                    const int pb = static_cast<int>(g & 1u);
-                    if (!wait_bounded(&p_empty[pb], ((g >> 1) & 1u) ^ 1u, wd) ||
+                    const int pb = static_cast<int>(g % Cfg::PB);
+                    if (!wait_bounded(&p_empty[pb], ((g / Cfg::PB) & 1u) ^ 1u, wd) ||
                         !wait_bounded(&full[s], (g / ST) & 1u, wd)) {
                         ok = false;
                         break;
@@ -244,61 +258,75 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             mma_commit(mma_drain);
         }
     } else {
-        // ------------------------------------------------------------ epilogue (warps 0-7)
-        const int quad = warp & 3, half = warp >> 2;
+        // ------------------------------------------------------------ epilogue
+        constexpr int CW = Cfg::CW;
+        const int quad = warp & 3, part = warp >> 2;
         const int r = quad * 32 + lane;  // tile row = TMEM lane
-        const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * 64;
+        const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) + part * CW;
+        // block G (counted over all tiles of the CTA): partial buffer G % PB, its
+        // use G / PB; scale stage G % SS, its use G / SS
+        auto fetch = [&](uint32_t (&dst)[CW], uint32_t G) -> bool {
+            const uint32_t pb = G % Cfg::PB;
+            if (!bs_warp_wait(&p_full[pb], (G / Cfg::PB) & 1u, wd)) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < CW; c += 32)
+                tmem_ld_32x32b_x32(tbase + pb * 128 + c, *reinterpret_cast<uint32_t(*)[32]>(dst + c));
+            return true;
+        };
+        auto retire = [&](uint32_t G) {  // the loads of block G are in registers: free its buffer
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_empty[G % Cfg::PB]);
+        };
+        auto promote = [&](float (&tot)[CW], const uint32_t (&v)[CW], uint32_t G) -> bool {
+            const int ss = static_cast<int>(G % SS);
+            if (!bs_warp_wait(&s_full[ss], (G / SS) & 1u, wd)) return false;
+            const float *sc = scales + ss * (Cfg::kScaleStage / 4);
+            const float sa = sc[r];
+            const float4 *sb4 = reinterpret_cast<const float4 *>(sc + 128 + part * CW);
+#pragma unroll
+            for (int j4 = 0; j4 < CW / 4; ++j4) {
+                const float4 b = sb4[j4];
+                tot[4 * j4 + 0] = fmaf(__uint_as_float(v[4 * j4 + 0]) * b.x, sa, tot[4 * j4 + 0]);
+                tot[4 * j4 + 1] = fmaf(__uint_as_float(v[4 * j4 + 1]) * b.y, sa, tot[4 * j4 + 1]);
+                tot[4 * j4 + 2] = fmaf(__uint_as_float(v[4 * j4 + 2]) * b.z, sa, tot[4 * j4 + 2]);
+                tot[4 * j4 + 3] = fmaf(__uint_as_float(v[4 * j4 + 3]) * b.w, sa, tot[4 * j4 + 3]);
+            }
+            fence_proxy_async_smem();  // generic reads before the bulk copy refills the stage
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_empty[ss]);
+            return true;
+        };
         uint32_t g = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < prm.num_tiles; u += gridDim.x) {
             int m0, n0;
             bs_tile(prm, u, m0, n0);
-            float tot[64];
+            float tot[CW];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) tot[j] = 0.0f;
-            for (int kb = 0; kb < kbt; ++kb, ++g) {
-                const int pb = static_cast<int>(g & 1u);
-                const int ss = static_cast<int>(g % SS);
-                if (!bs_warp_wait(&p_full[pb], (g >> 1) & 1u, wd) || !bs_warp_wait(&s_full[ss], (g / SS) & 1u, wd)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                uint32_t v[64];
-                tmem_ld_32x32b_x32(tbase + pb * 128, *reinterpret_cast<uint32_t(*)[32]>(v));
-                tmem_ld_32x32b_x32(tbase + pb * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&p_empty[pb]);  // the partial buffer may be rewritten
-                const float *sc = scales + ss * (Cfg::kScaleStage / 4);
-                const float sa = sc[r];
-                const float4 *sb4 = reinterpret_cast<const float4 *>(sc + 128 + half * 64);
-#pragma unroll
-                for (int j4 = 0; j4 < 16; ++j4) {
-                    const float4 b = sb4[j4];
-                    tot[4 * j4 + 0] = fmaf(__uint_as_float(v[4 * j4 + 0]) * b.x, sa, tot[4 * j4 + 0]);
-                    tot[4 * j4 + 1] = fmaf(__uint_as_float(v[4 * j4 + 1]) * b.y, sa, tot[4 * j4 + 1]);
-                    tot[4 * j4 + 2] = fmaf(__uint_as_float(v[4 * j4 + 2]) * b.z, sa, tot[4 * j4 + 2]);
-                    tot[4 * j4 + 3] = fmaf(__uint_as_float(v[4 * j4 + 3]) * b.w, sa, tot[4 * j4 + 3]);
-                }
-                fence_proxy_async_smem();  // generic reads before the bulk copy refills the stage
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s_empty[ss]);  // the scale stage may be refilled
+            for (int j = 0; j < CW; ++j) tot[j] = 0.0f;
+            uint32_t va[CW];
+            for (int kb = 0; ok && kb < kbt; ++kb, ++g) {
+                ok = fetch(va, g);
+                if (!ok) break;
+                retire(g);
+                ok = promote(tot, va, g);
             }
             if (!ok) break;
             const int m = m0 + r;
-            const int nb = n0 + half * 64;
+            const int nb = n0 + part * CW;
             if (m < prm.M) {
                 float *crow = prm.C + static_cast<int64_t>(m) * prm.N + nb;
-                if (nb + 64 <= prm.N && (prm.N & 3) == 0) {
+                if (nb + CW <= prm.N && (prm.N & 3) == 0) {
 #pragma unroll
-                    for (int j4 = 0; j4 < 16; ++j4)
+                    for (int j4 = 0; j4 < CW / 4; ++j4)
                         reinterpret_cast<float4 *>(crow)[j4] =
                             make_float4(tot[4 * j4], tot[4 * j4 + 1], tot[4 * j4 + 2], tot[4 * j4 + 3]);
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 64; ++j)
+                    for (int j = 0; j < CW; ++j)
                         if (nb + j < prm.N) crow[j] = tot[j];
                 }
             }
