@@ -1,14 +1,15 @@
 // Block-scaled fp8 GEMM (the tutorial's gemm_blockscaled): host side.  A pass
-// transposes the float32 scales to [KB][rows] (rows padded to whole 128-row
-// tiles with zeros) in a pool workspace; igemm_bs_kernel (gemm_bs_kernel.cuh)
-// launches early behind it and reads the scales only after it.
+// transposes the float32 scales to [KB][rows] (rows padded to whole tiles, and
+// for B to whole cluster slots, with zeros) in a pool workspace;
+// igemm_bs_kernel (gemm_bs_kernel.cuh) launches early behind it and reads the
+// scales only after it.
 #include "launch.cuh"
 #include "gemm_bs_kernel.cuh"
 
 namespace igemm {
 
-//                    operand stages  scale stages
-using CfgBs = BsCfg<6, 8>;
+//                  operand stages  scale stages  epilogue warps per quadrant  TMEM buffers  cluster
+using CfgBs = BsCfg<5, 8, 3, 2, 2>;
 
 // out[kb * pad + r] = sf[r * KB + kb] for r < rows, 0 for rows <= r < pad;
 // the SFA part first (pad_a rows), then the SFB part (pad_b rows).
@@ -47,7 +48,30 @@ int launch_fp8_blockscaled(const uint8_t *A, const uint8_t *B, const float *SFA,
         attr_set[dev] = true;
     }
     const int KB = (K + 127) / 128;
-    const int m_pad = (M + 127) / 128 * 128, n_pad = (N + 127) / 128 * 128;
+    const int m_tiles = (M + 127) / 128;
+    const int n_slots = ((N + Cfg::BN - 1) / Cfg::BN + Cfg::CL - 1) / Cfg::CL;
+    const int m_pad = m_tiles * 128, n_pad = n_slots * Cfg::CL * Cfg::BN;
+    int clusters = sm_count() / Cfg::CL;
+    if constexpr (Cfg::CL > 1) {
+        static int cache[64] = {};
+        if (dev < 64 && !cache[dev]) {
+            cudaLaunchConfig_t qc = {};
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = Cfg::CL;
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            qc.gridDim = dim3(Cfg::CL * sm_count(), 1, 1);
+            qc.blockDim = dim3(Cfg::kThreads, 1, 1);
+            qc.dynamicSmemBytes = Cfg::kSmemBytes;
+            qc.attrs = qa;
+            qc.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kernel, &qc) != cudaSuccess || n <= 0) return kCudaError;
+            cache[dev] = n;
+        }
+        if (dev < 64) clusters = cache[dev];
+    }
     const size_t a_bytes = ((size_t(KB) * m_pad * 4) + 255) & ~size_t(255);
     void *ws = nullptr;
     if (workspace_alloc(&ws, a_bytes + size_t(KB) * n_pad * 4, stream) != kOk) return kCudaError;
@@ -64,9 +88,9 @@ int launch_fp8_blockscaled(const uint8_t *A, const uint8_t *B, const float *SFA,
     }
     CUtensorMap mapA, mapB;
     if (rc == kOk)
-        rc = make_map(&mapA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+        rc = make_map(&mapA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, M, K, Cfg::kARows, 128, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc == kOk)
-        rc = make_map(&mapB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, N, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+        rc = make_map(&mapB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, N, K, Cfg::BN, 128, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc == kOk) {
         BsParams prm{};
         prm.C = C;
@@ -75,15 +99,15 @@ int launch_fp8_blockscaled(const uint8_t *A, const uint8_t *B, const float *SFA,
         prm.M = M;
         prm.N = N;
         prm.K = K;
-        prm.m_tiles = m_pad / 128;
-        prm.n_tiles = n_pad / 128;
+        prm.m_tiles = m_tiles;
+        prm.n_slots = n_slots;
         prm.kb_total = KB;
         prm.m_pad = m_pad;
         prm.n_pad = n_pad;
         // a group's A rows (32 MB) stay in L2 while every B tile passes
         prm.group_m = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(prm.m_tiles, (int64_t(32) << 20) /
                                                                                                 (int64_t(128) * K))));
-        prm.num_tiles = prm.m_tiles * prm.n_tiles;
+        prm.num_units = m_tiles * n_slots;
         prm.status = device_status_word();
         prm.limit_ns = watchdog_limit_ns();
         if (!prm.status) rc = kCudaError;
@@ -91,14 +115,21 @@ int launch_fp8_blockscaled(const uint8_t *A, const uint8_t *B, const float *SFA,
             const GemmEvents ev = take_gemm_events();
             if (ev.start && cudaEventRecord(ev.start, stream) != cudaSuccess) rc = kCudaError;
             cudaLaunchConfig_t cfg = {};
-            cudaLaunchAttribute attr[1];
+            cudaLaunchAttribute attr[2];
             int na = 0;
+            if constexpr (Cfg::CL > 1) {
+                attr[na].id = cudaLaunchAttributeClusterDimension;
+                attr[na].val.clusterDim.x = Cfg::CL;
+                attr[na].val.clusterDim.y = 1;
+                attr[na].val.clusterDim.z = 1;
+                ++na;
+            }
             if (!ev.start) {
                 attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
                 attr[na].val.programmaticStreamSerializationAllowed = 1;
                 ++na;
             }
-            cfg.gridDim = dim3(static_cast<unsigned>(std::min(prm.num_tiles, sm_count())), 1, 1);
+            cfg.gridDim = dim3(static_cast<unsigned>(Cfg::CL * std::min(prm.num_units, clusters)), 1, 1);
             cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
             cfg.dynamicSmemBytes = Cfg::kSmemBytes;
             cfg.stream = stream;

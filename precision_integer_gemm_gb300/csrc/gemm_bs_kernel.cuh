@@ -11,11 +11,13 @@
 // 128-k block is its own MMA sum and the scaling is done on the CUDA cores:
 //
 //  * tcgen05.mma kind::f8f6f4 (both operands in 128-byte-swizzled shared
-//    memory, TMA-loaded) writes the block's partial tile (128 x 128 float32)
-//    into one of PB TMEM buffers, so the MMAs of the next blocks run while
-//    block kb is promoted.
-//  * Epilogue warps (EPQ per TMEM lane quadrant, 128 / EPQ columns each) read
-//    the partial, multiply it by SFB[n,kb] and SFA[m,kb] and add it to float32
+//    memory, TMA-loaded) writes the block's partial tile (128 x BN float32,
+//    BN = 64 * EPQ) into one of PB TMEM buffers, so the MMAs of the next blocks
+//    run while block kb is promoted.  With CL = 2 the two CTAs of a cluster
+//    take neighbouring B tiles of the same A tile, each loading half of the A
+//    tile into both (TMA multicast).
+//  * Epilogue warps (EPQ per TMEM lane quadrant, 64 columns each) read the
+//    partial, multiply it by SFB[n,kb] and SFA[m,kb] and add it to float32
 //    totals held in registers; after the last block they store the tile.
 //  * The scales reach the CTA through their own small ring: a preparation
 //    pass has transposed them to [KB][rows] (one 512-byte row segment per
@@ -39,46 +41,50 @@ struct BsParams {
     const float *sfa_t;   // [KB][m_pad] transposed SFA
     const float *sfb_t;   // [KB][n_pad] transposed SFB
     int M, N, K;
-    int m_tiles, n_tiles, kb_total;
-    int m_pad, n_pad;     // multiples of 128
+    int m_tiles, n_slots, kb_total;  // n_slots: groups of CL neighbouring B tiles
+    int m_pad, n_pad;     // rows of the transposed scales: m_tiles * 128, n_slots * CL * BN
     int group_m;          // A tiles per group
-    int num_tiles;
+    int num_units;        // m_tiles * n_slots
     int *status;
     unsigned long long limit_ns;
 };
 
-template <int ST_, int SS_, int EPQ_ = 2, int PB_ = 4>
+template <int ST_, int SS_, int EPQ_ = 2, int PB_ = 4, int CL_ = 1>
 struct BsCfg {
     static constexpr int ST = ST_;          // operand stages (A + B of one 128-k block)
     static constexpr int SS = SS_;          // scale stages
     static constexpr int EPQ = EPQ_;        // epilogue warps per TMEM lane quadrant
-    static constexpr int CW = 128 / EPQ;    // partial-tile columns per epilogue warp
+    static constexpr int CW = 64;           // partial-tile columns per epilogue warp
+    static constexpr int BN = CW * EPQ;     // tile width (B rows)
     // partial-tile buffers in TMEM: the MMAs run up to PB - 1 blocks ahead of the
-    // promotion (with two, each block waited for a whole MMA -> commit -> load ->
-    // release round trip)
+    // promotion
     static constexpr int PB = PB_;
+    static constexpr int CL = CL_;          // CTAs per cluster sharing the A tile
     static constexpr int kEpiWarps = 4 * EPQ;
     static constexpr int kBK = 128;
     static constexpr int kTileA = 128 * 128;  // bytes
-    static constexpr int kTileB = 128 * 128;
+    static constexpr int kTileB = BN * 128;
+    static constexpr int kARows = 128 / CL;   // A rows each CTA of a cluster loads (multicast)
     static constexpr int kStage = kTileA + kTileB;
-    static constexpr int kScaleStage = 2 * 128 * 4;  // sa[128] then sb[128]
+    static constexpr int kScaleStage = (128 + BN) * 4;  // sa[128] then sb[BN]
     static constexpr int kIssuers = ST % 4 == 0 ? 4 : ST;  // operand-stage lanes
     // scale-stage lanes (the next ones; four measured 10 % slower than one)
     static constexpr int kScaleIssuers = 1;
     static_assert(SS % kScaleIssuers == 0, "each scale lane owns fixed stages");
     static constexpr int kWarpProd = kEpiWarps, kWarpMma = kEpiWarps + 1;
     static constexpr int kThreads = 32 * (kEpiWarps + 2);
-    static_assert(EPQ == 2 || EPQ == 4, "epilogue warps per quadrant");
-    static constexpr int kTmemCols = PB * 128 <= 256 ? 256 : 512;  // PB partial buffers of 128 columns
-    static_assert(PB == 2 || PB == 4, "partial buffers");
+    static_assert(EPQ >= 2 && EPQ <= 3, "epilogue warps per quadrant (the totals' registers)");
+    static_assert(CL == 1 || CL == 2, "cluster size");
+    static constexpr int kTmemCols = PB * BN <= 256 ? 256 : 512;  // PB partial buffers of BN columns
+    static_assert(PB * BN <= 512, "TMEM budget");
     static constexpr int kOffStages = 0;
     static constexpr int kOffScales = kOffStages + ST * kStage;
     static constexpr int kOffBars = kOffScales + SS * kScaleStage;
     static constexpr int kNumBars = 2 * ST + 2 * SS + 2 * PB + 1;
     static constexpr int kOffMisc = kOffBars + 8 * kNumBars;
     static constexpr int kSmemBytes = 1024 + kOffMisc + 64;
-    static_assert(ST % kIssuers == 0 && kIssuers + 4 <= 32, "each issuing lane owns fixed stages");
+    static_assert(kStage % 1024 == 0 && kScaleStage % 16 == 0 && kOffBars % 8 == 0, "alignment");
+    static_assert(ST % kIssuers == 0 && kIssuers + kScaleIssuers <= 32, "each issuing lane owns fixed stages");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -91,15 +97,19 @@ __device__ __forceinline__ void bulk_load_1d(void *dst, const void *src, uint32_
         : "memory");
 }
 
-__device__ __forceinline__ void bs_tile(const BsParams &prm, int u, int &m0, int &n0)
+// Unit u of a cluster: A tile and slot of CL neighbouring B tiles, in groups
+// of group_m A tiles (A fastest); rank r takes B tile slot * CL + r (past the
+// last tile: rows out of range, zeros, nothing stored).
+template <class Cfg>
+__device__ __forceinline__ void bs_tile(const BsParams &prm, int u, int rank, int &m0, int &n0)
 {
-    const int per_group = prm.group_m * prm.n_tiles;
+    const int per_group = prm.group_m * prm.n_slots;
     const int grp = u / per_group;
     const int first = grp * prm.group_m;
     const int gsize = min(prm.m_tiles - first, prm.group_m);
     const int r = u - grp * per_group;
     m0 = (first + r % gsize) * 128;
-    n0 = (r / gsize) * 128;
+    n0 = ((r / gsize) * Cfg::CL + rank) * Cfg::BN;
 }
 
 __device__ __forceinline__ bool bs_warp_wait(uint64_t *bar, uint32_t parity, const Watchdog &wd)
@@ -139,11 +149,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int kbt = prm.kb_total;
+    const int rank = Cfg::CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int cid = blockIdx.x / Cfg::CL;  // cluster index
+    const int ncl = gridDim.x / Cfg::CL;   // clusters
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], Cfg::CL);  // one MMA commit per CTA of the cluster (shared A halves)
         }
         for (int s = 0; s < SS; ++s) {
             mbar_init(&s_full[s], 1);
@@ -166,6 +179,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if constexpr (Cfg::CL > 1) cluster_sync_all();  // the peer's barriers are initialised
     const uint32_t tmem = *tmem_slot;
     const Watchdog wd{abort_flag, prm.status, prm.limit_ns};
 
@@ -175,9 +189,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             // operand stages: lane l issues the stages congruent to l
             uint32_t g = 0, issued_mask = 0, last_phase = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < prm.num_tiles; u += gridDim.x) {
+            for (int u = cid; ok && u < prm.num_units; u += ncl) {
                 int m0, n0;
-                bs_tile(prm, u, m0, n0);
+                bs_tile<Cfg>(prm, u, rank, m0, n0);
                 for (int kb = 0; kb < kbt; ++kb, ++g) {
                     const int s = static_cast<int>(g % ST);
                     if (s % Cfg::kIssuers != lane) continue;
@@ -188,7 +202,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     }
                     uint8_t *st = stages + s * Cfg::kStage;
                     mbar_arrive_expect_tx(&full[s], Cfg::kStage);
-                    tma_load_2d(st, &mapA, &full[s], kb * Cfg::kBK, m0);
+                    if constexpr (Cfg::CL > 1)  // this CTA's half of the A tile, into both CTAs' stage
+                        tma_load_2d_multicast(st + rank * (Cfg::kARows * 128), &mapA, &full[s], kb * Cfg::kBK,
+                                              m0 + rank * Cfg::kARows, 0x3);
+                    else
+                        tma_load_2d(st, &mapA, &full[s], kb * Cfg::kBK, m0);
                     tma_load_2d(st + Cfg::kTileA, &mapB, &full[s], kb * Cfg::kBK, n0);
                     issued_mask |= 1u << s;
                     last_phase = (last_phase & ~(1u << s)) | (ph << s);
@@ -197,6 +215,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 #pragma unroll 1
             for (int s = 0; s < ST; ++s)
                 if ((issued_mask >> s) & 1u) bs_wait_drain(&full[s], (last_phase >> s) & 1u, prm.limit_ns);
+            if constexpr (Cfg::CL > 1) {
+                // ... and no commit of the peer's MMAs still on its way here: wait for
+                // the release of each own stage's last load
+#pragma unroll 1
+                for (int s = 0; s < ST; ++s)
+                    if ((issued_mask >> s) & 1u) bs_wait_drain(&empty[s], (last_phase >> s) & 1u, prm.limit_ns);
+            }
         } else if (lane < Cfg::kIssuers + Cfg::kScaleIssuers) {
             // scale stages (lane j owns the stages congruent to j): the transposed
             // scales are written by the preparation pass this grid may overlap
@@ -204,9 +229,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const int j = lane - Cfg::kIssuers;
             uint32_t g = 0, issued_mask = 0, last_phase = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < prm.num_tiles; u += gridDim.x) {
+            for (int u = cid; ok && u < prm.num_units; u += ncl) {
                 int m0, n0;
-                bs_tile(prm, u, m0, n0);
+                bs_tile<Cfg>(prm, u, rank, m0, n0);
                 for (int kb = 0; kb < kbt; ++kb, ++g) {
                     const int s = static_cast<int>(g % SS);
                     if (s % Cfg::kScaleIssuers != j) continue;
@@ -218,7 +243,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     float *dst = scales + s * (Cfg::kScaleStage / 4);
                     mbar_arrive_expect_tx(&s_full[s], Cfg::kScaleStage);
                     bulk_load_1d(dst, prm.sfa_t + static_cast<int64_t>(kb) * prm.m_pad + m0, 512, &s_full[s]);
-                    bulk_load_1d(dst + 128, prm.sfb_t + static_cast<int64_t>(kb) * prm.n_pad + n0, 512, &s_full[s]);
+                    bulk_load_1d(dst + 128, prm.sfb_t + static_cast<int64_t>(kb) * prm.n_pad + n0, Cfg::BN * 4,
+                                 &s_full[s]);
                     issued_mask |= 1u << s;
                     last_phase = (last_phase & ~(1u << s)) | (ph << s);
                 }
@@ -230,11 +256,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     } else if (warp == Cfg::kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_e4m3_f32(128, 128);
+            constexpr uint32_t idesc = idesc_e4m3_f32(128, Cfg::BN);
             const uint64_t desc0 = sdesc_kmajor_sw128(smem_u32(stages));
             uint32_t g = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < prm.num_tiles; u += gridDim.x) {
+            for (int u = cid; ok && u < prm.num_units; u += ncl) {
                 for (int kb = 0; kb < kbt; ++kb, ++g) {
                     const int s = static_cast<int>(g % ST);
                     const int pb = static_cast<int>(g % Cfg::PB);
@@ -246,12 +272,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     tc_fence_after();
                     const uint64_t a0 = desc0 + static_cast<uint64_t>((s * Cfg::kStage) >> 4);
                     const uint64_t b0 = a0 + static_cast<uint64_t>(Cfg::kTileA >> 4);
-                    const uint32_t d_tmem = tmem + pb * 128;
+                    const uint32_t d_tmem = tmem + pb * Cfg::BN;
 #pragma unroll
                     for (int q = 0; q < Cfg::kBK / 32; ++q)
                         mma_f8f6f4(d_tmem, a0 + static_cast<uint64_t>(2 * q), b0 + static_cast<uint64_t>(2 * q), idesc,
                                    q > 0 ? 1u : 0u);
-                    mma_commit(&empty[s]);
+                    if constexpr (Cfg::CL > 1)  // both CTAs' halves of the A tile sit in this stage
+                        mma_commit_multicast(&empty[s], 0x3);
+                    else
+                        mma_commit(&empty[s]);
                     mma_commit(&p_full[pb]);
                 }
             }
@@ -264,35 +293,37 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         const int r = quad * 32 + lane;  // tile row = TMEM lane
         const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) + part * CW;
         // block G (counted over all tiles of the CTA): partial buffer G % PB, its
-        // use G / PB; scale stage G % SS, its use G / SS
-        auto fetch = [&](uint32_t (&dst)[CW], uint32_t G) -> bool {
+        // use G / PB; scale stage G % SS, its use G / SS.  The 64 columns go
+        // through registers 32 at a time (the totals take 64 registers already;
+        // 16 at a time measured 2.5 % slower).
+        auto block = [&](float (&tot)[CW], uint32_t G) -> bool {
             const uint32_t pb = G % Cfg::PB;
-            if (!bs_warp_wait(&p_full[pb], (G / Cfg::PB) & 1u, wd)) return false;
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < CW; c += 32)
-                tmem_ld_32x32b_x32(tbase + pb * 128 + c, *reinterpret_cast<uint32_t(*)[32]>(dst + c));
-            return true;
-        };
-        auto retire = [&](uint32_t G) {  // the loads of block G are in registers: free its buffer
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&p_empty[G % Cfg::PB]);
-        };
-        auto promote = [&](float (&tot)[CW], const uint32_t (&v)[CW], uint32_t G) -> bool {
             const int ss = static_cast<int>(G % SS);
+            if (!bs_warp_wait(&p_full[pb], (G / Cfg::PB) & 1u, wd)) return false;
             if (!bs_warp_wait(&s_full[ss], (G / SS) & 1u, wd)) return false;
+            tc_fence_after();
             const float *sc = scales + ss * (Cfg::kScaleStage / 4);
             const float sa = sc[r];
-            const float4 *sb4 = reinterpret_cast<const float4 *>(sc + 128 + part * CW);
 #pragma unroll
-            for (int j4 = 0; j4 < CW / 4; ++j4) {
-                const float4 b = sb4[j4];
-                tot[4 * j4 + 0] = fmaf(__uint_as_float(v[4 * j4 + 0]) * b.x, sa, tot[4 * j4 + 0]);
-                tot[4 * j4 + 1] = fmaf(__uint_as_float(v[4 * j4 + 1]) * b.y, sa, tot[4 * j4 + 1]);
-                tot[4 * j4 + 2] = fmaf(__uint_as_float(v[4 * j4 + 2]) * b.z, sa, tot[4 * j4 + 2]);
-                tot[4 * j4 + 3] = fmaf(__uint_as_float(v[4 * j4 + 3]) * b.w, sa, tot[4 * j4 + 3]);
+            for (int c = 0; c < CW; c += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tbase + pb * Cfg::BN + c, v);
+                tmem_ld_wait();
+                if (c + 32 == CW) {  // the partial buffer may be rewritten
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&p_empty[pb]);
+                }
+                const float4 *sb4 = reinterpret_cast<const float4 *>(sc + 128 + part * CW + c);
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const float4 b = sb4[j4];
+                    float *t = tot + c + 4 * j4;
+                    t[0] = fmaf(__uint_as_float(v[4 * j4 + 0]) * b.x, sa, t[0]);
+                    t[1] = fmaf(__uint_as_float(v[4 * j4 + 1]) * b.y, sa, t[1]);
+                    t[2] = fmaf(__uint_as_float(v[4 * j4 + 2]) * b.z, sa, t[2]);
+                    t[3] = fmaf(__uint_as_float(v[4 * j4 + 3]) * b.w, sa, t[3]);
+                }
             }
             fence_proxy_async_smem();  // generic reads before the bulk copy refills the stage
             __syncwarp();
@@ -301,19 +332,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         };
         uint32_t g = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < prm.num_tiles; u += gridDim.x) {
+        for (int u = cid; ok && u < prm.num_units; u += ncl) {
             int m0, n0;
-            bs_tile(prm, u, m0, n0);
+            bs_tile<Cfg>(prm, u, rank, m0, n0);
             float tot[CW];
 #pragma unroll
             for (int j = 0; j < CW; ++j) tot[j] = 0.0f;
-            uint32_t va[CW];
-            for (int kb = 0; ok && kb < kbt; ++kb, ++g) {
-                ok = fetch(va, g);
-                if (!ok) break;
-                retire(g);
-                ok = promote(tot, va, g);
-            }
+            for (int kb = 0; ok && kb < kbt; ++kb, ++g) ok = block(tot, g);
             if (!ok) break;
             const int m = m0 + r;
             const int nb = n0 + part * CW;
@@ -337,8 +362,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == Cfg::kWarpMma) {
-        if (lane == 0) bs_wait_drain(mma_drain, 0, prm.limit_ns);
+        if (lane == 0) bs_wait_drain(mma_drain, 0, prm.limit_ns);  // every MMA of this CTA is done
         __syncwarp();
+    }
+    // neither CTA of a cluster leaves while the other may still reach it
+    if constexpr (Cfg::CL > 1) cluster_sync_all();
+    if (warp == Cfg::kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, Cfg::kTmemCols);
     }
