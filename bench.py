@@ -158,6 +158,20 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(seconds: float, dist, device: str) -> float:
+    """The slowest rank's time: every rank's value reduced with MAX (NCCL on
+    the GPU machine, gloo in the CPU tests)."""
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(ops_per_step: float, steps: int, world: int, slowest_s: float) -> float:
+    """TOPS of the whole job: every replica's ops over the slowest rank's time."""
+    return ops_per_step * steps * world / slowest_s / 1e12
+
+
 # the block scales of the fp8bs workload (set in main)
 _SCALES = None
 
@@ -324,12 +338,10 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
     torch.cuda.synchronize()
     gemm_kernel_s = sum(s.elapsed_time(e) for s, e in zip(k_starts, k_ends)) / 1e3 / args.steps
     if dist is not None:
-        t = torch.tensor([total_s], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
+        total_s = max_over_ranks(total_s, dist, "cuda")
 
     ops = 2.0 * M * N * K
-    value = ops * args.steps * world / total_s / 1e12
+    value = whole_job_value(ops, args.steps, world, total_s)
 
     # end to end through the public API with pinned host buffers
     e2e_steps = max(1, min(args.steps, 5))
