@@ -311,10 +311,11 @@ def test_i4i4_extreme_constants(orc, K, av, bv):
 
 
 # Skinny path (M <= 32): split K with ragged last slices (K % 256 != 0), N
-# tails, both activation-row configurations (M <= 16, M <= 32), one and many
-# slices.
+# tails (N % 4 != 0 too), both activation-row configurations (M <= 16,
+# M <= 32), one and many slices, every split plan (one slice, a cluster of two
+# or four, atomics after the overlapped zeroing).
 SKINNY = [(1, 129, 8224), (7, 1000, 4128), (16, 2048, 65536), (17, 300, 2080), (32, 520, 8192), (24, 128, 256),
-          (16, 28672, 512)]
+          (16, 28672, 512), (3, 1001, 6400), (16, 4096, 8192)]
 
 
 @pytest.mark.parametrize("M,N,K", SKINNY)
@@ -482,6 +483,33 @@ def test_concurrent_streams_keep_their_workspaces_apart(orc):
         assert np.array_equal(C.cpu().numpy(), runs[j % 2][5]), j
 
 
+def test_concurrent_streams_skinny_path(orc):
+    # decode-shaped W4A8 calls on two streams at once (one plan zeroes C with a
+    # kernel the GEMM overlaps, the other sums K slices across a cluster)
+    shapes = [(16, 28672, 8192), (8, 20480, 8192)]
+    runs = []
+    for i, (M, N, K) in enumerate(shapes):
+        a = si.int8_values(18000 + i, (M, K))
+        b = si.int4_values(18100 + i, (N, K))
+        rng = np.random.default_rng(40 + i)
+        ms, ns = rng.integers(0, M, 512), rng.integers(0, N, 512)
+        runs.append((M, N, K, dev(a), gpu_pack(b), ms, ns, orc.w4a8_entries(a, orc.pack_int4(b), K, ms, ns)))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    outs = []
+    for rep in range(3):
+        for (M, N, K, at, bp, _, _, _), st in zip(runs, streams):
+            C = torch.empty((M, N), dtype=torch.int32, device="cuda")
+            C.record_stream(st)
+            pig.w4a8_gemm(at, bp, C, M, N, K, st)
+            outs.append(C)
+    torch.cuda.synchronize()
+    assert pig.igemm_last_status() == 0
+    for j, C in enumerate(outs):
+        M, N, K, _, _, ms, ns, want = runs[j % 2]
+        assert np.array_equal(C.cpu().numpy()[ms, ns].astype(np.int64), want), j
+
+
 def test_empty_and_zero_k():
     C = torch.full((4, 4), 7, dtype=torch.int32, device="cuda")
     pig.i4i4_gemm(None, None, C, 0, 4, 64)
@@ -491,6 +519,15 @@ def test_empty_and_zero_k():
     pig.i4i4_gemm(None, None, C, 4, 4, 0)
     torch.cuda.synchronize()
     assert bool((C == 0).all())
+    # the fp8 entry points: empty shapes leave C alone, K == 0 zeroes it
+    F = torch.full((4, 4), 7.0, dtype=torch.float32, device="cuda")
+    pig.fp8_gemm(None, None, F, 0, 4, 16)
+    pig.fp8_blockscaled_gemm(None, None, None, None, F, 4, 0, 16)
+    torch.cuda.synchronize()
+    assert bool((F == 7.0).all())
+    pig.fp8_blockscaled_gemm(None, None, None, None, F, 4, 4, 0)
+    torch.cuda.synchronize()
+    assert bool((F == 0.0).all())
 
 
 def test_misaligned_device_pointers_are_rejected():
