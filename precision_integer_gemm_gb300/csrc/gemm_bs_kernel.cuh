@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             for (int c = 0; c < CW; c += 32) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tbase + pb * Cfg::BN + c, v);
-                tmem_ld_wait();
+                tmem_ld_wait_regs(v);
                 if (c + 32 == CW) {  // the partial buffer may be rewritten
                     tc_fence_before();
                     __syncwarp();

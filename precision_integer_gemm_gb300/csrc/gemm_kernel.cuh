@@ -634,7 +634,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 for (int c0 = 0; c0 < Cfg::kQRows; c0 += 32, ++chunk) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tacc + c0, v);
-                    tmem_ld_wait();
+                    tmem_ld_wait_regs(v);
                     int *sqc = sumQ + (chunk & 1) * 32;
                     if (quad == 3 && lane == 31) {
 #pragma unroll
@@ -706,7 +706,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                         uint32_t vh[16], vl[16];
                         tmem_ld_32x32b_x16(tacc + j0 + h, vh);
                         tmem_ld_32x32b_x16(tacc + QA + j0 + h, vl);
-                        tmem_ld_wait();
+                        tmem_ld_wait_regs(vh, vl);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             uint32_t val;

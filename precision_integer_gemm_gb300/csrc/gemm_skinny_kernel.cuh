@@ -500,13 +500,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                         if constexpr (!Cfg::kActI4) {
                             uint32_t v1[16];
                             tmem_ld_32x32b_x16(tacc + QA + j, v1);
-                            tmem_ld_wait();
+                            tmem_ld_wait_regs(v0, v1);
 #pragma unroll
                             for (int e = 0; e < 16; ++e)
                                 val[j + e] += 16 * __float2int_rn(__uint_as_float(v0[e]) * 262144.0f) +
                                               __float2int_rn(__uint_as_float(v1[e]) * 262144.0f);
                         } else {
-                            tmem_ld_wait();
+                            tmem_ld_wait_regs(v0);
 #pragma unroll
                             for (int e = 0; e < 16; ++e)
                                 val[j + e] += __float2int_rn(__uint_as_float(v0[e]) * 262144.0f);

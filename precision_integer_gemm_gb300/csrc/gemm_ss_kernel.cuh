@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 for (int c0 = 0; c0 < Cfg::kQRows; c0 += 32) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tacc + c0, v);
-                    tmem_ld_wait();
+                    tmem_ld_wait_regs(v);
                     const int n0 = x.q0 + c0;
                     if constexpr (!Cfg::kFloat) {
                         // -8 sum uB of the chunk's 32 columns (the sums array is padded
@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                         uint32_t vh[16], vl[16];
                         tmem_ld_32x32b_x16(tacc + j0 + h, vh);
                         tmem_ld_32x32b_x16(tacc + QA + j0 + h, vl);
-                        tmem_ld_wait();
+                        tmem_ld_wait_regs(vh, vl);
                         const int4 *sq = reinterpret_cast<const int4 *>(prm.sumQ + x.q0 + j0 + h);
 #pragma unroll
                         for (int jj = 0; jj < 4; ++jj) {

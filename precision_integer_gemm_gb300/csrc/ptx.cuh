@@ -304,7 +304,28 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
         : "r"(taddr));
 }
 
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// tcgen05.ld fills its destination registers asynchronously; the compiler sees
+// them written by the load instruction itself.  These waits also mark the
+// registers as rewritten after the wait (an empty asm per register, ordered
+// after the wait like every volatile asm), so no use of a loaded value can be
+// scheduled before the wait.
+template <int N>
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[N])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+template <int N, int M>
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&a)[N], uint32_t (&b)[M])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(a[i]));
+#pragma unroll
+    for (int i = 0; i < M; ++i) asm volatile("" : "+r"(b[i]));
+}
 
 // D[tmem] (+)= A[tmem] * B[smem]^T: A is read from tensor memory (lane = row,
 // four e4m3 values per 32-bit column), B from a K-major shared-memory tile.
