@@ -15,7 +15,16 @@
  * memory pool on the current device (allocated and released in `stream`
  * order, so concurrent calls on different streams do not share it); the pool
  * keeps what it reserved for later calls until the process exits.  A failed
- * workspace allocation returns IGEMM_CUDA_ERROR.
+ * workspace allocation returns IGEMM_CUDA_ERROR.  w4a8_gemm_scaled (its int32
+ * product) and fp8_blockscaled_gemm (its transposed scales) take theirs from
+ * the same pool; skinny shapes (M <= 32) and fp8_gemm need none.
+ *
+ * Launch overlap.  Where a call launches a short pass before its GEMM kernel
+ * (the preparation of codes, the zeroing of C, the transposed scales), the GEMM
+ * kernel is launched with programmatic stream serialization: its set-up and
+ * the loads that do not depend on the pass run while the pass finishes, and it
+ * waits for the pass (griddepcontrol.wait) before it reads or writes what the
+ * pass touches.
  *
  * Operand formats
  *   Packed int4 matrix [rows, K/2] bytes, row-major: byte j of a row holds
@@ -190,20 +199,22 @@ IGEMM_API int pack_int4(const int8_t *logical, uint8_t *packed, int64_t rows, in
 /*
  * Number of kernels this library has launched in this process so far (all
  * devices and streams; a launch counts when it was enqueued).  One GEMM call
- * launches one kernel, or two on the prepared-codes path (the preparation
- * pass and the GEMM); a split K adds a memset, which is not a kernel.
+ * launches one kernel, or two: the preparation pass and the GEMM (prepared
+ * codes), the zeroing of C and the GEMM (skinny shapes whose K slices are
+ * summed with atomics), the scale transpose and the GEMM (block-scaled fp8).
+ * The split K of the other paths adds a memset, which is not a kernel.
  */
 IGEMM_API uint64_t igemm_kernels_launched(void);
 
 /*
  * Measurement hook: arms two caller-created CUDA events for the next GEMM call
- * (i4i4_gemm, i4i4_gemm_noalloc or w4a8_gemm) made by this host thread.  That
- * call records `start` on its stream right before it launches its GEMM kernel
- * and `stop` right after, so cudaEventElapsedTime(start, stop) is that
- * kernel's duration alone (without the preparation pass of the
- * prepared-codes path).  Calls that launch no GEMM kernel (empty shapes,
- * argument errors) leave the events armed.  IGEMM_INVALID_ARGUMENT for a null
- * event.
+ * (any of the GEMM entry points) made by this host thread.  That call records
+ * `start` on its stream right before it launches its GEMM kernel and `stop`
+ * right after, so cudaEventElapsedTime(start, stop) is that kernel's duration
+ * alone (without the preparation, zeroing or transpose pass before it; while
+ * the events are armed the GEMM is not launched to overlap that pass).  Calls
+ * that launch no GEMM kernel (empty shapes, argument errors) leave the events
+ * armed.  IGEMM_INVALID_ARGUMENT for a null event.
  */
 IGEMM_API int igemm_time_next_gemm(cudaEvent_t start, cudaEvent_t stop);
 
