@@ -125,7 +125,7 @@ Plan plan_units(int tiles, int kb_total, int64_t c_bytes, int64_t operand_bytes,
 
 SkinnyPlan plan_skinny(int n_tiles, int K, int max_slice_k, const SkinnyClusterOption *opts, int n_opts, int workers)
 {
-    constexpr int64_t kZeroingStages = 8;  // a memset of C and its launch, in packed-stage times
+    constexpr int64_t kZeroingStages = 8;  // zeroing C (a kernel the GEMM overlaps) and the atomics, in stage times
     const int sms = workers > 0 ? workers : sm_count();
     SkinnyPlan best{0, 0, 0, 1};
     int64_t best_cost = -1;

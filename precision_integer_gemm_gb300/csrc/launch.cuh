@@ -238,7 +238,7 @@ struct SkinnyClusterOption {
 };
 // Split K for igemm_skinny_kernel: the choice that minimises the packed stages
 // of the busiest CTA (plus one per tile for its hand-over, plus about eight
-// for zeroing C when slices are summed with atomics), each slice's activation
+// when slices are summed with atomics into a zeroed C), each slice's activation
 // codes fitting the kernel's shared-memory budget.
 SkinnyPlan plan_skinny(int n_tiles, int K, int max_slice_k, const SkinnyClusterOption *opts, int n_opts,
                        int workers = 0);
