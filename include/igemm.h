@@ -207,6 +207,23 @@ IGEMM_API int pack_int4(const int8_t *logical, uint8_t *packed, int64_t rows, in
 IGEMM_API uint64_t igemm_kernels_launched(void);
 
 /*
+ * Planning query, host only (no GPU is touched): the split of K that a call of
+ * i4i4_gemm (variant 0) or w4a8_gemm (variant 1) with 1 <= M <= 32 would use on
+ * a GPU with `sms` SMs where `pairs` clusters of two and `quads` clusters of
+ * four of the skinny kernel can be resident at once (0: none; the library asks
+ * the driver for these on a real call).  Writes out[0] = k slices, out[1] = k
+ * per slice (a multiple of 256), out[2] = CTAs launched (a multiple of the
+ * slices), out[3] = cluster size (1: one slice, or slices summed with atomics
+ * into C after a zeroing kernel; 2 or 4: the slices of a tile on one cluster,
+ * summed through distributed shared memory).  The pages have no counterpart;
+ * the kernel and the split are this library's.  IGEMM_INVALID_ARGUMENT for a
+ * variant other than 0 or 1, M outside [1, 32], N < 1, K < 32, K % 32 != 0,
+ * K > 65536, sms < 1, negative cluster counts or a null `out`;
+ * IGEMM_UNSUPPORTED_SHAPE when no plan fits.
+ */
+IGEMM_API int igemm_skinny_plan(int variant, int M, int N, int K, int sms, int pairs, int quads, int *out);
+
+/*
  * Measurement hook: arms two caller-created CUDA events for the next GEMM call
  * (any of the GEMM entry points) made by this host thread.  That call records
  * `start` on its stream right before it launches its GEMM kernel and `stop`

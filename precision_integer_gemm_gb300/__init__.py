@@ -22,13 +22,14 @@ __all__ = [
     "fp8_blockscaled_gemm", "unpack_int4",
     "igemm_strerror",
     "igemm_last_status", "igemm_watchdog_selftest", "igemm_kernels_launched", "igemm_time_next_gemm",
+    "igemm_skinny_plan",
     "EXPORTED_SYMBOLS", "LIB_PATH", "build_library",
 ]
 
 EXPORTED_SYMBOLS = ("i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "w4a8_gemm_scaled", "fp8_gemm",
                     "fp8_blockscaled_gemm", "pack_int4", "unpack_int4", "igemm_strerror", "igemm_last_status",
                     "igemm_watchdog_selftest", "igemm_kernels_launched",
-                    "igemm_time_next_gemm")
+                    "igemm_time_next_gemm", "igemm_skinny_plan")
 
 IGEMM_OK = 0
 IGEMM_INVALID_ARGUMENT = 1
@@ -87,6 +88,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.igemm_last_status.restype = i
     lib.igemm_time_next_gemm.argtypes = [p, p]
     lib.igemm_time_next_gemm.restype = i
+    lib.igemm_skinny_plan.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
+    lib.igemm_skinny_plan.restype = i
     lib.igemm_kernels_launched.argtypes = []
     lib.igemm_kernels_launched.restype = ctypes.c_uint64
     lib.igemm_watchdog_selftest.argtypes = [ctypes.c_uint32, p]
@@ -176,6 +179,15 @@ def igemm_time_next_gemm(start, stop) -> None:
     thread's next GEMM call."""
     h = [e if isinstance(e, int) else e.cuda_event for e in (start, stop)]
     _check(load().igemm_time_next_gemm(h[0], h[1]), "igemm_time_next_gemm")
+
+
+def igemm_skinny_plan(variant: str, M: int, N: int, K: int, sms: int, pairs: int, quads: int) -> dict:
+    """The K split a skinny (M <= 32) i4i4_gemm / w4a8_gemm call would use on a GPU with
+    `sms` SMs and room for `pairs` / `quads` clusters of two / four (host only)."""
+    out = (ctypes.c_int * 4)()
+    v = {"i4i4": 0, "w4a8": 1}[variant]
+    _check(load().igemm_skinny_plan(v, M, N, K, sms, pairs, quads, out), "igemm_skinny_plan")
+    return {"split": out[0], "slice_k": out[1], "ctas": out[2], "cluster": out[3]}
 
 
 def igemm_kernels_launched() -> int:

@@ -450,6 +450,21 @@ extern "C" int unpack_int4(const uint8_t *packed, int8_t *logical, int64_t rows,
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
 }
 
+extern "C" int igemm_skinny_plan(int variant, int M, int N, int K, int sms, int pairs, int quads, int *out)
+{
+    if ((variant != 0 && variant != 1) || M < 1 || M > 32 || N < 1 || K < 32 || K % 32 != 0 || K > kMaxK ||
+        sms < 1 || pairs < 0 || quads < 0 || !out)
+        return kInvalidArgument;
+    const SkinnyPlan p = variant == 0 ? skinny_plan_i4i4(M, N, K, sms, pairs, quads)
+                                      : skinny_plan_w4a8(M, N, K, sms, pairs, quads);
+    if (p.ctas < 1) return kUnsupportedShape;
+    out[0] = p.split;
+    out[1] = p.slice_k;
+    out[2] = p.ctas;
+    out[3] = p.cs;
+    return kOk;
+}
+
 extern "C" const char *igemm_strerror(int code)
 {
     switch (code) {

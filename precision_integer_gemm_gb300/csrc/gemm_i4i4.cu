@@ -55,11 +55,23 @@ static int run_i4i4_codes(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int 
     return rc != kOk ? rc : rf;
 }
 
+SkinnyPlan skinny_plan_i4i4(int M, int N, int K, int sms, int pairs, int quads)
+{
+    if (M <= 16) return skinny_plan_for<CfgI4I4Skinny16, CfgI4I4Skinny16C2, CfgI4I4Skinny16C4>(N, K, sms, pairs, quads);
+    return skinny_plan_for<CfgI4I4Skinny32>(N, K, sms, pairs, quads);
+}
+
 int launch_i4i4(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
 {
-    // few rows of A (decode-like): B streamed once, A's codes resident
-    if (M <= 16) return launch_skinny<CfgI4I4Skinny16, CfgI4I4Skinny16C2, CfgI4I4Skinny16C4>(Ap, Bp, C, M, N, K, stream);
-    if (M <= 32) return launch_skinny<CfgI4I4Skinny32>(Ap, Bp, C, M, N, K, stream);
+    // few rows of A (decode-like): B streamed once, A's codes resident (no
+    // skinny plan fits only on parts with fewer SMs than k slices needed: those
+    // shapes take the other paths)
+    if (M <= 32) {
+        const int rc = M <= 16 ? launch_skinny<CfgI4I4Skinny16, CfgI4I4Skinny16C2, CfgI4I4Skinny16C4>(Ap, Bp, C, M, N, K,
+                                                                                                     stream)
+                               : launch_skinny<CfgI4I4Skinny32>(Ap, Bp, C, M, N, K, stream);
+        if (rc != kUnsupportedShape) return rc;
+    }
     if (use_codes_i4i4(M, N)) return run_i4i4_codes(Ap, Bp, C, M, N, K, stream);
     using Cfg = CfgI4I4;
     CUtensorMap mapA, mapB, mapC32 = {}, mapC31 = {};

@@ -76,11 +76,23 @@ static int run_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N
                             stream);
 }
 
+SkinnyPlan skinny_plan_w4a8(int M, int N, int K, int sms, int pairs, int quads)
+{
+    if (M <= 16) return skinny_plan_for<CfgW4A8Skinny16, CfgW4A8Skinny16C2, CfgW4A8Skinny16C4>(N, K, sms, pairs, quads);
+    return skinny_plan_for<CfgW4A8Skinny32>(N, K, sms, pairs, quads);
+}
+
 int launch_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
 {
     const uint8_t *a = reinterpret_cast<const uint8_t *>(A);
-    if (M <= 16) return launch_skinny<CfgW4A8Skinny16, CfgW4A8Skinny16C2, CfgW4A8Skinny16C4>(a, Bp, C, M, N, K, stream);
-    if (M <= 32) return launch_skinny<CfgW4A8Skinny32>(a, Bp, C, M, N, K, stream);
+    // (no skinny plan fits only on parts with fewer SMs than k slices needed:
+    // those shapes take the other paths)
+    if (M <= 32) {
+        const int rc = M <= 16 ? launch_skinny<CfgW4A8Skinny16, CfgW4A8Skinny16C2, CfgW4A8Skinny16C4>(a, Bp, C, M, N, K,
+                                                                                                     stream)
+                               : launch_skinny<CfgW4A8Skinny32>(a, Bp, C, M, N, K, stream);
+        if (rc != kUnsupportedShape) return rc;
+    }
     if (N >= 256) return run_w4a8_codes(A, Bp, C, M, N, K, stream);
     return run_w4a8<CfgW4A8>(A, Bp, C, M, N, K, stream);
 }

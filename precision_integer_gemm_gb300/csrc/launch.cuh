@@ -356,6 +356,18 @@ int skinny_cluster_option(SkinnyClusterOption *o)
     return kOk;
 }
 
+// The plan launch_skinny<Cfg, Cfg2, Cfg4> would pick on a GPU with `sms` SMs
+// where `pairs` clusters of Cfg2 and `quads` of Cfg4 fit at once (host only).
+template <class Cfg, class Cfg2 = void, class Cfg4 = void>
+SkinnyPlan skinny_plan_for(int N, int K, int sms, int pairs, int quads)
+{
+    SkinnyClusterOption opts[2] = {};
+    int n_opts = 0;
+    if constexpr (!std::is_void<Cfg2>::value) opts[n_opts++] = SkinnyClusterOption{2, pairs, Cfg2::kMaxSliceK};
+    if constexpr (!std::is_void<Cfg4>::value) opts[n_opts++] = SkinnyClusterOption{4, quads, Cfg4::kMaxSliceK};
+    return plan_skinny((N + 127) / 128, K, Cfg::kMaxSliceK, opts, n_opts, sms);
+}
+
 // igemm_skinny_kernel over packed int4 weights Bp [N, K/2] and activations A
 // (int8 [M, K], or packed int4 [M, K/2]), M <= Cfg::QA: the cluster kernel
 // Cfg2 (pairs) or Cfg4 (clusters of four) when its plan is the better one,
@@ -385,6 +397,9 @@ int launch_skinny(const uint8_t *A, const uint8_t *Bp, int32_t *C, int M, int N,
 }
 
 int launch_i4i4(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);
+// Skinny-path plans (M <= 32) of each variant, for the planning query.
+SkinnyPlan skinny_plan_i4i4(int M, int N, int K, int sms, int pairs, int quads);
+SkinnyPlan skinny_plan_w4a8(int M, int N, int K, int sms, int pairs, int quads);
 
 // Fixed workspace of i4i4_gemm_noalloc (a file-scope device array).
 constexpr size_t kNoAllocWorkspaceBytes = size_t(32) << 20;
