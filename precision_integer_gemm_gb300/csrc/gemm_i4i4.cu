@@ -2,7 +2,7 @@
 //
 // Three paths.  M <= 32 takes igemm_skinny_kernel (gemm_skinny_kernel.cuh):
 // B's rows on the MMA A side, A's signed codes resident in shared memory per
-// k slice.  Shapes with M and N of at least 256 take the prepared-codes path:
+// k slice.  Large products (M, N >= 512 and M * N >= 4M) take the prepared-codes path:
 // one pass turns A and B into code rows and row sums (prep.cu), then
 // igemm_ss_kernel runs a TMA -> tcgen05.mma pipeline on 128 x 256 tiles with
 // both operands in shared memory.  Smaller shapes, where that pass would cost
@@ -24,7 +24,15 @@ using CfgI4I4Skinny16C2 = SkinnyCfg<true, 16, 8, 6, 2, 2, 2>;
 using CfgI4I4Skinny16C4 = SkinnyCfg<true, 16, 8, 6, 2, 2, 4>;
 using CfgI4I4Skinny32 = SkinnyCfg<true, 32, 8, 6, 2, 2, 1>;
 
-static bool use_codes_i4i4(int M, int N) { return M >= 256 && N >= 256; }
+// The preparation pass costs (M + N) * K bytes of codes written and read again;
+// it pays once the product is large.  Measured crossovers on GB300: the
+// in-kernel path is faster up to M * N of about 2M (1024^3: 19 vs 25 us; 256 x
+// 8192 x 8192: 42 vs 56 us), the prepared-codes path beyond (512 x 8192 x 8192:
+// 59 vs 68 us; 1024 x 4096 x 4096: 33 vs 42 us).
+static bool use_codes_i4i4(int M, int N)
+{
+    return M >= 512 && N >= 512 && int64_t(M) * N >= (int64_t(1) << 22);
+}
 
 static int run_i4i4_codes(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
 {

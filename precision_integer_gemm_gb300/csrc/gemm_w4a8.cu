@@ -2,8 +2,9 @@
 //
 // Skinny activation counts (M <= 32, decode) take igemm_skinny_kernel
 // (gemm_skinny_kernel.cuh): split K, each CTA's slice of the activations held
-// as codes in shared memory, the weights streamed once.  M > 32 and N >= 256
-// take the prepared-codes path: one pass writes weight code rows, activation
+// as codes in shared memory, the weights streamed once.  Large products
+// (M >= 768, M * N >= 4M) take the prepared-codes path: one pass writes weight
+// code rows, activation
 // high/low code planes and the row sums (prep.cu), then igemm_ss_kernel
 // multiplies 128 weight rows by 128 activation rows (256 code rows) per tile
 // from shared memory.  The rest takes igemm_tc_kernel below.  Swap-AB: the
@@ -93,7 +94,11 @@ int launch_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, in
                                : launch_skinny<CfgW4A8Skinny32>(a, Bp, C, M, N, K, stream);
         if (rc != kUnsupportedShape) return rc;
     }
-    if (N >= 256) return run_w4a8_codes(A, Bp, C, M, N, K, stream);
+    // the preparation pass writes N * K + 2 * M * K bytes of codes; measured on
+    // GB300 it pays from about M = 768 with M * N >= 4M (1024 x 4096 x 4096: 48 vs
+    // 52 us), not below (64 x 28672 x 8192: 130 vs 61 us; 1024^3: 28 vs 15 us)
+    if (M >= 768 && N >= 256 && int64_t(M) * N >= (int64_t(1) << 22))
+        return run_w4a8_codes(A, Bp, C, M, N, K, stream);
     return run_w4a8<CfgW4A8>(A, Bp, C, M, N, K, stream);
 }
 

@@ -144,8 +144,19 @@ def test_w4a8_matches_oracle(orc, M, N, K):
 # Shapes of the prepared-codes path (int4 x int4: M, N >= 256; W4A8: M > 32,
 # N >= 256): K below one 128-k block, K tails, ragged M and N, N % 4 != 0
 # (direct stores instead of bulk tensor stores) and a split K.
-CODES_I4I4 = [(256, 256, 32), (300, 520, 96), (257, 300, 8224), (1000, 777, 2080), (256, 258, 128),
-              (256, 256, 65536)]
+# (large products: int4 x int4 with M, N >= 512 and M * N >= 4M; W4A8 with
+# M >= 768 and M * N >= 4M).  Whole C where the oracle is quick, else sampled
+# entries; every case is also compared with the same product through
+# i4i4_gemm_noalloc, which always takes this path, for the small ones.
+CODES_I4I4 = [(2048, 2048, 32), (2100, 2056, 96), (2049, 2050, 1056), (2048, 2050, 128), (2048, 2048, 16384),
+              (1024, 4100, 8224)]
+
+
+def _check_entries(C, want_fn, M, N, seed):
+    rng = np.random.default_rng(seed)
+    ms = np.concatenate([rng.integers(0, M, 2000), [0, M - 1, M - 1, 0]])
+    ns = np.concatenate([rng.integers(0, N, 2000), [0, N - 1, 0, N - 1]])
+    assert np.array_equal(C[ms, ns].astype(np.int64), want_fn(ms, ns))
 
 
 @pytest.mark.parametrize("M,N,K", CODES_I4I4)
@@ -153,10 +164,13 @@ def test_i4i4_prepared_codes_path(orc, M, N, K):
     a = si.int4_values(5000 + M + K, (M, K))
     b = si.int4_values(6000 + N + K, (N, K))
     C, ap, bp = run_i4i4(a, b, orc)
-    assert np.array_equal(C, orc.i4i4_gemm(ap, bp, K))
+    if M * N * K <= 5e9:
+        assert np.array_equal(C, orc.i4i4_gemm(ap, bp, K))
+    else:
+        _check_entries(C, lambda ms, ns: orc.i4i4_entries(ap, bp, K, ms, ns), M, N, K)
 
 
-CODES_W4A8 = [(33, 256, 32), (130, 300, 4160), (1000, 258, 1056), (64, 512, 65536), (129, 1024, 384)]
+CODES_W4A8 = [(1024, 4096, 32), (1030, 4100, 4160), (2000, 2100, 1056), (1024, 4096, 65536), (1024, 4098, 384)]
 
 
 @pytest.mark.parametrize("M,N,K", CODES_W4A8)
@@ -164,7 +178,10 @@ def test_w4a8_prepared_codes_path(orc, M, N, K):
     a = si.int8_values(7000 + M + K, (M, K))
     b = si.int4_values(8000 + N + K, (N, K))
     C, bp = run_w4a8(a, b, orc)
-    assert np.array_equal(C, orc.w4a8_gemm(a, bp, K))
+    if M * N * K <= 5e9:
+        assert np.array_equal(C, orc.w4a8_gemm(a, bp, K))
+    else:
+        _check_entries(C, lambda ms, ns: orc.w4a8_entries(a, bp, K, ms, ns), M, N, K)
 
 
 # ---------------------------------------------------------------- W4A8 with per-channel dequantisation
@@ -302,8 +319,8 @@ def test_decode_workload_whole_c(orc):
 @pytest.mark.parametrize("K", [32, 8192, 65536])
 @pytest.mark.parametrize("av,bv", [(-8, -8), (7, 7), (-8, 7), (7, -8)])
 def test_i4i4_extreme_constants(orc, K, av, bv):
-    for M in (16, 32, 130):
-        N = 260
+    # skinny, in-kernel and (K <= 8192) prepared-codes paths
+    for M, N in ((16, 260), (32, 260), (130, 260)) + (((2048, 2048),) if K <= 8192 else ()):
         a = np.full((M, K), av, dtype=np.int8)
         b = np.full((N, K), bv, dtype=np.int8)
         C, _, _ = run_i4i4(a, b, orc)
@@ -332,8 +349,7 @@ def test_skinny_path_matches_oracle(orc, M, N, K):
 @pytest.mark.parametrize("K", [32, 8192, 65536])
 @pytest.mark.parametrize("av,bv", [(-128, -8), (127, 7), (-128, 7), (127, -8), (0, -8)])
 def test_w4a8_extreme_constants(orc, K, av, bv):
-    for M in (16, 32, 130):
-        N = 260
+    for M, N in ((16, 260), (32, 260), (130, 260)) + (((1024, 4096),) if K <= 8192 else ()):
         a = np.full((M, K), av, dtype=np.int8)
         b = np.full((N, K), bv, dtype=np.int8)
         C, _ = run_w4a8(a, b, orc)
@@ -420,10 +436,10 @@ def test_split_path_is_deterministic(orc):
 def test_kernel_launch_counter():
     # the prepared-codes path launches the preparation pass and the GEMM, the
     # in-kernel unpacking path one kernel; rejected and empty calls none
-    a = torch.zeros((512, 64), dtype=torch.uint8, device="cuda")
-    C = torch.empty((512, 512), dtype=torch.int32, device="cuda")
+    a = torch.zeros((2048, 64), dtype=torch.uint8, device="cuda")
+    C = torch.empty((2048, 2048), dtype=torch.int32, device="cuda")
     n0 = pig.igemm_kernels_launched()
-    pig.i4i4_gemm(a, a, C, 512, 512, 128)
+    pig.i4i4_gemm(a, a, C, 2048, 2048, 128)
     n1 = pig.igemm_kernels_launched()
     pig.i4i4_gemm(a, a, C, 100, 100, 128)
     n2 = pig.igemm_kernels_launched()
@@ -433,7 +449,9 @@ def test_kernel_launch_counter():
     n3 = pig.igemm_kernels_launched()
     # skinny path, one k slice: the GEMM alone
     a8 = torch.zeros((16, 256), dtype=torch.int8, device="cuda")
-    pig.w4a8_gemm(a8, a[:256, :128].contiguous(), C, 16, 256, 256)
+    w = torch.zeros((256, 128), dtype=torch.uint8, device="cuda")
+    C16 = torch.empty((16, 256), dtype=torch.int32, device="cuda")
+    pig.w4a8_gemm(a8, w, C16, 16, 256, 256)
     n4 = pig.igemm_kernels_launched()
     torch.cuda.synchronize()
     assert (n1 - n0, n2 - n1, n3 - n2, n4 - n3) == (2, 1, 0, 1)
@@ -462,7 +480,7 @@ def test_gemm_kernel_timing_hook():
 def test_concurrent_streams_keep_their_workspaces_apart(orc):
     # two prepared-codes GEMMs on two streams at once: each call's workspace is
     # allocated and released in its own stream's order, so neither sees the other's codes
-    shapes = [(512, 768, 1024), (640, 512, 2048)]
+    shapes = [(2048, 2048, 256), (2304, 2048, 512)]
     runs = []
     for i, (M, N, K) in enumerate(shapes):
         a = si.int4_values(17000 + i, (M, K))
