@@ -8,10 +8,10 @@
  * memory of the current device).  Device-side problems (a pipeline wait that
  * exceeded the watchdog limit) are reported later by igemm_last_status().
  *
- * Workspace.  Large GEMMs (int4 x int4 with M, N >= 256; W4A8 with M > 32 and
- * N >= 256) first write the operands as one code byte per value, with row
- * sums, into a workspace of (rows of A + rows of B) * K bytes (W4A8: N*K +
- * 2*M*K) plus a few KB.  The library takes it from its own stream-ordered
+ * Workspace.  Large GEMMs (M * N >= 2^22 and, for int4 x int4, M, N >= 512;
+ * for W4A8, M >= 768 and N >= 256) first write the operands as one code byte
+ * per value, with row sums, into a workspace of (rows of A + rows of B) * K
+ * bytes (W4A8: N*K + 2*M*K) plus a few KB.  The library takes it from its own stream-ordered
  * memory pool on the current device (allocated and released in `stream`
  * order, so concurrent calls on different streams do not share it); the pool
  * keeps what it reserved for later calls until the process exits.  A failed
