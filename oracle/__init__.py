@@ -9,8 +9,8 @@ Sources of what it computes (see ``oracle.c`` for the full statement):
 "[CUDA] Support int4 T.gemm" (tilelang PR #2063) example_tilelang_gemm_int4.py
 matmul_nt_int4; "[Example] add w4a8 gemm kernel" (tilelang PR #815) review of
 torch_convert / ref_program; TileLang tutorial low_precision_gemm.py
-matmul_int4 and pack_int4, and its gemm_fp8 and gemm_blockscaled (E4M3 values
-in float64; block scales applied per block of K).
+matmul_int4 and pack_int4, and its gemm_fp8 and gemm_blockscaled (E4M3 or E5M2
+values in float64; block scales applied per block of K).
 """
 
 from __future__ import annotations
@@ -25,6 +25,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lib = None
+FP8_FORMATS = {"e4m3": 0, "e5m2": 1}
 
 
 def build(out_path: str = _LIB_PATH, mutant: int = 0) -> str:
@@ -55,9 +56,11 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         fn.restype = ctypes.c_int
     lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
     lib.oracle_e4m3_value.restype = ctypes.c_double
-    lib.oracle_fp8_gemm.argtypes = [p, p, p, p, i64, i64, i64, ctypes.c_int]
+    lib.oracle_e5m2_value.argtypes = [ctypes.c_uint8]
+    lib.oracle_e5m2_value.restype = ctypes.c_double
+    lib.oracle_fp8_gemm.argtypes = [p, p, p, p, i64, i64, i64, ctypes.c_int, ctypes.c_int]
     lib.oracle_fp8_gemm.restype = ctypes.c_int
-    lib.oracle_fp8_blockscaled.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, ctypes.c_int]
+    lib.oracle_fp8_blockscaled.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int]
     lib.oracle_fp8_blockscaled.restype = ctypes.c_int
     for name in ("oracle_i4i4_entries", "oracle_w4a8_entries"):
         fn = getattr(lib, name)
@@ -162,24 +165,33 @@ class Oracle:
         table = np.array([self.lib.oracle_e4m3_value(c) for c in range(256)], dtype=np.float64)
         return table[codes]
 
-    def fp8_gemm(self, A: np.ndarray, B: np.ndarray, K: int, threads: int | None = None):
-        """(C, Cabs): C = A . B^T of E4M3 bytes A [M,K], B [N,K] in float64, and the
-        sum of the products' magnitudes per element (the scale of any rounding)."""
+    def e5m2_value(self, codes: np.ndarray) -> np.ndarray:
+        """float64 value of each E5M2 byte (+-inf for S.11111.00, NaN for S.11111.xx, xx != 0)."""
+        codes = np.asarray(codes, dtype=np.uint8)
+        table = np.array([self.lib.oracle_e5m2_value(c) for c in range(256)], dtype=np.float64)
+        return table[codes]
+
+    def fp8_gemm(self, A: np.ndarray, B: np.ndarray, K: int, threads: int | None = None, fmt: str = "e4m3"):
+        """(C, Cabs): C = A . B^T of fp8 bytes A [M,K], B [N,K] (both in format `fmt`,
+        "e4m3" or "e5m2") in float64, and the sum of the products' magnitudes per
+        element (the scale of any rounding)."""
         A = np.ascontiguousarray(A).view(np.uint8)
         B = np.ascontiguousarray(B).view(np.uint8)
         M, N = A.shape[0], B.shape[0]
         assert A.shape[1] == K and B.shape[1] == K
         C = np.empty((M, N), dtype=np.float64)
         Cabs = np.empty((M, N), dtype=np.float64)
-        rc = self.lib.oracle_fp8_gemm(_ptr(A), _ptr(B), _ptr(C), _ptr(Cabs), M, N, K, threads or default_threads())
+        rc = self.lib.oracle_fp8_gemm(_ptr(A), _ptr(B), _ptr(C), _ptr(Cabs), M, N, K, FP8_FORMATS[fmt],
+                                      threads or default_threads())
         if rc:
             raise RuntimeError(f"oracle_fp8_gemm failed ({rc})")
         return C, Cabs
 
     def fp8_blockscaled(self, A: np.ndarray, B: np.ndarray, SFA: np.ndarray, SFB: np.ndarray, K: int,
-                        g: int = 128, threads: int | None = None):
-        """(C, Cabs): the tutorial's block-scaled fp8 GEMM in float64: scales SFA [M, KB]
-        and SFB [N, KB] (float32, KB = ceil(K/g)) applied per block of g k."""
+                        g: int = 128, threads: int | None = None, fmt: str = "e4m3"):
+        """(C, Cabs): the tutorial's block-scaled fp8 GEMM in float64 (operands in format
+        `fmt`): scales SFA [M, KB] and SFB [N, KB] (float32, KB = ceil(K/g)) applied per
+        block of g k."""
         A = np.ascontiguousarray(A).view(np.uint8)
         B = np.ascontiguousarray(B).view(np.uint8)
         SFA = np.ascontiguousarray(SFA, dtype=np.float32)
@@ -190,7 +202,7 @@ class Oracle:
         C = np.empty((M, N), dtype=np.float64)
         Cabs = np.empty((M, N), dtype=np.float64)
         rc = self.lib.oracle_fp8_blockscaled(_ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(C), _ptr(Cabs), M, N, K, g,
-                                             threads or default_threads())
+                                             FP8_FORMATS[fmt], threads or default_threads())
         if rc:
             raise RuntimeError(f"oracle_fp8_blockscaled failed ({rc})")
         return C, Cabs

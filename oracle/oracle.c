@@ -228,6 +228,39 @@ double oracle_e4m3_value(uint8_t byte)
     return s ? -v : v;
 }
 
+/*
+ * E5M2 (the other 8-bit format of the tutorial's gemm_fp8; OCP 8-bit floating
+ * point, IEEE-like): 1 sign bit, 5 exponent bits with bias 15, 2 mantissa bits;
+ * exponent 0 holds the subnormals m/4 * 2^-14; exponent 31 is infinity (m = 0)
+ * or NaN (m != 0).  Largest finite value 57344.
+ */
+double oracle_e5m2_value(uint8_t byte)
+{
+    int s = byte >> 7, e = (byte >> 2) & 31, m = byte & 3;
+    double v;
+    if (e == 31) {
+        if (m) return 0.0 / 0.0;
+        v = 1.0 / 0.0;
+    } else if (e == 0) {
+#if ORACLE_MUTANT == 9 /* planted: subnormals decoded with the implicit leading one */
+        v = (1.0 + m / 4.0) / 16384.0;
+#else
+        v = (m / 4.0) / 16384.0;
+#endif
+    } else {
+        v = (1.0 + m / 4.0) * (double)(1u << e) / 32768.0;
+    }
+    return s ? -v : v;
+}
+
+/* Value of an fp8 byte in the given format (0 = E4M3, 1 = E5M2); -1 if unknown. */
+static int decode_fp8(const uint8_t *src, double *dst, int64_t count, int format)
+{
+    if (format != 0 && format != 1) return -1;
+    for (int64_t i = 0; i < count; ++i) dst[i] = format ? oracle_e5m2_value(src[i]) : oracle_e4m3_value(src[i]);
+    return 0;
+}
+
 struct fjob {
     const double *a, *b;
     double *c, *cabs;
@@ -253,16 +286,19 @@ static void *run_rows_f(void *arg)
     return NULL;
 }
 
-/* A [M, K], B [N, K] e4m3 bytes; C [M, N] = sum_k a*b and Cabs = sum_k |a*b| in
- * double.  Returns 0, or -1 on an allocation error. */
+/* A [M, K], B [N, K] fp8 bytes of `format` (0 = E4M3, 1 = E5M2, both operands);
+ * C [M, N] = sum_k a*b and Cabs = sum_k |a*b| in double.  Returns 0, or -1 on an
+ * allocation error or an unknown format. */
 int oracle_fp8_gemm(const uint8_t *A, const uint8_t *B, double *C, double *Cabs, int64_t M, int64_t N,
-                    int64_t K, int nthreads)
+                    int64_t K, int format, int nthreads)
 {
-    double *a = (double *)malloc(sizeof(double) * (size_t)(M * K));
-    double *b = (double *)malloc(sizeof(double) * (size_t)(N * K));
-    if (!a || !b) { free(a); free(b); return -1; }
-    for (int64_t i = 0; i < M * K; ++i) a[i] = oracle_e4m3_value(A[i]);
-    for (int64_t i = 0; i < N * K; ++i) b[i] = oracle_e4m3_value(B[i]);
+    double *a = (double *)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
+    double *b = (double *)malloc(sizeof(double) * (size_t)(N * K > 0 ? N * K : 1));
+    if (!a || !b || decode_fp8(A, a, M * K, format) || decode_fp8(B, b, N * K, format)) {
+        free(a);
+        free(b);
+        return -1;
+    }
     if (nthreads < 1) nthreads = 1;
     if (nthreads > M) nthreads = (int)(M > 0 ? M : 1);
     struct fjob *jobs = (struct fjob *)calloc((size_t)nthreads, sizeof(struct fjob));
@@ -286,13 +322,14 @@ int oracle_fp8_gemm(const uint8_t *A, const uint8_t *B, double *C, double *Cabs,
 
 /*
  * Block-scaled fp8 GEMM (the tutorial's gemm_blockscaled, low_precision_gemm.py):
- * A [M, K], B [N, K] e4m3 bytes; SFA [M, KB], SFB [N, KB] float32 scales with
+ * A [M, K], B [N, K] fp8 bytes of `format` (0 = E4M3, 1 = E5M2); SFA [M, KB],
+ * SFB [N, KB] float32 scales with
  * KB = ceil(K / g): the scales are applied along K per block of g values,
  *
  *   C[m,n] = sum_{kb} SFA[m,kb] * SFB[n,kb] * sum_{k in block kb} a[m,k]*b[n,k]
  *
  * in double; Cabs takes the same sums of magnitudes (the scale of any rounding).
- * Returns 0, or -1 on an allocation error.
+ * Returns 0, or -1 on an allocation error or an unknown format.
  */
 struct bjob {
     const double *a, *b;
@@ -338,15 +375,17 @@ static void *run_rows_b(void *arg)
 }
 
 int oracle_fp8_blockscaled(const uint8_t *A, const uint8_t *B, const float *SFA, const float *SFB, double *C,
-                           double *Cabs, int64_t M, int64_t N, int64_t K, int64_t g, int nthreads)
+                           double *Cabs, int64_t M, int64_t N, int64_t K, int64_t g, int format, int nthreads)
 {
     if (g < 1) return -1;
     const int64_t KB = (K + g - 1) / g;
     double *a = (double *)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
     double *b = (double *)malloc(sizeof(double) * (size_t)(N * K > 0 ? N * K : 1));
-    if (!a || !b) { free(a); free(b); return -1; }
-    for (int64_t i = 0; i < M * K; ++i) a[i] = oracle_e4m3_value(A[i]);
-    for (int64_t i = 0; i < N * K; ++i) b[i] = oracle_e4m3_value(B[i]);
+    if (!a || !b || decode_fp8(A, a, M * K, format) || decode_fp8(B, b, N * K, format)) {
+        free(a);
+        free(b);
+        return -1;
+    }
     if (nthreads < 1) nthreads = 1;
     if (nthreads > M) nthreads = (int)(M > 0 ? M : 1);
     struct bjob *jobs = (struct bjob *)calloc((size_t)nthreads, sizeof(struct bjob));

@@ -81,6 +81,19 @@ def e4m3_bytes(seed: int, shape) -> np.ndarray:
     return out.reshape(shape)
 
 
+def e5m2_bytes(seed: int, shape) -> np.ndarray:
+    """E5M2 bytes uniform over the 248 finite codes, as uint8: the top byte
+    modulo 248 is x in [0, 247], and x >= 0x7C moves up by four, which skips
+    +inf and the NaNs 0x7C..0x7F and ends at 0xFB (0xFC..0xFF never occur)."""
+    n = int(np.prod(shape, dtype=np.int64))
+    out = np.empty(n, dtype=np.uint8)
+    for s in range(0, n, _CHUNK):
+        e = min(n, s + _CHUNK)
+        x = (splitmix64(seed, e - s, start=s) >> np.uint64(56)).astype(np.int64) % 248
+        out[s:e] = np.where(x >= 0x7C, x + 4, x).astype(np.uint8)
+    return out.reshape(shape)
+
+
 def scale_values(seed: int, shape) -> np.ndarray:
     """Positive float32 scales (1 + u) * 2^e with u = the next 20 bits / 2^20 in
     [0, 1) and e = the top 3 bits - 4 in [-4, 3]: magnitudes over [1/16, 16)."""

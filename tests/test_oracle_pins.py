@@ -247,6 +247,66 @@ def check_fp8_integer_codes(o) -> bool:
     return bool(np.array_equal(C * 2.0 ** 18, (A.astype(np.int64) @ B.astype(np.int64).T).astype(np.float64)))
 
 
+def check_e5m2_decode(o) -> bool:
+    # every E5M2 byte against two decoders the oracle does not share: PyTorch's
+    # float8_e5m2 and IEEE half precision, whose top byte is E5M2 (same 5-bit
+    # exponent with bias 15, mantissa cut to 2 bits); infinities and NaNs included
+    torch = pytest.importorskip("torch")
+    mine = o.e5m2_value(np.arange(256))
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e5m2).to(torch.float64).numpy()
+    half = (np.arange(256, dtype=np.uint16) << 8).view(np.float16).astype(np.float64)
+    for other in (lib, half):
+        if not np.array_equal(np.isnan(mine), np.isnan(other)):
+            return False
+        if not np.array_equal(mine[~np.isnan(mine)], other[~np.isnan(other)]):
+            return False
+    want = {0x00: 0.0, 0x01: 2.0 ** -16, 0x03: 3 * 2.0 ** -16, 0x04: 2.0 ** -14, 0x3C: 1.0, 0x3E: 1.5,
+            0x7B: 57344.0, 0x7C: np.inf, 0xC0: -2.0, 0xFC: -np.inf}
+    return all(mine[c] == v for c, v in want.items()) and bool(np.isnan(mine[[0x7D, 0x7E, 0x7F, 0xFF]]).all())
+
+
+def check_fp8_gemm_e5m2(o) -> bool:
+    # E5M2 products against numpy's float64 matmul of the decoded values, and a
+    # closed form: with every a = 1.0 (byte 0x3C), C[m,n] is the sum of row n of B
+    rng = np.random.default_rng(10)
+    finite = np.array([c for c in range(256) if (c & 0x7C) != 0x7C], dtype=np.uint8)
+    A = rng.choice(finite, size=(6, 48))
+    B = rng.choice(finite, size=(5, 48))
+    C, Cabs = o.fp8_gemm(A, B, 48, fmt="e5m2")
+    a, b = o.e5m2_value(A), o.e5m2_value(B)
+    ref, refabs = a @ b.T, np.abs(a) @ np.abs(b).T
+    ok = np.allclose(C, ref, rtol=1e-12, atol=1e-12 * refabs.max()) and np.allclose(Cabs, refabs, rtol=1e-12)
+    # small integers in E5M2: 1 = 0x3C, 2 = 0x40, 3 = 0x42, 4 = 0x44, 6 = 0x46, 8 = 0x48, -3 = 0xC2
+    codes = {0x3C: 1, 0x40: 2, 0x42: 3, 0x44: 4, 0x46: 6, 0x48: 8, 0xC2: -3}
+    keys = np.array(list(codes), dtype=np.uint8)
+    Bi = rng.choice(keys, size=(4, 32))
+    ones = np.full((2, 32), 0x3C, dtype=np.uint8)
+    C1, _ = o.fp8_gemm(ones, Bi, 32, fmt="e5m2")
+    rows = [sum(codes[int(c)] for c in r) for r in Bi]
+    return bool(ok and np.array_equal(C1, np.array([rows, rows], dtype=np.float64)))
+
+
+def check_blockscaled_e5m2(o) -> bool:
+    # the block-scaled form over E5M2 operands: with unit scales it is the plain
+    # E5M2 GEMM; with power-of-two scales each block moves by its scale exactly
+    rng = np.random.default_rng(11)
+    finite = np.array([c for c in range(256) if (c & 0x7C) != 0x7C], dtype=np.uint8)
+    A = rng.choice(finite, size=(3, 260))
+    B = rng.choice(finite, size=(4, 260))
+    F, Fabs = o.fp8_gemm(A, B, 260, fmt="e5m2")
+    C, Cabs = o.fp8_blockscaled(A, B, np.ones((3, 3), np.float32), np.ones((4, 3), np.float32), 260, 128,
+                                fmt="e5m2")
+    a, b = o.e5m2_value(A), o.e5m2_value(B)
+    sfa = np.array([[1, 2, 0.5], [4, 1, 1], [0.25, 8, 2]], dtype=np.float32)
+    sfb = np.array([[2, 1, 1], [1, 0.5, 4], [1, 1, 1], [8, 2, 0.125]], dtype=np.float32)
+    S, _ = o.fp8_blockscaled(A, B, sfa, sfb, 260, 128, fmt="e5m2")
+    blocks = [(0, 128), (128, 256), (256, 260)]
+    want = sum(np.outer(sfa[:, i], sfb[:, i]) * (a[:, k0:k1] @ b[:, k0:k1].T) for i, (k0, k1) in enumerate(blocks))
+    scale = (np.abs(a) @ np.abs(b).T) * 16.0
+    return bool(np.allclose(C, F, rtol=1e-12, atol=1e-12 * Fabs.max()) and np.allclose(Cabs, Fabs, rtol=1e-12)
+                and np.allclose(S, want, rtol=1e-12, atol=1e-12 * scale.max()))
+
+
 def check_bf16_rounding(o) -> bool:
     # round-to-nearest-even float32 -> bfloat16 against PyTorch's conversion (a library
     # routine) on random values and on exact ties, and integers that bfloat16 holds exactly
@@ -303,7 +363,7 @@ def check_blockscaled_unit_scales(o) -> bool:
 PINS = [check_nibbles, check_roundtrip, check_golden_bytes, check_tiny_golden, check_brute_force,
         check_numpy_matmul, check_closed_forms, check_k_permutation, check_entries, check_e4m3_decode,
         check_fp8_gemm, check_fp8_integer_codes, check_bf16_rounding, check_blockscaled_closed_form,
-        check_blockscaled_unit_scales]
+        check_blockscaled_unit_scales, check_e5m2_decode, check_fp8_gemm_e5m2, check_blockscaled_e5m2]
 
 
 @pytest.fixture(scope="module")
@@ -346,13 +406,21 @@ def test_generator_ranges_and_determinism():
     assert np.array_equal(np.concatenate([si.splitmix64(42, 4), si.splitmix64(42, 6, start=4)]), s)
 
 
+def test_fp8_generators_cover_the_finite_codes():
+    e4 = si.e4m3_bytes(77, (512, 512))
+    e5 = si.e5m2_bytes(78, (512, 512))
+    assert set(np.unique(e4).tolist()) == set(range(256)) - {0x7F, 0xFF}
+    assert set(np.unique(e5).tolist()) == set(range(256)) - set(range(0x7C, 0x80)) - set(range(0xFC, 0x100))
+    assert np.array_equal(e5, si.e5m2_bytes(78, (512, 512)))
+
+
 def test_splitmix64_reference_value():
     # SplitMix64 with state 0: the first output is 0xE220A8397B1DCDAF (value
     # widely published with Vigna's splitmix64.c for seed 0).
     assert int(si.splitmix64(0, 1)[0]) == 0xE220A8397B1DCDAF
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9])
 def test_planted_mistakes_are_caught(tmp_path, mutant):
     path = oracle.build(str(tmp_path / f"liboracle_m{mutant}.so"), mutant=mutant)
     bad = oracle.Oracle(oracle.load(path))
