@@ -89,7 +89,7 @@ def recorded_traffic(workload):
 
 
 def workload_bytes(variant, M, N, K):
-    if variant == "fp8":
+    if variant in ("fp8", "fp8e5m2"):
         return (M + N) * K + 4 * M * N
     if variant == "fp8bs":
         return (M + N) * K + 4 * M * N + 4 * (M + N) * (-(-K // 128))
@@ -172,6 +172,9 @@ def whole_job_value(ops_per_step: float, steps: int, world: int, slowest_s: floa
     return ops_per_step * steps * world / slowest_s / 1e12
 
 
+# variants whose operands are fp8 bytes and whose C is float32
+FP8_VARIANTS = ("fp8", "fp8e5m2", "fp8bs")
+
 # the block scales of the fp8bs workload (set in main)
 _SCALES = None
 
@@ -179,8 +182,9 @@ _SCALES = None
 def oracle_sample_time(orc, variant, a, b, K, rows, threads):
     """Run the oracle on the first `rows` rows of A; returns seconds."""
     t0 = time.perf_counter()
-    if variant == "fp8":
-        orc.fp8_gemm(np.ascontiguousarray(a[:rows]), b, K, threads=threads)
+    if variant in ("fp8", "fp8e5m2"):
+        orc.fp8_gemm(np.ascontiguousarray(a[:rows]), b, K, threads=threads,
+                     fmt="e5m2" if variant == "fp8e5m2" else "e4m3")
     elif variant == "fp8bs":
         sfa, sfb = _SCALES
         orc.fp8_blockscaled(np.ascontiguousarray(a[:rows]), b, np.ascontiguousarray(sfa[:rows]), sfb, K,
@@ -242,14 +246,14 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
     # operands resident in HBM: logical -> packed by the library's pack kernel
     a_dev = torch.from_numpy(a).cuda()
     b_dev = torch.from_numpy(b).cuda()
-    if variant in ("fp8", "fp8bs"):
-        bp = b_dev  # E4M3 bytes as they are
+    if variant in FP8_VARIANTS:
+        bp = b_dev  # fp8 bytes as they are
     else:
         bp = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
         pig.pack_int4(b_dev, bp, N, K)
-    if variant == "fp8":
+    if variant in ("fp8", "fp8e5m2"):
         a_in = a_dev
-        gemm = pig.fp8_gemm
+        gemm = pig.fp8_gemm if variant == "fp8" else pig.fp8_gemm_e5m2
     elif variant == "fp8bs":
         a_in = a_dev
         sfa_d, sfb_d = (torch.from_numpy(x).cuda() for x in _SCALES)
@@ -264,7 +268,7 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
         a_in = a_dev
         gemm = pig.w4a8_gemm
     del b_dev
-    C = torch.empty((M, N), dtype=torch.float32 if variant in ("fp8", "fp8bs") else torch.int32, device="cuda")
+    C = torch.empty((M, N), dtype=torch.float32 if variant in FP8_VARIANTS else torch.int32, device="cuda")
     # L2 between steps: either every step reads its own copy of the operands,
     # rotating over copies worth three L2 capacities (a step's operands were last
     # touched two or more steps ago, and all later reads evicted them), or a
@@ -386,7 +390,7 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
                 "frac": achieved / peak, "traffic": traffic,
                 "kernel": "igemm_bs_kernel" if variant == "fp8bs" else "igemm_ss_kernel",
                 "kernel_ms": 1e3 * gemm_kernel_s, "algorithmic_ops_per_launch": ops,
-                "peak_source": f"{peak_src} bf16 burst x {E4M3_PER_BF16} (nominal e4m3/bf16 ratio)",
+                "peak_source": f"{peak_src} bf16 burst x {E4M3_PER_BF16} (nominal fp8/bf16 ratio)",
                 "mma_macs_per_op": 2 if variant == "w4a8" else 1}
 
     line = {
@@ -394,6 +398,7 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
         "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": {"i4i4": "int4", "w4a8": "int8xint4", "fp8": "e4m3 (float32 accumulate)",
+                  "fp8e5m2": "e5m2 (float32 accumulate)",
                   "fp8bs": "e4m3 with float32 block scales (float32 accumulate)"}[variant],
         "data": "synthetic (SplitMix64-seeded, uniform)",
         "config": {"workload": args.workload, "variant": variant, "M": M, "N": N, "K": K,

@@ -11,13 +11,14 @@
  * Workspace.  Large GEMMs (M * N >= 2^22 and, for int4 x int4, M, N >= 512;
  * for W4A8, M >= 768 and N >= 256) first write the operands as one code byte
  * per value, with row sums, into a workspace of (rows of A + rows of B) * K
- * bytes (W4A8: N*K + 2*M*K) plus a few KB.  The library takes it from its own stream-ordered
- * memory pool on the current device (allocated and released in `stream`
- * order, so concurrent calls on different streams do not share it); the pool
- * keeps what it reserved for later calls until the process exits.  A failed
- * workspace allocation returns IGEMM_CUDA_ERROR.  w4a8_gemm_scaled (its int32
- * product) and fp8_blockscaled_gemm (its transposed scales) take theirs from
- * the same pool; skinny shapes (M <= 32) and fp8_gemm need none.
+ * bytes (W4A8: N*K + 2*M*K) plus a few KB.  The library takes it from its own
+ * stream-ordered memory pool on the current device (allocated and released in
+ * `stream` order, so concurrent calls on different streams do not share it);
+ * the pool keeps what it reserved for later calls until the process exits.  A
+ * failed workspace allocation returns IGEMM_CUDA_ERROR.  w4a8_gemm_scaled (its
+ * int32 product) and fp8_blockscaled_gemm (its transposed scales) take theirs
+ * from the same pool; skinny shapes (M <= 32) and fp8_gemm (either format)
+ * need none.
  *
  * Launch overlap.  Where a call launches a short pass before its GEMM kernel
  * (the preparation of codes, the zeroing of C, the transposed scales), the GEMM
@@ -162,6 +163,15 @@ IGEMM_API int w4a8_gemm_scaled(const int8_t *A, const uint8_t *Bp, const float *
 IGEMM_API int fp8_gemm(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, cudaStream_t stream);
 
 /*
+ * The same GEMM for E5M2 operands (the page's other fp8 dtype; both A and B
+ * in E5M2: 5 exponent bits with bias 15, 2 mantissa bits, largest finite
+ * value 57344).  Arguments, rules and rounding as for fp8_gemm.  Products and
+ * sums of finite inputs stay finite in float32 for every K the int argument
+ * can hold; infinities and NaNs among the inputs are not given a meaning here.
+ */
+IGEMM_API int fp8_gemm_e5m2(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, cudaStream_t stream);
+
+/*
  * Block-scaled fp8 GEMM (TileLang tutorial page low_precision_gemm.py,
  * gemm_blockscaled: fp8 A (M,K) and B (N,K), float32 scale tensors SFA
  * (M, ceil(K/g)) and SFB (N, ceil(K/g)) applied along K per block of g values,
@@ -183,6 +193,13 @@ IGEMM_API int fp8_gemm(const uint8_t *A, const uint8_t *B, float *C, int M, int 
  */
 IGEMM_API int fp8_blockscaled_gemm(const uint8_t *A, const uint8_t *B, const float *SFA, const float *SFB, float *C,
                                    int M, int N, int K, cudaStream_t stream);
+
+/*
+ * The same block-scaled GEMM for E5M2 operands (A and B both E5M2); scales,
+ * arguments and rules as for fp8_blockscaled_gemm.
+ */
+IGEMM_API int fp8_blockscaled_gemm_e5m2(const uint8_t *A, const uint8_t *B, const float *SFA, const float *SFB,
+                                        float *C, int M, int N, int K, cudaStream_t stream);
 
 /*
  * Pack logical int4 values two per byte (TileLang tutorial page

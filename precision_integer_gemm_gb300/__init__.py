@@ -19,7 +19,7 @@ from .build import LIB_PATH, build as build_library
 
 __all__ = [
     "IgemmError", "load", "i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "w4a8_gemm_scaled", "fp8_gemm", "pack_int4",
-    "fp8_blockscaled_gemm", "unpack_int4",
+    "fp8_blockscaled_gemm", "fp8_gemm_e5m2", "fp8_blockscaled_gemm_e5m2", "unpack_int4",
     "igemm_strerror",
     "igemm_last_status", "igemm_watchdog_selftest", "igemm_kernels_launched", "igemm_time_next_gemm",
     "igemm_skinny_plan",
@@ -27,7 +27,7 @@ __all__ = [
 ]
 
 EXPORTED_SYMBOLS = ("i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "w4a8_gemm_scaled", "fp8_gemm",
-                    "fp8_blockscaled_gemm", "pack_int4", "unpack_int4", "igemm_strerror", "igemm_last_status",
+                    "fp8_gemm_e5m2", "fp8_blockscaled_gemm", "fp8_blockscaled_gemm_e5m2", "pack_int4", "unpack_int4", "igemm_strerror", "igemm_last_status",
                     "igemm_watchdog_selftest", "igemm_kernels_launched",
                     "igemm_time_next_gemm", "igemm_skinny_plan")
 
@@ -72,10 +72,12 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.i4i4_gemm_noalloc.restype = i
     lib.w4a8_gemm_scaled.argtypes = [p, p, p, p, p, i, i, i, p]
     lib.w4a8_gemm_scaled.restype = i
-    lib.fp8_gemm.argtypes = [p, p, p, i, i, i, p]
-    lib.fp8_gemm.restype = i
-    lib.fp8_blockscaled_gemm.argtypes = [p, p, p, p, p, i, i, i, p]
-    lib.fp8_blockscaled_gemm.restype = i
+    for name in ("fp8_gemm", "fp8_gemm_e5m2"):
+        getattr(lib, name).argtypes = [p, p, p, i, i, i, p]
+        getattr(lib, name).restype = i
+    for name in ("fp8_blockscaled_gemm", "fp8_blockscaled_gemm_e5m2"):
+        getattr(lib, name).argtypes = [p, p, p, p, p, i, i, i, p]
+        getattr(lib, name).restype = i
     lib.w4a8_gemm.argtypes = [p, p, p, i, i, i, p]
     lib.w4a8_gemm.restype = i
     lib.pack_int4.argtypes = [p, p, i64, i64, p]
@@ -148,11 +150,22 @@ def fp8_gemm(A, B, C, M: int, N: int, K: int, stream=None) -> None:
     _check(load().fp8_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(stream)), "fp8_gemm")
 
 
+def fp8_gemm_e5m2(A, B, C, M: int, N: int, K: int, stream=None) -> None:
+    """C[M,N] (float32) = A . B^T for E5M2 byte matrices A [M,K] and B [N,K]."""
+    _check(load().fp8_gemm_e5m2(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(stream)), "fp8_gemm_e5m2")
+
+
 def fp8_blockscaled_gemm(A, B, SFA, SFB, C, M: int, N: int, K: int, stream=None) -> None:
     """C[M,N] (float32) = sum over 128-k blocks kb of SFA[m,kb] * SFB[n,kb] * (A . B^T over the block),
     for E4M3 byte matrices A [M,K], B [N,K] and float32 scales SFA [M,ceil(K/128)], SFB [N,ceil(K/128)]."""
     _check(load().fp8_blockscaled_gemm(_ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(C), M, N, K, _stream(stream)),
            "fp8_blockscaled_gemm")
+
+
+def fp8_blockscaled_gemm_e5m2(A, B, SFA, SFB, C, M: int, N: int, K: int, stream=None) -> None:
+    """fp8_blockscaled_gemm for E5M2 byte matrices A [M,K] and B [N,K]."""
+    _check(load().fp8_blockscaled_gemm_e5m2(_ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(C), M, N, K,
+                                            _stream(stream)), "fp8_blockscaled_gemm_e5m2")
 
 
 def pack_int4(logical, packed, rows: int, K: int, stream=None) -> None:

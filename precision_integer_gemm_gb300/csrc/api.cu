@@ -385,7 +385,8 @@ extern "C" int w4a8_gemm_scaled(const int8_t *A, const uint8_t *Bp, const float 
     return rc != kOk ? rc : rf;
 }
 
-extern "C" int fp8_gemm(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, cudaStream_t stream)
+static int fp8_gemm_checked(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, int fmt,
+                            cudaStream_t stream)
 {
     if (M < 0 || N < 0 || K < 0) return kInvalidArgument;
     if (M == 0 || N == 0) return kOk;
@@ -395,13 +396,23 @@ extern "C" int fp8_gemm(const uint8_t *A, const uint8_t *B, float *C, int M, int
     if (K == 0) return cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 4, stream) == cudaSuccess ? kOk : kCudaError;
     if (!A || !B) return kInvalidArgument;
     if (!aligned16(A) || !aligned16(B)) return kMisaligned;
-    return launch_fp8(A, B, C, M, N, K, stream);
+    return launch_fp8(A, B, C, M, N, K, fmt, stream);
+}
+
+extern "C" int fp8_gemm(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, cudaStream_t stream)
+{
+    return fp8_gemm_checked(A, B, C, M, N, K, 0, stream);
+}
+
+extern "C" int fp8_gemm_e5m2(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, cudaStream_t stream)
+{
+    return fp8_gemm_checked(A, B, C, M, N, K, 1, stream);
 }
 
 static bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-extern "C" int fp8_blockscaled_gemm(const uint8_t *A, const uint8_t *B, const float *SFA, const float *SFB, float *C,
-                                    int M, int N, int K, cudaStream_t stream)
+static int fp8_blockscaled_checked(const uint8_t *A, const uint8_t *B, const float *SFA, const float *SFB, float *C,
+                                   int M, int N, int K, int fmt, cudaStream_t stream)
 {
     if (M < 0 || N < 0 || K < 0) return kInvalidArgument;
     if (M == 0 || N == 0) return kOk;
@@ -411,7 +422,19 @@ extern "C" int fp8_blockscaled_gemm(const uint8_t *A, const uint8_t *B, const fl
     if (K == 0) return cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 4, stream) == cudaSuccess ? kOk : kCudaError;
     if (!A || !B || !SFA || !SFB) return kInvalidArgument;
     if (!aligned16(A) || !aligned16(B) || !aligned4(SFA) || !aligned4(SFB)) return kMisaligned;
-    return launch_fp8_blockscaled(A, B, SFA, SFB, C, M, N, K, stream);
+    return launch_fp8_blockscaled(A, B, SFA, SFB, C, M, N, K, fmt, stream);
+}
+
+extern "C" int fp8_blockscaled_gemm(const uint8_t *A, const uint8_t *B, const float *SFA, const float *SFB, float *C,
+                                    int M, int N, int K, cudaStream_t stream)
+{
+    return fp8_blockscaled_checked(A, B, SFA, SFB, C, M, N, K, 0, stream);
+}
+
+extern "C" int fp8_blockscaled_gemm_e5m2(const uint8_t *A, const uint8_t *B, const float *SFA, const float *SFB,
+                                         float *C, int M, int N, int K, cudaStream_t stream)
+{
+    return fp8_blockscaled_checked(A, B, SFA, SFB, C, M, N, K, 1, stream);
 }
 
 extern "C" int pack_int4(const int8_t *logical, uint8_t *packed, int64_t rows, int64_t K, cudaStream_t stream)

@@ -8,8 +8,9 @@
 
 namespace igemm {
 
-//                  operand stages  scale stages  epilogue warps per quadrant  TMEM buffers  cluster
+//                  operand stages  scale stages  epilogue warps per quadrant  TMEM buffers  cluster  format
 using CfgBs = BsCfg<5, 8, 3, 2, 2>;
+using CfgBsE5m2 = BsCfg<5, 8, 3, 2, 2, 1>;
 
 // out[kb * pad + r] = sf[r * KB + kb] for r < rows, 0 for rows <= r < pad;
 // the SFA part first (pad_a rows), then the SFB part (pad_b rows).
@@ -33,10 +34,10 @@ __global__ void transpose_scales_kernel(const float *__restrict__ sfa, int rows_
     }
 }
 
-int launch_fp8_blockscaled(const uint8_t *A, const uint8_t *B, const float *SFA, const float *SFB, float *C, int M,
-                           int N, int K, cudaStream_t stream)
+template <class Cfg>
+static int launch_bs_cfg(const uint8_t *A, const uint8_t *B, const float *SFA, const float *SFB, float *C, int M, int N,
+                         int K, cudaStream_t stream)
 {
-    using Cfg = CfgBs;
     auto kernel = igemm_bs_kernel<Cfg>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return kCudaError;
@@ -142,6 +143,13 @@ int launch_fp8_blockscaled(const uint8_t *A, const uint8_t *B, const float *SFA,
     }
     const int rf = workspace_free(ws, stream);
     return rc != kOk ? rc : rf;
+}
+
+int launch_fp8_blockscaled(const uint8_t *A, const uint8_t *B, const float *SFA, const float *SFB, float *C, int M,
+                           int N, int K, int fmt, cudaStream_t stream)
+{
+    return fmt == 0 ? launch_bs_cfg<CfgBs>(A, B, SFA, SFB, C, M, N, K, stream)
+                    : launch_bs_cfg<CfgBsE5m2>(A, B, SFA, SFB, C, M, N, K, stream);
 }
 
 }  // namespace igemm

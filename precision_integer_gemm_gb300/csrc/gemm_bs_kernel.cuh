@@ -1,5 +1,5 @@
 // Block-scaled fp8 GEMM: the TileLang tutorial's gemm_blockscaled
-// (low_precision_gemm.py): A [M, K] and B [N, K] E4M3, float32 scales
+// (low_precision_gemm.py): A [M, K] and B [N, K] E4M3 (or both E5M2), float32 scales
 // SFA [M, KB] and SFB [N, KB] with KB = ceil(K / 128), applied along K per
 // block of 128 values (the granularity the page gives for sm100), float32
 // accumulation and output:
@@ -49,7 +49,7 @@ struct BsParams {
     unsigned long long limit_ns;
 };
 
-template <int ST_, int SS_, int EPQ_ = 2, int PB_ = 4, int CL_ = 1>
+template <int ST_, int SS_, int EPQ_ = 2, int PB_ = 4, int CL_ = 1, int FMT_ = 0>
 struct BsCfg {
     static constexpr int ST = ST_;          // operand stages (A + B of one 128-k block)
     static constexpr int SS = SS_;          // scale stages
@@ -60,6 +60,7 @@ struct BsCfg {
     // promotion
     static constexpr int PB = PB_;
     static constexpr int CL = CL_;          // CTAs per cluster sharing the A tile
+    static constexpr int kFmt = FMT_;       // operand format: 0 = E4M3, 1 = E5M2
     static constexpr int kEpiWarps = 4 * EPQ;
     static constexpr int kBK = 128;
     static constexpr int kTileA = 128 * 128;  // bytes
@@ -75,6 +76,7 @@ struct BsCfg {
     static constexpr int kThreads = 32 * (kEpiWarps + 2);
     static_assert(EPQ >= 2 && EPQ <= 3, "epilogue warps per quadrant (the totals' registers)");
     static_assert(CL == 1 || CL == 2, "cluster size");
+    static_assert(FMT_ == 0 || FMT_ == 1, "fp8 format");
     static constexpr int kTmemCols = PB * BN <= 256 ? 256 : 512;  // PB partial buffers of BN columns
     static_assert(PB * BN <= 512, "TMEM budget");
     static constexpr int kOffStages = 0;
@@ -256,7 +258,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     } else if (warp == Cfg::kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_e4m3_f32(128, Cfg::BN);
+            constexpr uint32_t idesc = idesc_f8_f32(128, Cfg::BN, Cfg::kFmt);
             const uint64_t desc0 = sdesc_kmajor_sw128(smem_u32(stages));
             uint32_t g = 0;
             bool ok = true;

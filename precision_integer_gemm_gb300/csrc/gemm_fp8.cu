@@ -1,18 +1,19 @@
-// fp8 GEMM: C[M,N] (float32) = A[M,K] . B[N,K]^T for E4M3 operands, the
-// gemm_fp8 of the TileLang tutorial page low_precision_gemm.py (fp8 dtype in,
-// float32 accumulator).  The operands are already what tcgen05.mma kind::f8f6f4
+// fp8 GEMM: C[M,N] (float32) = A[M,K] . B[N,K]^T for E4M3 or E5M2 operands
+// (both in the same format), the gemm_fp8 of the TileLang tutorial page
+// low_precision_gemm.py (fp8 dtype in, float32 accumulator).  The operands are already what tcgen05.mma kind::f8f6f4
 // consumes, so igemm_ss_kernel runs on them directly (no preparation pass) and
 // its epilogue stores the float32 accumulator; split K reduce-adds float32.
 #include "launch.cuh"
 
 namespace igemm {
 
-//                     W4A8   BN  stages CL  float out
+//                         W4A8   BN  stages CL  float out  format
 using CfgFp8 = SsCfg<false, 256, 4, 2, true>;
+using CfgFp8E5m2 = SsCfg<false, 256, 4, 2, true, 1>;
 
-int launch_fp8(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, cudaStream_t stream)
+template <class Cfg>
+static int launch_fp8_cfg(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, cudaStream_t stream)
 {
-    using Cfg = CfgFp8;
     CUtensorMap mapP, mapQ, mapC = {};
     if (make_map(&mapP, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, M, K, Cfg::kPRows, Cfg::kBK, CU_TENSOR_MAP_SWIZZLE_128B) !=
         kOk)
@@ -26,6 +27,12 @@ int launch_fp8(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K
         return kCudaError;
     return launch_ss<Cfg>(mapP, mapQ, mapC, tma_store, reinterpret_cast<int32_t *>(C), M, N, K, nullptr, nullptr, M,
                           N, (int64_t(M) + N) * K, stream);
+}
+
+int launch_fp8(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, int fmt, cudaStream_t stream)
+{
+    return fmt == 0 ? launch_fp8_cfg<CfgFp8>(A, B, C, M, N, K, stream)
+                    : launch_fp8_cfg<CfgFp8E5m2>(A, B, C, M, N, K, stream);
 }
 
 }  // namespace igemm

@@ -41,11 +41,13 @@
 
 namespace igemm {
 
-template <bool W4A8, int BN_, int ST_, int CL_ = 1, bool FLOAT_ = false>
+template <bool W4A8, int BN_, int ST_, int CL_ = 1, bool FLOAT_ = false, int FMT_ = 0>
 struct SsCfg {
     static constexpr bool kW4A8 = W4A8;
-    // kFloat: plain e4m3 operands (the fp8 GEMM), C = the float32 accumulator
+    // kFloat: plain fp8 operands (the fp8 GEMM), C = the float32 accumulator;
+    // kFmt: their format, 0 = E4M3 (also the integer codes), 1 = E5M2
     static constexpr bool kFloat = FLOAT_;
+    static constexpr int kFmt = FMT_;
     static constexpr int kQRows = BN_;                 // MMA N
     static constexpr int QA = W4A8 ? BN_ / 2 : BN_;    // Q source rows per tile
     static constexpr int ST = ST_;                     // pipeline stages
@@ -79,6 +81,7 @@ struct SsCfg {
     static_assert(ST <= 32, "stage masks");
     static_assert(CL == 1 || CL == 2, "cluster size");
     static_assert(!(FLOAT_ && W4A8), "the fp8 GEMM uses the int4 x int4 tile layout");
+    static_assert(FMT_ == 0 || (FLOAT_ && FMT_ == 1), "E5M2 only for the fp8 GEMM");
     static_assert(W4A8 || kQBoxRows % 8 == 0, "Q half tiles start on 1024-byte boundaries");
 };
 
@@ -265,7 +268,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     } else if (warp == 4) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_e4m3_f32(Cfg::kPRows, Cfg::kQRows);
+            constexpr uint32_t idesc = idesc_f8_f32(Cfg::kPRows, Cfg::kQRows, Cfg::kFmt);
             uint32_t g = 0, nacc = 0;
             bool ok = true;
             for (int u = cid; ok && u < prm.num_units; u += ncl, ++nacc) {

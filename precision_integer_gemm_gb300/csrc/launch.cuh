@@ -405,8 +405,9 @@ SkinnyPlan skinny_plan_w4a8(int M, int N, int K, int sms, int pairs, int quads);
 constexpr size_t kNoAllocWorkspaceBytes = size_t(32) << 20;
 int launch_i4i4_noalloc(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);
 int launch_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);
-int launch_fp8(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, cudaStream_t stream);
+// fp8 operands: fmt 0 = E4M3, 1 = E5M2 (both operands).
+int launch_fp8(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, int fmt, cudaStream_t stream);
 int launch_fp8_blockscaled(const uint8_t *A, const uint8_t *B, const float *SFA, const float *SFB, float *C, int M,
-                           int N, int K, cudaStream_t stream);
+                           int N, int K, int fmt, cudaStream_t stream);
 
 }  // namespace igemm

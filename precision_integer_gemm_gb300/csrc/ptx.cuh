@@ -248,7 +248,8 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, both operands K-major, e4m3 x e4m3 -> f32.
+// D[tmem] (+)= A[smem] * B[smem]^T, both operands K-major, fp8 x fp8 -> f32
+// (the operand formats are those of `idesc`).
 __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                            uint32_t accumulate)
 {
@@ -450,6 +451,13 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t smem_addr)
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N)
 {
     return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// The same with A and B both in fp8 format `fmt`: 0 = E4M3, 1 = E5M2 (the
+// format codes of bits 7-9 and 10-12).
+__host__ __device__ constexpr uint32_t idesc_f8_f32(uint32_t M, uint32_t N, uint32_t fmt)
+{
+    return idesc_e4m3_f32(M, N) | (fmt << 7) | (fmt << 10);
 }
 
 }  // namespace igemm

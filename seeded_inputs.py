@@ -122,14 +122,18 @@ WORKLOADS = {
     "fp8_8192": ("fp8", 8192, 8192, 8192, 7),
     # the tutorial's block-scaled fp8 GEMM (a "next" row): plus float32 scales per 128-k block
     "fp8bs_8192": ("fp8bs", 8192, 8192, 8192, 8),
+    # the fp8 GEMM on the page's other fp8 dtype: E5M2 operands, float32 C
+    "fp8e5m2_8192": ("fp8e5m2", 8192, 8192, 8192, 9),
 }
 
 
 def logical_operands(variant: str, M: int, N: int, K: int, index: int):
     """Logical (unpacked) operands: A [M,K] int8 and B [N,K] int8 (int4 range);
-    for "fp8" and "fp8bs", A [M,K] and B [N,K] E4M3 bytes."""
+    for "fp8" and "fp8bs", A [M,K] and B [N,K] E4M3 bytes; for "fp8e5m2", E5M2 bytes."""
     if variant in ("fp8", "fp8bs"):
         return e4m3_bytes(workload_seed(index, 0), (M, K)), e4m3_bytes(workload_seed(index, 1), (N, K))
+    if variant == "fp8e5m2":
+        return e5m2_bytes(workload_seed(index, 0), (M, K)), e5m2_bytes(workload_seed(index, 1), (N, K))
     if variant == "i4i4":
         a = int4_values(workload_seed(index, 0), (M, K))
     elif variant == "w4a8":

@@ -83,8 +83,9 @@ def test_pack_argument_validation(lib):
     assert lib.pack_int4(None, FAKE, 4, 8, None) == pig.IGEMM_INVALID_ARGUMENT
 
 
-def test_fp8_blockscaled_argument_validation(lib):
-    f = lib.fp8_blockscaled_gemm
+@pytest.mark.parametrize("name", ["fp8_blockscaled_gemm", "fp8_blockscaled_gemm_e5m2"])
+def test_fp8_blockscaled_argument_validation(lib, name):
+    f = getattr(lib, name)
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 4, 16, None) == pig.IGEMM_INVALID_ARGUMENT
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 24, None) == pig.IGEMM_UNSUPPORTED_SHAPE
     assert f(None, None, None, None, None, 0, 4, 16, None) == pig.IGEMM_OK

@@ -203,11 +203,11 @@ def test_w4a8_scaled_matches_oracle(orc, M, N, K):
 
 # ---------------------------------------------------------------- fp8 GEMM (E4M3, float32 accumulate)
 
-def run_fp8(A: np.ndarray, B: np.ndarray):
+def run_fp8(A: np.ndarray, B: np.ndarray, fmt: str = "e4m3"):
     M, K = A.shape
     N = B.shape[0]
     C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
-    pig.fp8_gemm(dev(A), dev(B), C, M, N, K)
+    (pig.fp8_gemm if fmt == "e4m3" else pig.fp8_gemm_e5m2)(dev(A), dev(B), C, M, N, K)
     assert pig.igemm_last_status() == 0
     return C.cpu().numpy().astype(np.float64)
 
@@ -234,11 +234,12 @@ FP8BS_SHAPES = [(128, 128, 128), (1, 1, 16), (130, 300, 304), (256, 260, 1040), 
                 (1024, 1024, 2048)]
 
 
-def run_fp8bs(A, B, sfa, sfb):
+def run_fp8bs(A, B, sfa, sfb, fmt: str = "e4m3"):
     M, K = A.shape
     N = B.shape[0]
     C = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    pig.fp8_blockscaled_gemm(dev(A), dev(B), dev(sfa), dev(sfb), C, M, N, K)
+    f = pig.fp8_blockscaled_gemm if fmt == "e4m3" else pig.fp8_blockscaled_gemm_e5m2
+    f(dev(A), dev(B), dev(sfa), dev(sfb), C, M, N, K)
     assert pig.igemm_last_status() == 0
     return C.cpu().numpy().astype(np.float64)
 
@@ -299,6 +300,62 @@ def test_fp8_integer_codes_are_exact(orc, M, N, K):
     C = run_fp8(A, B)
     want = (A.astype(np.int64) @ B.astype(np.int64).T).astype(np.float64) * 2.0 ** -18
     assert np.array_equal(C, want)
+
+
+# ---------------------------------------------------------------- E5M2 operands (the page's other fp8 dtype)
+
+@pytest.mark.parametrize("M,N,K", FP8_SHAPES)
+def test_fp8_e5m2_matches_oracle(orc, M, N, K):
+    A = si.e5m2_bytes(15000 + M + K, (M, K))
+    B = si.e5m2_bytes(16000 + N + K, (N, K))
+    C = run_fp8(A, B, "e5m2")
+    want, mag = orc.fp8_gemm(A, B, K, fmt="e5m2")
+    tol = K * 2.0 ** -23 * mag + 1e-30
+    assert np.all(np.abs(C - want) <= tol), float(np.max(np.abs(C - want) / np.maximum(mag, 1e-30)))
+
+
+# E5M2 bytes of small integers (2 mantissa bits: 1, 1.25, 1.5, 1.75 times 2^e)
+E5M2_INTS = {0x00: 0, 0x3C: 1, 0x40: 2, 0x42: 3, 0x44: 4, 0x45: 5, 0x46: 6, 0x47: 7, 0x48: 8, 0x49: 10, 0x4A: 12,
+             0x4B: 14, 0x4C: 16}
+
+
+@pytest.mark.parametrize("M,N,K,vmax", [(256, 256, 4096, 16), (130, 300, 96, 16), (128, 128, 65536, 8)])
+def test_fp8_e5m2_integer_values_are_exact(orc, M, N, K, vmax):
+    # signed integers of magnitude <= vmax: every partial sum is an integer of
+    # magnitude <= K * vmax^2 <= 2^24, which float32 holds exactly in any order
+    codes = np.array([c for c, v in E5M2_INTS.items() if v <= vmax], dtype=np.uint8)
+    rng = np.random.default_rng(M + N + K)
+    A = rng.choice(codes, size=(M, K)) | (rng.integers(0, 2, size=(M, K)).astype(np.uint8) << 7)
+    B = rng.choice(codes, size=(N, K)) | (rng.integers(0, 2, size=(N, K)).astype(np.uint8) << 7)
+    lut = np.zeros(256, dtype=np.int64)
+    for c, v in E5M2_INTS.items():
+        lut[c], lut[c | 0x80] = v, -v
+    want = (lut[A] @ lut[B].T).astype(np.float64)
+    C = run_fp8(A, B, "e5m2")
+    assert np.array_equal(C, want)
+    if M * N * K <= (1 << 28):
+        assert np.array_equal(orc.fp8_gemm(A, B, K, fmt="e5m2")[0], want)
+
+
+@pytest.mark.parametrize("M,N,K", FP8BS_SHAPES)
+def test_fp8_blockscaled_e5m2_matches_oracle(orc, M, N, K):
+    A = si.e5m2_bytes(17100 + M, (M, K))
+    B = si.e5m2_bytes(17200 + N, (N, K))
+    sfa = si.scale_values(17300 + M, (M, -(-K // 128)))
+    sfb = si.scale_values(17400 + N, (N, -(-K // 128)))
+    got = run_fp8bs(A, B, sfa, sfb, "e5m2")
+    want, wabs = orc.fp8_blockscaled(A, B, sfa, sfb, K, fmt="e5m2")
+    tol = max(K, 16) * 2.0 ** -23 * wabs + 1e-30
+    assert np.all(np.abs(got - want) <= tol), float(np.max(np.abs(got - want) / np.maximum(wabs, 1e-30)))
+
+
+def test_fp8_e5m2_full_size_sampled(orc):
+    # the E5M2 bench workload, 8192^3: sampled rows
+    variant, M, N, K, A, B = si.workload_operands("fp8e5m2_8192")
+    C = run_fp8(A, B, "e5m2")
+    rows = np.unique(np.random.default_rng(17).integers(0, M, 16))
+    want, mag = orc.fp8_gemm(np.ascontiguousarray(A[rows]), B, K, fmt="e5m2")
+    assert np.all(np.abs(C[rows] - want) <= K * 2.0 ** -23 * mag + 1e-30)
 
 
 def test_configured_small_workloads(orc):
@@ -541,9 +598,19 @@ def test_empty_and_zero_k():
     F = torch.full((4, 4), 7.0, dtype=torch.float32, device="cuda")
     pig.fp8_gemm(None, None, F, 0, 4, 16)
     pig.fp8_blockscaled_gemm(None, None, None, None, F, 4, 0, 16)
+    pig.fp8_gemm_e5m2(None, None, F, 0, 4, 16)
+    pig.fp8_blockscaled_gemm_e5m2(None, None, None, None, F, 4, 0, 16)
     torch.cuda.synchronize()
     assert bool((F == 7.0).all())
     pig.fp8_blockscaled_gemm(None, None, None, None, F, 4, 4, 0)
+    torch.cuda.synchronize()
+    assert bool((F == 0.0).all())
+    F.fill_(7.0)
+    pig.fp8_gemm_e5m2(None, None, F, 4, 4, 0)
+    torch.cuda.synchronize()
+    assert bool((F == 0.0).all())
+    F.fill_(7.0)
+    pig.fp8_blockscaled_gemm_e5m2(None, None, None, None, F, 4, 4, 0)
     torch.cuda.synchronize()
     assert bool((F == 0.0).all())
 
