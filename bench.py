@@ -358,20 +358,32 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
     extra_inputs = [(x.cpu().pin_memory(), x) for x in (sfa_d, sfb_d)] if variant == "fp8bs" else []
     e_s = torch.cuda.Event(enable_timing=True)
     e_e = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e_s.record(stream)
-    for _ in range(e2e_steps):
+    # the integer GEMMs have host-buffer entry points (copies inside the call,
+    # overlapped with the GEMM in row chunks); the fp8 ones are called on
+    # device buffers after torch copies in the same stream
+    host_gemm = {"i4i4": pig.i4i4_gemm_host, "w4a8": pig.w4a8_gemm_host}.get(variant)
+
+    def e2e_step():
+        if host_gemm is not None:
+            host_gemm(a_host, bp_host, c_host, M, N, K, stream)
+            return
         a_e.copy_(a_host, non_blocking=True)
         bp_e.copy_(bp_host, non_blocking=True)
         for host, devt in extra_inputs:
             devt.copy_(host, non_blocking=True)
         gemm(a_e, bp_e, C_e, M, N, K, stream)
         c_host.copy_(C_e, non_blocking=True)
+
+    e2e_step()  # untimed: the first call sizes the library's memory pool for the call's buffers
+    torch.cuda.synchronize()
+    e_s.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
     e_e.record(stream)
     torch.cuda.synchronize()
     e2e_s = e_s.elapsed_time(e_e) / 1e3
     e2e_value = ops * e2e_steps * world / e2e_s / 1e12  # replicas run concurrently
-    if not torch.equal(C_e, C):
+    if not torch.equal(c_host, C.cpu()):
         raise RuntimeError("end-to-end result differs from the device-resident result")
 
     peaks, peak_src = load_peaks()
@@ -413,7 +425,9 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
         "e2e": {"value": e2e_value, "unit": UNIT,
                 "h2d_bytes_per_step": int(a_in.numel() * a_in.element_size() + bp.numel() +
                                           sum(d.numel() * d.element_size() for _, d in extra_inputs)),
-                "d2h_bytes_per_step": int(C.numel() * 4)},
+                "d2h_bytes_per_step": int(C.numel() * 4),
+                "call": (f"{variant}_gemm_host (host buffers, copies inside the call)" if host_gemm is not None
+                         else "torch copies to device buffers, then the device entry point, one stream")},
         "roofline": roof,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

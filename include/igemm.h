@@ -126,6 +126,30 @@ IGEMM_API int i4i4_gemm_noalloc(const uint8_t *Ap, const uint8_t *Bp, int32_t *C
 IGEMM_API int w4a8_gemm(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);
 
 /*
+ * The same two GEMMs with A, Bp and C in HOST memory (pinned memory lets the
+ * copies run asynchronously and overlap; pageable memory works but the copies
+ * then block the calling thread).  The call copies Bp to the device, then A in
+ * row chunks (about eight chunks of at least 1024 rows, one chunk below 2048
+ * rows), runs the device entry point on each chunk in `stream`, and copies each
+ * chunk of C back while later chunks compute.  The copies run on two copy
+ * streams of the library's own (per device, created on first use); `stream`
+ * waits for them, so C is complete on the host once `stream` has reached the
+ * end of the call (e.g. after cudaStreamSynchronize(stream)).  The host buffers
+ * must stay valid and unchanged until then.  Device memory for Bp, two chunks
+ * of A and two chunks of C comes from the library's pool.
+ *   Ap / A  [M, K/2] packed int4 / [M, K] int8 (host), read only
+ *   Bp      [N, K/2] packed int4 (host), read only
+ *   C       [M, N] int32 (host), written
+ * Rules as for i4i4_gemm / w4a8_gemm (K % 32 == 0, K <= 65536, empty shapes
+ * are no-ops, K == 0 zeroes C), except that host pointers need no alignment.
+ * igemm_time_next_gemm times the GEMM kernel of the first chunk only.
+ */
+IGEMM_API int i4i4_gemm_host(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K,
+                             cudaStream_t stream);
+IGEMM_API int w4a8_gemm_host(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K,
+                             cudaStream_t stream);
+
+/*
  * W4A8 GEMM with per-channel dequantisation (the "scaled epilogue" step that
  * follows the integer product in W4A8 inference; the pages show scales only
  * as the per-block structure of the tutorial's gemm_blockscaled):

@@ -18,7 +18,7 @@ import os
 from .build import LIB_PATH, build as build_library
 
 __all__ = [
-    "IgemmError", "load", "i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "w4a8_gemm_scaled", "fp8_gemm", "pack_int4",
+    "IgemmError", "load", "i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "i4i4_gemm_host", "w4a8_gemm_host", "w4a8_gemm_scaled", "fp8_gemm", "pack_int4",
     "fp8_blockscaled_gemm", "fp8_gemm_e5m2", "fp8_blockscaled_gemm_e5m2", "unpack_int4",
     "igemm_strerror",
     "igemm_last_status", "igemm_watchdog_selftest", "igemm_kernels_launched", "igemm_time_next_gemm",
@@ -26,7 +26,7 @@ __all__ = [
     "EXPORTED_SYMBOLS", "LIB_PATH", "build_library",
 ]
 
-EXPORTED_SYMBOLS = ("i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "w4a8_gemm_scaled", "fp8_gemm",
+EXPORTED_SYMBOLS = ("i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "i4i4_gemm_host", "w4a8_gemm_host", "w4a8_gemm_scaled", "fp8_gemm",
                     "fp8_gemm_e5m2", "fp8_blockscaled_gemm", "fp8_blockscaled_gemm_e5m2", "pack_int4", "unpack_int4", "igemm_strerror", "igemm_last_status",
                     "igemm_watchdog_selftest", "igemm_kernels_launched",
                     "igemm_time_next_gemm", "igemm_skinny_plan")
@@ -80,6 +80,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         getattr(lib, name).restype = i
     lib.w4a8_gemm.argtypes = [p, p, p, i, i, i, p]
     lib.w4a8_gemm.restype = i
+    for name in ("i4i4_gemm_host", "w4a8_gemm_host"):
+        getattr(lib, name).argtypes = [p, p, p, i, i, i, p]
+        getattr(lib, name).restype = i
     lib.pack_int4.argtypes = [p, p, i64, i64, p]
     lib.pack_int4.restype = i
     lib.unpack_int4.argtypes = [p, p, i64, i64, p]
@@ -137,6 +140,18 @@ def i4i4_gemm_noalloc(Ap, Bp, C, M: int, N: int, K: int, stream=None) -> None:
 def w4a8_gemm(A, Bp, C, M: int, N: int, K: int, stream=None) -> None:
     """C[M,N] (int32) = A . B^T for int8 A [M,K] and packed int4 Bp [N,K/2]."""
     _check(load().w4a8_gemm(_ptr(A), _ptr(Bp), _ptr(C), M, N, K, _stream(stream)), "w4a8_gemm")
+
+
+def i4i4_gemm_host(Ap, Bp, C, M: int, N: int, K: int, stream=None) -> None:
+    """i4i4_gemm with Ap, Bp and C in host memory (CPU tensors, pinned for overlap);
+    C is complete once `stream` has reached the end of the call."""
+    _check(load().i4i4_gemm_host(_ptr(Ap), _ptr(Bp), _ptr(C), M, N, K, _stream(stream)), "i4i4_gemm_host")
+
+
+def w4a8_gemm_host(A, Bp, C, M: int, N: int, K: int, stream=None) -> None:
+    """w4a8_gemm with A, Bp and C in host memory (CPU tensors, pinned for overlap);
+    C is complete once `stream` has reached the end of the call."""
+    _check(load().w4a8_gemm_host(_ptr(A), _ptr(Bp), _ptr(C), M, N, K, _stream(stream)), "w4a8_gemm_host")
 
 
 def w4a8_gemm_scaled(A, Bp, scale_a, scale_b, C, M: int, N: int, K: int, stream=None) -> None:

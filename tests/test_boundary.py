@@ -74,6 +74,21 @@ def test_gemm_argument_validation(lib, fn):
     assert f(FAKE, FAKE + 8, FAKE, 8, 8, 32, None) == pig.IGEMM_MISALIGNED
 
 
+@pytest.mark.parametrize("fn", ["i4i4_gemm_host", "w4a8_gemm_host"])
+def test_host_gemm_argument_validation(lib, fn):
+    # the host-buffer entry points reject bad arguments before any CUDA call
+    f = getattr(lib, fn)
+    assert f(FAKE, FAKE, FAKE, -1, 8, 32, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert f(None, None, None, 0, 8, 32, None) == pig.IGEMM_OK
+    assert f(None, None, None, 8, 0, 32, None) == pig.IGEMM_OK
+    assert f(FAKE, FAKE, None, 8, 8, 32, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert f(None, FAKE, FAKE, 8, 8, 32, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert f(FAKE, None, FAKE, 8, 8, 32, None) == pig.IGEMM_INVALID_ARGUMENT
+    for k in (2, 16, 48):
+        assert f(FAKE, FAKE, FAKE, 8, 8, k, None) == pig.IGEMM_UNSUPPORTED_SHAPE
+    assert f(FAKE, FAKE, FAKE, 8, 8, 65536 + 32, None) == pig.IGEMM_OVERFLOW_BOUND
+
+
 def test_pack_argument_validation(lib):
     assert lib.pack_int4(FAKE, FAKE, -1, 8, None) == pig.IGEMM_INVALID_ARGUMENT
     assert lib.pack_int4(FAKE, FAKE, 4, -2, None) == pig.IGEMM_INVALID_ARGUMENT

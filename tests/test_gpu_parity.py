@@ -302,6 +302,56 @@ def test_fp8_integer_codes_are_exact(orc, M, N, K):
     assert np.array_equal(C, want)
 
 
+# ---------------------------------------------------------------- host-buffer entry points
+
+def host_buf(x, pinned: bool):
+    t = x if isinstance(x, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(x))
+    return t.pin_memory() if pinned else t.clone()
+
+
+# one chunk (skinny, small), two chunks, four chunks with a short last one, eight chunks
+HOST_SHAPES = [("w4a8", 16, 1024, 1024), ("i4i4", 300, 136, 256), ("i4i4", 2048, 300, 256),
+               ("w4a8", 3000, 640, 192), ("i4i4", 4100, 520, 128), ("w4a8", 9000, 264, 64)]
+
+
+@pytest.mark.parametrize("variant,M,N,K", HOST_SHAPES)
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_host_entry_points_match_oracle(orc, variant, M, N, K, pinned):
+    a = (si.int4_values if variant == "i4i4" else si.int8_values)(21000 + M, (M, K))
+    b = si.int4_values(22000 + N, (N, K))
+    bp = host_buf(gpu_pack(b).cpu(), pinned)
+    a_in = host_buf(gpu_pack(a).cpu() if variant == "i4i4" else a, pinned)
+    C = host_buf(np.full((M, N), 0x5A5A5A5A, dtype=np.int32), pinned)
+    (pig.i4i4_gemm_host if variant == "i4i4" else pig.w4a8_gemm_host)(a_in, bp, C, M, N, K)
+    torch.cuda.current_stream().synchronize()
+    assert pig.igemm_last_status() == 0
+    bpo = orc.pack_int4(b)
+    want = orc.i4i4_gemm(orc.pack_int4(a), bpo, K) if variant == "i4i4" else orc.w4a8_gemm(a, bpo, K)
+    assert np.array_equal(C.numpy(), want)
+
+
+def test_host_entry_points_on_a_side_stream_and_edge_cases(orc):
+    M, N, K = 2100, 200, 96
+    a = si.int4_values(23001, (M, K))
+    b = si.int4_values(23002, (N, K))
+    ap, bp = host_buf(gpu_pack(a).cpu(), True), host_buf(gpu_pack(b).cpu(), True)
+    C = host_buf(np.zeros((M, N), dtype=np.int32), True)
+    side = torch.cuda.Stream()
+    pig.i4i4_gemm_host(ap, bp, C, M, N, K, side)
+    side.synchronize()
+    assert np.array_equal(C.numpy(), orc.i4i4_gemm(orc.pack_int4(a), orc.pack_int4(b), K))
+    # K == 0 zeroes C; empty shapes leave it alone
+    C2 = host_buf(np.full((5, 7), 9, dtype=np.int32), True)
+    pig.w4a8_gemm_host(None, None, C2, 0, 7, 64)
+    pig.i4i4_gemm_host(None, None, C2, 5, 0, 64)
+    torch.cuda.current_stream().synchronize()
+    assert bool((C2 == 9).all())
+    pig.w4a8_gemm_host(None, None, C2, 5, 7, 0)
+    torch.cuda.current_stream().synchronize()
+    assert bool((C2 == 0).all())
+    assert pig.igemm_last_status() == 0
+
+
 # ---------------------------------------------------------------- E5M2 operands (the page's other fp8 dtype)
 
 @pytest.mark.parametrize("M,N,K", FP8_SHAPES)
