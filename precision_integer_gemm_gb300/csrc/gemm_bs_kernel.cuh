@@ -68,8 +68,12 @@ struct BsCfg {
     static constexpr int kARows = 128 / CL;   // A rows each CTA of a cluster loads (multicast)
     static constexpr int kStage = kTileA + kTileB;
     static constexpr int kScaleStage = (128 + BN) * 4;  // sa[128] then sb[BN]
-    static constexpr int kIssuers = ST % 4 == 0 ? 4 : ST;  // operand-stage lanes
-    // scale-stage lanes (the next ones; four measured 10 % slower than one)
+    // operand-stage lanes of the producer warp (lane l issues the stages s with
+    // s % kIssuers == l): one; five measured 7 % slower, their waits on
+    // different barriers holding each other up
+    static constexpr int kIssuers = 1;
+    // scale-stage lanes, the next lanes of the producer warp (four measured 10 %
+    // slower than one; a warp of their own, no faster)
     static constexpr int kScaleIssuers = 1;
     static_assert(SS % kScaleIssuers == 0, "each scale lane owns fixed stages");
     static constexpr int kWarpProd = kEpiWarps, kWarpMma = kEpiWarps + 1;
@@ -288,7 +292,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             }
             mma_commit(mma_drain);
         }
-    } else {
+    } else if (warp < Cfg::kEpiWarps) {
         // ------------------------------------------------------------ epilogue
         constexpr int CW = Cfg::CW;
         const int quad = warp & 3, part = warp >> 2;

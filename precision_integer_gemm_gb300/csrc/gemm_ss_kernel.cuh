@@ -30,9 +30,7 @@
 //   warps 0-3   epilogue: TMEM -> registers -> int32 -> shared staging ->
 //               bulk tensor store (reduce-add for split K) into C
 //   warp 4      TMEM allocation + MMA issue (one thread)
-//   warp 5      TMA producer (several lanes, each owning every kIssuers-th
-//               stage: one thread completes only about one stage per
-//               microsecond)
+//   warp 5      TMA producer (one lane)
 // Every wait is bounded (ptx.cuh wait_bounded).
 #pragma once
 #include <cstdint>
@@ -57,7 +55,10 @@ struct SsCfg {
     static constexpr int kQBoxRows = W4A8 ? QA : QA / CL;
     static constexpr int kBK = 128;                    // k per stage
     static constexpr int kPRows = 128;                 // MMA M
-    static constexpr int kIssuers = ST % 4 == 0 ? 4 : ST % 3 == 0 ? 3 : ST % 2 == 0 ? 2 : 1;
+    // producer lanes, lane l issuing the stages s with s % kIssuers == l: one lane
+    // (two or four lanes of one warp measured 4-13 % slower per call: their
+    // waits on different barriers hold each other up)
+    static constexpr int kIssuers = 1;
     static constexpr int kAccCols = kQRows;
     static constexpr int kAccBufs = 2 * kAccCols <= 512 ? 2 : 1;
     static constexpr int kTmemCols = kAccBufs * kAccCols <= 128 ? 128 : kAccBufs * kAccCols <= 256 ? 256 : 512;
