@@ -131,6 +131,24 @@ __device__ __forceinline__ void bs_wait_drain(uint64_t *bar, uint32_t parity, un
     }
 }
 
+// t0, t1 += (v0 * b0, v1 * b1) * sa as one pair (mul.rn.f32x2, then
+// fma.rn.f32x2): per element the same two roundings as fmaf(v * b, sa, t), in
+// half the instructions (the promotion is issue-bound; measured 857 -> 760 us
+// at 8192^3, bit-identical)
+__device__ __forceinline__ void fma2_scaled(float &t0, float &t1, float v0, float v1, float b0, float b1, float sa)
+{
+    asm("{\n\t.reg .b64 vv, bb, pp, ss, tt;\n\t"
+        "mov.b64 vv, {%2, %3};\n\t"
+        "mov.b64 bb, {%4, %5};\n\t"
+        "mul.rn.f32x2 pp, vv, bb;\n\t"
+        "mov.b64 ss, {%6, %6};\n\t"
+        "mov.b64 tt, {%0, %1};\n\t"
+        "fma.rn.f32x2 tt, pp, ss, tt;\n\t"
+        "mov.b64 {%0, %1}, tt;\n\t}"
+        : "+f"(t0), "+f"(t1)
+        : "f"(v0), "f"(v1), "f"(b0), "f"(b1), "f"(sa));
+}
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::kThreads, 1)
     igemm_bs_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
@@ -325,10 +343,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 for (int j4 = 0; j4 < 8; ++j4) {
                     const float4 b = sb4[j4];
                     float *t = tot + c + 4 * j4;
-                    t[0] = fmaf(__uint_as_float(v[4 * j4 + 0]) * b.x, sa, t[0]);
-                    t[1] = fmaf(__uint_as_float(v[4 * j4 + 1]) * b.y, sa, t[1]);
-                    t[2] = fmaf(__uint_as_float(v[4 * j4 + 2]) * b.z, sa, t[2]);
-                    t[3] = fmaf(__uint_as_float(v[4 * j4 + 3]) * b.w, sa, t[3]);
+                    fma2_scaled(t[0], t[1], __uint_as_float(v[4 * j4 + 0]), __uint_as_float(v[4 * j4 + 1]), b.x, b.y,
+                                sa);
+                    fma2_scaled(t[2], t[3], __uint_as_float(v[4 * j4 + 2]), __uint_as_float(v[4 * j4 + 3]), b.z, b.w,
+                                sa);
                 }
             }
             fence_proxy_async_smem();  // generic reads before the bulk copy refills the stage
