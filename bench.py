@@ -225,7 +225,8 @@ def run_reference(args, variant, M, N, K, a, b, rank, world):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64" if variant in FP8_VARIANTS else "int64",
         "data": "synthetic (SplitMix64-seeded, uniform)",
         "config": {"workload": args.workload, "variant": variant, "M": M, "N": N, "K": K},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
