@@ -376,6 +376,19 @@ def test_pin(orc, pin):
     assert pin(orc)
 
 
+def test_numpy_matmul_at_1024(orc):
+    # the library special case at the size of the 1024^3 workload (and a ragged
+    # W4A8 shape): numpy's int64 matmul of the values the oracle's own unpacking
+    # returns, against the oracle's GEMMs, element for element
+    a4 = si.int4_values(si.workload_seed(2, 0), (1024, 1024))
+    b4 = si.int4_values(si.workload_seed(2, 1), (1024, 1024))
+    ap, bp = orc.pack_int4(a4), orc.pack_int4(b4)
+    assert np.array_equal(orc.i4i4_gemm(ap, bp, 1024), a4.astype(np.int64) @ b4.astype(np.int64).T)
+    a8 = si.int8_values(77, (300, 544))
+    b = si.int4_values(78, (520, 544))
+    assert np.array_equal(orc.w4a8_gemm(a8, orc.pack_int4(b), 544), a8.astype(np.int64) @ b.astype(np.int64).T)
+
+
 def test_pack_shape_pin(orc):
     # tutorial low_precision_gemm.py main(): a (1024, 1024) logical tensor packs to (1024, 512)
     logical = si.int4_values(5, (1024, 1024))
