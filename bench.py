@@ -59,15 +59,20 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+# CUDA sources without device code (the host-buffer entry points: copies and
+# calls of the device entry points), left out of the digest below
+HOST_ONLY_SOURCES = ("host.cu",)
+
+
 def sources_digest():
-    """SHA-256 over the CUDA sources (csrc/*.cu, *.cuh, by name): the DRAM
-    traffic recorded in profiles/traffic.json is used only for this exact
-    kernel code."""
+    """SHA-256 over the CUDA sources that hold device code or launch planning
+    (csrc/*.cu, *.cuh by name, HOST_ONLY_SOURCES left out): the DRAM traffic
+    recorded in profiles/traffic.json is used only for this exact kernel code."""
     import hashlib
     d = os.path.join(ROOT, "precision_integer_gemm_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh")):
+        if name.endswith((".cu", ".cuh")) and name not in HOST_ONLY_SOURCES:
             h.update(name.encode())
             with open(os.path.join(d, name), "rb") as f:
                 h.update(f.read())
