@@ -226,6 +226,24 @@ IGEMM_API int fp8_blockscaled_gemm_e5m2(const uint8_t *A, const uint8_t *B, cons
                                         float *C, int M, int N, int K, cudaStream_t stream);
 
 /*
+ * Host-buffer twins of the four fp8 entry points above: A, B, C (and SFA, SFB)
+ * in HOST memory, moved and computed in row chunks exactly as i4i4_gemm_host
+ * does (B and SFB copied whole, A and the matching rows of SFA per chunk).
+ * Arguments and rules as for the device entry points, except that host
+ * pointers need no alignment; C is complete once `stream` has reached the end
+ * of the call.  A chunk's GEMM may plan its split of K differently from a
+ * whole-matrix call, so the last bits of a float32 C can differ from the device
+ * entry point's where that call would split K.
+ */
+IGEMM_API int fp8_gemm_host(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, cudaStream_t stream);
+IGEMM_API int fp8_gemm_e5m2_host(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K,
+                                 cudaStream_t stream);
+IGEMM_API int fp8_blockscaled_gemm_host(const uint8_t *A, const uint8_t *B, const float *SFA, const float *SFB,
+                                        float *C, int M, int N, int K, cudaStream_t stream);
+IGEMM_API int fp8_blockscaled_gemm_e5m2_host(const uint8_t *A, const uint8_t *B, const float *SFA, const float *SFB,
+                                             float *C, int M, int N, int K, cudaStream_t stream);
+
+/*
  * Pack logical int4 values two per byte (TileLang tutorial page
  * low_precision_gemm.py, pack_int4): packed[r, j] = (logical[r, 2j] & 0xF) |
  * ((logical[r, 2j+1] & 0xF) << 4).  Values outside [-8, 7] are masked to four

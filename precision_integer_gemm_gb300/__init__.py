@@ -19,7 +19,8 @@ from .build import LIB_PATH, build as build_library
 
 __all__ = [
     "IgemmError", "load", "i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "i4i4_gemm_host", "w4a8_gemm_host", "w4a8_gemm_scaled", "fp8_gemm", "pack_int4",
-    "fp8_blockscaled_gemm", "fp8_gemm_e5m2", "fp8_blockscaled_gemm_e5m2", "unpack_int4",
+    "fp8_blockscaled_gemm", "fp8_gemm_e5m2", "fp8_blockscaled_gemm_e5m2", "fp8_gemm_host", "fp8_gemm_e5m2_host",
+    "fp8_blockscaled_gemm_host", "fp8_blockscaled_gemm_e5m2_host", "unpack_int4",
     "igemm_strerror",
     "igemm_last_status", "igemm_watchdog_selftest", "igemm_kernels_launched", "igemm_time_next_gemm",
     "igemm_skinny_plan",
@@ -27,7 +28,8 @@ __all__ = [
 ]
 
 EXPORTED_SYMBOLS = ("i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "i4i4_gemm_host", "w4a8_gemm_host", "w4a8_gemm_scaled", "fp8_gemm",
-                    "fp8_gemm_e5m2", "fp8_blockscaled_gemm", "fp8_blockscaled_gemm_e5m2", "pack_int4", "unpack_int4", "igemm_strerror", "igemm_last_status",
+                    "fp8_gemm_e5m2", "fp8_blockscaled_gemm", "fp8_blockscaled_gemm_e5m2", "fp8_gemm_host",
+                    "fp8_gemm_e5m2_host", "fp8_blockscaled_gemm_host", "fp8_blockscaled_gemm_e5m2_host", "pack_int4", "unpack_int4", "igemm_strerror", "igemm_last_status",
                     "igemm_watchdog_selftest", "igemm_kernels_launched",
                     "igemm_time_next_gemm", "igemm_skinny_plan")
 
@@ -72,10 +74,11 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.i4i4_gemm_noalloc.restype = i
     lib.w4a8_gemm_scaled.argtypes = [p, p, p, p, p, i, i, i, p]
     lib.w4a8_gemm_scaled.restype = i
-    for name in ("fp8_gemm", "fp8_gemm_e5m2"):
+    for name in ("fp8_gemm", "fp8_gemm_e5m2", "fp8_gemm_host", "fp8_gemm_e5m2_host"):
         getattr(lib, name).argtypes = [p, p, p, i, i, i, p]
         getattr(lib, name).restype = i
-    for name in ("fp8_blockscaled_gemm", "fp8_blockscaled_gemm_e5m2"):
+    for name in ("fp8_blockscaled_gemm", "fp8_blockscaled_gemm_e5m2", "fp8_blockscaled_gemm_host",
+                 "fp8_blockscaled_gemm_e5m2_host"):
         getattr(lib, name).argtypes = [p, p, p, p, p, i, i, i, p]
         getattr(lib, name).restype = i
     lib.w4a8_gemm.argtypes = [p, p, p, i, i, i, p]
@@ -181,6 +184,28 @@ def fp8_blockscaled_gemm_e5m2(A, B, SFA, SFB, C, M: int, N: int, K: int, stream=
     """fp8_blockscaled_gemm for E5M2 byte matrices A [M,K] and B [N,K]."""
     _check(load().fp8_blockscaled_gemm_e5m2(_ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(C), M, N, K,
                                             _stream(stream)), "fp8_blockscaled_gemm_e5m2")
+
+
+def fp8_gemm_host(A, B, C, M: int, N: int, K: int, stream=None) -> None:
+    """fp8_gemm with A, B and C in host memory (CPU tensors, pinned for overlap)."""
+    _check(load().fp8_gemm_host(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(stream)), "fp8_gemm_host")
+
+
+def fp8_gemm_e5m2_host(A, B, C, M: int, N: int, K: int, stream=None) -> None:
+    """fp8_gemm_e5m2 with A, B and C in host memory (CPU tensors, pinned for overlap)."""
+    _check(load().fp8_gemm_e5m2_host(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(stream)), "fp8_gemm_e5m2_host")
+
+
+def fp8_blockscaled_gemm_host(A, B, SFA, SFB, C, M: int, N: int, K: int, stream=None) -> None:
+    """fp8_blockscaled_gemm with A, B, SFA, SFB and C in host memory."""
+    _check(load().fp8_blockscaled_gemm_host(_ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(C), M, N, K,
+                                            _stream(stream)), "fp8_blockscaled_gemm_host")
+
+
+def fp8_blockscaled_gemm_e5m2_host(A, B, SFA, SFB, C, M: int, N: int, K: int, stream=None) -> None:
+    """fp8_blockscaled_gemm_e5m2 with A, B, SFA, SFB and C in host memory."""
+    _check(load().fp8_blockscaled_gemm_e5m2_host(_ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(C), M, N, K,
+                                                 _stream(stream)), "fp8_blockscaled_gemm_e5m2_host")
 
 
 def pack_int4(logical, packed, rows: int, K: int, stream=None) -> None:

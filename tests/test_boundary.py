@@ -89,6 +89,26 @@ def test_host_gemm_argument_validation(lib, fn):
     assert f(FAKE, FAKE, FAKE, 8, 8, 65536 + 32, None) == pig.IGEMM_OVERFLOW_BOUND
 
 
+@pytest.mark.parametrize("fn", ["fp8_gemm_host", "fp8_gemm_e5m2_host"])
+def test_fp8_host_argument_validation(lib, fn):
+    f = getattr(lib, fn)
+    assert f(FAKE, FAKE, FAKE, -1, 8, 16, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert f(None, None, None, 0, 8, 16, None) == pig.IGEMM_OK
+    assert f(FAKE, FAKE, None, 8, 8, 16, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert f(None, FAKE, FAKE, 8, 8, 16, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert f(FAKE, FAKE, FAKE, 8, 8, 24, None) == pig.IGEMM_UNSUPPORTED_SHAPE
+
+
+@pytest.mark.parametrize("fn", ["fp8_blockscaled_gemm_host", "fp8_blockscaled_gemm_e5m2_host"])
+def test_fp8_blockscaled_host_argument_validation(lib, fn):
+    f = getattr(lib, fn)
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 4, 16, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert f(None, None, None, None, None, 4, 0, 16, None) == pig.IGEMM_OK
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 24, None) == pig.IGEMM_UNSUPPORTED_SHAPE
+    assert f(FAKE, FAKE, None, FAKE, FAKE, 4, 4, 16, None) == pig.IGEMM_INVALID_ARGUMENT
+    assert f(FAKE, FAKE, FAKE, None, FAKE, 4, 4, 16, None) == pig.IGEMM_INVALID_ARGUMENT
+
+
 def test_pack_argument_validation(lib):
     assert lib.pack_int4(FAKE, FAKE, -1, 8, None) == pig.IGEMM_INVALID_ARGUMENT
     assert lib.pack_int4(FAKE, FAKE, 4, -2, None) == pig.IGEMM_INVALID_ARGUMENT

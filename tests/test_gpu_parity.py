@@ -352,6 +352,40 @@ def test_host_entry_points_on_a_side_stream_and_edge_cases(orc):
     assert pig.igemm_last_status() == 0
 
 
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("M,N,K", [(300, 136, 96), (2100, 264, 160), (4100, 130, 64)])
+def test_fp8_host_entry_points_match_oracle(orc, fmt, M, N, K):
+    gen = si.e4m3_bytes if fmt == "e4m3" else si.e5m2_bytes
+    A, B = gen(24000 + M, (M, K)), gen(25000 + N, (N, K))
+    C = host_buf(np.full((M, N), np.nan, dtype=np.float32), True)
+    f = pig.fp8_gemm_host if fmt == "e4m3" else pig.fp8_gemm_e5m2_host
+    f(host_buf(A, True), host_buf(B, True), C, M, N, K)
+    torch.cuda.current_stream().synchronize()
+    assert pig.igemm_last_status() == 0
+    want, mag = orc.fp8_gemm(A, B, K, fmt=fmt)
+    got = C.numpy().astype(np.float64)
+    assert np.all(np.abs(got - want) <= K * 2.0 ** -23 * mag + 1e-30)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("M,N,K", [(200, 130, 304), (2200, 200, 272)])
+def test_fp8_blockscaled_host_entry_points_match_oracle(orc, fmt, M, N, K):
+    gen = si.e4m3_bytes if fmt == "e4m3" else si.e5m2_bytes
+    A, B = gen(26000 + M, (M, K)), gen(27000 + N, (N, K))
+    sfa = si.scale_values(28000 + M, (M, -(-K // 128)))
+    sfb = si.scale_values(29000 + N, (N, -(-K // 128)))
+    C = host_buf(np.full((M, N), np.nan, dtype=np.float32), False)
+    f = pig.fp8_blockscaled_gemm_host if fmt == "e4m3" else pig.fp8_blockscaled_gemm_e5m2_host
+    f(host_buf(A, False), host_buf(B, False), host_buf(sfa, False), host_buf(sfb, False), C, M, N, K)
+    torch.cuda.current_stream().synchronize()
+    assert pig.igemm_last_status() == 0
+    want, wabs = orc.fp8_blockscaled(A, B, sfa, sfb, K, fmt=fmt)
+    got = C.numpy().astype(np.float64)
+    assert np.all(np.abs(got - want) <= max(K, 16) * 2.0 ** -23 * wabs + 1e-30)
+    # the block-scaled result does not depend on how the rows are chunked: equal to the device call
+    assert np.array_equal(got, run_fp8bs(A, B, sfa, sfb, fmt))
+
+
 # ---------------------------------------------------------------- E5M2 operands (the page's other fp8 dtype)
 
 @pytest.mark.parametrize("M,N,K", FP8_SHAPES)
