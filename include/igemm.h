@@ -5,7 +5,8 @@
  * return an igemm_status synchronously: argument errors are reported before
  * anything is enqueued, and nothing is launched when the return value is not
  * IGEMM_OK.  Every pointer argument is caller-owned device memory (global
- * memory of the current device).  Device-side problems (a pipeline wait that
+ * memory of the current device), except the array arguments of the *_host
+ * entry points, which are caller-owned host memory.  Device-side problems (a pipeline wait that
  * exceeded the watchdog limit) are reported later by igemm_last_status().
  *
  * Workspace.  Large GEMMs (M * N >= 2^22 and, for int4 x int4, M, N >= 512;
@@ -142,7 +143,10 @@ IGEMM_API int w4a8_gemm(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, i
  *   C       [M, N] int32 (host), written
  * Rules as for i4i4_gemm / w4a8_gemm (K % 32 == 0, K <= 65536, empty shapes
  * are no-ops, K == 0 zeroes C), except that host pointers need no alignment.
- * igemm_time_next_gemm times the GEMM kernel of the first chunk only.
+ * igemm_time_next_gemm times the GEMM kernel of the first chunk only.  A CUDA
+ * error after the first chunk was enqueued (IGEMM_CUDA_ERROR) leaves the earlier
+ * chunks' work in the streams; the call still joins its copy streams to
+ * `stream` before it returns.
  */
 IGEMM_API int i4i4_gemm_host(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K,
                              cudaStream_t stream);
