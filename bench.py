@@ -432,6 +432,11 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
         threads = os.cpu_count() or 1
         rows = calibrate_rows(orc, variant, a, b, K, threads, args.cpu_seconds)
         t = oracle_sample_time(orc, variant, a, b, K, rows, threads)
+        if t < args.cpu_seconds / 2 and rows < M:
+            # the small calibration sample overstates the per-row cost: size once more
+            # from this run so that the reported sample is about --cpu-seconds long
+            rows = min(M, max(rows + 1, int(rows * args.cpu_seconds / max(t, 1e-3))))
+            t = oracle_sample_time(orc, variant, a, b, K, rows, threads)
         line["cpu_baseline"] = {"value": 2.0 * rows * N * K / t / 1e12, "unit": UNIT, "cores": threads,
                                 "kind": "oracle",
                                 "sample": f"rows 0..{rows - 1} of A against all {N} rows of B, K={K}; {t:.1f} s"}
