@@ -311,7 +311,8 @@ def host_buf(x, pinned: bool):
 
 # one chunk (skinny, small), two chunks, four chunks with a short last one, eight chunks
 HOST_SHAPES = [("w4a8", 16, 1024, 1024), ("i4i4", 300, 136, 256), ("i4i4", 2048, 300, 256),
-               ("w4a8", 3000, 640, 192), ("i4i4", 4100, 520, 128), ("w4a8", 9000, 264, 64)]
+               ("w4a8", 3000, 640, 192), ("i4i4", 4100, 520, 128), ("w4a8", 9000, 264, 64),
+               ("i4i4", 2100, 262, 64), ("w4a8", 2300, 1030, 96)]  # N % 4 != 0: C rows not 16-byte multiples
 
 
 @pytest.mark.parametrize("variant,M,N,K", HOST_SHAPES)
