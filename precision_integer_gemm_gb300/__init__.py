@@ -105,12 +105,31 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     return lib
 
 
-def _ptr(x) -> int | None:
-    if x is None:
-        return None
-    if isinstance(x, int):
+def _arg(x, nbytes: int, on_device: bool, what: str) -> int | None:
+    """Address of an array argument after the checks a raw pointer cannot get:
+    a tensor must live where the entry point reads it (CUDA memory, or host
+    memory for the *_host entry points), be contiguous and hold at least
+    `nbytes` bytes.  None and raw integer addresses pass through unchecked."""
+    if x is None or isinstance(x, int):
         return x
+    if bool(x.is_cuda) != on_device:
+        raise ValueError(f"{what} must be a {'CUDA' if on_device else 'host (CPU)'} tensor")
+    if not x.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    have = x.numel() * x.element_size()
+    if have < nbytes:
+        raise ValueError(f"{what} holds {have} bytes; the call needs {nbytes}")
     return x.data_ptr()
+
+
+def _n(*dims: int) -> int:
+    """Product of sizes, 0 if any is negative (the library rejects those itself)."""
+    out = 1
+    for d in dims:
+        if d < 0:
+            return 0
+        out *= d
+    return out
 
 
 def _stream(stream) -> int | None:
@@ -127,9 +146,16 @@ def _check(code: int, where: str) -> None:
         raise IgemmError(code, where)
 
 
+def _int_gemm_args(A, Bp, C, M, N, K, a_bytes, on_device, where):
+    return (_arg(A, a_bytes, on_device, f"{where}: A"),
+            _arg(Bp, _n(N, K) // 2, on_device, f"{where}: Bp"),
+            _arg(C, 4 * _n(M, N), on_device, f"{where}: C"))
+
+
 def i4i4_gemm(Ap, Bp, C, M: int, N: int, K: int, stream=None) -> None:
     """C[M,N] (int32) = A . B^T for packed int4 Ap [M,K/2] and Bp [N,K/2]."""
-    _check(load().i4i4_gemm(_ptr(Ap), _ptr(Bp), _ptr(C), M, N, K, _stream(stream)), "i4i4_gemm")
+    a, b, c = _int_gemm_args(Ap, Bp, C, M, N, K, _n(M, K) // 2, True, "i4i4_gemm")
+    _check(load().i4i4_gemm(a, b, c, M, N, K, _stream(stream)), "i4i4_gemm")
 
 
 def i4i4_gemm_noalloc(Ap, Bp, C, M: int, N: int, K: int, stream=None) -> None:
@@ -137,85 +163,114 @@ def i4i4_gemm_noalloc(Ap, Bp, C, M: int, N: int, K: int, stream=None) -> None:
     instead of allocated memory (for callers that cannot allocate during a
     call); larger problems raise with IGEMM_WORKSPACE_LIMIT.  Calls that
     overlap on the GPU share that workspace and race."""
-    _check(load().i4i4_gemm_noalloc(_ptr(Ap), _ptr(Bp), _ptr(C), M, N, K, _stream(stream)), "i4i4_gemm_noalloc")
+    a, b, c = _int_gemm_args(Ap, Bp, C, M, N, K, _n(M, K) // 2, True, "i4i4_gemm_noalloc")
+    _check(load().i4i4_gemm_noalloc(a, b, c, M, N, K, _stream(stream)), "i4i4_gemm_noalloc")
 
 
 def w4a8_gemm(A, Bp, C, M: int, N: int, K: int, stream=None) -> None:
     """C[M,N] (int32) = A . B^T for int8 A [M,K] and packed int4 Bp [N,K/2]."""
-    _check(load().w4a8_gemm(_ptr(A), _ptr(Bp), _ptr(C), M, N, K, _stream(stream)), "w4a8_gemm")
+    a, b, c = _int_gemm_args(A, Bp, C, M, N, K, _n(M, K), True, "w4a8_gemm")
+    _check(load().w4a8_gemm(a, b, c, M, N, K, _stream(stream)), "w4a8_gemm")
 
 
 def i4i4_gemm_host(Ap, Bp, C, M: int, N: int, K: int, stream=None) -> None:
     """i4i4_gemm with Ap, Bp and C in host memory (CPU tensors, pinned for overlap);
     C is complete once `stream` has reached the end of the call."""
-    _check(load().i4i4_gemm_host(_ptr(Ap), _ptr(Bp), _ptr(C), M, N, K, _stream(stream)), "i4i4_gemm_host")
+    a, b, c = _int_gemm_args(Ap, Bp, C, M, N, K, _n(M, K) // 2, False, "i4i4_gemm_host")
+    _check(load().i4i4_gemm_host(a, b, c, M, N, K, _stream(stream)), "i4i4_gemm_host")
 
 
 def w4a8_gemm_host(A, Bp, C, M: int, N: int, K: int, stream=None) -> None:
     """w4a8_gemm with A, Bp and C in host memory (CPU tensors, pinned for overlap);
     C is complete once `stream` has reached the end of the call."""
-    _check(load().w4a8_gemm_host(_ptr(A), _ptr(Bp), _ptr(C), M, N, K, _stream(stream)), "w4a8_gemm_host")
+    a, b, c = _int_gemm_args(A, Bp, C, M, N, K, _n(M, K), False, "w4a8_gemm_host")
+    _check(load().w4a8_gemm_host(a, b, c, M, N, K, _stream(stream)), "w4a8_gemm_host")
 
 
 def w4a8_gemm_scaled(A, Bp, scale_a, scale_b, C, M: int, N: int, K: int, stream=None) -> None:
     """C[M,N] (bfloat16) = per-channel dequantised W4A8 product: bf16(float(A . B^T) * scale_a[m] * scale_b[n])."""
-    _check(load().w4a8_gemm_scaled(_ptr(A), _ptr(Bp), _ptr(scale_a), _ptr(scale_b), _ptr(C), M, N, K,
-                                   _stream(stream)), "w4a8_gemm_scaled")
+    w = "w4a8_gemm_scaled"
+    a, b, _ = _int_gemm_args(A, Bp, None, M, N, K, _n(M, K), True, w)
+    _check(load().w4a8_gemm_scaled(a, b, _arg(scale_a, 4 * _n(M), True, f"{w}: scale_a"),
+                                   _arg(scale_b, 4 * _n(N), True, f"{w}: scale_b"),
+                                   _arg(C, 2 * _n(M, N), True, f"{w}: C"), M, N, K, _stream(stream)), w)
+
+
+def _fp8_args(A, B, C, M, N, K, on_device, where):
+    return (_arg(A, _n(M, K), on_device, f"{where}: A"), _arg(B, _n(N, K), on_device, f"{where}: B"),
+            _arg(C, 4 * _n(M, N), on_device, f"{where}: C"))
+
+
+def _fp8bs_args(A, B, SFA, SFB, C, M, N, K, on_device, where):
+    kb = -(-K // 128) if K > 0 else 0
+    return (_arg(A, _n(M, K), on_device, f"{where}: A"), _arg(B, _n(N, K), on_device, f"{where}: B"),
+            _arg(SFA, 4 * _n(M, kb), on_device, f"{where}: SFA"), _arg(SFB, 4 * _n(N, kb), on_device, f"{where}: SFB"),
+            _arg(C, 4 * _n(M, N), on_device, f"{where}: C"))
 
 
 def fp8_gemm(A, B, C, M: int, N: int, K: int, stream=None) -> None:
     """C[M,N] (float32) = A . B^T for E4M3 byte matrices A [M,K] and B [N,K]."""
-    _check(load().fp8_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(stream)), "fp8_gemm")
+    _check(load().fp8_gemm(*_fp8_args(A, B, C, M, N, K, True, "fp8_gemm"), M, N, K, _stream(stream)), "fp8_gemm")
 
 
 def fp8_gemm_e5m2(A, B, C, M: int, N: int, K: int, stream=None) -> None:
     """C[M,N] (float32) = A . B^T for E5M2 byte matrices A [M,K] and B [N,K]."""
-    _check(load().fp8_gemm_e5m2(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(stream)), "fp8_gemm_e5m2")
+    _check(load().fp8_gemm_e5m2(*_fp8_args(A, B, C, M, N, K, True, "fp8_gemm_e5m2"), M, N, K, _stream(stream)),
+           "fp8_gemm_e5m2")
 
 
 def fp8_blockscaled_gemm(A, B, SFA, SFB, C, M: int, N: int, K: int, stream=None) -> None:
     """C[M,N] (float32) = sum over 128-k blocks kb of SFA[m,kb] * SFB[n,kb] * (A . B^T over the block),
     for E4M3 byte matrices A [M,K], B [N,K] and float32 scales SFA [M,ceil(K/128)], SFB [N,ceil(K/128)]."""
-    _check(load().fp8_blockscaled_gemm(_ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(C), M, N, K, _stream(stream)),
-           "fp8_blockscaled_gemm")
+    _check(load().fp8_blockscaled_gemm(*_fp8bs_args(A, B, SFA, SFB, C, M, N, K, True, "fp8_blockscaled_gemm"), M, N,
+                                       K, _stream(stream)), "fp8_blockscaled_gemm")
 
 
 def fp8_blockscaled_gemm_e5m2(A, B, SFA, SFB, C, M: int, N: int, K: int, stream=None) -> None:
     """fp8_blockscaled_gemm for E5M2 byte matrices A [M,K] and B [N,K]."""
-    _check(load().fp8_blockscaled_gemm_e5m2(_ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(C), M, N, K,
-                                            _stream(stream)), "fp8_blockscaled_gemm_e5m2")
+    _check(load().fp8_blockscaled_gemm_e5m2(*_fp8bs_args(A, B, SFA, SFB, C, M, N, K, True,
+                                                          "fp8_blockscaled_gemm_e5m2"), M, N, K, _stream(stream)),
+           "fp8_blockscaled_gemm_e5m2")
 
 
 def fp8_gemm_host(A, B, C, M: int, N: int, K: int, stream=None) -> None:
     """fp8_gemm with A, B and C in host memory (CPU tensors, pinned for overlap)."""
-    _check(load().fp8_gemm_host(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(stream)), "fp8_gemm_host")
+    _check(load().fp8_gemm_host(*_fp8_args(A, B, C, M, N, K, False, "fp8_gemm_host"), M, N, K, _stream(stream)),
+           "fp8_gemm_host")
 
 
 def fp8_gemm_e5m2_host(A, B, C, M: int, N: int, K: int, stream=None) -> None:
     """fp8_gemm_e5m2 with A, B and C in host memory (CPU tensors, pinned for overlap)."""
-    _check(load().fp8_gemm_e5m2_host(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(stream)), "fp8_gemm_e5m2_host")
+    _check(load().fp8_gemm_e5m2_host(*_fp8_args(A, B, C, M, N, K, False, "fp8_gemm_e5m2_host"), M, N, K,
+                                     _stream(stream)), "fp8_gemm_e5m2_host")
 
 
 def fp8_blockscaled_gemm_host(A, B, SFA, SFB, C, M: int, N: int, K: int, stream=None) -> None:
     """fp8_blockscaled_gemm with A, B, SFA, SFB and C in host memory."""
-    _check(load().fp8_blockscaled_gemm_host(_ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(C), M, N, K,
-                                            _stream(stream)), "fp8_blockscaled_gemm_host")
+    _check(load().fp8_blockscaled_gemm_host(*_fp8bs_args(A, B, SFA, SFB, C, M, N, K, False,
+                                                          "fp8_blockscaled_gemm_host"), M, N, K, _stream(stream)),
+           "fp8_blockscaled_gemm_host")
 
 
 def fp8_blockscaled_gemm_e5m2_host(A, B, SFA, SFB, C, M: int, N: int, K: int, stream=None) -> None:
     """fp8_blockscaled_gemm_e5m2 with A, B, SFA, SFB and C in host memory."""
-    _check(load().fp8_blockscaled_gemm_e5m2_host(_ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(C), M, N, K,
+    _check(load().fp8_blockscaled_gemm_e5m2_host(*_fp8bs_args(A, B, SFA, SFB, C, M, N, K, False,
+                                                               "fp8_blockscaled_gemm_e5m2_host"), M, N, K,
                                                  _stream(stream)), "fp8_blockscaled_gemm_e5m2_host")
 
 
 def pack_int4(logical, packed, rows: int, K: int, stream=None) -> None:
     """packed [rows,K/2] = two int4 values per byte of logical [rows,K] (low nibble = even k)."""
-    _check(load().pack_int4(_ptr(logical), _ptr(packed), rows, K, _stream(stream)), "pack_int4")
+    _check(load().pack_int4(_arg(logical, _n(rows, K), True, "pack_int4: logical"),
+                            _arg(packed, _n(rows, K) // 2, True, "pack_int4: packed"), rows, K, _stream(stream)),
+           "pack_int4")
 
 
 def unpack_int4(packed, logical, rows: int, K: int, stream=None) -> None:
     """logical [rows,K] int8 = the sign-extended nibbles of packed [rows,K/2] (low nibble = even k)."""
-    _check(load().unpack_int4(_ptr(packed), _ptr(logical), rows, K, _stream(stream)), "unpack_int4")
+    _check(load().unpack_int4(_arg(packed, _n(rows, K) // 2, True, "unpack_int4: packed"),
+                              _arg(logical, _n(rows, K), True, "unpack_int4: logical"), rows, K, _stream(stream)),
+           "unpack_int4")
 
 
 def igemm_strerror(code: int) -> str:

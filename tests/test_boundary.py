@@ -143,6 +143,29 @@ def test_watchdog_selftest_argument_validation(lib):
     assert lib.igemm_watchdog_selftest(2_000_000, None) == pig.IGEMM_INVALID_ARGUMENT
 
 
+def test_python_binding_checks_tensor_arguments(lib):
+    # tensors are checked before the library is called: placement, contiguity, size
+    torch = pytest.importorskip("torch")
+    M, N, K = 8, 8, 64
+    a = torch.zeros((M, K // 2), dtype=torch.uint8)
+    b = torch.zeros((N, K // 2), dtype=torch.uint8)
+    c = torch.zeros((M, N), dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        pig.i4i4_gemm(a, b, c, M, N, K, stream=0)  # host tensors to a device entry point
+    with pytest.raises(ValueError, match="CUDA"):
+        pig.fp8_gemm(a, b, c, M, N, K, stream=0)
+    with pytest.raises(ValueError, match="bytes"):
+        pig.i4i4_gemm_host(a[: M // 2], b, c, M, N, K, stream=0)  # too few rows of A
+    with pytest.raises(ValueError, match="bytes"):
+        pig.w4a8_gemm_host(a, b, c, M, N, K, stream=0)  # int8 A needs K bytes per row
+    with pytest.raises(ValueError, match="contiguous"):
+        pig.i4i4_gemm_host(a, b, torch.zeros((N, M), dtype=torch.int32).t(), M, N, K, stream=0)
+    with pytest.raises(ValueError, match="bytes"):
+        pig.fp8_blockscaled_gemm_host(torch.zeros((M, K), dtype=torch.uint8), torch.zeros((N, K), dtype=torch.uint8),
+                                      torch.zeros((M, 0), dtype=torch.float32), torch.zeros((N, 1)), c.float(), M, N,
+                                      K, stream=0)
+
+
 def test_python_binding_raises_with_status(lib):
     with pytest.raises(pig.IgemmError) as e:
         pig.i4i4_gemm(FAKE, FAKE, FAKE, 8, 8, 40, stream=0)
