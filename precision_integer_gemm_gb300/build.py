@@ -58,6 +58,17 @@ def build(force: bool = False, ptxas_verbose: bool = False, quiet: bool = True) 
     if not force and up_to_date() and not ptxas_verbose:
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
+    import fcntl
+    # one builder at a time (the ranks of one job, parallel test workers): the
+    # others wait here and find the library up to date
+    with open(os.path.join(BUILD_DIR, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and up_to_date() and not ptxas_verbose:
+            return LIB_PATH
+        return _build_locked(ptxas_verbose, quiet)
+
+
+def _build_locked(ptxas_verbose: bool, quiet: bool) -> str:
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         results = list(ex.map(lambda s: _compile(s, ptxas_verbose), SOURCES))
     logs = "".join(log for _, log in results)
