@@ -8,13 +8,18 @@ every step reads its own copy of the operands, rotating over copies worth
 three L2 capacities; --l2 flush instead writes 256 MB before every step
 (outside the timed events).  Prints one JSON line.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
-                  [--l2 rotate|flush]
+  python bench.py [--gpus 1] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                  [--l2 rotate|flush] [--seconds S]
 
 --impl reference times the CPU oracle (plain C, int64 accumulation) on the
 host cores, each step a bounded row sample of the same workload.
-Under torchrun every rank runs an independent replica (the GEMM is not
-sharded: "replicas only"); value = all ranks' ops / the slowest rank's time.
+--seconds S adds a sustained leg: steps back to back for about S seconds
+under one pair of events, with the SM clock sampled meanwhile.
+
+One GPU only.  The library is a single-GPU library (the GEMM is not sharded;
+its cluster kernels share operand tiles between the CTAs of one GPU), so the
+benchmark refuses --gpus other than 1 and any launch with WORLD_SIZE above 1
+(a torchrun job), with a one-line message and exit status 2.
 """
 
 from __future__ import annotations
@@ -163,20 +168,6 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def max_over_ranks(seconds: float, dist, device: str) -> float:
-    """The slowest rank's time: every rank's value reduced with MAX (NCCL on
-    the GPU machine, gloo in the CPU tests)."""
-    import torch
-    t = torch.tensor([seconds], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def whole_job_value(ops_per_step: float, steps: int, world: int, slowest_s: float) -> float:
-    """TOPS of the whole job: every replica's ops over the slowest rank's time."""
-    return ops_per_step * steps * world / slowest_s / 1e12
-
-
 # variants whose operands are fp8 bytes and whose C is float32
 FP8_VARIANTS = ("fp8", "fp8e5m2", "fp8bs")
 
@@ -212,10 +203,8 @@ def calibrate_rows(orc, variant, a, b, K, threads, target_s):
     return rows
 
 
-def run_reference(args, variant, M, N, K, a, b, rank, world):
+def run_reference(args, variant, M, N, K, a, b):
     import oracle
-    if rank != 0:
-        return
     orc = oracle.Oracle()
     threads = os.cpu_count() or 1
     step_target = max(0.5, min(4.0, 150.0 / max(1, args.steps + args.warmup)))
@@ -228,7 +217,7 @@ def run_reference(args, variant, M, N, K, a, b, rank, world):
     value = ops * args.steps / total / 1e12
     sample = f"rows 0..{rows - 1} of A against all {N} rows of B, K={K} (each step)"
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64" if variant in FP8_VARIANTS else "int64",
@@ -240,13 +229,12 @@ def run_reference(args, variant, M, N, K, a, b, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
+def run_ours(args, variant, M, N, K, a, b):
     import torch
     import precision_integer_gemm_gb300 as pig
 
     pig.build_library()
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
+    torch.cuda.set_device(0)
     stream = torch.cuda.current_stream()
 
     # operands resident in HBM: logical -> packed by the library's pack kernel
@@ -315,9 +303,7 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
     for ev in k_starts + k_ends:
         ev.record(stream)
     torch.cuda.synchronize()
-    sampler = ClockSampler(local)
-    if dist is not None:
-        dist.barrier()
+    sampler = ClockSampler(0)
     torch.cuda.synchronize()
     sampler.start()
     launched0 = pig.igemm_kernels_launched()
@@ -329,8 +315,6 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
         ends[i].record(stream)
     torch.cuda.synchronize()
     launched = pig.igemm_kernels_launched() - launched0  # this library's kernels in the timed region
-    if dist is not None:
-        dist.barrier()
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
     if pig.igemm_last_status(stream) != 0:
@@ -347,11 +331,41 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
         step()
     torch.cuda.synchronize()
     gemm_kernel_s = sum(s.elapsed_time(e) for s, e in zip(k_starts, k_ends)) / 1e3 / args.steps
-    if dist is not None:
-        total_s = max_over_ranks(total_s, dist, "cuda")
 
     ops = 2.0 * M * N * K
-    value = whole_job_value(ops, args.steps, world, total_s)
+    value = ops * args.steps / total_s / 1e12
+    peaks, peak_src = load_peaks()
+
+    # sustained leg (opt-in): steps back to back for about --seconds, one pair
+    # of events around all of them, SM clocks sampled meanwhile
+    sustained = None
+    if args.seconds > 0:
+        n_sus = max(args.steps, int(args.seconds / max(total_s / args.steps, 1e-6)))
+        sus_s, sus_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sus_sampler = ClockSampler(0)
+        torch.cuda.synchronize()
+        sus_sampler.start()
+        sus_s.record(stream)
+        for _ in range(n_sus):
+            before_step()
+            step()
+        sus_e.record(stream)
+        torch.cuda.synchronize()
+        sus_clocks = sus_sampler.stop()
+        if pig.igemm_last_status(stream) != 0:
+            raise RuntimeError("device status after the sustained leg is not ok")
+        sus_total = sus_s.elapsed_time(sus_e) / 1e3
+        sus_ms = 1e3 * sus_total / n_sus
+        sustained = {"value": ops * n_sus / sus_total / 1e12, "unit": UNIT, "steps": n_sus,
+                     "seconds": sus_total, "ms_per_step": sus_ms, "clocks": sus_clocks,
+                     "kcycles_per_step": (sus_ms * sus_clocks["sm_mhz"]) if sus_clocks.get("sm_mhz") else None,
+                     "burst_kcycles_per_step": (1e3 * total_s / args.steps * clocks["sm_mhz"])
+                     if clocks.get("sm_mhz") else None}
+        if not args.workload.startswith("w4a8_decode") and peaks.get("bf16_tflops_sustained"):
+            sus_peak = E4M3_PER_BF16 * peaks["bf16_tflops_sustained"]
+            sustained.update({"peak": sus_peak, "frac": sustained["value"] / sus_peak,
+                              "peak_source": f"{peak_src} bf16 sustained x {E4M3_PER_BF16}; the step "
+                                             f"(preparation pass included) against it"})
 
     # end to end through the public API with pinned host buffers
     e2e_steps = max(1, min(args.steps, 5))
@@ -379,11 +393,10 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
     e_e.record(stream)
     torch.cuda.synchronize()
     e2e_s = e_s.elapsed_time(e_e) / 1e3
-    e2e_value = ops * e2e_steps * world / e2e_s / 1e12  # replicas run concurrently
+    e2e_value = ops * e2e_steps / e2e_s / 1e12
     if not torch.equal(c_host, C.cpu()):
         raise RuntimeError("end-to-end result differs from the device-resident result")
 
-    peaks, peak_src = load_peaks()
     nbytes = workload_bytes(variant, M, N, K)
     traffic = recorded_traffic(args.workload)
     if args.workload.startswith("w4a8_decode"):
@@ -403,7 +416,7 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
                 "mma_macs_per_op": 2 if variant == "w4a8" else 1}
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": {"i4i4": "int4", "w4a8": "int8xint4", "fp8": "e4m3 (float32 accumulate)",
@@ -415,7 +428,7 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
                           f"3x L2 or more): each step's operands were evicted from L2 before it; no flush"
                           if args.l2 == "rotate" else
                           "flushed before every step (256 MB write, outside the timed events)"),
-                   "parallelism": "replicas" if world > 1 else "single"},
+                   "parallelism": "single"},
         "wall_ms_per_step": 1e3 * wall / args.steps,
         "gpu_launches": launched,
         "clocks": clocks,
@@ -426,7 +439,9 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
                 "call": f"{host_call} (host buffers, copies inside the call)"},
         "roofline": roof,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if sustained is not None:
+        line["sustained"] = sustained
+    if not args.no_cpu_baseline:
         import oracle
         orc = oracle.Oracle()
         threads = os.cpu_count() or 1
@@ -440,8 +455,20 @@ def run_ours(args, variant, M, N, K, a, b, rank, world, dist):
         line["cpu_baseline"] = {"value": 2.0 * rows * N * K / t / 1e12, "unit": UNIT, "cores": threads,
                                 "kind": "oracle",
                                 "sample": f"rows 0..{rows - 1} of A against all {N} rows of B, K={K}; {t:.1f} s"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    print(json.dumps(line), flush=True)
+
+
+def refuse_multi_gpu(gpus: int) -> str | None:
+    """The one-line reason this run is refused, or None for a one-GPU run."""
+    world = os.environ.get("WORLD_SIZE", "1")
+    try:
+        world_n = int(world)
+    except ValueError:
+        world_n = 2
+    if gpus != 1 or world_n > 1:
+        return (f"bench.py runs on one GPU only (got --gpus {gpus}, WORLD_SIZE={world}): the library is a "
+                f"single-GPU library, its cluster kernels share tiles between CTAs of one GPU")
+    return None
 
 
 def main():
@@ -455,33 +482,25 @@ def main():
     p.add_argument("--l2", choices=["rotate", "flush"], default="rotate",
                    help="keep operands out of L2 between steps by rotating copies, or by a 256 MB write")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--seconds", type=float, default=0.0,
+                   help="add a sustained leg of about this many seconds (0: none)")
     args = p.parse_args()
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
+    why = refuse_multi_gpu(args.gpus)
+    if why:
+        print(why, file=sys.stderr, flush=True)
+        sys.exit(2)
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
     variant, M, N, K, a, b = si.workload_operands(args.workload)
     if variant == "fp8bs":
         global _SCALES
         _SCALES = si.block_scales(M, N, K, si.WORKLOADS[args.workload][4])
 
     if args.impl == "reference":
-        run_reference(args, variant, M, N, K, a, b, rank, world)
+        run_reference(args, variant, M, N, K, a, b)
         return
-
-    dist = None
-    if world > 1:
-        import torch
-        import torch.distributed as tdist
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-        tdist.init_process_group("nccl")
-        dist = tdist
-    try:
-        run_ours(args, variant, M, N, K, a, b, rank, world, dist)
-    finally:
-        if dist is not None:
-            dist.destroy_process_group()
+    run_ours(args, variant, M, N, K, a, b)
 
 
 if __name__ == "__main__":

@@ -101,9 +101,12 @@ IGEMM_API int i4i4_gemm(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M,
  * problems return IGEMM_WORKSPACE_LIMIT before anything is enqueued.  The
  * call makes no cudaMalloc, cudaFree or pool allocation.
  *
- * The first call on each device looks up the device address of the array
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  All calls share the one array and each call
+ * The first call on each device does the set-up: it looks up the device
+ * address of the array (cudaGetSymbolAddress, with that device current), and
+ * with CUDA's lazy module loading (the default) it may be the call that loads
+ * the library's device code, which is when the 32 MiB array is mapped.  So
+ * make one call per device during set-up, before any stream capture; from the
+ * second call on nothing is reserved.  All calls share the one array and each call
  * rewrites what it reads, so results never depend on an earlier call; but
  * calls whose work overlaps on the GPU (on different streams, or from
  * different threads without ordering) race on the array and give wrong

@@ -65,7 +65,7 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     for name in ("oracle_i4i4_entries", "oracle_w4a8_entries"):
         fn = getattr(lib, name)
         fn.argtypes = [p, p, i64, p, p, i64, p]
-        fn.restype = None
+        fn.restype = ctypes.c_int
     return lib
 
 
@@ -147,7 +147,9 @@ class Oracle:
         ms = np.ascontiguousarray(ms, dtype=np.int64)
         ns = np.ascontiguousarray(ns, dtype=np.int64)
         out = np.empty(ms.shape[0], dtype=np.int64)
-        self.lib.oracle_i4i4_entries(_ptr(Ap), _ptr(Bp), K, _ptr(ms), _ptr(ns), ms.shape[0], _ptr(out))
+        rc = self.lib.oracle_i4i4_entries(_ptr(Ap), _ptr(Bp), K, _ptr(ms), _ptr(ns), ms.shape[0], _ptr(out))
+        if rc:
+            raise RuntimeError(f"oracle_i4i4_entries failed ({rc})")
         return out
 
     def w4a8_entries(self, A, Bp, K: int, ms, ns) -> np.ndarray:
@@ -156,7 +158,9 @@ class Oracle:
         ms = np.ascontiguousarray(ms, dtype=np.int64)
         ns = np.ascontiguousarray(ns, dtype=np.int64)
         out = np.empty(ms.shape[0], dtype=np.int64)
-        self.lib.oracle_w4a8_entries(_ptr(A), _ptr(Bp), K, _ptr(ms), _ptr(ns), ms.shape[0], _ptr(out))
+        rc = self.lib.oracle_w4a8_entries(_ptr(A), _ptr(Bp), K, _ptr(ms), _ptr(ns), ms.shape[0], _ptr(out))
+        if rc:
+            raise RuntimeError(f"oracle_w4a8_entries failed ({rc})")
         return out
 
     def e4m3_value(self, codes: np.ndarray) -> np.ndarray:

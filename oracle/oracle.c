@@ -176,32 +176,42 @@ int oracle_w4a8_gemm(const int8_t *A, const uint8_t *Bp, int32_t *C, int64_t M, 
 }
 
 /* Single elements, for sampled checks at sizes too large for the full loop.
- * `ms`, `ns` list `count` (m, n) pairs; out[i] receives C[ms[i], ns[i]]. */
-void oracle_i4i4_entries(const uint8_t *Ap, const uint8_t *Bp, int64_t K, const int64_t *ms,
-                         const int64_t *ns, int64_t count, int64_t *out)
+ * `ms`, `ns` list `count` (m, n) pairs; out[i] receives C[ms[i], ns[i]].
+ * Returns 0, 4 if an entry exceeds the no-overflow bound K*amax*bmax (as
+ * gemm_logical does), or -1 on an allocation error. */
+int oracle_i4i4_entries(const uint8_t *Ap, const uint8_t *Bp, int64_t K, const int64_t *ms,
+                        const int64_t *ns, int64_t count, int64_t *out)
 {
-    int8_t *a = (int8_t *)malloc((size_t)K);
-    int8_t *b = (int8_t *)malloc((size_t)K);
-    if (!a || !b) { free(a); free(b); return; }
+    int8_t *a = (int8_t *)malloc((size_t)(K > 0 ? K : 1));
+    int8_t *b = (int8_t *)malloc((size_t)(K > 0 ? K : 1));
+    if (!a || !b) { free(a); free(b); return -1; }
+    const int64_t bound = K * 8 * 8;
+    int rc = 0;
     for (int64_t i = 0; i < count; ++i) {
         oracle_unpack_int4(Ap + ms[i] * (K / 2), a, 1, K);
         oracle_unpack_int4(Bp + ns[i] * (K / 2), b, 1, K);
         out[i] = dot_i64(a, b, K);
+        if (out[i] > bound || out[i] < -bound) rc = 4;
     }
     free(a);
     free(b);
+    return rc;
 }
 
-void oracle_w4a8_entries(const int8_t *A, const uint8_t *Bp, int64_t K, const int64_t *ms,
-                         const int64_t *ns, int64_t count, int64_t *out)
+int oracle_w4a8_entries(const int8_t *A, const uint8_t *Bp, int64_t K, const int64_t *ms,
+                        const int64_t *ns, int64_t count, int64_t *out)
 {
-    int8_t *b = (int8_t *)malloc((size_t)K);
-    if (!b) return;
+    int8_t *b = (int8_t *)malloc((size_t)(K > 0 ? K : 1));
+    if (!b) return -1;
+    const int64_t bound = K * 128 * 8;
+    int rc = 0;
     for (int64_t i = 0; i < count; ++i) {
         oracle_unpack_int4(Bp + ns[i] * (K / 2), b, 1, K);
         out[i] = dot_i64(A + ms[i] * K, b, K);
+        if (out[i] > bound || out[i] < -bound) rc = 4;
     }
     free(b);
+    return rc;
 }
 
 /* ---------------------------------------------------------------- fp8 GEMM

@@ -2,6 +2,7 @@
 // validation, tensor maps, the device status word, pack_int4 and the
 // watchdog self-test.  The GEMM kernels live in gemm_kernel.cuh.
 #include <atomic>
+#include <mutex>
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cstdlib>
@@ -30,9 +31,11 @@ GemmEvents take_gemm_events()
 
 int *device_status_word()
 {
+    static std::mutex mu;
     static int *cache[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);  // first calls from several host threads
     if (!cache[dev]) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
@@ -54,9 +57,11 @@ unsigned long long watchdog_limit_ns()
 
 int sm_count()
 {
+    static std::mutex mu;
     static int cache[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    std::lock_guard<std::mutex> lock(mu);
     if (!cache[dev]) {
         int n = 0;
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;

@@ -3,6 +3,7 @@
 // for B to whole cluster slots, with zeros) in a pool workspace;
 // igemm_bs_kernel (gemm_bs_kernel.cuh) launches early behind it and reads the
 // scales only after it.
+#include <mutex>
 #include "launch.cuh"
 #include "gemm_bs_kernel.cuh"
 
@@ -41,12 +42,16 @@ static int launch_bs_cfg(const uint8_t *A, const uint8_t *B, const float *SFA, c
     auto kernel = igemm_bs_kernel<Cfg>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return kCudaError;
-    static bool attr_set[64] = {};
-    if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) !=
-            cudaSuccess)
-            return kCudaError;
-        attr_set[dev] = true;
+    {
+        static std::mutex mu;  // one per kernel instantiation; first calls from several threads
+        static bool attr_set[64] = {};
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && !attr_set[dev]) {
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) !=
+                cudaSuccess)
+                return kCudaError;
+            attr_set[dev] = true;
+        }
     }
     const int KB = (K + 127) / 128;
     const int m_tiles = (M + 127) / 128;
@@ -54,7 +59,9 @@ static int launch_bs_cfg(const uint8_t *A, const uint8_t *B, const float *SFA, c
     const int m_pad = m_tiles * 128, n_pad = n_slots * Cfg::CL * Cfg::BN;
     int clusters = sm_count() / Cfg::CL;
     if constexpr (Cfg::CL > 1) {
+        static std::mutex cmu;
         static int cache[64] = {};
+        std::lock_guard<std::mutex> clock(cmu);
         if (dev < 64 && !cache[dev]) {
             cudaLaunchConfig_t qc = {};
             cudaLaunchAttribute qa[1];

@@ -1,6 +1,7 @@
 // Host-side launch plumbing shared by the GEMM translation units.
 #pragma once
 #include <algorithm>
+#include <mutex>
 #include <type_traits>
 #include <cstdint>
 #include <cuda.h>
@@ -63,12 +64,16 @@ int launch_gemm(const CUtensorMap &mapA, const CUtensorMap &mapB, const CUtensor
     auto kernel = igemm_tc_kernel<Cfg>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return kCudaError;
-    static bool attr_set[64] = {};
-    if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) !=
-            cudaSuccess)
-            return kCudaError;
-        attr_set[dev] = true;
+    {
+        static std::mutex mu;  // one per kernel instantiation; first calls from several threads
+        static bool attr_set[64] = {};
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && !attr_set[dev]) {
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) !=
+                cudaSuccess)
+                return kCudaError;
+            attr_set[dev] = true;
+        }
     }
     GemmParams prm{};
     prm.C = C;
@@ -122,9 +127,11 @@ int ss_resident_ctas(Kernel k)
     if constexpr (Cfg::CL == 1) {
         return sm_count();
     } else {
+        static std::mutex mu;
         static int cache[64] = {};
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+        std::lock_guard<std::mutex> lock(mu);
         if (!cache[dev]) {
             cudaLaunchConfig_t cfg = {};
             cudaLaunchAttribute attr[1];
@@ -153,12 +160,16 @@ int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMa
     auto kernel = igemm_ss_kernel<Cfg>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return kCudaError;
-    static bool attr_set[64] = {};
-    if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) !=
-            cudaSuccess)
-            return kCudaError;
-        attr_set[dev] = true;
+    {
+        static std::mutex mu;  // one per kernel instantiation; first calls from several threads
+        static bool attr_set[64] = {};
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && !attr_set[dev]) {
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) !=
+                cudaSuccess)
+                return kCudaError;
+            attr_set[dev] = true;
+        }
     }
     const int resident = ss_resident_ctas<Cfg>(kernel);
     if (resident < Cfg::CL) return kCudaError;
@@ -248,9 +259,11 @@ SkinnyPlan plan_skinny(int n_tiles, int K, int max_slice_k, const SkinnyClusterO
 template <class Cfg>
 int skinny_max_clusters()
 {
+    static std::mutex mu;
     static int cache[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
     if (!cache[dev]) {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
@@ -276,7 +289,9 @@ int skinny_set_smem()
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return kCudaError;
+    static std::mutex mu;  // one per kernel instantiation; first calls from several threads
     static bool attr_set[64] = {};
+    std::lock_guard<std::mutex> lock(mu);
     if (dev < 64 && !attr_set[dev]) {
         if (cudaFuncSetAttribute(igemm_skinny_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg::kSmemBytes) != cudaSuccess)

@@ -44,6 +44,34 @@ def _read_tiny():
     return (np.array(A, dtype=np.int8), np.array(B, dtype=np.int8), np.array(C, dtype=np.int64))
 
 
+def _read_scaled():
+    """The hand-worked cases of golden/w4a8_scaled_bf16.txt: a list of
+    (C int64 [M,N], scale_a float32 [M], scale_b float32 [N], want uint16 [M,N])."""
+    cases, mat = [], {}
+
+    def rows(text, conv):
+        return [[conv(v) for v in r.split()] for r in text.split("/")]
+
+    with open(os.path.join(GOLDEN, "w4a8_scaled_bf16.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            tag, rest = line.split(None, 1)
+            if tag == "matrix":
+                key, text = rest.split(None, 1)
+                mat[key] = text
+            else:
+                c, sa, sb, want = rest.split()
+                cases.append((np.array([[int(c)]], np.int64), np.array([float.fromhex(sa)], np.float32),
+                              np.array([float.fromhex(sb)], np.float32), np.array([[int(want, 16)]], np.uint16)))
+    cases.insert(0, (np.array(rows(mat["C"], int), np.int64),
+                     np.array(rows(mat["scale_a"], float.fromhex)[0], np.float32),
+                     np.array(rows(mat["scale_b"], float.fromhex)[0], np.float32),
+                     np.array(rows(mat["want"], lambda v: int(v, 16)), np.uint16)))
+    return cases
+
+
 def _shift_sign_extend(n4: int) -> int:
     """Sign-extend a 4-bit field by the shift method (place it in the high
     nibble of a byte, read the byte as signed, arithmetic-shift right by 4)."""
@@ -323,6 +351,18 @@ def check_bf16_rounding(o) -> bool:
     return bool(np.array_equal(back.ravel(), ints.astype(np.float32)))
 
 
+def check_scaled_golden(o) -> bool:
+    # the per-channel dequantisation steps on hand-worked cases: which scale goes
+    # by row and which by column (a 2 x 3 product), bfloat16 ties to even, the
+    # float32 conversion of C, and the order of the two scalings (overflow)
+    with np.errstate(over="ignore"):
+        for C, sa, sb, want in _read_scaled():
+            got = o.w4a8_scaled_bf16(C.astype(np.int32), sa, sb)
+            if got.shape != want.shape or not np.array_equal(got, want):
+                return False
+    return True
+
+
 def check_blockscaled_closed_form(o) -> bool:
     # tutorial gemm_blockscaled: scales along K per block of 128.  With every a and b
     # equal to 1.0 (e4m3 byte 0x38) each block's partial sum is its length, so
@@ -363,7 +403,8 @@ def check_blockscaled_unit_scales(o) -> bool:
 PINS = [check_nibbles, check_roundtrip, check_golden_bytes, check_tiny_golden, check_brute_force,
         check_numpy_matmul, check_closed_forms, check_k_permutation, check_entries, check_e4m3_decode,
         check_fp8_gemm, check_fp8_integer_codes, check_bf16_rounding, check_blockscaled_closed_form,
-        check_blockscaled_unit_scales, check_e5m2_decode, check_fp8_gemm_e5m2, check_blockscaled_e5m2]
+        check_blockscaled_unit_scales, check_e5m2_decode, check_fp8_gemm_e5m2, check_blockscaled_e5m2,
+        check_scaled_golden]
 
 
 @pytest.fixture(scope="module")
@@ -446,3 +487,65 @@ def test_planted_mistakes_are_caught(tmp_path, mutant):
         if not ok:
             failed.append(pin.__name__)
     assert failed, f"mutant {mutant} passed every pin"
+
+
+# Plausible mistakes in the per-channel dequantisation (the oracle's numpy
+# steps, not its C code): each must fail a pin.
+class _ScaledMistake(oracle.Oracle):
+    def __init__(self, kind):
+        super().__init__()
+        self.kind = kind
+
+    def w4a8_scaled_bf16(self, C, scale_a, scale_b):
+        sa = np.asarray(scale_a, dtype=np.float32)
+        sb = np.asarray(scale_b, dtype=np.float32)
+        if self.kind == "scales_swapped":      # scale_a by column, scale_b by row
+            v = (C.astype(np.float32) * sb[:, None]) * sa[None, :]
+        elif self.kind == "scales_first":      # C * (scale_a * scale_b)
+            v = C.astype(np.float32) * (sa[:, None] * sb[None, :])
+        elif self.kind == "scale_b_first":     # (C * scale_b) * scale_a
+            v = (C.astype(np.float32) * sb[None, :]) * sa[:, None]
+        elif self.kind == "float64_steps":     # the products in float64, one rounding
+            v = ((C.astype(np.float64) * sa[:, None]) * sb[None, :]).astype(np.float32)
+        elif self.kind == "truncate":          # bfloat16 by truncation
+            v = (C.astype(np.float32) * sa[:, None]) * sb[None, :]
+            return (np.ascontiguousarray(v, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        elif self.kind == "exact_to_bf16":     # C rounded straight to bfloat16 (no float32 step)
+            v64 = (C.astype(np.float64) * sa[:, None]) * sb[None, :]
+            bits = v64.view(np.uint64)
+            # round the float64 to 8 significant bits, ties to even, then take the pattern
+            keep = 52 - 7
+            r = (bits + ((np.uint64(1) << np.uint64(keep - 1)) - np.uint64(1)) +
+                 ((bits >> np.uint64(keep)) & np.uint64(1))) >> np.uint64(keep) << np.uint64(keep)
+            return self.bf16_rne(r.view(np.float64).astype(np.float32))
+        else:
+            raise ValueError(self.kind)
+        return self.bf16_rne(v)
+
+
+@pytest.mark.parametrize("kind", ["scales_swapped", "scales_first", "scale_b_first", "float64_steps", "truncate",
+                                  "exact_to_bf16"])
+def test_scaled_mistakes_are_caught(kind):
+    bad = _ScaledMistake(kind)
+    try:
+        ok = check_scaled_golden(bad)
+    except Exception:
+        ok = False
+    assert not ok, f"{kind} passed the scaled-epilogue pin"
+
+
+def test_bound_check_fires_on_out_of_range_values(tmp_path):
+    # The no-overflow bound |C| <= K * 8 * 8 cannot be exceeded by in-range int4
+    # values, so it is shown to fire with the planted mistake that drops the sign
+    # extension (nibbles read as 0..15): all-0xFF bytes then give 15 * 15 * K.
+    good = oracle.Oracle()
+    K = 64
+    ones = np.full((3, K // 2), 0xFF, dtype=np.uint8)
+    assert np.all(good.i4i4_gemm(ones, ones, K) == K)  # (-1) * (-1) per k
+    bad = oracle.Oracle(oracle.load(oracle.build(str(tmp_path / "liboracle_m2.so"), mutant=2)))
+    with pytest.raises(RuntimeError, match="failed \\(4\\)"):
+        bad.i4i4_gemm(ones, ones, K)
+    with pytest.raises(RuntimeError, match="failed \\(4\\)"):
+        bad.i4i4_entries(ones, ones, K, [0, 2], [1, 0])
+    with pytest.raises(RuntimeError, match="failed \\(4\\)"):
+        bad.w4a8_entries(np.full((2, K), -128, np.int8), ones, K, [0, 1], [2, 2])
