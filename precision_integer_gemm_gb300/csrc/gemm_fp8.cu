@@ -8,8 +8,8 @@
 namespace igemm {
 
 //                         W4A8   BN  stages CL  float out  format
-using CfgFp8 = SsCfg<false, 256, 4, 2, true>;
-using CfgFp8E5m2 = SsCfg<false, 256, 4, 2, true, 1>;
+using CfgFp8 = SsCfg<false, 256, 6, 2, true>;
+using CfgFp8E5m2 = SsCfg<false, 256, 6, 2, true, 1>;
 
 template <class Cfg>
 static int launch_fp8_cfg(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, cudaStream_t stream)

@@ -14,22 +14,34 @@
 // preparation pass.  Codes past K are zero (TMA fill): they add nothing to S,
 // and the row sums and the K term count the real k only.
 //
-// Tiles: the MMA M side ("P") is 128 code rows of the int4 operand (A for
-// int4 x int4; the weights for W4A8, swap-AB); the N side ("Q") is BN code
-// rows: BN rows of B (int4 x int4), or QA = BN/2 activation rows as a block of
-// QA high-part rows followed by QA low-part rows (W4A8).  One pipeline stage
-// is one 128-k block of both, 128-byte swizzled K-major.
+// Tiles: the MMA M side ("P") is code rows of the int4 operand (A for int4 x
+// int4; the weights for W4A8, swap-AB); the N side ("Q") is BN code rows: BN
+// rows of B (int4 x int4), or QA = BN/2 activation rows as a block of QA
+// high-part rows followed by QA low-part rows (W4A8).  One pipeline stage is
+// one 128-k block of both, 128-byte swizzled K-major.
 //
-// Clusters (CL = 2): the two CTAs of a cluster take P tiles 2i and 2i + 1 of
-// the same Q tile and k range.  Each loads its own P tile and one half of the
-// Q tile, multicast into both CTAs' stage, so the Q tile leaves L2 once for
-// two MMAs.  A stage is free again only when both CTAs' MMAs have read it:
-// every MMA commit arrives on the empty barrier of both CTAs.
+// CTA pairs (CL = 2): the two CTAs of a cluster run ONE tcgen05.mma of M = 256
+// (.cta_group::2): CTA r holds P rows 128 r .. 128 r + 127 of the pair's P
+// tile and half of the Q tile (int4 x int4: Q rows 128 r ..; W4A8: the
+// high-code block in CTA 0, the low-code block in CTA 1), each loaded by its
+// own TMA into its own shared memory.  The MMA reads A and B from both CTAs,
+// so a CTA's stage is 16 KB of P + 16 KB of Q: half the Q tile is never
+// duplicated, and six stages fit where four stages of a whole Q tile did.  The
+// even CTA issues the MMAs; its commits arrive on the barriers of both CTAs.
+// Its MMA thread learns that the odd CTA's half of a stage landed from a relay
+// thread there (an arrival on the even CTA's barrier), and the odd CTA's
+// epilogue warps release an accumulator with arrivals on the even CTA's
+// barrier too.  These hand-overs carry no data written by the arriving thread
+// (TMA wrote the stage, the tensor core the accumulator), so they arrive with
+// the default CTA-scope semantics: a cluster-scope release costs a fence that
+// measured about 0.8 us per stage with six stages of copies in flight.  Each CTA's accumulator (TMEM lanes 0-127) holds its own
+// P rows times the whole Q tile.
 //
 // Warp roles (persistent CTAs, one per SM, work units = (tile, k split)):
 //   warps 0-3   epilogue: TMEM -> registers -> int32 -> shared staging ->
 //               bulk tensor store (reduce-add for split K) into C
-//   warp 4      TMEM allocation + MMA issue (one thread)
+//   warp 4      TMEM allocation (both CTAs of a pair), MMA issue (one thread;
+//               the even CTA of a pair), relay (one thread; the odd CTA)
 //   warp 5      TMA producer (one lane)
 // Every wait is bounded (ptx.cuh wait_bounded).
 #pragma once
@@ -49,12 +61,14 @@ struct SsCfg {
     static constexpr int kQRows = BN_;                 // MMA N
     static constexpr int QA = W4A8 ? BN_ / 2 : BN_;    // Q source rows per tile
     static constexpr int ST = ST_;                     // pipeline stages
-    static constexpr int CL = CL_;                     // CTAs per cluster sharing the Q tile
+    static constexpr int CL = CL_;                     // 2: CTA pairs running one M = 256 MMA
     // rows of the Q box one CTA loads: int4 x int4 splits the Q tile by rows;
-    // W4A8 with CL = 2 gives the high-code block to one CTA, the low to the other
+    // W4A8 gives the high-code block to CTA 0, the low to CTA 1 (a single CTA
+    // loads both blocks with two boxes)
     static constexpr int kQBoxRows = W4A8 ? QA : QA / CL;
     static constexpr int kBK = 128;                    // k per stage
-    static constexpr int kPRows = 128;                 // MMA M
+    static constexpr int kPRows = 128;                 // P rows per CTA (MMA M = 128 * CL)
+    static constexpr int kMmaM = kPRows * CL;
     // producer lanes, lane l issuing the stages s with s % kIssuers == l: one lane
     // (two or four lanes of one warp measured 4-13 % slower per call: their
     // waits on different barriers hold each other up)
@@ -63,24 +77,26 @@ struct SsCfg {
     static constexpr int kAccBufs = 2 * kAccCols <= 512 ? 2 : 1;
     static constexpr int kTmemCols = kAccBufs * kAccCols <= 128 ? 128 : kAccBufs * kAccCols <= 256 ? 256 : 512;
     static constexpr int kStageA = kPRows * kBK;
-    static constexpr int kStageB = kQRows * kBK;
+    static constexpr int kStageB = kQRows / CL * kBK;  // this CTA's part of the Q tile
     static constexpr int kStage = kStageA + kStageB;
     static constexpr int kStageRows = W4A8 ? (QA < 32 ? QA : 32) : 32;  // C staging box rows
     static constexpr int kCStage = 32 * 32 * 4;
     static constexpr int kOffStages = 0;
     static constexpr int kOffCStage = kOffStages + ST * kStage;
     static constexpr int kOffBars = kOffCStage + 4 * kCStage;
-    static constexpr int kNumBars = 2 * ST + 4 + 1;
+    static constexpr int kNumBars = 3 * ST + 4 + 1;
     static constexpr int kOffMisc = ((kOffBars + 8 * kNumBars + 127) / 128) * 128;
     static constexpr int kSmemBytes = kOffMisc + 128 + 1024;  // + alignment slack
     static constexpr int kThreads = 6 * 32;
     static_assert(kQRows % 16 == 0 && kQRows <= 256, "MMA N");
+    static_assert(CL == 1 || (kQRows % 32 == 0 && kQRows >= 64), "MMA N of an M = 256 pair MMA");
     static_assert(!W4A8 || QA % 8 == 0, "high and low blocks start on 1024-byte boundaries");
     static_assert(kStageB % 1024 == 0 && kStage % 1024 == 0, "1024-byte aligned stages");
     static_assert(kAccBufs * kAccCols <= 512, "TMEM budget");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
     static_assert(ST <= 32, "stage masks");
     static_assert(CL == 1 || CL == 2, "cluster size");
+    static_assert(!W4A8 || CL == 1 || kQBoxRows * CL == kQRows, "W4A8 pair: one code block per CTA");
     static_assert(!(FLOAT_ && W4A8), "the fp8 GEMM uses the int4 x int4 tile layout");
     static_assert(FMT_ == 0 || (FLOAT_ && FMT_ == 1), "E5M2 only for the fp8 GEMM");
     static_assert(W4A8 || kQBoxRows % 8 == 0, "Q half tiles start on 1024-byte boundaries");
@@ -158,33 +174,37 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     const __grid_constant__ CUtensorMap mapC, const SsParams prm)
 {
     constexpr int ST = Cfg::ST, QA = Cfg::QA;
+    constexpr bool kPair = Cfg::CL == 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t *stages = smem + Cfg::kOffStages;
     uint8_t *cstage = smem + Cfg::kOffCStage;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBars);
-    uint64_t *full = bars;              // [ST] stage landed (1 arrival + tx)
-    uint64_t *empty = full + ST;        // [ST] stage consumed (MMA commit)
+    uint64_t *full = bars;              // [ST] this CTA's part of a stage landed (1 arrival + tx)
+    uint64_t *pfull = full + ST;        // [ST] pair: the odd CTA's part landed (relay, even CTA only)
+    uint64_t *empty = pfull + ST;       // [ST] stage consumed (MMA commit)
     uint64_t *acc_full = empty + ST;    // [2] accumulator complete (commit)
-    uint64_t *acc_empty = acc_full + 2; // [2] accumulator drained (4 epilogue warps)
+    uint64_t *acc_empty = acc_full + 2; // [2] accumulator drained (the epilogue warps of the pair)
     uint64_t *mma_drain = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int rank = Cfg::CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int rank = kPair ? static_cast<int>(cluster_ctarank()) : 0;
+    const bool leader = rank == 0;              // issues the MMAs
     const int cid = blockIdx.x / Cfg::CL;       // cluster index
     const int ncl = gridDim.x / Cfg::CL;        // clusters
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], Cfg::CL);  // one MMA commit per CTA of the cluster
+            mbar_init(&pfull[s], 1);
+            mbar_init(&empty[s], 1);  // the even CTA's MMA commit reaches both CTAs
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 4);
+            mbar_init(&acc_empty[b], 4 * Cfg::CL);  // 4 epilogue warps per CTA of the pair
         }
         mbar_init(mma_drain, 1);
         *abort_flag = 0;
@@ -194,14 +214,20 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         if (prm.tma_store) tma_prefetch_map(&mapC);
     }
     if (warp == 4) {
-        tmem_alloc(tmem_slot, Cfg::kTmemCols);
-        tmem_relinquish();
+        // a pair allocates together: warp 4 of both CTAs, the same slot offset
+        if constexpr (kPair) {
+            tmem_alloc_pair(tmem_slot, Cfg::kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, Cfg::kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     // the peer's barriers are initialised before anything reaches them
-    if constexpr (Cfg::CL > 1) cluster_sync_all();
+    if constexpr (kPair) cluster_sync_all();
     const uint32_t tmem = *tmem_slot;
     const Watchdog wd{abort_flag, prm.status, prm.limit_ns};
 
@@ -232,17 +258,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     const int kx = (x.kb0 + i) * Cfg::kBK;
                     mbar_arrive_expect_tx(&full[s], Cfg::kStage);
                     tma_load_2d_hint(st, &mapP, &full[s], kx, x.p0, keep);
-                    if constexpr (Cfg::CL > 1) {
-                        // this CTA's share of the Q tile, into both CTAs' stage
-                        int qy, qoff;
-                        if constexpr (Cfg::kW4A8) {
-                            qy = rank == 0 ? x.q0 : prm.q_rows + x.q0;
-                            qoff = rank * QA * Cfg::kBK;
-                        } else {
-                            qy = x.q0 + rank * Cfg::kQBoxRows;
-                            qoff = rank * Cfg::kQBoxRows * Cfg::kBK;
-                        }
-                        tma_load_2d_multicast(st + Cfg::kStageA + qoff, &mapQ, &full[s], kx, qy, 0x3);
+                    if constexpr (kPair) {
+                        // this CTA's half of the Q tile, into its own stage
+                        const int qy = Cfg::kW4A8 ? (rank == 0 ? x.q0 : prm.q_rows + x.q0)
+                                                  : x.q0 + rank * Cfg::kQBoxRows;
+                        tma_load_2d(st + Cfg::kStageA, &mapQ, &full[s], kx, qy);
                     } else if constexpr (Cfg::kW4A8) {
                         // high-part rows q0.., low-part rows M + q0.. (the code planes are stacked)
                         tma_load_2d(st + Cfg::kStageA, &mapQ, &full[s], kx, x.q0);
@@ -255,21 +275,20 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 }
             }
             // never leave with copies in flight: the last load of each own stage
+            // ... and no MMA commit still on its way to this CTA's barriers: the
+            // release of each own stage's last load
 #pragma unroll 1
-            for (int s = 0; s < ST; ++s)
-                if ((issued_mask >> s) & 1u) ss_wait_drain(&full[s], (last_phase >> s) & 1u, prm.limit_ns);
-            if constexpr (Cfg::CL > 1) {
-                // ... and no commit of the peer's MMA still on its way to this
-                // CTA's barriers: wait for the release of each own stage's last load
-#pragma unroll 1
-                for (int s = 0; s < ST; ++s)
-                    if ((issued_mask >> s) & 1u) ss_wait_drain(&empty[s], (last_phase >> s) & 1u, prm.limit_ns);
+            for (int s = 0; s < ST; ++s) {
+                if ((issued_mask >> s) & 1u) {
+                    ss_wait_drain(&full[s], (last_phase >> s) & 1u, prm.limit_ns);
+                    ss_wait_drain(&empty[s], (last_phase >> s) & 1u, prm.limit_ns);
+                }
             }
         }
     } else if (warp == 4) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f8_f32(Cfg::kPRows, Cfg::kQRows, Cfg::kFmt);
+        if (leader && lane == 0) {
+            // -------------------------------------------------------- MMA issuer
+            constexpr uint32_t idesc = idesc_f8_f32(Cfg::kMmaM, Cfg::kQRows, Cfg::kFmt);
             uint32_t g = 0, nacc = 0;
             bool ok = true;
             for (int u = cid; ok && u < prm.num_units; u += ncl, ++nacc) {
@@ -281,7 +300,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 tc_fence_after();
                 for (int i = 0; i < x.nkb; ++i, ++g) {
                     const int s = static_cast<int>(g % ST);
-                    if (!wait_bounded(&full[s], (g / ST) & 1u, wd)) {
+                    const uint32_t ph = (g / ST) & 1u;
+                    if (!wait_bounded(&full[s], ph, wd) || (kPair && !wait_bounded(&pfull[s], ph, wd))) {
                         ok = false;
                         break;
                     }
@@ -289,17 +309,48 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     const uint32_t a_base = smem_u32(stages + s * Cfg::kStage);
                     const uint32_t b_base = a_base + Cfg::kStageA;
 #pragma unroll
-                    for (int kk = 0; kk < Cfg::kBK / 32; ++kk)
-                        mma_f8f6f4(d_tmem, sdesc_kmajor_sw128(a_base + 32 * kk), sdesc_kmajor_sw128(b_base + 32 * kk),
-                                   idesc, (i > 0 || kk > 0) ? 1u : 0u);
-                    if constexpr (Cfg::CL > 1)
-                        mma_commit_multicast(&empty[s], 0x3);
+                    for (int kk = 0; kk < Cfg::kBK / 32; ++kk) {
+                        const uint64_t ad = sdesc_kmajor_sw128(a_base + 32 * kk);
+                        const uint64_t bd = sdesc_kmajor_sw128(b_base + 32 * kk);
+                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                        if constexpr (kPair)
+                            mma_f8f6f4_pair(d_tmem, ad, bd, idesc, acc);
+                        else
+                            mma_f8f6f4(d_tmem, ad, bd, idesc, acc);
+                    }
+                    if constexpr (kPair)
+                        mma_commit_pair_multicast(&empty[s], 0x3);
                     else
                         mma_commit(&empty[s]);
                 }
-                if (ok) mma_commit(&acc_full[ab]);
+                if (ok) {
+                    if constexpr (kPair)
+                        mma_commit_pair_multicast(&acc_full[ab], 0x3);
+                    else
+                        mma_commit(&acc_full[ab]);
+                }
             }
-            mma_commit(mma_drain);
+            if constexpr (kPair)
+                mma_commit_pair(mma_drain);
+            else
+                mma_commit(mma_drain);
+        } else if (kPair && !leader && lane == 0) {
+            // -------------------------------------------------------- relay (odd CTA of a pair)
+            // each stage of this CTA that landed, in order, to the even CTA's MMA thread
+            const uint32_t pfull_remote = cluster_map(smem_u32(pfull), 0u);
+            uint32_t g = 0;
+            bool ok = true;
+            for (int u = cid; ok && u < prm.num_units; u += ncl) {
+                const SsUnit x = ss_unit<Cfg>(prm, u, rank);
+                for (int i = 0; i < x.nkb; ++i, ++g) {
+                    const int s = static_cast<int>(g % ST);
+                    if (!wait_bounded(&full[s], (g / ST) & 1u, wd)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_peer(pfull_remote + 8u * static_cast<uint32_t>(s));
+                }
+            }
         }
     } else {
         // ------------------------------------------------------------ epilogue (warps 0-3)
@@ -310,6 +361,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         uint8_t *stg = cstage + quad * Cfg::kCStage;
         const bool reduce = prm.split > 1;
         const uint64_t out_policy = l2_policy_evict_first();  // C is not read again
+        // where this warp releases an accumulator: the even CTA's barrier
+        const uint32_t acc_empty_leader = kPair ? cluster_map(smem_u32(acc_empty), 0u) : 0u;
         uint32_t nacc = 0;
         for (int u = cid; u < prm.num_units; u += ncl, ++nacc) {
             const SsUnit x = ss_unit<Cfg>(prm, u, rank);
@@ -445,7 +498,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[ab]);
+            if (lane == 0) {
+                if (leader)
+                    mbar_arrive(&acc_empty[ab]);
+                else
+                    mbar_arrive_peer(acc_empty_leader + 8u * ab);
+            }
         }
         if (lane == 0) bulk_wait_group_all();
     }
@@ -454,14 +512,18 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 4) {
-        if (lane == 0) ss_wait_drain(mma_drain, 0, prm.limit_ns);  // every MMA of this CTA is done
+        // every MMA is done (of a pair: the even CTA's, which wrote both TMEMs)
+        if (leader && lane == 0) ss_wait_drain(mma_drain, 0, prm.limit_ns);
         __syncwarp();
     }
-    // neither CTA of a cluster leaves while the other may still reach it
-    if constexpr (Cfg::CL > 1) cluster_sync_all();
+    // neither CTA of a pair frees TMEM or leaves while the other may still reach it
+    if constexpr (kPair) cluster_sync_all();
     if (warp == 4) {
         tc_fence_after();
-        tmem_dealloc(tmem, Cfg::kTmemCols);
+        if constexpr (kPair)
+            tmem_dealloc_pair(tmem, Cfg::kTmemCols);
+        else
+            tmem_dealloc(tmem, Cfg::kTmemCols);
     }
 }
 
