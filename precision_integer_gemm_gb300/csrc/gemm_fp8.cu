@@ -7,9 +7,9 @@
 
 namespace igemm {
 
-//                         W4A8   BN  stages CL  float out  format
-using CfgFp8 = SsCfg<false, 256, 6, 2, true>;
-using CfgFp8E5m2 = SsCfg<false, 256, 6, 2, true, 1>;
+//                         W4A8   BN  stages CL  float out  format  k blocks per stage
+using CfgFp8 = SsCfg<false, 256, 3, 2, true, 0, 2>;
+using CfgFp8E5m2 = SsCfg<false, 256, 3, 2, true, 1, 2>;
 
 template <class Cfg>
 static int launch_fp8_cfg(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, cudaStream_t stream)

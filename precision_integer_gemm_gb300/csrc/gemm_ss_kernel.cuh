@@ -18,7 +18,7 @@
 // int4; the weights for W4A8, swap-AB); the N side ("Q") is BN code rows: BN
 // rows of B (int4 x int4), or QA = BN/2 activation rows as a block of QA
 // high-part rows followed by QA low-part rows (W4A8).  One pipeline stage is
-// one 128-k block of both, 128-byte swizzled K-major.
+// one or two 128-k blocks of both, 128-byte swizzled K-major.
 //
 // CTA pairs (CL = 2): the two CTAs of a cluster run ONE tcgen05.mma of M = 256
 // (.cta_group::2): CTA r holds P rows 128 r .. 128 r + 127 of the pair's P
@@ -51,7 +51,7 @@
 
 namespace igemm {
 
-template <bool W4A8, int BN_, int ST_, int CL_ = 1, bool FLOAT_ = false, int FMT_ = 0>
+template <bool W4A8, int BN_, int ST_, int CL_ = 1, bool FLOAT_ = false, int FMT_ = 0, int KB_ = 1>
 struct SsCfg {
     static constexpr bool kW4A8 = W4A8;
     // kFloat: plain fp8 operands (the fp8 GEMM), C = the float32 accumulator;
@@ -66,7 +66,11 @@ struct SsCfg {
     // W4A8 gives the high-code block to CTA 0, the low to CTA 1 (a single CTA
     // loads both blocks with two boxes)
     static constexpr int kQBoxRows = W4A8 ? QA : QA / CL;
-    static constexpr int kBK = 128;                    // k per stage
+    static constexpr int kBK = 128;                    // k per k block (one TMA box of 128 bytes per row)
+    // k blocks per pipeline stage: each stage costs the MMA thread two barrier
+    // waits, a fence and a commit while the tensor pipe drains; two blocks (8
+    // MMAs) per stage halve that per MMA
+    static constexpr int kKB = KB_;
     static constexpr int kPRows = 128;                 // P rows per CTA (MMA M = 128 * CL)
     static constexpr int kMmaM = kPRows * CL;
     // producer lanes, lane l issuing the stages s with s % kIssuers == l: one lane
@@ -76,8 +80,10 @@ struct SsCfg {
     static constexpr int kAccCols = kQRows;
     static constexpr int kAccBufs = 2 * kAccCols <= 512 ? 2 : 1;
     static constexpr int kTmemCols = kAccBufs * kAccCols <= 128 ? 128 : kAccBufs * kAccCols <= 256 ? 256 : 512;
-    static constexpr int kStageA = kPRows * kBK;
-    static constexpr int kStageB = kQRows / CL * kBK;  // this CTA's part of the Q tile
+    static constexpr int kBoxA = kPRows * kBK;         // one k block of P
+    static constexpr int kBoxB = kQRows / CL * kBK;    // one k block of this CTA's part of the Q tile
+    static constexpr int kStageA = kKB * kBoxA;
+    static constexpr int kStageB = kKB * kBoxB;
     static constexpr int kStage = kStageA + kStageB;
     static constexpr int kStageRows = W4A8 ? (QA < 32 ? QA : 32) : 32;  // C staging box rows
     static constexpr int kCStage = 32 * 32 * 4;
@@ -91,7 +97,8 @@ struct SsCfg {
     static_assert(kQRows % 16 == 0 && kQRows <= 256, "MMA N");
     static_assert(CL == 1 || (kQRows % 32 == 0 && kQRows >= 64), "MMA N of an M = 256 pair MMA");
     static_assert(!W4A8 || QA % 8 == 0, "high and low blocks start on 1024-byte boundaries");
-    static_assert(kStageB % 1024 == 0 && kStage % 1024 == 0, "1024-byte aligned stages");
+    static_assert(kBoxB % 1024 == 0 && kStage % 1024 == 0, "1024-byte aligned stages");
+    static_assert(kKB == 1 || kKB == 2, "k blocks per stage");
     static_assert(kAccBufs * kAccCols <= 512, "TMEM budget");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
     static_assert(ST <= 32, "stage masks");
@@ -246,7 +253,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             bool ok = true;
             for (int u = cid; ok && u < prm.num_units; u += ncl) {
                 const SsUnit x = ss_unit<Cfg>(prm, u, rank);
-                for (int i = 0; i < x.nkb; ++i, ++g) {
+                const int nst = (x.nkb + Cfg::kKB - 1) / Cfg::kKB;
+                for (int j = 0; j < nst; ++j, ++g) {
                     const int s = static_cast<int>(g % ST);
                     if (s % Cfg::kIssuers != lane) continue;
                     const uint32_t ph = (g / ST) & 1u;
@@ -255,20 +263,27 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                         break;
                     }
                     uint8_t *st = stages + s * Cfg::kStage;
-                    const int kx = (x.kb0 + i) * Cfg::kBK;
+                    // every box of the stage is loaded (a last stage with one k block of
+                    // the unit loads the next block too, unused: zeros past K)
                     mbar_arrive_expect_tx(&full[s], Cfg::kStage);
-                    tma_load_2d_hint(st, &mapP, &full[s], kx, x.p0, keep);
-                    if constexpr (kPair) {
-                        // this CTA's half of the Q tile, into its own stage
-                        const int qy = Cfg::kW4A8 ? (rank == 0 ? x.q0 : prm.q_rows + x.q0)
-                                                  : x.q0 + rank * Cfg::kQBoxRows;
-                        tma_load_2d(st + Cfg::kStageA, &mapQ, &full[s], kx, qy);
-                    } else if constexpr (Cfg::kW4A8) {
-                        // high-part rows q0.., low-part rows M + q0.. (the code planes are stacked)
-                        tma_load_2d(st + Cfg::kStageA, &mapQ, &full[s], kx, x.q0);
-                        tma_load_2d(st + Cfg::kStageA + QA * Cfg::kBK, &mapQ, &full[s], kx, prm.q_rows + x.q0);
-                    } else {
-                        tma_load_2d(st + Cfg::kStageA, &mapQ, &full[s], kx, x.q0);
+#pragma unroll
+                    for (int b = 0; b < Cfg::kKB; ++b) {
+                        const int kx = (x.kb0 + j * Cfg::kKB + b) * Cfg::kBK;
+                        uint8_t *sa = st + b * Cfg::kBoxA;
+                        uint8_t *sb = st + Cfg::kStageA + b * Cfg::kBoxB;
+                        tma_load_2d_hint(sa, &mapP, &full[s], kx, x.p0, keep);
+                        if constexpr (kPair) {
+                            // this CTA's half of the Q tile, into its own stage
+                            const int qy = Cfg::kW4A8 ? (rank == 0 ? x.q0 : prm.q_rows + x.q0)
+                                                      : x.q0 + rank * Cfg::kQBoxRows;
+                            tma_load_2d(sb, &mapQ, &full[s], kx, qy);
+                        } else if constexpr (Cfg::kW4A8) {
+                            // high-part rows q0.., low-part rows M + q0.. (the code planes are stacked)
+                            tma_load_2d(sb, &mapQ, &full[s], kx, x.q0);
+                            tma_load_2d(sb + QA * Cfg::kBK, &mapQ, &full[s], kx, prm.q_rows + x.q0);
+                        } else {
+                            tma_load_2d(sb, &mapQ, &full[s], kx, x.q0);
+                        }
                     }
                     issued_mask |= 1u << s;
                     last_phase = (last_phase & ~(1u << s)) | (ph << s);
@@ -298,7 +313,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 const uint32_t d_tmem = tmem + ab * Cfg::kAccCols;
                 if (!wait_bounded(&acc_empty[ab], aph ^ 1u, wd)) break;
                 tc_fence_after();
-                for (int i = 0; i < x.nkb; ++i, ++g) {
+                const int nst = (x.nkb + Cfg::kKB - 1) / Cfg::kKB;
+                for (int j = 0; j < nst; ++j, ++g) {
                     const int s = static_cast<int>(g % ST);
                     const uint32_t ph = (g / ST) & 1u;
                     if (!wait_bounded(&full[s], ph, wd) || (kPair && !wait_bounded(&pfull[s], ph, wd))) {
@@ -308,15 +324,21 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     tc_fence_after();
                     const uint32_t a_base = smem_u32(stages + s * Cfg::kStage);
                     const uint32_t b_base = a_base + Cfg::kStageA;
+                    const int nb = min(Cfg::kKB, x.nkb - j * Cfg::kKB);  // the unit's k blocks in this stage
 #pragma unroll
-                    for (int kk = 0; kk < Cfg::kBK / 32; ++kk) {
-                        const uint64_t ad = sdesc_kmajor_sw128(a_base + 32 * kk);
-                        const uint64_t bd = sdesc_kmajor_sw128(b_base + 32 * kk);
-                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                        if constexpr (kPair)
-                            mma_f8f6f4_pair(d_tmem, ad, bd, idesc, acc);
-                        else
-                            mma_f8f6f4(d_tmem, ad, bd, idesc, acc);
+                    for (int b = 0; b < Cfg::kKB; ++b) {
+                        if (b < nb) {
+#pragma unroll
+                            for (int kk = 0; kk < Cfg::kBK / 32; ++kk) {
+                                const uint64_t ad = sdesc_kmajor_sw128(a_base + b * Cfg::kBoxA + 32 * kk);
+                                const uint64_t bd = sdesc_kmajor_sw128(b_base + b * Cfg::kBoxB + 32 * kk);
+                                const uint32_t acc = (j > 0 || b > 0 || kk > 0) ? 1u : 0u;
+                                if constexpr (kPair)
+                                    mma_f8f6f4_pair(d_tmem, ad, bd, idesc, acc);
+                                else
+                                    mma_f8f6f4(d_tmem, ad, bd, idesc, acc);
+                            }
+                        }
                     }
                     if constexpr (kPair)
                         mma_commit_pair_multicast(&empty[s], 0x3);
@@ -342,7 +364,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             bool ok = true;
             for (int u = cid; ok && u < prm.num_units; u += ncl) {
                 const SsUnit x = ss_unit<Cfg>(prm, u, rank);
-                for (int i = 0; i < x.nkb; ++i, ++g) {
+                const int nst = (x.nkb + Cfg::kKB - 1) / Cfg::kKB;
+                for (int j = 0; j < nst; ++j, ++g) {
                     const int s = static_cast<int>(g % ST);
                     if (!wait_bounded(&full[s], (g / ST) & 1u, wd)) {
                         ok = false;

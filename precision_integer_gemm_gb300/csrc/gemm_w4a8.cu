@@ -22,8 +22,8 @@ using CfgW4A8Skinny16 = SkinnyCfg<false, 16, 8, 6, 2, 2, 1>;
 using CfgW4A8Skinny16C2 = SkinnyCfg<false, 16, 6, 6, 2, 2, 2>;
 using CfgW4A8Skinny16C4 = SkinnyCfg<false, 16, 8, 6, 2, 2, 4>;
 using CfgW4A8Skinny32 = SkinnyCfg<false, 32, 6, 4, 2, 2, 1>;
-//                    W4A8  BN  stages
-using CfgW4A8Ss = SsCfg<true, 256, 6, 2>;
+//                    W4A8  BN  stages CL  float out  format  k blocks per stage
+using CfgW4A8Ss = SsCfg<true, 256, 3, 2, false, 0, 2>;
 
 static int run_w4a8_codes(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
 {
