@@ -18,7 +18,7 @@
  * the pool keeps what it reserved for later calls until the process exits.  A
  * failed workspace allocation returns IGEMM_CUDA_ERROR.  w4a8_gemm_scaled (its
  * int32 product) and fp8_blockscaled_gemm (its transposed scales) take theirs
- * from the same pool; skinny shapes (M <= 32) and fp8_gemm (either format)
+ * from the same pool; skinny shapes (M <= 64) and fp8_gemm (either format)
  * need none.
  *
  * Launch overlap.  Where a call launches a short pass before its GEMM kernel
@@ -274,7 +274,7 @@ IGEMM_API uint64_t igemm_kernels_launched(void);
 
 /*
  * Planning query, host only (no GPU is touched): the split of K that a call of
- * i4i4_gemm (variant 0) or w4a8_gemm (variant 1) with 1 <= M <= 32 would use on
+ * i4i4_gemm (variant 0) or w4a8_gemm (variant 1) with 1 <= M <= 64 would use on
  * a GPU with `sms` SMs where `pairs` clusters of two and `quads` clusters of
  * four of the skinny kernel can be resident at once (0: none; the library asks
  * the driver for these on a real call).  Writes out[0] = k slices, out[1] = k
@@ -283,7 +283,7 @@ IGEMM_API uint64_t igemm_kernels_launched(void);
  * into C after a zeroing kernel; 2 or 4: the slices of a tile on one cluster,
  * summed through distributed shared memory).  The pages have no counterpart;
  * the kernel and the split are this library's.  IGEMM_INVALID_ARGUMENT for a
- * variant other than 0 or 1, M outside [1, 32], N < 1, K < 32, K % 32 != 0,
+ * variant other than 0 or 1, M outside [1, 64], N < 1, K < 32, K % 32 != 0,
  * K > 65536, sms < 1, negative cluster counts or a null `out`;
  * IGEMM_UNSUPPORTED_SHAPE when no plan fits.
  */

@@ -290,7 +290,7 @@ def igemm_time_next_gemm(start, stop) -> None:
 
 
 def igemm_skinny_plan(variant: str, M: int, N: int, K: int, sms: int, pairs: int, quads: int) -> dict:
-    """The K split a skinny (M <= 32) i4i4_gemm / w4a8_gemm call would use on a GPU with
+    """The K split a skinny (M <= 64) i4i4_gemm / w4a8_gemm call would use on a GPU with
     `sms` SMs and room for `pairs` / `quads` clusters of two / four (host only)."""
     out = (ctypes.c_int * 4)()
     v = {"i4i4": 0, "w4a8": 1}[variant]

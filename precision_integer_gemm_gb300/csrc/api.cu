@@ -480,7 +480,7 @@ extern "C" int unpack_int4(const uint8_t *packed, int8_t *logical, int64_t rows,
 
 extern "C" int igemm_skinny_plan(int variant, int M, int N, int K, int sms, int pairs, int quads, int *out)
 {
-    if ((variant != 0 && variant != 1) || M < 1 || M > 32 || N < 1 || K < 32 || K % 32 != 0 || K > kMaxK ||
+    if ((variant != 0 && variant != 1) || M < 1 || M > 64 || N < 1 || K < 32 || K % 32 != 0 || K > kMaxK ||
         sms < 1 || pairs < 0 || quads < 0 || !out)
         return kInvalidArgument;
     const SkinnyPlan p = variant == 0 ? skinny_plan_i4i4(M, N, K, sms, pairs, quads)

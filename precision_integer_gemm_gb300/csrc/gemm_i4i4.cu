@@ -1,6 +1,6 @@
 // int4 x int4 -> int32: A [M, K/2] and B [N, K/2] packed (low nibble = even k).
 //
-// Three paths.  M <= 32 takes igemm_skinny_kernel (gemm_skinny_kernel.cuh):
+// Three paths.  M <= 64 takes igemm_skinny_kernel (gemm_skinny_kernel.cuh):
 // B's rows on the MMA A side, A's signed codes resident in shared memory per
 // k slice.  Large products (M, N >= 512 and M * N >= 4M) take the prepared-codes path:
 // one pass turns A and B into code rows and row sums (prep.cu), then
@@ -23,6 +23,7 @@ using CfgI4I4Skinny16 = SkinnyCfg<true, 16, 8, 6, 2, 2, 1>;
 using CfgI4I4Skinny16C2 = SkinnyCfg<true, 16, 8, 6, 2, 2, 2>;
 using CfgI4I4Skinny16C4 = SkinnyCfg<true, 16, 8, 6, 2, 2, 4>;
 using CfgI4I4Skinny32 = SkinnyCfg<true, 32, 8, 6, 2, 2, 1>;
+using CfgI4I4Skinny64 = SkinnyCfg<true, 64, 8, 4, 2, 1, 1>;
 
 // The preparation pass costs (M + N) * K bytes of codes written and read again;
 // it pays once the product is large.  Measured crossovers on GB300: the
@@ -66,7 +67,8 @@ static int run_i4i4_codes(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int 
 SkinnyPlan skinny_plan_i4i4(int M, int N, int K, int sms, int pairs, int quads)
 {
     if (M <= 16) return skinny_plan_for<CfgI4I4Skinny16, CfgI4I4Skinny16C2, CfgI4I4Skinny16C4>(N, K, sms, pairs, quads);
-    return skinny_plan_for<CfgI4I4Skinny32>(N, K, sms, pairs, quads);
+    if (M <= 32) return skinny_plan_for<CfgI4I4Skinny32>(N, K, sms, pairs, quads);
+    return skinny_plan_for<CfgI4I4Skinny64>(N, K, sms, pairs, quads);
 }
 
 int launch_i4i4(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
@@ -74,10 +76,11 @@ int launch_i4i4(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, 
     // few rows of A (decode-like): B streamed once, A's codes resident (no
     // skinny plan fits only on parts with fewer SMs than k slices needed: those
     // shapes take the other paths)
-    if (M <= 32) {
+    if (M <= 64) {
         const int rc = M <= 16 ? launch_skinny<CfgI4I4Skinny16, CfgI4I4Skinny16C2, CfgI4I4Skinny16C4>(Ap, Bp, C, M, N, K,
                                                                                                      stream)
-                               : launch_skinny<CfgI4I4Skinny32>(Ap, Bp, C, M, N, K, stream);
+                     : M <= 32 ? launch_skinny<CfgI4I4Skinny32>(Ap, Bp, C, M, N, K, stream)
+                               : launch_skinny<CfgI4I4Skinny64>(Ap, Bp, C, M, N, K, stream);
         if (rc != kUnsupportedShape) return rc;
     }
     if (use_codes_i4i4(M, N)) return run_i4i4_codes(Ap, Bp, C, M, N, K, stream);

@@ -1,4 +1,4 @@
-// Skinny GEMM kernel (decode shapes, M <= 32): C[M,N] = A[M,K] . B[N,K]^T,
+// Skinny GEMM kernel (decode shapes, M <= 64): C[M,N] = A[M,K] . B[N,K]^T,
 // exact int32, B packed int4 (the weights: N large), A either int8 (W4A8,
 // "[Example] add w4a8 gemm kernel", tilelang PR #815) or packed int4
 // (int4 x int4, "[CUDA] Support int4 T.gemm", tilelang PR #2063).  Packing:
@@ -88,7 +88,7 @@ struct SkinnyCfg {
     // two accumulators (tile parity) per MMA issuer, then the code ring
     static constexpr int kACol0 = 2 * kMmaIssuers * kAccCols;
     static constexpr int kTmemCols = 512;
-    static_assert(QA == 16 || QA == 32, "activation rows");
+    static_assert(QA == 16 || QA == 32 || QA == 64, "activation rows");
     static_assert(kQRows % 16 == 0 && kQRows <= 256, "MMA N for M = 128");
     static_assert(kACol0 + TS * kTStageCols <= kTmemCols, "TMEM budget");
     static_assert(TS % kASets == 0, "each unpack set owns fixed TMEM stages");

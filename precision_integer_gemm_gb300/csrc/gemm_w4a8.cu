@@ -1,6 +1,6 @@
 // W4A8 -> int32: A [M, K] int8 activations, B [N, K/2] packed int4 weights.
 //
-// Skinny activation counts (M <= 32, decode) take igemm_skinny_kernel
+// Skinny activation counts (M <= 64, decode) take igemm_skinny_kernel
 // (gemm_skinny_kernel.cuh): split K, each CTA's slice of the activations held
 // as codes in shared memory, the weights streamed once.  Large products
 // (M >= 768, M * N >= 4M) take the prepared-codes path: one pass writes weight
@@ -22,6 +22,9 @@ using CfgW4A8Skinny16 = SkinnyCfg<false, 16, 8, 6, 2, 2, 1>;
 using CfgW4A8Skinny16C2 = SkinnyCfg<false, 16, 6, 6, 2, 2, 2>;
 using CfgW4A8Skinny16C4 = SkinnyCfg<false, 16, 8, 6, 2, 2, 4>;
 using CfgW4A8Skinny32 = SkinnyCfg<false, 32, 6, 4, 2, 2, 1>;
+// 64 rows: 128 code rows on the MMA N side, one MMA thread (its two accumulators
+// of 128 columns and four TMEM code stages fill the 512 columns)
+using CfgW4A8Skinny64 = SkinnyCfg<false, 64, 6, 4, 2, 1, 1>;
 //                    W4A8  BN  stages CL  float out  format  k blocks per stage
 using CfgW4A8Ss = SsCfg<true, 256, 3, 2, false, 0, 2>;
 
@@ -80,7 +83,8 @@ static int run_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N
 SkinnyPlan skinny_plan_w4a8(int M, int N, int K, int sms, int pairs, int quads)
 {
     if (M <= 16) return skinny_plan_for<CfgW4A8Skinny16, CfgW4A8Skinny16C2, CfgW4A8Skinny16C4>(N, K, sms, pairs, quads);
-    return skinny_plan_for<CfgW4A8Skinny32>(N, K, sms, pairs, quads);
+    if (M <= 32) return skinny_plan_for<CfgW4A8Skinny32>(N, K, sms, pairs, quads);
+    return skinny_plan_for<CfgW4A8Skinny64>(N, K, sms, pairs, quads);
 }
 
 int launch_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
@@ -88,10 +92,11 @@ int launch_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, in
     const uint8_t *a = reinterpret_cast<const uint8_t *>(A);
     // (no skinny plan fits only on parts with fewer SMs than k slices needed:
     // those shapes take the other paths)
-    if (M <= 32) {
+    if (M <= 64) {
         const int rc = M <= 16 ? launch_skinny<CfgW4A8Skinny16, CfgW4A8Skinny16C2, CfgW4A8Skinny16C4>(a, Bp, C, M, N, K,
                                                                                                      stream)
-                               : launch_skinny<CfgW4A8Skinny32>(a, Bp, C, M, N, K, stream);
+                     : M <= 32 ? launch_skinny<CfgW4A8Skinny32>(a, Bp, C, M, N, K, stream)
+                               : launch_skinny<CfgW4A8Skinny64>(a, Bp, C, M, N, K, stream);
         if (rc != kUnsupportedShape) return rc;
     }
     // the preparation pass writes N * K + 2 * M * K bytes of codes; measured on

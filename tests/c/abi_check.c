@@ -33,7 +33,7 @@ int main(void)
     EXPECT(igemm_skinny_plan(1, 16, 28672, 8192, 152, 76, 36, plan) == IGEMM_OK);
     EXPECT(plan[0] >= 1 && plan[1] > 0 && plan[1] % 256 == 0 && plan[2] >= 1 && plan[2] <= 152);
     EXPECT(plan[3] == 1 || plan[3] == 2 || plan[3] == 4);
-    EXPECT(igemm_skinny_plan(1, 33, 28672, 8192, 152, 76, 36, plan) == IGEMM_INVALID_ARGUMENT);
+    EXPECT(igemm_skinny_plan(1, 65, 28672, 8192, 152, 76, 36, plan) == IGEMM_INVALID_ARGUMENT);
     printf("c abi ok: split %d, slice %d, ctas %d, cluster %d\n", plan[0], plan[1], plan[2], plan[3]);
     return 0;
 }

@@ -447,19 +447,21 @@ def test_decode_workload_whole_c(orc):
 @pytest.mark.parametrize("av,bv", [(-8, -8), (7, 7), (-8, 7), (7, -8)])
 def test_i4i4_extreme_constants(orc, K, av, bv):
     # skinny, in-kernel and (K <= 8192) prepared-codes paths
-    for M, N in ((16, 260), (32, 260), (130, 260)) + (((2048, 2048),) if K <= 8192 else ()):
+    for M, N in ((16, 260), (32, 260), (64, 260), (130, 260)) + (((2048, 2048),) if K <= 8192 else ()):
         a = np.full((M, K), av, dtype=np.int8)
         b = np.full((N, K), bv, dtype=np.int8)
         C, _, _ = run_i4i4(a, b, orc)
         assert np.all(C == av * bv * K), (M, K, av, bv)
 
 
-# Skinny path (M <= 32): split K with ragged last slices (K % 256 != 0), N
-# tails (N % 4 != 0 too), both activation-row configurations (M <= 16,
-# M <= 32), one and many slices, every split plan (one slice, a cluster of two
-# or four, atomics after the overlapped zeroing).
+# Skinny path (M <= 64): split K with ragged last slices (K % 256 != 0), N
+# tails (N % 4 != 0 too), the three activation-row configurations (M <= 16,
+# M <= 32, M <= 64), one and many slices, every split plan (one slice, a
+# cluster of two or four, atomics after the overlapped zeroing).
 SKINNY = [(1, 129, 8224), (7, 1000, 4128), (16, 2048, 65536), (17, 300, 2080), (32, 520, 8192), (24, 128, 256),
-          (16, 28672, 512), (3, 1001, 6400), (16, 4096, 8192)]
+          (16, 28672, 512), (3, 1001, 6400), (16, 4096, 8192),
+          # the 64-row configuration: ragged M above 32, deep K (many slices), N tails
+          (33, 300, 2080), (48, 1000, 4128), (64, 28672, 512), (64, 520, 8192), (40, 129, 65536)]
 
 
 @pytest.mark.parametrize("M,N,K", SKINNY)
@@ -476,7 +478,7 @@ def test_skinny_path_matches_oracle(orc, M, N, K):
 @pytest.mark.parametrize("K", [32, 8192, 65536])
 @pytest.mark.parametrize("av,bv", [(-128, -8), (127, 7), (-128, 7), (127, -8), (0, -8)])
 def test_w4a8_extreme_constants(orc, K, av, bv):
-    for M, N in ((16, 260), (32, 260), (130, 260)) + (((1024, 4096),) if K <= 8192 else ()):
+    for M, N in ((16, 260), (32, 260), (64, 260), (130, 260)) + (((1024, 4096),) if K <= 8192 else ()):
         a = np.full((M, K), av, dtype=np.int8)
         b = np.full((N, K), bv, dtype=np.int8)
         C, _ = run_w4a8(a, b, orc)

@@ -1,4 +1,4 @@
-"""Host logic of the skinny path (M <= 32) on CPU: the K split the library plans,
+"""Host logic of the skinny path (M <= 64) on CPU: the K split the library plans,
 through the planning query igemm_skinny_plan (no GPU involved)."""
 
 import itertools
@@ -35,19 +35,21 @@ def test_decode_shape_plans(lib):
 
 @pytest.mark.parametrize("variant", ["i4i4", "w4a8"])
 def test_plan_invariants(lib, variant):
-    Ms = [1, 7, 16, 17, 32]
+    Ms = [1, 7, 16, 17, 32, 33, 48, 64]
     Ns = [1, 129, 1000, 4096, 28672, 65536]
     Ks = [32, 256, 480, 2080, 8192, 8224, 20000 // 32 * 32, 65536]
     machines = [(152, 76, 36), (152, 0, 0), (8, 4, 2), (132, 66, 33)]
     # the largest single-CTA activation slice of each configuration (int4 codes
     # take one byte per value and row, W4A8 codes two)
-    budget = {("i4i4", True): 6144, ("i4i4", False): 3072, ("w4a8", True): 3072, ("w4a8", False): 2048}
+    budget = {("i4i4", 16): 6144, ("i4i4", 32): 3072, ("i4i4", 64): 1536,
+              ("w4a8", 16): 3072, ("w4a8", 32): 2048, ("w4a8", 64): 1024}
+    rows = lambda M: 16 if M <= 16 else 32 if M <= 32 else 64
     for M, N, K, (sms, pairs, quads) in itertools.product(Ms, Ns, Ks, machines):
         try:
             p = plan(variant, M, N, K, sms, pairs, quads)
         except pig.IgemmError as e:
             # only a part with fewer SMs than the k slices the budget needs has no plan
-            assert e.code == pig.IGEMM_UNSUPPORTED_SHAPE and -(-K // budget[(variant, M <= 16)]) > sms, (M, N, K, sms)
+            assert e.code == pig.IGEMM_UNSUPPORTED_SHAPE and -(-K // budget[(variant, rows(M))]) > sms, (M, N, K, sms)
             continue
         S, sl, ctas, cl = p["split"], p["slice_k"], p["ctas"], p["cluster"]
         n_tiles = -(-N // 128)
@@ -60,7 +62,7 @@ def test_plan_invariants(lib, variant):
             assert S == cl and M <= 16, p
             assert ctas // cl <= (pairs if cl == 2 else quads), p
         if cl == 1:
-            assert sl <= budget[(variant, M <= 16)], p
+            assert sl <= budget[(variant, rows(M))], p
 
 
 def test_plan_argument_validation(lib):
@@ -68,7 +70,7 @@ def test_plan_argument_validation(lib):
     out = (ctypes.c_int * 4)()
     f = lib.igemm_skinny_plan
     assert f(2, 16, 128, 256, 152, 0, 0, out) == pig.IGEMM_INVALID_ARGUMENT
-    assert f(1, 33, 128, 256, 152, 0, 0, out) == pig.IGEMM_INVALID_ARGUMENT
+    assert f(1, 65, 128, 256, 152, 0, 0, out) == pig.IGEMM_INVALID_ARGUMENT
     assert f(1, 16, 128, 48, 152, 0, 0, out) == pig.IGEMM_INVALID_ARGUMENT
     assert f(1, 16, 128, 65568, 152, 0, 0, out) == pig.IGEMM_INVALID_ARGUMENT
     assert f(1, 16, 128, 256, 0, 0, 0, out) == pig.IGEMM_INVALID_ARGUMENT
