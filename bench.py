@@ -149,7 +149,7 @@ class ClockSampler:
             self.proc.kill()
         self.thread.join(timeout=5)
         out = "".join(self.lines)
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons, mask = [], [], [], set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.splitlines():
             parts = [p.strip() for p in line.split(",")]
@@ -160,12 +160,21 @@ class ClockSampler:
                 smax.append(float(parts[2]))
             except ValueError:
                 continue
+            try:
+                power.append(float(parts[3]))
+            except ValueError:
+                pass
+            try:
+                mask |= int(parts[4], 16)  # every clock-event reason seen (NVML bit mask)
+            except ValueError:
+                pass
             for name, val in zip(names, parts[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "reasons_mask": hex(mask), "power_w_max": max(power) if power else None}
 
 
 # variants whose operands are fp8 bytes and whose C is float32
