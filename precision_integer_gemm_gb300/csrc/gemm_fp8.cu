@@ -25,8 +25,11 @@ static int launch_fp8_cfg(const uint8_t *A, const uint8_t *B, float *C, int M, i
     if (tma_store &&
         make_map(&mapC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, M, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B) != kOk)
         return kCudaError;
+    // (no preparation pass to zero C: no tail split)
+    SsPlan plan;
+    if (ss_plan<Cfg>(M, N, K, M, N, (int64_t(M) + N) * K, false, &plan) != kOk) return kCudaError;
     return launch_ss<Cfg>(mapP, mapQ, mapC, tma_store, reinterpret_cast<int32_t *>(C), M, N, K, nullptr, nullptr, M,
-                          N, (int64_t(M) + N) * K, stream);
+                          N, plan, stream);
 }
 
 int launch_fp8(const uint8_t *A, const uint8_t *B, float *C, int M, int N, int K, int fmt, cudaStream_t stream)

@@ -46,7 +46,11 @@ static int run_i4i4_codes(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int 
     uint8_t *a_codes = base + lay.p_codes, *b_codes = base + lay.q_codes;
     int32_t *a_sums = reinterpret_cast<int32_t *>(base + lay.p_sums);
     int32_t *b_sums = reinterpret_cast<int32_t *>(base + lay.q_sums);
-    int rc = launch_prep(Ap, M, Bp, N, false, K, a_codes, b_codes, a_sums, b_sums, stream);
+    SsPlan plan;
+    int rc = ss_plan<Cfg>(M, N, K, M, N, (int64_t(M) + N) * K, true, &plan);
+    if (rc == kOk)
+        rc = launch_prep(Ap, M, Bp, N, false, K, a_codes, b_codes, a_sums, b_sums, ss_tail_zero<Cfg>(plan, C, M, N),
+                         stream);
     CUtensorMap mapP, mapQ, mapC = {};
     if (rc == kOk)
         rc = make_map(&mapP, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, M, K, Cfg::kPRows, Cfg::kBK,
@@ -58,8 +62,7 @@ static int run_i4i4_codes(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int 
     if (rc == kOk && tma_store)
         rc = make_map(&mapC, CU_TENSOR_MAP_DATA_TYPE_INT32, C, M, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc == kOk)
-        rc = launch_ss<Cfg>(mapP, mapQ, mapC, tma_store, C, M, N, K, a_sums, b_sums, M, N,
-                            (int64_t(M) + N) * K, stream, true);
+        rc = launch_ss<Cfg>(mapP, mapQ, mapC, tma_store, C, M, N, K, a_sums, b_sums, M, N, plan, stream, true);
     const int rf = workspace_free(ws, stream);
     return rc != kOk ? rc : rf;
 }
@@ -145,7 +148,11 @@ int launch_i4i4_noalloc(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M,
     int32_t *b_sums = reinterpret_cast<int32_t *>(base + lay.q_sums);
     // the preparation pass rewrites every code row and row sum the GEMM reads,
     // so nothing left in the array by an earlier call is used
-    rc = launch_prep(Ap, M, Bp, N, false, K, a_codes, b_codes, a_sums, b_sums, stream);
+    SsPlan plan;
+    rc = ss_plan<Cfg>(M, N, K, M, N, (int64_t(M) + N) * K, true, &plan);
+    if (rc == kOk)
+        rc = launch_prep(Ap, M, Bp, N, false, K, a_codes, b_codes, a_sums, b_sums, ss_tail_zero<Cfg>(plan, C, M, N),
+                         stream);
     CUtensorMap mapP, mapQ, mapC = {};
     if (rc == kOk)
         rc = make_map(&mapP, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, M, K, Cfg::kPRows, Cfg::kBK,
@@ -157,8 +164,7 @@ int launch_i4i4_noalloc(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M,
     if (rc == kOk && tma_store)
         rc = make_map(&mapC, CU_TENSOR_MAP_DATA_TYPE_INT32, C, M, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc == kOk)
-        rc = launch_ss<Cfg>(mapP, mapQ, mapC, tma_store, C, M, N, K, a_sums, b_sums, M, N,
-                            (int64_t(M) + N) * K, stream);
+        rc = launch_ss<Cfg>(mapP, mapQ, mapC, tma_store, C, M, N, K, a_sums, b_sums, M, N, plan, stream);
     return rc;
 }
 

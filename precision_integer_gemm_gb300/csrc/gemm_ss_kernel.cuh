@@ -118,6 +118,9 @@ struct SsParams {
     int p_tiles, q_tiles;
     int group_p;          // tiles run in groups of group_p P-tile slots (slot fastest)
     int kb_total, kb_per_split, split, num_units;
+    // tail split: units from tail_from on are pieces of the last tiles, tail_split
+    // pieces of kb_per_piece k blocks per tile (split == 1), added into C
+    int tail_from, tail_split, kb_per_piece;
     int tma_store;
     int *status;
     unsigned long long limit_ns;
@@ -132,8 +135,18 @@ template <class Cfg>
 __device__ __forceinline__ SsUnit ss_unit(const SsParams &prm, int u, int rank)
 {
     const int p_slots = (prm.p_tiles + Cfg::CL - 1) / Cfg::CL;
-    const int tile = u / prm.split;
-    const int s = u - tile * prm.split;
+    int tile, s, kb_per;
+    if (u < prm.tail_from) {
+        tile = u / prm.split;
+        s = u - tile * prm.split;
+        kb_per = prm.kb_per_split;
+    } else {
+        // a piece of one of the last tiles (split == 1, so unit tail_from is tile tail_from)
+        const int j = u - prm.tail_from;
+        tile = prm.tail_from + j / prm.tail_split;
+        s = j % prm.tail_split;
+        kb_per = prm.kb_per_piece;
+    }
     // Grouped order: group_p P tiles times every Q tile, P fastest.  The CTAs
     // of one wave share a few Q tiles through L2 and the group's P tiles
     // stay in L2 for the whole group, so each operand comes from DRAM about
@@ -148,8 +161,8 @@ __device__ __forceinline__ SsUnit ss_unit(const SsParams &prm, int u, int rank)
     SsUnit x;
     x.p0 = pt * Cfg::kPRows;
     x.q0 = qt * Cfg::QA;
-    x.kb0 = s * prm.kb_per_split;
-    x.nkb = min(prm.kb_total - x.kb0, prm.kb_per_split);
+    x.kb0 = s * kb_per;
+    x.nkb = min(prm.kb_total - x.kb0, kb_per);
     return x;
 }
 
@@ -382,13 +395,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         const int p = quad * 32 + lane;
         const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         uint8_t *stg = cstage + quad * Cfg::kCStage;
-        const bool reduce = prm.split > 1;
         const uint64_t out_policy = l2_policy_evict_first();  // C is not read again
         // where this warp releases an accumulator: the even CTA's barrier
         const uint32_t acc_empty_leader = kPair ? cluster_map(smem_u32(acc_empty), 0u) : 0u;
         uint32_t nacc = 0;
         for (int u = cid; u < prm.num_units; u += ncl, ++nacc) {
             const SsUnit x = ss_unit<Cfg>(prm, u, rank);
+            // the k ranges of a split tile add into C (zeroed before this grid)
+            const bool reduce = prm.split > 1 || u >= prm.tail_from;
             const uint32_t ab = nacc % Cfg::kAccBufs;
             if (!ss_warp_wait(&acc_full[ab], (nacc / Cfg::kAccBufs) & 1u, wd)) break;
             tc_fence_after();

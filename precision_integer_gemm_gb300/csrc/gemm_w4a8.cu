@@ -39,8 +39,11 @@ static int run_w4a8_codes(const int8_t *A, const uint8_t *Bp, int32_t *C, int M,
     uint8_t *w_codes = base + lay.p_codes, *a_codes = base + lay.q_codes;
     int32_t *w_sums = reinterpret_cast<int32_t *>(base + lay.p_sums);
     int32_t *a_sums = reinterpret_cast<int32_t *>(base + lay.q_sums);
-    int rc = launch_prep(Bp, N, reinterpret_cast<const uint8_t *>(A), M, true, K, w_codes, a_codes, w_sums, a_sums,
-                         stream);
+    SsPlan plan;
+    int rc = ss_plan<Cfg>(M, N, K, N, M, int64_t(N) * K + 2 * int64_t(M) * K, true, &plan);
+    if (rc == kOk)
+        rc = launch_prep(Bp, N, reinterpret_cast<const uint8_t *>(A), M, true, K, w_codes, a_codes, w_sums, a_sums,
+                         ss_tail_zero<Cfg>(plan, C, M, N), stream);
     CUtensorMap mapP, mapQ, mapC = {};
     if (rc == kOk)
         rc = make_map(&mapP, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_codes, N, K, Cfg::kPRows, Cfg::kBK,
@@ -53,8 +56,7 @@ static int run_w4a8_codes(const int8_t *A, const uint8_t *Bp, int32_t *C, int M,
     if (rc == kOk && tma_store)
         rc = make_map(&mapC, CU_TENSOR_MAP_DATA_TYPE_INT32, C, M, N, Cfg::kStageRows, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc == kOk)
-        rc = launch_ss<Cfg>(mapP, mapQ, mapC, tma_store, C, M, N, K, w_sums, a_sums, N, M,
-                            int64_t(N) * K + 2 * int64_t(M) * K, stream, true);
+        rc = launch_ss<Cfg>(mapP, mapQ, mapC, tma_store, C, M, N, K, w_sums, a_sums, N, M, plan, stream, true);
     const int rf = workspace_free(ws, stream);
     return rc != kOk ? rc : rf;
 }

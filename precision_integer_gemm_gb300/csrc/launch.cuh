@@ -110,10 +110,23 @@ struct CodesLayout {
 // q_rows sums of Q; returns the total size.
 size_t codes_layout(int p_rows, int q_code_rows, int q_rows, int K, CodesLayout *lay);
 
+// C regions to zero before a GEMM whose tail tiles add their pieces into C:
+// tiles first_tile .. first_tile + tiles - 1 of igemm_ss_kernel's grouped
+// order, each p_rows P rows by q_cols Q rows (C[P, Q], or C[Q, P] when
+// q_is_row: W4A8, whose P rows are the weights).
+struct TailZero {
+    int32_t *C;
+    int M, N;
+    int tiles, first_tile;
+    int group_p, p_slots, q_tiles;
+    int p_rows, q_cols, q_is_row;
+};
+
 // Codes and row sums of P (packed int4) and Q (packed int4, or int8 when
-// q_int8: high-code plane then low-code plane).
+// q_int8: high-code plane then low-code plane); and zeros in the C regions of
+// `zero` (one more CTA per tile).
 int launch_prep(const uint8_t *P, int p_rows, const uint8_t *Q, int q_rows, bool q_int8, int K, uint8_t *p_codes,
-                uint8_t *q_codes, int32_t *p_sums, int32_t *q_sums, cudaStream_t stream);
+                uint8_t *q_codes, int32_t *p_sums, int32_t *q_sums, const TailZero &zero, cudaStream_t stream);
 
 // Stream-ordered workspace from the library's own per-device pool.
 int workspace_alloc(void **p, size_t bytes, cudaStream_t stream);
@@ -152,14 +165,23 @@ int ss_resident_ctas(Kernel k)
     }
 }
 
+// The unit plan of igemm_ss_kernel<Cfg> for one call (host side): the tiles,
+// their grouped order, the split of K and the tail split.
+struct SsPlan {
+    int p_tiles, q_tiles, p_slots, group_p, kb_total;
+    int split, kb_per_split;                  // every tile in `split` k ranges (split K)
+    int tail_from, tail_split, kb_per_piece;  // tiles from tail_from on: tail_split pieces each
+    int num_units, clusters;
+};
+
+// The kernel's shared-memory attribute (once per device) and the clusters that
+// can be resident at once.
 template <class Cfg>
-int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMap &mapC, bool tma_store, int32_t *C,
-              int M, int N, int K, const int32_t *sumP, const int32_t *sumQ, int p_rows, int q_rows,
-              int64_t operand_bytes, cudaStream_t stream, bool after_prep = false)
+int ss_clusters()
 {
     auto kernel = igemm_ss_kernel<Cfg>;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return kCudaError;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     {
         static std::mutex mu;  // one per kernel instantiation; first calls from several threads
         static bool attr_set[64] = {};
@@ -167,12 +189,96 @@ int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMa
         if (dev < 64 && !attr_set[dev]) {
             if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) !=
                 cudaSuccess)
-                return kCudaError;
+                return 0;
             attr_set[dev] = true;
         }
     }
-    const int resident = ss_resident_ctas<Cfg>(kernel);
-    if (resident < Cfg::CL) return kCudaError;
+    return ss_resident_ctas<Cfg>(kernel) / Cfg::CL;
+}
+
+// Tail split: with T tiles on W clusters, the first (T / W) * W tiles run whole
+// and the last r = T mod W tiles run as S pieces of their k range each, S
+// chosen to minimise the time of that last partial wave (ceil(r S / W) waves of
+// 1/S of a tile); the pieces add into C, which the preparation pass zeroes for
+// those tiles.  `allow_tail` false: no tail split.
+template <class Cfg>
+int ss_plan(int M, int N, int K, int p_rows, int q_rows, int64_t operand_bytes, bool allow_tail, SsPlan *pl)
+{
+    const int W = ss_clusters<Cfg>();
+    if (W < 1) return kCudaError;
+    pl->p_tiles = (p_rows + Cfg::kPRows - 1) / Cfg::kPRows;
+    pl->q_tiles = (q_rows + Cfg::QA - 1) / Cfg::QA;
+    pl->p_slots = (pl->p_tiles + Cfg::CL - 1) / Cfg::CL;
+    // a group's P tiles (kGroupBytes of codes) stay in L2 while it runs
+    constexpr int64_t kGroupBytes = int64_t(32) << 20;
+    const int64_t slot_bytes = int64_t(Cfg::CL) * Cfg::kPRows * K;
+    pl->group_p = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(pl->p_slots, kGroupBytes / slot_bytes)));
+    pl->kb_total = (K + Cfg::kBK - 1) / Cfg::kBK;
+    const int tiles = pl->p_slots * pl->q_tiles;
+    // the split plan counts cluster units against the clusters that fit at once
+    const Plan plan = plan_units(tiles, pl->kb_total, int64_t(M) * N * 4, operand_bytes, W);
+    pl->split = plan.split;
+    pl->kb_per_split = plan.kb_per_split;
+    pl->num_units = tiles * plan.split;
+    pl->tail_from = pl->num_units;
+    pl->tail_split = 1;
+    pl->kb_per_piece = pl->kb_total;
+    const int r = tiles % W;
+    if (allow_tail && plan.split == 1 && tiles > W && r > 0 && pl->kb_total >= 2 * Cfg::kKB) {
+        int best_s = 1;
+        double best = 1.0;  // the last partial wave, in tiles of time
+        for (int S = 2; S <= 8; ++S) {
+            // pieces of eight stages at least: each piece ends with an epilogue
+            // that adds its tile into C (measured: pieces of four stages made W4A8
+            // 4096^3 slower, their epilogues outlasting their main loops)
+            if ((pl->kb_total + S - 1) / S < 8 * Cfg::kKB) break;
+            const double waves = static_cast<double>((r * S + W - 1) / W) / S;
+            if (waves < best - 0.02) {
+                best = waves;
+                best_s = S;
+            }
+        }
+        if (best_s > 1) {
+            // pieces of whole pipeline stages
+            const int kbpp = ((pl->kb_total + best_s - 1) / best_s + Cfg::kKB - 1) / Cfg::kKB * Cfg::kKB;
+            const int S = (pl->kb_total + kbpp - 1) / kbpp;
+            if (S >= 2) {
+                pl->tail_from = tiles - r;
+                pl->tail_split = S;
+                pl->kb_per_piece = kbpp;
+                pl->num_units = tiles - r + r * S;
+            }
+        }
+    }
+    pl->clusters = std::min(pl->num_units, W);
+    return kOk;
+}
+
+// The C regions of the tail tiles of a plan, for the preparation pass to zero.
+template <class Cfg>
+TailZero ss_tail_zero(const SsPlan &pl, int32_t *C, int M, int N)
+{
+    TailZero z{};
+    z.C = C;
+    z.M = M;
+    z.N = N;
+    z.tiles = pl.split == 1 ? (pl.num_units - pl.tail_from) / pl.tail_split : 0;
+    z.first_tile = pl.tail_from;
+    z.group_p = pl.group_p;
+    z.p_slots = pl.p_slots;
+    z.q_tiles = pl.q_tiles;
+    z.p_rows = Cfg::kPRows * Cfg::CL;
+    z.q_cols = Cfg::QA;
+    z.q_is_row = Cfg::kW4A8 ? 1 : 0;
+    return z;
+}
+
+template <class Cfg>
+int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMap &mapC, bool tma_store, int32_t *C,
+              int M, int N, int K, const int32_t *sumP, const int32_t *sumQ, int p_rows, int q_rows,
+              const SsPlan &pl, cudaStream_t stream, bool after_prep = false)
+{
+    auto kernel = igemm_ss_kernel<Cfg>;
     SsParams prm{};
     prm.C = C;
     prm.M = M;
@@ -182,27 +288,21 @@ int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMa
     prm.sumQ = sumQ;
     prm.p_rows = p_rows;
     prm.q_rows = q_rows;
-    prm.p_tiles = (p_rows + Cfg::kPRows - 1) / Cfg::kPRows;
-    prm.q_tiles = (q_rows + Cfg::QA - 1) / Cfg::QA;
-    const int p_slots = (prm.p_tiles + Cfg::CL - 1) / Cfg::CL;
-    // a group's P tiles (kGroupBytes of codes) stay in L2 while it runs
-    constexpr int64_t kGroupBytes = int64_t(32) << 20;
-    const int64_t slot_bytes = int64_t(Cfg::CL) * Cfg::kPRows * K;
-    prm.group_p = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(p_slots, kGroupBytes / slot_bytes)));
-    prm.kb_total = (K + Cfg::kBK - 1) / Cfg::kBK;
-    // the split plan counts cluster units against the clusters that fit at once
-    Plan plan = plan_units(p_slots * prm.q_tiles, prm.kb_total, int64_t(M) * N * 4, operand_bytes,
-                           resident / Cfg::CL);
-    prm.kb_per_split = plan.kb_per_split;
-    prm.split = plan.split;
-    prm.num_units = p_slots * prm.q_tiles * plan.split;
+    prm.p_tiles = pl.p_tiles;
+    prm.q_tiles = pl.q_tiles;
+    prm.group_p = pl.group_p;
+    prm.kb_total = pl.kb_total;
+    prm.kb_per_split = pl.kb_per_split;
+    prm.split = pl.split;
+    prm.tail_from = pl.tail_from;
+    prm.tail_split = pl.tail_split;
+    prm.kb_per_piece = pl.kb_per_piece;
+    prm.num_units = pl.num_units;
     prm.tma_store = tma_store ? 1 : 0;
     prm.status = device_status_word();
     prm.limit_ns = watchdog_limit_ns();
     if (!prm.status) return kCudaError;
-    if (plan.split > 1 && cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 4, stream) != cudaSuccess)
-        return kCudaError;
-    const int clusters = std::min(prm.num_units, resident / Cfg::CL);
+    if (pl.split > 1 && cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 4, stream) != cudaSuccess) return kCudaError;
     const GemmEvents ev = take_gemm_events();
     if (ev.start && cudaEventRecord(ev.start, stream) != cudaSuccess) return kCudaError;
     cudaLaunchConfig_t cfg = {};
@@ -217,12 +317,13 @@ int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMa
     }
     // right after the preparation pass (no memset or armed event in between):
     // launch early; the kernel waits for the pass before it reads codes or sums
-    if (after_prep && plan.split == 1 && !ev.start) {
+    // or touches C
+    if (after_prep && pl.split == 1 && !ev.start) {
         attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[na].val.programmaticStreamSerializationAllowed = 1;
         ++na;
     }
-    cfg.gridDim = dim3(Cfg::CL * clusters, 1, 1);
+    cfg.gridDim = dim3(Cfg::CL * pl.clusters, 1, 1);
     cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = stream;

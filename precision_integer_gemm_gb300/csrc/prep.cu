@@ -44,19 +44,60 @@ __device__ __forceinline__ int block_sum(int v, int *red)
     return t;
 }
 
-// One CTA per row: rows [0, p_rows) of the packed int4 operand P, then rows
-// [p_rows, p_rows + q_rows) of Q (packed int4, or int8 when kQInt8).
+// Zeros in part `part` (of kZeroParts row bands) of the C region of tail tile
+// `t` of the GEMM that follows (its tiles in igemm_ss_kernel's grouped order:
+// group_p P-tile slots times every Q tile, slot fastest).
+constexpr int kZeroParts = 8;
+__device__ void zero_tail_tile(const TailZero &z, int t, int part)
+{
+    const int tile = z.first_tile + t;
+    const int per_group = z.group_p * z.q_tiles;
+    const int grp = tile / per_group;
+    const int first = grp * z.group_p;
+    const int gsize = min(z.p_slots - first, z.group_p);
+    const int r = tile - grp * per_group;
+    const int p0 = (first + r % gsize) * z.p_rows, q0 = (r / gsize) * z.q_cols;
+    const int row0 = z.q_is_row ? q0 : p0, col0 = z.q_is_row ? p0 : q0;
+    const int rows = min(z.q_is_row ? z.q_cols : z.p_rows, z.M - row0);
+    const int cols = min(z.q_is_row ? z.p_rows : z.q_cols, z.N - col0);
+    const int band = (rows + kZeroParts - 1) / kZeroParts;
+    const int r0 = part * band, r1 = min(rows, r0 + band);
+    if (z.N % 4 == 0 && col0 % 4 == 0 && cols % 4 == 0) {
+        // 16-byte stores (C is 16-byte aligned, rows a multiple of 16 bytes)
+        const int c4 = cols / 4;
+        for (int i = threadIdx.x; i < (r1 - r0) * c4; i += blockDim.x) {
+            const int rr = r0 + i / c4, cc = 4 * (i - (i / c4) * c4);
+            *reinterpret_cast<int4 *>(z.C + static_cast<int64_t>(row0 + rr) * z.N + col0 + cc) = make_int4(0, 0, 0, 0);
+        }
+    } else {
+        for (int i = threadIdx.x; i < (r1 - r0) * cols; i += blockDim.x) {
+            const int rr = r0 + i / cols, cc = i - (i / cols) * cols;
+            z.C[static_cast<int64_t>(row0 + rr) * z.N + col0 + cc] = 0;
+        }
+    }
+}
+
+// First kZeroParts CTAs per tail tile of `zero` (they run among the first CTAs,
+// not after the rows); then one CTA per row: rows [0, p_rows) of the packed
+// int4 operand P, then rows [p_rows, p_rows + q_rows) of Q (packed int4, or
+// int8 when kQInt8).
 template <bool kQInt8>
 __global__ void __launch_bounds__(256) prep_codes_kernel(const uint8_t *__restrict__ P, int p_rows,
                                                          const uint8_t *__restrict__ Q, int q_rows, int K,
                                                          uint8_t *__restrict__ p_codes, uint8_t *__restrict__ q_codes,
-                                                         int32_t *__restrict__ p_sums, int32_t *__restrict__ q_sums)
+                                                         int32_t *__restrict__ p_sums, int32_t *__restrict__ q_sums,
+                                                         const TailZero zero)
 {
     __shared__ int red[8];
     // the GEMM that follows may launch now; it waits for this grid before it
-    // reads any code or sum
+    // reads any code or sum, or touches C
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int row = blockIdx.x;
+    const int zero_ctas = kZeroParts * zero.tiles;
+    if (static_cast<int>(blockIdx.x) < zero_ctas) {
+        zero_tail_tile(zero, blockIdx.x / kZeroParts, blockIdx.x % kZeroParts);
+        return;
+    }
+    const int row = blockIdx.x - zero_ctas;
     int sum = 0;
     const bool is_p = row < p_rows;
     const int r = is_p ? row : row - p_rows;
@@ -93,13 +134,16 @@ __global__ void __launch_bounds__(256) prep_codes_kernel(const uint8_t *__restri
 }
 
 int launch_prep(const uint8_t *P, int p_rows, const uint8_t *Q, int q_rows, bool q_int8, int K, uint8_t *p_codes,
-                uint8_t *q_codes, int32_t *p_sums, int32_t *q_sums, cudaStream_t stream)
+                uint8_t *q_codes, int32_t *p_sums, int32_t *q_sums, const TailZero &zero, cudaStream_t stream)
 {
-    const unsigned grid = static_cast<unsigned>(p_rows) + static_cast<unsigned>(q_rows);
+    const unsigned grid = static_cast<unsigned>(p_rows) + static_cast<unsigned>(q_rows) +
+                          static_cast<unsigned>(kZeroParts * zero.tiles);
     if (q_int8)
-        prep_codes_kernel<true><<<grid, 256, 0, stream>>>(P, p_rows, Q, q_rows, K, p_codes, q_codes, p_sums, q_sums);
+        prep_codes_kernel<true><<<grid, 256, 0, stream>>>(P, p_rows, Q, q_rows, K, p_codes, q_codes, p_sums, q_sums,
+                                                          zero);
     else
-        prep_codes_kernel<false><<<grid, 256, 0, stream>>>(P, p_rows, Q, q_rows, K, p_codes, q_codes, p_sums, q_sums);
+        prep_codes_kernel<false><<<grid, 256, 0, stream>>>(P, p_rows, Q, q_rows, K, p_codes, q_codes, p_sums, q_sums,
+                                                           zero);
     note_launch();
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
 }

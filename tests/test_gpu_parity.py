@@ -145,9 +145,14 @@ def test_w4a8_matches_oracle(orc, M, N, K):
 # Shapes of the prepared-codes path (large products: int4 x int4 with M, N >=
 # 512 and M * N >= 4M; W4A8 with M >= 768 and M * N >= 4M): K below one
 # 128-k block, K tails, ragged M and N, N % 4 != 0 (direct stores instead of
-# bulk tensor stores) and a split K.  Whole C, element by element.
+# bulk tensor stores), a split K, and tile counts above the CTA pairs, whose
+# last tiles run as k pieces (W4A8 1030 x 4100 / 4102 x 4160, 1024 x 4096 x
+# 65536).  Whole C, element by element.
 CODES_I4I4 = [(2048, 2048, 32), (2100, 2056, 96), (2049, 2050, 1056), (2048, 2050, 128), (2048, 2048, 16384),
-              (1024, 4100, 8224)]
+              (1024, 4100, 8224),
+              # more tiles than CTA pairs: the last tiles run as k pieces added into C
+              # (N % 4 != 0: scalar atomic adds)
+              (2560, 2050, 4096), (4096, 4096, 4096)]
 
 
 @pytest.mark.parametrize("M,N,K", CODES_I4I4)
@@ -158,7 +163,8 @@ def test_i4i4_prepared_codes_path(orc, M, N, K):
     assert np.array_equal(C, orc.i4i4_gemm(ap, bp, K))
 
 
-CODES_W4A8 = [(1024, 4096, 32), (1030, 4100, 4160), (2000, 2100, 1056), (1024, 4096, 65536), (1024, 4098, 384)]
+CODES_W4A8 = [(1024, 4096, 32), (1030, 4100, 4160), (2000, 2100, 1056), (1024, 4096, 65536), (1024, 4098, 384),
+              (1030, 4102, 4160)]
 
 
 @pytest.mark.parametrize("M,N,K", CODES_W4A8)
