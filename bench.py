@@ -419,7 +419,9 @@ def run_ours(args, variant, M, N, K, a, b):
         achieved = ops / gemm_kernel_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "kernel": "igemm_bs_kernel" if variant == "fp8bs" else "igemm_ss_kernel",
+                "kernel": ("igemm_bs_kernel" if variant == "fp8bs"
+                           else "igemm_small_kernel" if args.workload in ("i4i4_256", "i4i4_1024")
+                           else "igemm_ss_kernel"),
                 "kernel_ms": 1e3 * gemm_kernel_s, "algorithmic_ops_per_launch": ops,
                 "peak_source": f"{peak_src} bf16 burst x {E4M3_PER_BF16} (nominal fp8/bf16 ratio)",
                 "mma_macs_per_op": 2 if variant == "w4a8" else 1}

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libigemm.so")
-SOURCES = ["api.cu", "prep.cu", "gemm_i4i4.cu", "gemm_w4a8.cu", "gemm_fp8.cu", "gemm_bs.cu", "host.cu"]
+SOURCES = ["api.cu", "prep.cu", "gemm_i4i4.cu", "gemm_small.cu", "gemm_w4a8.cu", "gemm_fp8.cu", "gemm_bs.cu", "host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

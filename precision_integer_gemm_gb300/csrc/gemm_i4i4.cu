@@ -1,14 +1,17 @@
 // int4 x int4 -> int32: A [M, K/2] and B [N, K/2] packed (low nibble = even k).
 //
-// Three paths.  M <= 64 takes igemm_skinny_kernel (gemm_skinny_kernel.cuh):
+// Four paths.  M <= 64 takes igemm_skinny_kernel (gemm_skinny_kernel.cuh):
 // B's rows on the MMA A side, A's signed codes resident in shared memory per
-// k slice.  Large products (M, N >= 512 and M * N >= 4M) take the prepared-codes path:
-// one pass turns A and B into code rows and row sums (prep.cu), then
-// igemm_ss_kernel runs a TMA -> tcgen05.mma pipeline on 128 x 256 tiles with
-// both operands in shared memory.  Smaller shapes, where that pass would cost
-// more than it saves, take igemm_tc_kernel, which unpacks every tile in the
-// kernel: MMA A side = A (127 data rows + a row of ones per tile, codes in
-// TMEM), B side = B (192 rows per tile, codes in shared memory).
+// k slice.  Products of at most about one wave of output tiles take
+// igemm_small_kernel (gemm_small.cu): one launch, one CTA per 128 x 64 or
+// 128 x 128 tile, codes made in the kernel.  Large products (M, N >= 512 and
+// M * N >= 4M) take the prepared-codes path: one pass turns A and B into code
+// rows and row sums (prep.cu), then igemm_ss_kernel runs a TMA -> tcgen05.mma
+// pipeline on 256 x 256 tiles of CTA pairs with both operands in shared
+// memory.  The remaining shapes, where that pass would cost more than it
+// saves, take igemm_tc_kernel, which unpacks every tile in the kernel: MMA A
+// side = A (127 data rows + a row of ones per tile, codes in TMEM), B side = B
+// (192 rows per tile, codes in shared memory).
 #include <mutex>
 #include "launch.cuh"
 
@@ -33,6 +36,25 @@ using CfgI4I4Skinny64 = SkinnyCfg<true, 64, 8, 4, 2, 1, 1>;
 static bool use_codes_i4i4(int M, int N)
 {
     return M >= 512 && N >= 512 && int64_t(M) * N >= (int64_t(1) << 22);
+}
+
+// Output-tile width of the small-product kernel for this shape, 0 if another
+// path is faster.  Its CTAs run one tile each with no split of K, so it wins
+// while the tiles fit about one wave of SMs.  Measured on GB300 (call time,
+// L2 flushed; other path in parentheses): 1024^3 10.9 us with 64-wide tiles
+// (19.1), 512 x 4096 x 4096 23.2 us with 128-wide tiles (34.4), 1536^3 15.0
+// (19.1), 2048 x 2048 x 512 17.1 (22.2, two waves of 128-wide tiles), 1024 x
+// 1024 x 8192 31.4 (33.4); it loses at 2048^3 (27.3 vs 26.3) and 4096 x 4096
+// x 1024 (56 vs 45).  Few tiles with a long K go to the paths that split K.
+static int small_tile_width(int M, int N, int K)
+{
+    const int64_t sms = sm_count();
+    const int64_t rows = (M + 127) / 128;
+    const int64_t t64 = rows * ((N + 63) / 64), t128 = rows * ((N + 127) / 128);
+    if (t64 <= sms && (K <= 4096 || 2 * t64 >= sms)) return 64;
+    if (t128 <= sms && K <= 4096) return 128;
+    if (t128 <= 2 * sms && K <= 1024) return 128;
+    return 0;
 }
 
 static int run_i4i4_codes(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
@@ -86,6 +108,7 @@ int launch_i4i4(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, 
                                : launch_skinny<CfgI4I4Skinny64>(Ap, Bp, C, M, N, K, stream);
         if (rc != kUnsupportedShape) return rc;
     }
+    if (const int bn = small_tile_width(M, N, K)) return launch_i4i4_small(Ap, Bp, C, M, N, K, bn, stream);
     if (use_codes_i4i4(M, N)) return run_i4i4_codes(Ap, Bp, C, M, N, K, stream);
     using Cfg = CfgI4I4;
     CUtensorMap mapA, mapB, mapC32 = {}, mapC31 = {};

@@ -1,0 +1,414 @@
+// int4 x int4 -> int32 for small products (a few dozen to a few hundred
+// 128-row output tiles, e.g. 1024^3): C[M,N] = A[M,K] . B[N,K]^T exactly, A
+// and B packed (low nibble = even k, the packing of the TileLang tutorial's
+// pack_int4), the contract of "[CUDA] Support int4 T.gemm" (tilelang PR
+// #2063, matmul_nt_int4).
+//
+// At these sizes a call is bound by latency, not by any throughput: the
+// prepared-codes path pays a second launch and a round trip through memory,
+// the warp-specialised kernels several hand-overs per stage.  This kernel is
+// one launch with one CTA per 128 x BN output tile: eight converting warps and
+// one MMA warp.
+//
+//  * the CTA walks K in chunks of 256 k (128 packed bytes per row).  The MMA
+//    thread loads each chunk's packed A and B rows with two TMA boxes (128
+//    bytes x 128 and x BN rows) into a ring of three raw slots, refilling a
+//    slot as soon as its chunk is converted; rows past M or N and bytes past
+//    K arrive as zeros;
+//  * eight converting warps turn every nibble v into the e4m3 code
+//    u = v + 8 (value u * 2^-9, exact) and sum the codes per row (dp4a).
+//    A codes go to tensor memory: warp w converts k block w / 4 of the chunk
+//    (four 16-byte pieces) for A rows 32 (w % 4) .. 32 (w % 4) + 31, one row
+//    per thread, and stores them with tcgen05.st.  B codes go to a
+//    128-byte-swizzled K-major tile in shared memory: thread (g, p) =
+//    (tid / 8, tid % 8) converts bytes 16 p .. 16 p + 15 of B rows g + 32 i, so
+//    eight lanes share a row.  Codes past K and rows past M or N are 0.  Each
+//    warp then arrives on the code buffer's mbarrier;
+//  * the MMA thread waits for the eight arrivals, issues the chunk's
+//    tcgen05.mma (A from tensor memory, B from shared memory, M = 128,
+//    N = BN, f32 accumulator in TMEM, exact: every partial sum is an integer
+//    times 2^-18 below 2^24 * 2^-18 for K <= 65536) and commits to the
+//    buffer's second mbarrier; three code buffers let the converters run
+//    ahead of the MMAs;
+//  * the epilogue reads the accumulator (warp w: TMEM lanes 32 (w % 4), half
+//    w / 4 of the columns), restores the signed result
+//    C = S - 8 sum uA - 8 sum uB + 64 K, stages the tile in shared memory and
+//    writes it out row by row (coalesced 16-byte stores).
+//
+// Code order inside a piece of 32 k (16 packed bytes, words w0..w3): code
+// chunk X = (even k of w0, odd k of w0, even k of w1, odd k of w1), chunk Y the
+// same for w2, w3.  In k block 0 X comes first, in k block 1 Y does (so that
+// the eight lanes of a B store phase hit eight distinct bank groups).  Both
+// operands use the same order, which leaves every dot product unchanged.
+// Every wait is bounded (ptx.cuh).
+#include "launch.cuh"
+
+namespace igemm {
+
+constexpr int kSmallConvThreads = 256;                 // eight converting warps
+constexpr int kSmallThreads = kSmallConvThreads + 32;  // + the MMA warp
+constexpr int kSmallRowsA = 128;
+constexpr int kSmallRaw = 3;  // raw slots: chunks of packed rows loaded ahead
+
+template <int BN>
+struct SmallCfg {
+    static constexpr int kBRowsPerThread = BN / 32;
+    static constexpr int kBufs = 3;                         // code buffers
+    static constexpr int kACols = 64;                       // TMEM columns of one chunk of A codes
+    static constexpr int kTmemUsed = BN + kBufs * kACols;   // accumulator, then the A code buffers
+    static constexpr int kTmemCols = kTmemUsed <= 256 ? 256 : 512;
+    static constexpr int kRawA = kSmallRowsA * 128;          // packed bytes of one chunk
+    static constexpr int kRawStage = kRawA + BN * 128;
+    static constexpr int kBlockB = BN * 128;                 // one 128-k block of B codes
+    static constexpr int kCodeBuf = 2 * kBlockB;
+    static constexpr int kStage = kSmallRowsA * BN * 4;      // the int32 tile, over the code buffers
+    static_assert(kStage <= kBufs * kCodeBuf, "epilogue tile fits over the code buffers");
+    static constexpr int kSmem = 1024 + kBufs * kCodeBuf + kSmallRaw * kRawStage + 4 * (2 * kSmallRowsA + BN) +
+                                 8 * (2 * kBufs + kSmallRaw) + 16;
+    static_assert(kSmem <= 232448, "shared memory per CTA");
+};
+
+// Four bytes of nibbles -> codes of the even-k nibbles and of the odd-k nibbles.
+__device__ __forceinline__ void small_codes(uint32_t x, uint32_t &lo, uint32_t &hi)
+{
+    lo = (x & 0x0F0F0F0Fu) ^ 0x08080808u;
+    hi = ((x >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+}
+
+// Convert one 16-byte piece (32 k) of a row into two 16-byte code chunks at
+// `dst0` and `dst1`, adding the codes to `sum`; an invalid piece gives zeros.
+__device__ __forceinline__ void small_piece(const uint4 x, bool valid, uint8_t *dst0, uint8_t *dst1, int &sum)
+{
+    uint32_t c[8];
+    small_codes(x.x, c[0], c[1]);
+    small_codes(x.y, c[2], c[3]);
+    small_codes(x.z, c[4], c[5]);
+    small_codes(x.w, c[6], c[7]);
+    if (!valid) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = 0u;  // code 0 adds nothing
+    }
+    // bytes of lo + hi stay below 31: one dp4a per word
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) sum = __dp4a(static_cast<int>(c[i] + c[i + 1]), 0x01010101, sum);
+    *reinterpret_cast<uint4 *>(dst0) = make_uint4(c[0], c[1], c[2], c[3]);
+    *reinterpret_cast<uint4 *>(dst1) = make_uint4(c[4], c[5], c[6], c[7]);
+}
+
+// Codes of one 16-byte piece: X (w0, w1) and Y (w2, w3), each as even-k
+// word, odd-k word; an invalid piece gives zeros.  Returns the codes' sum
+// added to `sum`.
+__device__ __forceinline__ void small_piece_codes(const uint4 x, bool valid, uint32_t (&c)[8], int &sum)
+{
+    small_codes(x.x, c[0], c[1]);
+    small_codes(x.y, c[2], c[3]);
+    small_codes(x.z, c[4], c[5]);
+    small_codes(x.w, c[6], c[7]);
+    if (!valid) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) sum = __dp4a(static_cast<int>(c[i] + c[i + 1]), 0x01010101, sum);
+}
+
+// k block KB of a chunk of one A row (pieces 4 KB .. 4 KB + 3, chunk j of
+// the raw row stored at j ^ (row % 8)) -> 32 code words for tcgen05.st (bit
+// t of valid_mask: piece 4 KB + t lies inside K).
+template <int KB>
+__device__ __forceinline__ void small_a_codes(const uint8_t *raw_row, uint32_t sw, uint32_t valid_mask,
+                                              uint32_t (&code)[32], int &sum)
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int piece = 4 * KB + j;
+        const uint4 x = *reinterpret_cast<const uint4 *>(raw_row + ((piece ^ sw) << 4));
+        uint32_t cw[8];
+        small_piece_codes(x, (valid_mask >> j) & 1u, cw, sum);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            code[8 * j + t] = KB == 0 ? cw[t] : cw[4 + t];  // k block 1: Y before X
+            code[8 * j + 4 + t] = KB == 0 ? cw[4 + t] : cw[t];
+        }
+    }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kSmallThreads, 1)
+    igemm_small_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                       int32_t *__restrict__ C, int M, int N, int K, int *status, unsigned long long limit_ns)
+{
+    using Cfg = SmallCfg<BN>;
+    constexpr int RB = Cfg::kBRowsPerThread;
+    constexpr int NB = Cfg::kBufs;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint8_t *codes = smem;                                       // [NB][2 k blocks][BN rows][128]: B codes
+    uint8_t *raw = smem + NB * Cfg::kCodeBuf;                    // [kSmallRaw][A rows | B rows], 128 bytes a row
+    int *sumA = reinterpret_cast<int *>(raw + kSmallRaw * Cfg::kRawStage);  // [2 k blocks][128]
+    int *sumB = sumA + 2 * kSmallRowsA;                                      // [BN]
+    uint64_t *conv = reinterpret_cast<uint64_t *>(sumB + BN);    // [NB] code buffer written
+    uint64_t *done = conv + NB;                                  // [NB] code buffer read by the MMAs
+    uint64_t *full = done + NB;                                  // [kSmallRaw] raw slot loaded
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(full + kSmallRaw);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool converter = warp < kSmallConvThreads / 32;
+    const bool mma_thread = warp == kSmallConvThreads / 32 && lane == 0;
+    const int m0 = blockIdx.y * kSmallRowsA, n0 = blockIdx.x * BN;
+    const int kh = K / 2;  // packed bytes per row (a multiple of 16)
+    const int nchunks = (K + 255) / 256;
+
+    // chunk c's packed rows into raw slot c % kSmallRaw (MMA thread)
+    auto load = [&](int c) {
+        const int s = c % kSmallRaw;
+        uint8_t *dst = raw + s * Cfg::kRawStage;
+        mbar_arrive_expect_tx(&full[s], Cfg::kRawStage);
+        tma_load_2d(dst, &mapA, &full[s], c * 128, m0);
+        tma_load_2d(dst + Cfg::kRawA, &mapB, &full[s], c * 128, n0);
+    };
+    if (mma_thread) {
+        tma_prefetch_map(&mapA);
+        tma_prefetch_map(&mapB);
+        for (int i = 0; i < NB; ++i) {
+            mbar_init(&conv[i], kSmallConvThreads / 32);
+            mbar_init(&done[i], 1);
+        }
+        for (int i = 0; i < kSmallRaw; ++i) mbar_init(&full[i], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        for (int c = 0; c < kSmallRaw && c < nchunks; ++c) load(c);
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Watchdog wd{abort_flag, status, limit_ns};
+
+    bool ok = true;
+    uint32_t issued = 0;   // commits issued (MMA thread)
+    int loads = 0;         // chunks whose loads were issued (MMA thread)
+    if (mma_thread) loads = min(kSmallRaw, nchunks);
+
+    if (converter) {
+        // A: row ra, k block kba (32 TMEM columns) of every chunk
+        const int quad = warp & 3, kba = warp >> 2;
+        const int ra = quad * 32 + lane;
+        const bool a_ok = m0 + ra < M;
+        const uint32_t a_tcol = tmem + (static_cast<uint32_t>(quad * 32) << 16) + BN + 32 * kba;
+        // B: thread (g, p) takes bytes 16 p .. of rows g + 32 i; where its two
+        // code chunks of a piece go: k block p / 4, chunks 2 (p % 4) and
+        // 2 (p % 4) + 1, the first of them taken by X in k block 0 and by Y in
+        // k block 1; the 16-byte chunk index is swizzled by row % 8
+        const int g = tid >> 3, p = tid & 7;
+        const int kb = p >> 2;
+        const int cx = 2 * (p & 3) + kb, cy = 2 * (p & 3) + 1 - kb;
+        bool b_ok[RB];
+#pragma unroll
+        for (int i = 0; i < RB; ++i) b_ok[i] = n0 + g + 32 * i < N;
+        int sa = 0, sb[RB];
+#pragma unroll
+        for (int i = 0; i < RB; ++i) sb[i] = 0;
+#pragma unroll 1
+        for (int c = 0; c < nchunks; ++c) {
+            const int s = c % kSmallRaw, use = c / NB, buf = c - use * NB;
+            ok = __all_sync(0xffffffffu, wait_bounded(&full[s], (c / kSmallRaw) & 1u, wd));
+            // the MMAs of chunk c - NB read this code buffer
+            if (ok && use > 0) ok = __all_sync(0xffffffffu, wait_bounded(&done[buf], (use - 1) & 1u, wd));
+            if (!ok) break;  // the whole warp
+            tc_fence_after();
+            const uint8_t *slot = raw + s * Cfg::kRawStage;
+            // pieces of this chunk inside K: bytes c * 128 + 16 j < kh
+            const int left = (kh - c * 128) >> 4;  // > 0
+            {
+                uint32_t code[32];
+                const uint32_t vmask = a_ok ? (left >= 8 ? 0xFFu : ((1u << left) - 1u)) >> (4 * kba) : 0u;
+                if (kba == 0)
+                    small_a_codes<0>(slot + ra * 128, ra & 7, vmask, code, sa);
+                else
+                    small_a_codes<1>(slot + ra * 128, ra & 7, vmask, code, sa);
+                tmem_st_32x32b_x32(a_tcol + buf * Cfg::kACols, code);
+            }
+            const bool in = p < left;
+            uint8_t *bs = codes + buf * Cfg::kCodeBuf + kb * Cfg::kBlockB;
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+                const int r = g + 32 * i, sw = r & 7;
+                const uint4 x = *reinterpret_cast<const uint4 *>(slot + Cfg::kRawA + r * 128 + 16 * p);
+                uint8_t *row = bs + r * 128;
+                small_piece(x, in && b_ok[i], row + ((cx ^ sw) << 4), row + ((cy ^ sw) << 4), sb[i]);
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();  // generic writes, read next by the tensor core
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&conv[buf]);
+        }
+        // the last chunk's commit covers every MMA before it
+        if (ok) {
+            const int c = nchunks - 1, use = c / NB;
+            ok = wait_bounded(&done[c - use * NB], use & 1u, wd);
+        }
+        sumA[kba * kSmallRowsA + ra] = sa;
+        // B row sums: the eight lanes of a row hold one partial sum each
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+            int v = sb[i];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            if (p == 0) sumB[g + 32 * i] = v;
+        }
+    } else if (mma_thread) {
+        // ---------------------------------------------------------------- MMA thread
+        constexpr uint32_t idesc = idesc_e4m3_f32(kSmallRowsA, BN);
+#pragma unroll 1
+        for (int c = 0; c < nchunks; ++c) {
+            const int use = c / NB, buf = c - use * NB;
+            ok = wait_bounded(&conv[buf], use & 1u, wd);
+            if (!ok) break;
+            // chunk c is converted: its raw slot takes chunk c + kSmallRaw
+            if (loads < nchunks) load(loads++);
+            tc_fence_after();
+            const uint32_t a0 = tmem + BN + buf * Cfg::kACols;
+            const uint8_t *b0 = codes + buf * Cfg::kCodeBuf;
+            const int nkb = min(2, (K - c * 256 + 127) / 128);  // k blocks with data in this chunk
+            for (int b = 0; b < nkb; ++b) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f8f6f4_tmem_a(tmem, a0 + 32 * b + 8 * kk,
+                                      sdesc_kmajor_sw128(smem_u32(b0 + b * Cfg::kBlockB + 32 * kk)), idesc,
+                                      (c > 0 || b > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&done[buf]);
+            ++issued;
+        }
+    }
+    tc_fence_after();
+    if (__syncthreads_and(ok) && converter) {
+        // ---------------------------------------------------------------- epilogue
+        constexpr int kHalf = BN / 2;        // columns per warp
+        constexpr int kRowChunks = BN / 4;   // 16-byte chunks of a C row
+        uint8_t *tile = codes;               // [128][BN] int32, chunk index swizzled by row % 8
+        const int r = (warp & 3) * 32 + lane;
+        const int col0 = (warp >> 2) * kHalf;
+        const int base = 64 * K - 8 * (sumA[r] + sumA[kSmallRowsA + r]);
+        const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        uint32_t v[kHalf];
+        if constexpr (kHalf == 64) {
+            uint32_t (&v0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[0]);
+            uint32_t (&v1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[32]);
+            tmem_ld_32x32b_x32(trow + col0, v0);
+            tmem_ld_32x32b_x32(trow + col0 + 32, v1);
+            tmem_ld_wait_regs(v0, v1);
+        } else {
+            uint32_t (&v0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[0]);
+            tmem_ld_32x32b_x32(trow + col0, v0);
+            tmem_ld_wait_regs(v0);
+        }
+#pragma unroll
+        for (int q = 0; q < kHalf / 4; ++q) {
+            const int n = col0 + 4 * q;
+            const int4 sbv = *reinterpret_cast<const int4 *>(sumB + n);
+            int4 o;
+            o.x = __float2int_rn(__uint_as_float(v[4 * q + 0]) * 262144.0f) + base - 8 * sbv.x;
+            o.y = __float2int_rn(__uint_as_float(v[4 * q + 1]) * 262144.0f) + base - 8 * sbv.y;
+            o.z = __float2int_rn(__uint_as_float(v[4 * q + 2]) * 262144.0f) + base - 8 * sbv.z;
+            o.w = __float2int_rn(__uint_as_float(v[4 * q + 3]) * 262144.0f) + base - 8 * sbv.w;
+            const int chunk = (n >> 2) ^ (r & 7);
+            *reinterpret_cast<int4 *>(tile + r * (BN * 4) + (chunk << 4)) = o;
+        }
+        named_barrier_sync(1, kSmallConvThreads);
+        // write out: per instruction a warp covers 32 / kRowChunks whole rows
+        constexpr int kRowsPerInstr = 32 / kRowChunks;
+        const int q = lane % kRowChunks;
+        const int n = n0 + 4 * q;
+        const bool vec = (N & 3) == 0 && n + 4 <= N;
+        constexpr int kRowsPerWarp = kSmallRowsA / (kSmallConvThreads / 32);
+#pragma unroll 1
+        for (int rr = warp * kRowsPerWarp; rr < (warp + 1) * kRowsPerWarp; rr += kRowsPerInstr) {
+            const int row = rr + lane / kRowChunks, m = m0 + row;
+            const int4 o = *reinterpret_cast<const int4 *>(tile + row * (BN * 4) + ((q ^ (row & 7)) << 4));
+            if (m < M) {
+                int32_t *dst = C + static_cast<int64_t>(m) * N + n;
+                if (vec) {
+                    *reinterpret_cast<int4 *>(dst) = o;
+                } else {
+                    if (n + 0 < N) dst[0] = o.x;
+                    if (n + 1 < N) dst[1] = o.y;
+                    if (n + 2 < N) dst[2] = o.z;
+                    if (n + 3 < N) dst[3] = o.w;
+                }
+            }
+        }
+    }
+    // ---------------------------------------------------------------- teardown
+    // every MMA and every load of this CTA is done before TMEM and shared
+    // memory are given up (a CTA that gave up waits, bounded, for its last
+    // commit and its last loads of each raw slot)
+    if (mma_thread) {
+        const uint64_t t0 = globaltimer_ns();
+        if (issued > 0) {
+            const uint32_t c = issued - 1, use = c / NB;
+            while (!mbar_try_wait(&done[c - use * NB], use & 1u) && globaltimer_ns() - t0 < limit_ns) {
+            }
+        }
+        for (int c = loads - kSmallRaw < 0 ? 0 : loads - kSmallRaw; c < loads; ++c)
+            while (!mbar_try_wait(&full[c % kSmallRaw], (c / kSmallRaw) & 1u) && globaltimer_ns() - t0 < limit_ns) {
+            }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Cfg::kTmemCols);
+    }
+}
+
+template <int BN>
+static int launch_small(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return kCudaError;
+    {
+        static std::mutex mu;  // first calls from several threads
+        static bool attr_set[64] = {};
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && !attr_set[dev]) {
+            if (cudaFuncSetAttribute(igemm_small_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SmallCfg<BN>::kSmem) != cudaSuccess)
+                return kCudaError;
+            attr_set[dev] = true;
+        }
+    }
+    int *status = device_status_word();
+    if (!status) return kCudaError;
+    // packed rows, 128 bytes (one chunk) by 128 A rows (16-byte chunk j of row r
+    // stored at j ^ (r % 8)) or BN B rows (plain) per box
+    CUtensorMap mapA, mapB;
+    if (make_map(&mapA, CU_TENSOR_MAP_DATA_TYPE_UINT8, Ap, M, K / 2, kSmallRowsA, 128, CU_TENSOR_MAP_SWIZZLE_128B) !=
+            kOk ||
+        make_map(&mapB, CU_TENSOR_MAP_DATA_TYPE_UINT8, Bp, N, K / 2, BN, 128, CU_TENSOR_MAP_SWIZZLE_NONE) != kOk)
+        return kCudaError;
+    const dim3 grid((N + BN - 1) / BN, (M + kSmallRowsA - 1) / kSmallRowsA, 1);
+    const GemmEvents ev = take_gemm_events();
+    if (ev.start && cudaEventRecord(ev.start, stream) != cudaSuccess) return kCudaError;
+    igemm_small_kernel<BN><<<grid, kSmallThreads, SmallCfg<BN>::kSmem, stream>>>(mapA, mapB, C, M, N, K, status,
+                                                                                 watchdog_limit_ns());
+    note_launch();
+    if (ev.stop && cudaEventRecord(ev.stop, stream) != cudaSuccess) return kCudaError;
+    return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
+}
+
+int launch_i4i4_small(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, int bn,
+                      cudaStream_t stream)
+{
+    return bn == 64 ? launch_small<64>(Ap, Bp, C, M, N, K, stream) : launch_small<128>(Ap, Bp, C, M, N, K, stream);
+}
+
+}  // namespace igemm

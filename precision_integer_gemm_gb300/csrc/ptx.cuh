@@ -102,6 +102,12 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, con
     }
 }
 
+// Barrier `id` (1..15) over the first `count` threads of the CTA (a multiple of 32).
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y)
 {

@@ -45,9 +45,10 @@ def test_noalloc_rejects_bad_arguments_and_oversized_problems(lib):
     assert "32 MiB" in pig.igemm_strerror(pig.IGEMM_WORKSPACE_LIMIT)
 
 
-# (M, N, K): shapes i4i4_gemm sends through its in-kernel unpacking path (N <
-# 512), a ragged one with a K tail, one that fills half the array, a deep K
-# that the launch plan splits; then shapes that reach this kernel only through
+# (M, N, K): shapes i4i4_gemm sends through its small-product path (300 x 200)
+# or its in-kernel unpacking path (513 x 770, ragged, with a K tail; 128 x 128
+# with a deep K that the launch plan splits), one that fills half the array;
+# then shapes that reach this kernel only through
 # this entry point: a single row of A (the second CTA of a cluster has no rows
 # at all), 16 rows against a wide B, a row count just past and just below a
 # tile edge, N % 4 != 0 (scalar stores instead of bulk tensor stores) and N
