@@ -41,27 +41,31 @@
 // the eight lanes of a B store phase hit eight distinct bank groups).  Both
 // operands use the same order, which leaves every dot product unchanged.
 // Every wait is bounded (ptx.cuh).
+#include <type_traits>
 #include "launch.cuh"
 
 namespace igemm {
 
-constexpr int kSmallConvThreads = 256;                 // eight converting warps
-constexpr int kSmallThreads = kSmallConvThreads + 32;  // + the MMA warp
 constexpr int kSmallRowsA = 128;
-constexpr int kSmallRaw = 3;  // raw slots: chunks of packed rows loaded ahead
+constexpr int kSmallRaw = 3;     // raw slots: chunks of packed rows loaded ahead
+constexpr int kSmallAWarps = 8;  // A converters, then the epilogue
 
 template <int BN>
 struct SmallCfg {
-    static constexpr int kBRowsPerThread = BN / 32;
-    static constexpr int kBufs = 3;                         // code buffers
-    static constexpr int kACols = 64;                       // TMEM columns of one chunk of A codes
-    static constexpr int kTmemUsed = BN + kBufs * kACols;   // accumulator, then the A code buffers
+    static constexpr int kBWarps = 8;                          // B converters
+    static constexpr int kBPieces = BN / 32;                   // B pieces a thread converts per chunk
+    static constexpr int kConvWarps = kSmallAWarps + kBWarps;
+    static constexpr int kWarpMma = kConvWarps, kWarpProd = kConvWarps + 1;
+    static constexpr int kThreads = 32 * (kConvWarps + 2);
+    static constexpr int kBufs = 3;                            // code buffers
+    static constexpr int kACols = 64;                          // TMEM columns of one chunk of A codes
+    static constexpr int kTmemUsed = BN + kBufs * kACols;      // accumulator, then the A code buffers
     static constexpr int kTmemCols = kTmemUsed <= 256 ? 256 : 512;
-    static constexpr int kRawA = kSmallRowsA * 128;          // packed bytes of one chunk
+    static constexpr int kRawA = kSmallRowsA * 128;             // packed bytes of one chunk
     static constexpr int kRawStage = kRawA + BN * 128;
-    static constexpr int kBlockB = BN * 128;                 // one 128-k block of B codes
+    static constexpr int kBlockB = BN * 128;                    // one 128-k block of B codes
     static constexpr int kCodeBuf = 2 * kBlockB;
-    static constexpr int kStage = kSmallRowsA * BN * 4;      // the int32 tile, over the code buffers
+    static constexpr int kStage = kSmallRowsA * BN * 4;         // the int32 tile, over the code buffers
     static_assert(kStage <= kBufs * kCodeBuf, "epilogue tile fits over the code buffers");
     static constexpr int kSmem = 1024 + kBufs * kCodeBuf + kSmallRaw * kRawStage + 4 * (2 * kSmallRowsA + BN) +
                                  8 * (2 * kBufs + kSmallRaw) + 16;
@@ -134,12 +138,11 @@ __device__ __forceinline__ void small_a_codes(const uint8_t *raw_row, uint32_t s
 }
 
 template <int BN>
-__global__ void __launch_bounds__(kSmallThreads, 1)
+__global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1)
     igemm_small_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                        int32_t *__restrict__ C, int M, int N, int K, int *status, unsigned long long limit_ns)
 {
     using Cfg = SmallCfg<BN>;
-    constexpr int RB = Cfg::kBRowsPerThread;
     constexpr int NB = Cfg::kBufs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -154,13 +157,15 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool converter = warp < kSmallConvThreads / 32;
-    const bool mma_thread = warp == kSmallConvThreads / 32 && lane == 0;
+    const bool a_warp = warp < kSmallAWarps;
+    const bool b_warp = warp >= kSmallAWarps && warp < Cfg::kConvWarps;
+    const bool mma_thread = warp == Cfg::kWarpMma && lane == 0;
+    const bool producer = warp == Cfg::kWarpProd && lane == 0;
     const int m0 = blockIdx.y * kSmallRowsA, n0 = blockIdx.x * BN;
     const int kh = K / 2;  // packed bytes per row (a multiple of 16)
     const int nchunks = (K + 255) / 256;
 
-    // chunk c's packed rows into raw slot c % kSmallRaw (MMA thread)
+    // chunk c's packed rows into raw slot c % kSmallRaw (producer)
     auto load = [&](int c) {
         const int s = c % kSmallRaw;
         uint8_t *dst = raw + s * Cfg::kRawStage;
@@ -168,11 +173,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         tma_load_2d(dst, &mapA, &full[s], c * 128, m0);
         tma_load_2d(dst + Cfg::kRawA, &mapB, &full[s], c * 128, n0);
     };
-    if (mma_thread) {
+    if (producer) {
         tma_prefetch_map(&mapA);
         tma_prefetch_map(&mapB);
         for (int i = 0; i < NB; ++i) {
-            mbar_init(&conv[i], kSmallConvThreads / 32);
+            mbar_init(&conv[i], Cfg::kConvWarps);
             mbar_init(&done[i], 1);
         }
         for (int i = 0; i < kSmallRaw; ++i) mbar_init(&full[i], 1);
@@ -191,29 +196,33 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     const Watchdog wd{abort_flag, status, limit_ns};
 
     bool ok = true;
-    uint32_t issued = 0;   // commits issued (MMA thread)
-    int loads = 0;         // chunks whose loads were issued (MMA thread)
-    if (mma_thread) loads = min(kSmallRaw, nchunks);
+    uint32_t issued = 0;  // commits issued (MMA thread)
+    int loads = producer ? min(kSmallRaw, nchunks) : 0;  // chunks whose loads were issued (producer)
+    const bool tile_full = m0 + kSmallRowsA <= M && n0 + BN <= N;
 
-    if (converter) {
-        // A: row ra, k block kba (32 TMEM columns) of every chunk
-        const int quad = warp & 3, kba = warp >> 2;
+    if (a_warp || b_warp) {
+        // A warp w: row ra = 32 (w % 4) + lane, k block kba = w / 4 of every chunk,
+        // codes into TMEM.  B thread (g, p): bytes 16 p .. of rows g + 32 i,
+        // codes into shared memory at k block p / 4, chunks 2 (p % 4) and
+        // 2 (p % 4) + 1, the first of them taken by X in k block 0 and by Y in k
+        // block 1, the 16-byte chunk index swizzled by row % 8.
+        constexpr int kBStride = 4 * Cfg::kBWarps;  // 32
+        constexpr int PBT = Cfg::kBPieces;
+        const int quad = warp & 3, kba = (warp >> 2) & 1;
         const int ra = quad * 32 + lane;
         const bool a_ok = m0 + ra < M;
         const uint32_t a_tcol = tmem + (static_cast<uint32_t>(quad * 32) << 16) + BN + 32 * kba;
-        // B: thread (g, p) takes bytes 16 p .. of rows g + 32 i; where its two
-        // code chunks of a piece go: k block p / 4, chunks 2 (p % 4) and
-        // 2 (p % 4) + 1, the first of them taken by X in k block 0 and by Y in
-        // k block 1; the 16-byte chunk index is swizzled by row % 8
-        const int g = tid >> 3, p = tid & 7;
+        const int tb = tid - 32 * kSmallAWarps;
+        const int g = tb >> 3, p = tb & 7;
         const int kb = p >> 2;
         const int cx = 2 * (p & 3) + kb, cy = 2 * (p & 3) + 1 - kb;
-        bool b_ok[RB];
+        bool b_ok[PBT];
+        int sa = 0, sb[PBT];
 #pragma unroll
-        for (int i = 0; i < RB; ++i) b_ok[i] = n0 + g + 32 * i < N;
-        int sa = 0, sb[RB];
-#pragma unroll
-        for (int i = 0; i < RB; ++i) sb[i] = 0;
+        for (int i = 0; i < PBT; ++i) {
+            b_ok[i] = n0 + g + kBStride * i < N;
+            sb[i] = 0;
+        }
 #pragma unroll 1
         for (int c = 0; c < nchunks; ++c) {
             const int s = c % kSmallRaw, use = c / NB, buf = c - use * NB;
@@ -221,76 +230,101 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
             // the MMAs of chunk c - NB read this code buffer
             if (ok && use > 0) ok = __all_sync(0xffffffffu, wait_bounded(&done[buf], (use - 1) & 1u, wd));
             if (!ok) break;  // the whole warp
-            tc_fence_after();
             const uint8_t *slot = raw + s * Cfg::kRawStage;
             // pieces of this chunk inside K: bytes c * 128 + 16 j < kh
             const int left = (kh - c * 128) >> 4;  // > 0
-            {
-                uint32_t code[32];
-                const uint32_t vmask = a_ok ? (left >= 8 ? 0xFFu : ((1u << left) - 1u)) >> (4 * kba) : 0u;
-                if (kba == 0)
-                    small_a_codes<0>(slot + ra * 128, ra & 7, vmask, code, sa);
-                else
-                    small_a_codes<1>(slot + ra * 128, ra & 7, vmask, code, sa);
-                tmem_st_32x32b_x32(a_tcol + buf * Cfg::kACols, code);
-            }
-            const bool in = p < left;
-            uint8_t *bs = codes + buf * Cfg::kCodeBuf + kb * Cfg::kBlockB;
+            // FULL: every row of the tile and every piece of the chunk is inside
+            // the matrices (no code to clear; the same for the whole CTA)
+            auto convert = [&](auto full_tag) {
+                constexpr bool FULL = decltype(full_tag)::value;
+                if (a_warp) {
+                    tc_fence_after();  // the MMAs that read this TMEM buffer are done
+                    uint32_t code[32];
+                    const uint32_t vmask =
+                        FULL ? 0xFu : a_ok ? (left >= 8 ? 0xFFu : ((1u << left) - 1u)) >> (4 * kba) : 0u;
+                    if (kba == 0)
+                        small_a_codes<0>(slot + ra * 128, ra & 7, vmask, code, sa);
+                    else
+                        small_a_codes<1>(slot + ra * 128, ra & 7, vmask, code, sa);
+                    tmem_st_32x32b_x32(a_tcol + buf * Cfg::kACols, code);
+                    tmem_st_wait();
+                    tc_fence_before();
+                } else {
+                    const bool in = FULL || p < left;
+                    uint8_t *bs = codes + buf * Cfg::kCodeBuf + kb * Cfg::kBlockB;
 #pragma unroll
-            for (int i = 0; i < RB; ++i) {
-                const int r = g + 32 * i, sw = r & 7;
-                const uint4 x = *reinterpret_cast<const uint4 *>(slot + Cfg::kRawA + r * 128 + 16 * p);
-                uint8_t *row = bs + r * 128;
-                small_piece(x, in && b_ok[i], row + ((cx ^ sw) << 4), row + ((cy ^ sw) << 4), sb[i]);
-            }
-            tmem_st_wait();
-            fence_proxy_async_smem();  // generic writes, read next by the tensor core
-            tc_fence_before();
+                    for (int i = 0; i < PBT; ++i) {
+                        const int r = g + kBStride * i, sw = r & 7;
+                        const uint4 x = *reinterpret_cast<const uint4 *>(slot + Cfg::kRawA + r * 128 + 16 * p);
+                        uint8_t *row = bs + r * 128;
+                        small_piece(x, FULL || (in && b_ok[i]), row + ((cx ^ sw) << 4), row + ((cy ^ sw) << 4),
+                                    sb[i]);
+                    }
+                    fence_proxy_async_smem();  // generic writes, read next by the tensor core
+                }
+            };
+            if (tile_full && left >= 8)
+                convert(std::true_type{});
+            else
+                convert(std::false_type{});
             __syncwarp();
             if (lane == 0) mbar_arrive(&conv[buf]);
         }
-        // the last chunk's commit covers every MMA before it
-        if (ok) {
-            const int c = nchunks - 1, use = c / NB;
-            ok = wait_bounded(&done[c - use * NB], use & 1u, wd);
-        }
-        sumA[kba * kSmallRowsA + ra] = sa;
-        // B row sums: the eight lanes of a row hold one partial sum each
+        if (a_warp) {
+            // the last chunk's commit covers every MMA before it
+            if (ok) {
+                const int c = nchunks - 1, use = c / NB;
+                ok = wait_bounded(&done[c - use * NB], use & 1u, wd);
+            }
+            sumA[kba * kSmallRowsA + ra] = sa;
+        } else {
+            // B row sums: the eight lanes of a row hold one partial sum each
 #pragma unroll
-        for (int i = 0; i < RB; ++i) {
-            int v = sb[i];
-            v += __shfl_xor_sync(0xffffffffu, v, 1);
-            v += __shfl_xor_sync(0xffffffffu, v, 2);
-            v += __shfl_xor_sync(0xffffffffu, v, 4);
-            if (p == 0) sumB[g + 32 * i] = v;
+            for (int i = 0; i < PBT; ++i) {
+                int v = sb[i];
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                if (p == 0) sumB[g + kBStride * i] = v;
+            }
         }
     } else if (mma_thread) {
         // ---------------------------------------------------------------- MMA thread
         constexpr uint32_t idesc = idesc_e4m3_f32(kSmallRowsA, BN);
+        // B descriptors differ only in the start-address field (address >> 4)
+        const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(codes));
 #pragma unroll 1
         for (int c = 0; c < nchunks; ++c) {
             const int use = c / NB, buf = c - use * NB;
-            ok = wait_bounded(&conv[buf], use & 1u, wd);
+            ok = wait_spin_bounded(&conv[buf], use & 1u, wd);
             if (!ok) break;
-            // chunk c is converted: its raw slot takes chunk c + kSmallRaw
-            if (loads < nchunks) load(loads++);
             tc_fence_after();
             const uint32_t a0 = tmem + BN + buf * Cfg::kACols;
-            const uint8_t *b0 = codes + buf * Cfg::kCodeBuf;
+            const uint64_t b0 = bdesc0 + static_cast<uint64_t>((buf * Cfg::kCodeBuf) >> 4);
             const int nkb = min(2, (K - c * 256 + 127) / 128);  // k blocks with data in this chunk
             for (int b = 0; b < nkb; ++b) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_f8f6f4_tmem_a(tmem, a0 + 32 * b + 8 * kk,
-                                      sdesc_kmajor_sw128(smem_u32(b0 + b * Cfg::kBlockB + 32 * kk)), idesc,
+                                      b0 + static_cast<uint64_t>((b * Cfg::kBlockB + 32 * kk) >> 4), idesc,
                                       (c > 0 || b > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit(&done[buf]);
             ++issued;
         }
+    } else if (producer) {
+        // ---------------------------------------------------------------- TMA producer
+        // chunk c converted: its raw slot takes chunk c + kSmallRaw
+#pragma unroll 1
+        for (int c = 0; loads < nchunks; ++c) {
+            const int use = c / NB;
+            ok = wait_bounded(&conv[c - use * NB], use & 1u, wd);
+            if (!ok) break;
+            load(loads++);
+        }
     }
     tc_fence_after();
-    if (__syncthreads_and(ok) && converter) {
+    if (__syncthreads_and(ok) && a_warp) {
         // ---------------------------------------------------------------- epilogue
         constexpr int kHalf = BN / 2;        // columns per warp
         constexpr int kRowChunks = BN / 4;   // 16-byte chunks of a C row
@@ -323,13 +357,13 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
             const int chunk = (n >> 2) ^ (r & 7);
             *reinterpret_cast<int4 *>(tile + r * (BN * 4) + (chunk << 4)) = o;
         }
-        named_barrier_sync(1, kSmallConvThreads);
+        named_barrier_sync(1, 32 * kSmallAWarps);
         // write out: per instruction a warp covers 32 / kRowChunks whole rows
         constexpr int kRowsPerInstr = 32 / kRowChunks;
         const int q = lane % kRowChunks;
         const int n = n0 + 4 * q;
         const bool vec = (N & 3) == 0 && n + 4 <= N;
-        constexpr int kRowsPerWarp = kSmallRowsA / (kSmallConvThreads / 32);
+        constexpr int kRowsPerWarp = kSmallRowsA / kSmallAWarps;
 #pragma unroll 1
         for (int rr = warp * kRowsPerWarp; rr < (warp + 1) * kRowsPerWarp; rr += kRowsPerInstr) {
             const int row = rr + lane / kRowChunks, m = m0 + row;
@@ -351,13 +385,14 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     // every MMA and every load of this CTA is done before TMEM and shared
     // memory are given up (a CTA that gave up waits, bounded, for its last
     // commit and its last loads of each raw slot)
-    if (mma_thread) {
+    if (mma_thread && issued > 0) {
         const uint64_t t0 = globaltimer_ns();
-        if (issued > 0) {
-            const uint32_t c = issued - 1, use = c / NB;
-            while (!mbar_try_wait(&done[c - use * NB], use & 1u) && globaltimer_ns() - t0 < limit_ns) {
-            }
+        const uint32_t c = issued - 1, use = c / NB;
+        while (!mbar_try_wait(&done[c - use * NB], use & 1u) && globaltimer_ns() - t0 < limit_ns) {
         }
+    }
+    if (producer) {
+        const uint64_t t0 = globaltimer_ns();
         for (int c = loads - kSmallRaw < 0 ? 0 : loads - kSmallRaw; c < loads; ++c)
             while (!mbar_try_wait(&full[c % kSmallRaw], (c / kSmallRaw) & 1u) && globaltimer_ns() - t0 < limit_ns) {
             }
@@ -398,7 +433,7 @@ static int launch_small(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M,
     const dim3 grid((N + BN - 1) / BN, (M + kSmallRowsA - 1) / kSmallRowsA, 1);
     const GemmEvents ev = take_gemm_events();
     if (ev.start && cudaEventRecord(ev.start, stream) != cudaSuccess) return kCudaError;
-    igemm_small_kernel<BN><<<grid, kSmallThreads, SmallCfg<BN>::kSmem, stream>>>(mapA, mapB, C, M, N, K, status,
+    igemm_small_kernel<BN><<<grid, SmallCfg<BN>::kThreads, SmallCfg<BN>::kSmem, stream>>>(mapA, mapB, C, M, N, K, status,
                                                                                  watchdog_limit_ns());
     note_launch();
     if (ev.stop && cudaEventRecord(ev.stop, stream) != cudaSuccess) return kCudaError;

@@ -71,6 +71,20 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
     return ok != 0;
 }
 
+// Non-blocking test of phase `parity` (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Shared state of the bounded waits of one CTA.  `abort_flag` lives in shared
 // memory: once any wait of the CTA times out, every other wait returns false
 // at its next check, so all roles drain to the teardown.
@@ -106,6 +120,26 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, con
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Like wait_bounded, but polling without suspending the thread: for a thread
+// on the critical path whose waits are short (it reacts to the phase change
+// within tens of cycles instead of being woken up later).
+__device__ __forceinline__ bool wait_spin_bounded(uint64_t *bar, uint32_t parity, const Watchdog &wd)
+{
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*wd.abort_flag) return false;
+            if (globaltimer_ns() - t0 > wd.limit_ns) {
+                *wd.abort_flag = 1;
+                atomicCAS(wd.status, 0, kStatusTimeout);
+                return false;
+            }
+        }
+    }
 }
 
 // ---------------------------------------------------------------- TMA
