@@ -40,20 +40,22 @@ static bool use_codes_i4i4(int M, int N)
 
 // Output-tile width of the small-product kernel for this shape, 0 if another
 // path is faster.  Its CTAs run one tile each with no split of K, so it wins
-// while the tiles fit about one wave of SMs.  Measured on GB300 (call time,
-// L2 flushed; other path in parentheses): 1024^3 10.9 us with 64-wide tiles
-// (19.1), 512 x 4096 x 4096 23.2 us with 128-wide tiles (34.4), 1536^3 15.0
-// (19.1), 2048 x 2048 x 512 17.1 (22.2, two waves of 128-wide tiles), 1024 x
-// 1024 x 8192 31.4 (33.4); it loses at 2048^3 (27.3 vs 26.3) and 4096 x 4096
-// x 1024 (56 vs 45).  Few tiles with a long K go to the paths that split K.
+// while the tiles fill a few waves of SMs and K is not long for their number.
+// Measured on GB300 (call time, L2 flushed; the other paths in parentheses):
+// 1024^3 10.9 us on 64-wide tiles (19.1), 1024 x 1024 x 8192 27.3 (33.4);
+// 128-wide tiles: 1536^3 12.9 (19.1), 2048 x 2048 x 1024 19.1 (24.3), 2048^3
+// 23.2 (27.3), 2560 x 2560 x 1024 25.2 (31.4), 1024 x 8192 x 1024 31.4 (35.6),
+// 256 x 8192 x 8192 31.4 (41.6); it loses at 2048 x 2048 x 4096 (35.5 vs
+// 31.5), 4096 x 4096 x 1024 (49.8 vs 44.8), 640 x 640 x 8192 (27.3 vs 22.4)
+// and 1024 x 1024 x 16384 (45.7 vs 41.6), where the other paths split K.
 static int small_tile_width(int M, int N, int K)
 {
     const int64_t sms = sm_count();
     const int64_t rows = (M + 127) / 128;
     const int64_t t64 = rows * ((N + 63) / 64), t128 = rows * ((N + 127) / 128);
-    if (t64 <= sms && (K <= 4096 || 2 * t64 >= sms)) return 64;
-    if (t128 <= sms && K <= 4096) return 128;
-    if (t128 <= 2 * sms && K <= 1024) return 128;
+    if (t64 <= sms && (K <= 4096 || (K <= 8192 && 2 * t64 >= sms))) return 64;
+    if (t128 <= sms && (K <= 4096 || (K <= 8192 && 2 * t128 >= sms))) return 128;
+    if (t128 <= 4 * sms && K <= 2048) return 128;
     return 0;
 }
 

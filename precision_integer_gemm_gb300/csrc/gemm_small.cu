@@ -7,31 +7,32 @@
 // At these sizes a call is bound by latency, not by any throughput: the
 // prepared-codes path pays a second launch and a round trip through memory,
 // the warp-specialised kernels several hand-overs per stage.  This kernel is
-// one launch with one CTA per 128 x BN output tile: eight converting warps and
-// one MMA warp.
+// one launch with one CTA per 128 x BN output tile (BN = 64 or 128): eight A
+// converting warps (then the epilogue), eight B converting warps, one MMA
+// warp and one producer warp.
 //
-//  * the CTA walks K in chunks of 256 k (128 packed bytes per row).  The MMA
-//    thread loads each chunk's packed A and B rows with two TMA boxes (128
-//    bytes x 128 and x BN rows) into a ring of three raw slots, refilling a
-//    slot as soon as its chunk is converted; rows past M or N and bytes past
+//  * the CTA walks K in chunks of 256 k (128 packed bytes per row).  The
+//    producer thread loads each chunk's packed A and B rows with two TMA boxes
+//    (128 bytes x 128 and x BN rows) into a ring of three raw slots, refilling
+//    a slot as soon as its chunk is converted; rows past M or N and bytes past
 //    K arrive as zeros;
-//  * eight converting warps turn every nibble v into the e4m3 code
-//    u = v + 8 (value u * 2^-9, exact) and sum the codes per row (dp4a).
-//    A codes go to tensor memory: warp w converts k block w / 4 of the chunk
-//    (four 16-byte pieces) for A rows 32 (w % 4) .. 32 (w % 4) + 31, one row
-//    per thread, and stores them with tcgen05.st.  B codes go to a
-//    128-byte-swizzled K-major tile in shared memory: thread (g, p) =
-//    (tid / 8, tid % 8) converts bytes 16 p .. 16 p + 15 of B rows g + 32 i, so
+//  * the converting warps turn every nibble v into the e4m3 code u = v + 8
+//    (value u * 2^-9, exact) and sum the codes per row (dp4a).  A codes go to
+//    tensor memory: A warp w converts k block w / 4 of the chunk (four
+//    16-byte pieces) for A rows 32 (w % 4) .. 32 (w % 4) + 31, one row per
+//    thread, and stores them with tcgen05.st.  B codes go to a
+//    128-byte-swizzled K-major tile in shared memory: B thread (g, p) =
+//    (t / 8, t % 8) converts bytes 16 p .. 16 p + 15 of B rows g + 32 i, so
 //    eight lanes share a row.  Codes past K and rows past M or N are 0.  Each
 //    warp then arrives on the code buffer's mbarrier;
-//  * the MMA thread waits for the eight arrivals, issues the chunk's
-//    tcgen05.mma (A from tensor memory, B from shared memory, M = 128,
-//    N = BN, f32 accumulator in TMEM, exact: every partial sum is an integer
-//    times 2^-18 below 2^24 * 2^-18 for K <= 65536) and commits to the
+//  * the MMA thread waits (polling) for the sixteen arrivals, issues the
+//    chunk's tcgen05.mma (A from tensor memory, B from shared memory,
+//    M = 128, N = BN, f32 accumulator in TMEM, exact: every partial sum is an
+//    integer times 2^-18 below 2^24 * 2^-18 for K <= 65536) and commits to the
 //    buffer's second mbarrier; three code buffers let the converters run
 //    ahead of the MMAs;
-//  * the epilogue reads the accumulator (warp w: TMEM lanes 32 (w % 4), half
-//    w / 4 of the columns), restores the signed result
+//  * the epilogue (the A warps) reads the accumulator (warp w: TMEM lanes
+//    32 (w % 4), half w / 4 of the columns), restores the signed result
 //    C = S - 8 sum uA - 8 sum uB + 64 K, stages the tile in shared memory and
 //    writes it out row by row (coalesced 16-byte stores).
 //

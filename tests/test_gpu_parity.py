@@ -135,10 +135,14 @@ def test_i4i4_matches_oracle(orc, M, N, K):
 # end inside a 256-k chunk (96, 160, 1056, 4128), ragged M and N, N % 4 != 0
 # (per-element stores), 128-wide tiles (1024 x 2048, 1536^3), two waves of
 # them (2048 x 2048 x 512) and a long K on 64-wide tiles (8192 = 32 chunks,
-# the three raw slots and code buffers reused many times).
+# the three raw slots and code buffers reused many times); 128-wide tiles in
+# up to four waves (2560^2, 1030 x 8190 with ragged edges and N % 4 != 0) and
+# one wave of them with K = 8192.
 SMALL_PATH_I4I4 = [(65, 64, 32), (128, 64, 256), (129, 257, 96), (200, 130, 32), (300, 200, 1056),
                    (130, 1000, 160), (512, 512, 512), (1024, 2048, 1024), (1536, 1536, 1536), (2048, 2048, 512),
-                   (1024, 1024, 8192), (640, 1030, 4128)]
+                   (1024, 1024, 8192), (640, 1030, 4128),
+                   # 128-wide tiles in up to four waves, and one wave with a long K
+                   (2560, 2560, 1024), (1030, 8190, 544), (256, 8192, 8192)]
 
 
 @pytest.mark.parametrize("M,N,K", SMALL_PATH_I4I4)
@@ -152,7 +156,7 @@ def test_i4i4_small_product_path(orc, M, N, K):
 # Shapes that none of the other paths take (more tiles than the small-product
 # kernel runs in a wave, too few rows for the prepared codes; few tiles with a
 # K long enough to split): the in-kernel unpack path.
-TC_I4I4 = [(300, 20000, 256), (200, 300, 16384), (300, 9000, 1056)]
+TC_I4I4 = [(300, 40000, 256), (200, 300, 16384), (300, 9000, 4128)]
 
 
 @pytest.mark.parametrize("M,N,K", TC_I4I4)
@@ -181,7 +185,7 @@ def test_w4a8_matches_oracle(orc, M, N, K):
 # bulk tensor stores), a split K, and tile counts above the CTA pairs, whose
 # last tiles run as k pieces (W4A8 1030 x 4100 / 4102 x 4160, 1024 x 4096 x
 # 65536).  Whole C, element by element.
-CODES_I4I4 = [(4096, 2048, 32), (4100, 2056, 96), (2049, 2050, 1056), (4096, 2050, 128), (2048, 2048, 16384),
+CODES_I4I4 = [(8192, 2048, 32), (8200, 2056, 96), (2049, 2050, 4128), (8192, 2050, 128), (2048, 2048, 16384),
               (1024, 4100, 8224),
               # more tiles than CTA pairs: the last tiles run as k pieces added into C
               # (N % 4 != 0: scalar atomic adds)
@@ -485,8 +489,9 @@ def test_decode_workload_whole_c(orc):
 @pytest.mark.parametrize("K", [32, 8192, 65536])
 @pytest.mark.parametrize("av,bv", [(-8, -8), (7, 7), (-8, 7), (7, -8)])
 def test_i4i4_extreme_constants(orc, K, av, bv):
-    # skinny, small-product (130 x 260 at K = 32, 1024 x 1024), in-kernel and
-    # (K <= 8192) prepared-codes paths
+    # skinny, small-product (130 x 260 at K = 32; 1024 x 1024 up to K = 8192,
+    # 2048 x 2048 at K = 32), in-kernel and (2048 x 2048 at K = 8192)
+    # prepared-codes paths
     for M, N in ((16, 260), (32, 260), (64, 260), (130, 260), (1024, 1024)) + (((2048, 2048),) if K <= 8192 else ()):
         a = np.full((M, K), av, dtype=np.int8)
         b = np.full((N, K), bv, dtype=np.int8)
@@ -592,10 +597,10 @@ def test_split_path_is_deterministic(orc):
 def test_kernel_launch_counter():
     # the prepared-codes path launches the preparation pass and the GEMM, the
     # small-product path one kernel; rejected and empty calls none
-    a = torch.zeros((4096, 64), dtype=torch.uint8, device="cuda")
-    C = torch.empty((4096, 2048), dtype=torch.int32, device="cuda")
+    a = torch.zeros((8192, 64), dtype=torch.uint8, device="cuda")
+    C = torch.empty((8192, 2048), dtype=torch.int32, device="cuda")
     n0 = pig.igemm_kernels_launched()
-    pig.i4i4_gemm(a, a, C, 4096, 2048, 128)
+    pig.i4i4_gemm(a, a, C, 8192, 2048, 128)
     n1 = pig.igemm_kernels_launched()
     pig.i4i4_gemm(a, a, C, 100, 100, 128)
     n2 = pig.igemm_kernels_launched()
@@ -636,7 +641,7 @@ def test_gemm_kernel_timing_hook():
 def test_concurrent_streams_keep_their_workspaces_apart(orc):
     # two prepared-codes GEMMs on two streams at once: each call's workspace is
     # allocated and released in its own stream's order, so neither sees the other's codes
-    shapes = [(4096, 2048, 256), (4352, 2048, 512)]
+    shapes = [(8192, 2048, 256), (8704, 2048, 512)]
     runs = []
     for i, (M, N, K) in enumerate(shapes):
         a = si.int4_values(17000 + i, (M, K))
