@@ -41,8 +41,12 @@
  *   K == 0 with M, N > 0 sets C to zero.
  *   K % 32 == 0 for the integer GEMMs (a packed row is a whole number of
  *   16-byte units, the TMA row-pitch rule) else IGEMM_UNSUPPORTED_SHAPE.
- *   K <= 65536 else IGEMM_OVERFLOW_BOUND: the accumulation is exact only up to
- *   this depth (the int32 result itself would fit far beyond it).
+ *   K <= 33554431 (int4 x int4: |a b| <= 64, so |C| <= 64 K < 2^31) or
+ *   K <= 2097151 (W4A8: |a b| <= 1024) else IGEMM_OVERFLOW_BOUND, the int32
+ *   range of the result.  One f32 MMA accumulation is exact over at most
+ *   65536 k; a longer K runs on the prepared-codes path in pieces of at most
+ *   65536 k whose exact int32 results add into C (its workspace then holds
+ *   (M + N) * K, or N * K + 2 * M * K, bytes of codes).
  *   Every non-empty operand base address and C must be 16-byte aligned, else
  *   IGEMM_MISALIGNED.
  */
@@ -67,7 +71,7 @@ typedef enum igemm_status {
     IGEMM_INVALID_ARGUMENT = 1,  /* null pointer for a non-empty operand, negative size */
     IGEMM_UNSUPPORTED_SHAPE = 2, /* K % 32 != 0 (GEMM); odd K (pack_int4) */
     IGEMM_MISALIGNED = 3,        /* a base address is not 16-byte aligned */
-    IGEMM_OVERFLOW_BOUND = 4,    /* K above the exact-accumulation bound (65536) */
+    IGEMM_OVERFLOW_BOUND = 4,    /* K above the int32 bound (33554431 int4 x int4, 2097151 W4A8) */
     IGEMM_CUDA_ERROR = 5,        /* tensor-map encoding, memset or launch failed */
     IGEMM_DEVICE_TIMEOUT = 6,    /* a kernel's bounded wait expired (see igemm_last_status) */
     IGEMM_WORKSPACE_LIMIT = 7    /* i4i4_gemm_noalloc: the problem needs more than its fixed workspace */
@@ -144,8 +148,9 @@ IGEMM_API int w4a8_gemm(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, i
  *   Ap / A  [M, K/2] packed int4 / [M, K] int8 (host), read only
  *   Bp      [N, K/2] packed int4 (host), read only
  *   C       [M, N] int32 (host), written
- * Rules as for i4i4_gemm / w4a8_gemm (K % 32 == 0, K <= 65536, empty shapes
- * are no-ops, K == 0 zeroes C), except that host pointers need no alignment.
+ * Rules as for i4i4_gemm / w4a8_gemm (K % 32 == 0, the same K bounds, empty
+ * shapes are no-ops, K == 0 zeroes C), except that host pointers need no
+ * alignment.
  * igemm_time_next_gemm times the GEMM kernel of the first chunk only.  A CUDA
  * error after the first chunk was enqueued (IGEMM_CUDA_ERROR) leaves the earlier
  * chunks' work in the streams; the call still joins its copy streams to

@@ -309,15 +309,15 @@ static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 using namespace igemm;
 
-static int gemm_common_checks(const void *a, const void *b, int32_t *C, int M, int N, int K, cudaStream_t stream,
-                              bool *done)
+static int gemm_common_checks(const void *a, const void *b, int32_t *C, int M, int N, int K, int max_k,
+                              cudaStream_t stream, bool *done)
 {
     *done = true;
     if (M < 0 || N < 0 || K < 0) return kInvalidArgument;
     if (M == 0 || N == 0) return kOk;
     if (!C) return kInvalidArgument;
     if (K % 32 != 0) return kUnsupportedShape;
-    if (K > kMaxK) return kOverflowBound;
+    if (K > max_k) return kOverflowBound;
     if (!aligned16(C)) return kMisaligned;
     if (K == 0) {
         return cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 4, stream) == cudaSuccess ? kOk : kCudaError;
@@ -332,7 +332,7 @@ extern "C" int i4i4_gemm(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M
                          cudaStream_t stream)
 {
     bool done;
-    const int rc = gemm_common_checks(Ap, Bp, C, M, N, K, stream, &done);
+    const int rc = gemm_common_checks(Ap, Bp, C, M, N, K, kMaxKI4I4, stream, &done);
     if (done) return rc;
     return launch_i4i4(Ap, Bp, C, M, N, K, stream);
 }
@@ -341,7 +341,7 @@ extern "C" int w4a8_gemm(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, 
                          cudaStream_t stream)
 {
     bool done;
-    const int rc = gemm_common_checks(A, Bp, C, M, N, K, stream, &done);
+    const int rc = gemm_common_checks(A, Bp, C, M, N, K, kMaxKW4A8, stream, &done);
     if (done) return rc;
     return launch_w4a8(A, Bp, C, M, N, K, stream);
 }
@@ -350,7 +350,7 @@ extern "C" int i4i4_gemm_noalloc(const uint8_t *Ap, const uint8_t *Bp, int32_t *
                                  cudaStream_t stream)
 {
     bool done;
-    const int rc = gemm_common_checks(Ap, Bp, C, M, N, K, stream, &done);
+    const int rc = gemm_common_checks(Ap, Bp, C, M, N, K, kMaxKI4I4, stream, &done);
     if (done) return rc;
     return launch_i4i4_noalloc(Ap, Bp, C, M, N, K, stream);
 }
@@ -362,7 +362,7 @@ extern "C" int w4a8_gemm_scaled(const int8_t *A, const uint8_t *Bp, const float 
     if (M == 0 || N == 0) return kOk;
     if (!C || !scale_a || !scale_b) return kInvalidArgument;
     if (K % 32 != 0) return kUnsupportedShape;
-    if (K > kMaxK) return kOverflowBound;
+    if (K > kMaxKW4A8) return kOverflowBound;
     if (!aligned16(C) || !aligned16(scale_a) || !aligned16(scale_b)) return kMisaligned;
     if (K == 0) return cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 2, stream) == cudaSuccess ? kOk : kCudaError;
     if (!A || !Bp) return kInvalidArgument;
@@ -502,7 +502,7 @@ extern "C" const char *igemm_strerror(int code)
         return "unsupported shape (integer GEMMs: K must be a multiple of 32; fp8_gemm: of 16; pack_int4 and "
                "unpack_int4: K must be even)";
     case kMisaligned: return "misaligned pointer (operand and C base addresses must be 16-byte aligned)";
-    case kOverflowBound: return "K above the exact-accumulation bound (65536)";
+    case kOverflowBound: return "K above the int32 bound of the result (33554431 int4 x int4, 2097151 W4A8)";
     case kCudaError: return "CUDA error (tensor-map encoding, memset, launch or synchronization failed)";
     case kDeviceTimeout: return "device timeout (a kernel's bounded pipeline wait expired; its output is not valid)";
     case kWorkspaceLimit:

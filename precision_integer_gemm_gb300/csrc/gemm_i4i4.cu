@@ -100,6 +100,9 @@ SkinnyPlan skinny_plan_i4i4(int M, int N, int K, int sms, int pairs, int quads)
 
 int launch_i4i4(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
 {
+    // K past one exact f32 accumulation: the prepared-codes path, whose plan
+    // cuts K into pieces of at most 65536 that add into C as int32
+    if (K > kMaxK) return run_i4i4_codes(Ap, Bp, C, M, N, K, stream);
     // few rows of A (decode-like): B streamed once, A's codes resident (no
     // skinny plan fits only on parts with fewer SMs than k slices needed: those
     // shapes take the other paths)

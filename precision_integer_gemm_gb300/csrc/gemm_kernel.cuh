@@ -55,7 +55,11 @@ namespace igemm {
 
 constexpr int kBK = 128;       // k values per pipeline stage
 constexpr int kPRows = 128;    // MMA M
-constexpr int kMaxK = 65536;   // exactness bound of the f32 accumulation
+constexpr int kMaxK = 65536;   // exactness bound of one f32 accumulation (longer K runs as pieces)
+// Spec bounds on K (the int32 result cannot overflow): |a b| <= 64 (int4 x
+// int4) or 1024 (W4A8), so |C| <= 64 K < 2^31 and 1024 K < 2^31
+constexpr int kMaxKI4I4 = 33554431;
+constexpr int kMaxKW4A8 = 2097151;
 constexpr int kAStageCols = kBK / 4;
 constexpr uint32_t kOnes = 0x01010101u;  // four e4m3 codes of value 1 (x 2^-9)
 

@@ -415,7 +415,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             if constexpr (!Cfg::kW4A8) {
                 // C[m, n] = S - 8 sum uA[m] - 8 sum uB[n] + 64 K   (first split adds the terms)
                 const int m = x.p0 + p;
-                const uint32_t rowterm = static_cast<uint32_t>(first ? 64 * prm.K - 8 * sp : 0) -
+                // (in unsigned arithmetic: the terms can pass 2^31 for long K while C
+                // itself stays in range, and int32 results wrap the same way)
+                const uint32_t rowterm = (first ? 64u * static_cast<uint32_t>(prm.K) - 8u * static_cast<uint32_t>(sp)
+                                                : 0u) -
                                          (magic ? kSsMagic : 0u);
 #pragma unroll 1
                 for (int c0 = 0; c0 < Cfg::kQRows; c0 += 32) {
@@ -434,8 +437,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const int i = 4 * j + e;
-                                v[i] = (magic ? ss_magic(v[i]) : static_cast<uint32_t>(ss_exact(v[i]))) + rowterm +
-                                       static_cast<uint32_t>(-8 * qq[e]);
+                                v[i] = (magic ? ss_magic(v[i]) : static_cast<uint32_t>(ss_exact(v[i]))) + rowterm -
+                                       8u * static_cast<uint32_t>(qq[e]);
                             }
                         }
                     }  // else: v holds the float32 sums, stored as they are
@@ -475,7 +478,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 // C[m, n] for n = this thread's weight row, m = q0 + j, staged as [m][n] boxes:
                 // C = 16 S_h + S_l - 8 sum a[m] - 128 sum ub[n]
                 const int n = x.p0 + p;
-                const uint32_t colterm = static_cast<uint32_t>(-128 * sp) - (magic ? 17u * kSsMagic : 0u);
+                const uint32_t colterm = 0u - 128u * static_cast<uint32_t>(sp) - (magic ? 17u * kSsMagic : 0u);
                 constexpr int kChunk = Cfg::kStageRows;
                 int *sbi = reinterpret_cast<int *>(stg);
 #pragma unroll 1
@@ -503,7 +506,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                                     val = 16u * ss_magic(vh[i]) + ss_magic(vl[i]);
                                 else
                                     val = static_cast<uint32_t>(16 * ss_exact(vh[i]) + ss_exact(vl[i]));
-                                val += colterm + static_cast<uint32_t>(-8 * qq[e]);
+                                val += colterm - 8u * static_cast<uint32_t>(qq[e]);
                                 if (prm.tma_store) {
                                     sbi[(h + i) * 32 + lane] = static_cast<int>(val);
                                 } else {

@@ -92,6 +92,9 @@ SkinnyPlan skinny_plan_w4a8(int M, int N, int K, int sms, int pairs, int quads)
 int launch_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
 {
     const uint8_t *a = reinterpret_cast<const uint8_t *>(A);
+    // K past one exact f32 accumulation: the prepared-codes path, whose plan
+    // cuts K into pieces of at most 65536 that add into C as int32
+    if (K > kMaxK) return run_w4a8_codes(A, Bp, C, M, N, K, stream);
     // (no skinny plan fits only on parts with fewer SMs than k slices needed:
     // those shapes take the other paths)
     if (M <= 64) {

@@ -211,7 +211,7 @@ extern "C" int i4i4_gemm_host(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, 
                               cudaStream_t stream)
 {
     bool done;
-    const int rc = host_checks(Ap, Bp, C, M, N, K, 32, kMaxK, &done);
+    const int rc = host_checks(Ap, Bp, C, M, N, K, 32, kMaxKI4I4, &done);
     if (done) return rc;
     const HostGemm g{size_t(K) / 2, 0, size_t(N) * (size_t(K) / 2), 0, size_t(N) * 4, gemm_i4i4_dev};
     return run_host(g, Ap, Bp, nullptr, nullptr, reinterpret_cast<uint8_t *>(C), M, N, K, stream);
@@ -221,7 +221,7 @@ extern "C" int w4a8_gemm_host(const int8_t *A, const uint8_t *Bp, int32_t *C, in
                               cudaStream_t stream)
 {
     bool done;
-    const int rc = host_checks(A, Bp, C, M, N, K, 32, kMaxK, &done);
+    const int rc = host_checks(A, Bp, C, M, N, K, 32, kMaxKW4A8, &done);
     if (done) return rc;
     const HostGemm g{size_t(K), 0, size_t(N) * (size_t(K) / 2), 0, size_t(N) * 4, gemm_w4a8_dev};
     return run_host(g, reinterpret_cast<const uint8_t *>(A), Bp, nullptr, nullptr, reinterpret_cast<uint8_t *>(C), M,

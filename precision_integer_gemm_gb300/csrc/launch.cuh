@@ -216,7 +216,18 @@ int ss_plan(int M, int N, int K, int p_rows, int q_rows, int64_t operand_bytes, 
     pl->kb_total = (K + Cfg::kBK - 1) / Cfg::kBK;
     const int tiles = pl->p_slots * pl->q_tiles;
     // the split plan counts cluster units against the clusters that fit at once
-    const Plan plan = plan_units(tiles, pl->kb_total, int64_t(M) * N * 4, operand_bytes, W);
+    Plan plan = plan_units(tiles, pl->kb_total, int64_t(M) * N * 4, operand_bytes, W);
+    if constexpr (!Cfg::kFloat) {
+        // an integer unit's f32 accumulator is exact over at most kMaxK k: longer
+        // K runs as more splits (pieces of whole stages), whose int32 results
+        // add into C
+        constexpr int kMaxKb = kMaxK / Cfg::kBK;
+        if (plan.kb_per_split > kMaxKb) {
+            const int s = (pl->kb_total + kMaxKb - 1) / kMaxKb;
+            plan.kb_per_split = ((pl->kb_total + s - 1) / s + Cfg::kKB - 1) / Cfg::kKB * Cfg::kKB;
+            plan.split = (pl->kb_total + plan.kb_per_split - 1) / plan.kb_per_split;
+        }
+    }
     pl->split = plan.split;
     pl->kb_per_split = plan.kb_per_split;
     pl->num_units = tiles * plan.split;

@@ -21,7 +21,8 @@ int main(void)
 
     EXPECT(i4i4_gemm(fake, fake, c, -1, 8, 64, 0) == IGEMM_INVALID_ARGUMENT);
     EXPECT(i4i4_gemm(fake, fake, c, 8, 8, 48, 0) == IGEMM_UNSUPPORTED_SHAPE);
-    EXPECT(i4i4_gemm(fake, fake, c, 8, 8, 65536 + 32, 0) == IGEMM_OVERFLOW_BOUND);
+    EXPECT(i4i4_gemm(fake, fake, c, 8, 8, 33554432, 0) == IGEMM_OVERFLOW_BOUND);
+    EXPECT(w4a8_gemm((const int8_t *)fake, fake, c, 8, 8, 2097152, 0) == IGEMM_OVERFLOW_BOUND);
     EXPECT(w4a8_gemm((const int8_t *)fake, fake, c + 1, 8, 8, 64, 0) == IGEMM_MISALIGNED);
     EXPECT(w4a8_gemm(NULL, NULL, NULL, 0, 8, 64, 0) == IGEMM_OK);
     EXPECT(i4i4_gemm_host(fake, fake, NULL, 8, 8, 64, 0) == IGEMM_INVALID_ARGUMENT);

@@ -49,6 +49,10 @@ def test_strerror_covers_every_status(lib):
 
 FAKE = 0x10000  # a 16-byte-aligned address that is never dereferenced here
 
+# first K past the int32 bound of each variant (|C| <= 64 K or 1024 K < 2^31):
+# rejected before any launch.  (No call here passes FAKE with a valid shape.)
+K_PAST_BOUND = {"i4i4": 33554432, "w4a8": 2097152}
+
 
 @pytest.mark.parametrize("fn", ["i4i4_gemm", "w4a8_gemm"])
 def test_gemm_argument_validation(lib, fn):
@@ -64,10 +68,11 @@ def test_gemm_argument_validation(lib, fn):
     assert f(FAKE, FAKE, None, 8, 8, 32, None) == pig.IGEMM_INVALID_ARGUMENT
     assert f(None, FAKE, FAKE, 8, 8, 32, None) == pig.IGEMM_INVALID_ARGUMENT
     assert f(FAKE, None, FAKE, 8, 8, 32, None) == pig.IGEMM_INVALID_ARGUMENT
-    # K must be a multiple of 32 and at most 65536
+    # K must be a multiple of 32 and within the int32 bound of the variant
     for k in (2, 16, 48, 1000):
         assert f(FAKE, FAKE, FAKE, 8, 8, k, None) == pig.IGEMM_UNSUPPORTED_SHAPE
-    assert f(FAKE, FAKE, FAKE, 8, 8, 65536 + 32, None) == pig.IGEMM_OVERFLOW_BOUND
+    assert f(FAKE, FAKE, FAKE, 8, 8, K_PAST_BOUND[fn[:4]], None) == pig.IGEMM_OVERFLOW_BOUND
+    assert f(FAKE, FAKE, FAKE, 8, 8, 2 * K_PAST_BOUND[fn[:4]], None) == pig.IGEMM_OVERFLOW_BOUND
     # 16-byte alignment of every base address
     assert f(FAKE, FAKE, FAKE + 4, 8, 8, 32, None) == pig.IGEMM_MISALIGNED
     assert f(FAKE + 1, FAKE, FAKE, 8, 8, 32, None) == pig.IGEMM_MISALIGNED
@@ -86,7 +91,7 @@ def test_host_gemm_argument_validation(lib, fn):
     assert f(FAKE, None, FAKE, 8, 8, 32, None) == pig.IGEMM_INVALID_ARGUMENT
     for k in (2, 16, 48):
         assert f(FAKE, FAKE, FAKE, 8, 8, k, None) == pig.IGEMM_UNSUPPORTED_SHAPE
-    assert f(FAKE, FAKE, FAKE, 8, 8, 65536 + 32, None) == pig.IGEMM_OVERFLOW_BOUND
+    assert f(FAKE, FAKE, FAKE, 8, 8, K_PAST_BOUND[fn[:4]], None) == pig.IGEMM_OVERFLOW_BOUND
 
 
 @pytest.mark.parametrize("fn", ["fp8_gemm_host", "fp8_gemm_e5m2_host"])

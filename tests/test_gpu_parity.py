@@ -530,6 +530,49 @@ def test_w4a8_extreme_constants(orc, K, av, bv):
         assert np.all(C == av * bv * K), (M, K, av, bv)
 
 
+# K past one exact f32 accumulation (65536 k): the prepared-codes path cuts K
+# into pieces of at most 512 k blocks whose exact int32 results add into a
+# zeroed C (the first piece adds the row-sum terms of the whole K); K tails,
+# ragged M and N, N % 4 != 0, few activation rows for W4A8.
+LONG_K = [("i4i4", 300, 200, 131104), ("i4i4", 65, 1030, 70016), ("w4a8", 16, 300, 131104),
+          ("w4a8", 1030, 260, 70016)]
+
+
+@pytest.mark.parametrize("variant,M,N,K", LONG_K)
+def test_long_k_matches_oracle(orc, variant, M, N, K):
+    b = si.int4_values(8100 + N + K, (N, K))
+    if variant == "i4i4":
+        a = si.int4_values(8000 + M + K, (M, K))
+        C, ap, bp = run_i4i4(a, b, orc)
+        assert np.array_equal(C, orc.i4i4_gemm(ap, bp, K))
+    else:
+        a = si.int8_values(8000 + M + K, (M, K))
+        C, bp = run_w4a8(a, b, orc)
+        assert np.array_equal(C, orc.w4a8_gemm(a, bp, K))
+
+
+# Constant operands at K near the int32 bound: W4A8 K = 2097120 (the largest
+# multiple of 32 below 2^31 / 1024) reaches |C| = 1024 K = 2147450880, and the
+# row-sum terms (-8 sum a, -128 sum u) pass 2^31 on their own; int4 x int4 at
+# K = 2^21 (64 pieces).  C = a b K in closed form.
+@pytest.mark.parametrize("av,bv", [(-128, -8), (127, 7), (-128, 7), (127, -8), (0, -8)])
+def test_w4a8_near_the_int32_bound(orc, av, bv):
+    M, N, K = 16, 260, 2097120
+    a = np.full((M, K), av, dtype=np.int8)
+    b = np.full((N, K), bv, dtype=np.int8)
+    C, _ = run_w4a8(a, b, orc)
+    assert np.all(C.astype(np.int64) == av * bv * K), (av, bv)
+
+
+@pytest.mark.parametrize("av,bv", [(-8, -8), (7, 7), (-8, 7), (7, -8)])
+def test_i4i4_long_k_constants(orc, av, bv):
+    M, N, K = 128, 260, 1 << 21
+    a = np.full((M, K), av, dtype=np.int8)
+    b = np.full((N, K), bv, dtype=np.int8)
+    C, _, _ = run_i4i4(a, b, orc)
+    assert np.all(C.astype(np.int64) == av * bv * K), (av, bv)
+
+
 def test_adversarial_partial_sums(orc):
     # a long run of maximal products followed by +/-1 terms: any lost low bit
     # in a large accumulator shows up

@@ -37,7 +37,7 @@ def test_noalloc_rejects_bad_arguments_and_oversized_problems(lib):
     f = lib.i4i4_gemm_noalloc
     assert f(FAKE, FAKE, FAKE, -1, 8, 32, None) == pig.IGEMM_INVALID_ARGUMENT
     assert f(FAKE, FAKE, FAKE, 8, 8, 48, None) == pig.IGEMM_UNSUPPORTED_SHAPE
-    assert f(FAKE, FAKE, FAKE, 8, 8, 65536 + 32, None) == pig.IGEMM_OVERFLOW_BOUND
+    assert f(FAKE, FAKE, FAKE, 8, 8, 33554432, None) == pig.IGEMM_OVERFLOW_BOUND
     assert f(FAKE + 8, FAKE, FAKE, 8, 8, 32, None) == pig.IGEMM_MISALIGNED
     assert f(None, None, None, 0, 8, 32, None) == pig.IGEMM_OK
     # (M + N) * K = 64 MiB of codes: more than the fixed 32 MiB workspace
@@ -47,13 +47,14 @@ def test_noalloc_rejects_bad_arguments_and_oversized_problems(lib):
 
 # (M, N, K): shapes i4i4_gemm sends through its small-product path (300 x 200)
 # or its in-kernel unpacking path (513 x 770, ragged, with a K tail; 128 x 128
-# with a deep K that the launch plan splits), one that fills half the array;
+# with a deep K that the launch plan splits), one that fills half the array,
+# one with K past 65536 (pieces added into C);
 # then shapes that reach this kernel only through
 # this entry point: a single row of A (the second CTA of a cluster has no rows
 # at all), 16 rows against a wide B, a row count just past and just below a
 # tile edge, N % 4 != 0 (scalar stores instead of bulk tensor stores) and N
 # below one tile.
-SHAPES = [(300, 200, 1056), (513, 770, 4128), (2048, 2048, 4096), (128, 128, 65536),
+SHAPES = [(300, 200, 1056), (513, 770, 4128), (2048, 2048, 4096), (128, 128, 65536), (64, 100, 131104),
           (1, 8, 64), (16, 28672, 256), (33, 7, 96), (3, 13, 32), (127, 260, 512), (129, 126, 160)]
 
 
