@@ -38,9 +38,10 @@
 //    integer atomics: integer addition is associative, so the result does not
 //    depend on the order in which the slices arrive.
 //
-// Warp roles:
-//   warps 0-3                 epilogue (TMEM lane quadrant = warp)
-//   warps 4 .. 4+4*ASETS-1    weight unpack, ASETS sets of four warps taking
+// Warp roles (E = 4 epilogue warps, 8 for 64 activation rows):
+//   warps 0 .. E-1            epilogue (TMEM lane quadrant = warp % 4; with
+//                             E = 8 warp / 4 picks half of the activations)
+//   warps E .. E+4*ASETS-1    weight unpack, ASETS sets of four warps taking
 //                             alternate packed stages (quadrant = warp % 4)
 //   next warp                 TMA producer (several issuing lanes)
 //   next one or two warps     MMA issue (one thread each, alternate stages,
@@ -107,8 +108,15 @@ struct SkinnyCfg {
     static constexpr int kIssuers = ST % 4 == 0 ? 4 : (ST <= 8 ? ST : 1);
     // the first ring round goes out kRamp stages at a time (see the producer)
     static constexpr int kRamp = ST < 2 ? ST : 2;
-    static constexpr int kWarpU0 = 4;
-    static constexpr int kWarpTma = 4 + 4 * kASets;
+    // epilogue warps: one per TMEM lane quadrant, two (each half of the
+    // activation columns) for 64 activation rows, whose per-tile epilogue
+    // would otherwise outlast a tile's main loop
+    static constexpr int kEpiWarps = QA == 64 ? 8 : 4;
+    static constexpr int kEpiCols = QA * 4 / kEpiWarps;  // activation columns per epilogue warp
+    static_assert(kEpiWarps == 4 || CS == 1, "split epilogue with atomics or plain stores only");
+    static_assert(kEpiCols % 16 == 0, "epilogue TMEM loads of 16 columns");
+    static constexpr int kWarpU0 = kEpiWarps;
+    static constexpr int kWarpTma = kWarpU0 + 4 * kASets;
     static constexpr int kWarpMma = kWarpTma + 1;  // TMEM allocation; MMA issuers kWarpMma ..
     static constexpr int kThreads = 32 * (kWarpMma + kMmaIssuers);
     static constexpr int kBuildThreads = kThreads - 32;  // all but the producer warp
@@ -281,7 +289,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], Cfg::kMmaIssuers);
-            mbar_init(&acc_empty[b], 4);
+            mbar_init(&acc_empty[b], Cfg::kEpiWarps);
         }
         mbar_init(mma_drain, Cfg::kMmaIssuers);
         if constexpr (Cfg::CS > 1) {
@@ -470,11 +478,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 }
             }
         } else {
-            // -------------------------------------------------------- epilogue (warps 0-3)
+            // -------------------------------------------------------- epilogue (warps 0 .. kEpiWarps-1)
             // C may still be being zeroed by the grid this one was launched to
             // overlap (no-op without such a grid)
             asm volatile("griddepcontrol.wait;" ::: "memory");
-            const int quad = warp;
+            constexpr int QE = Cfg::kEpiCols;
+            const int quad = warp & 3;
+            const int me = (warp >> 2) * QE;  // this warp's first activation column
             const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
             const bool reduce = prm.split > 1;
             const int mq = min(prm.M, QA);
@@ -484,17 +494,17 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             for (int t = t0; t < prm.n_tiles; t += tstep, g0 += nst) {
                 if (!sk_warp_wait(&acc_full[acc], acc_ph, wd)) break;
                 tc_fence_after();
-                int val[QA];
+                int val[QE];
 #pragma unroll
-                for (int m = 0; m < QA; ++m) val[m] = 0;
+                for (int m = 0; m < QE; ++m) val[m] = 0;
 #pragma unroll 1
                 for (int jj = 0; jj < Cfg::kMmaIssuers; ++jj) {
                     // an issuer with no stage in this tile (a one-stage tile) left its
                     // accumulator untouched
                     if (nst < Cfg::kMmaIssuers && static_cast<int>(g0 % Cfg::kMmaIssuers) != jj) continue;
-                    const uint32_t tacc = trow + (2 * jj + acc) * Cfg::kAccCols;
+                    const uint32_t tacc = trow + (2 * jj + acc) * Cfg::kAccCols + me;
 #pragma unroll
-                    for (int j = 0; j < QA; j += 16) {
+                    for (int j = 0; j < QE; j += 16) {
                         uint32_t v0[16];
                         tmem_ld_32x32b_x16(tacc + j, v0);
                         if constexpr (!Cfg::kActI4) {
@@ -560,9 +570,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 } else if (n < prm.N) {
                     int32_t *cp = prm.C + n;
 #pragma unroll
-                    for (int m = 0; m < QA; ++m) {
+                    for (int e = 0; e < QE; ++e) {
+                        const int m = me + e;
                         if (m < mq) {
-                            const int v = val[m] - 8 * sums[m];
+                            const int v = val[e] - 8 * sums[m];
                             if (reduce)
                                 atomicAdd(cp + static_cast<int64_t>(m) * prm.N, v);
                             else
