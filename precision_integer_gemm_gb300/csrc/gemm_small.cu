@@ -447,4 +447,330 @@ int launch_i4i4_small(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, i
     return bn == 64 ? launch_small<64>(Ap, Bp, C, M, N, K, stream) : launch_small<128>(Ap, Bp, C, M, N, K, stream);
 }
 
+
+// ---------------------------------------------------------------------------
+// W4A8 on the same plan ("[Example] add w4a8 gemm kernel", tilelang PR #815:
+// int8 activations A [M, K] times packed int4 weights B [N, K/2]) for small
+// prefill batches: one CTA per tile of 128 weight rows x BA activation rows.
+//
+//  * the weights are the MMA A side, in tensor memory, converted exactly as
+//    int4 x int4's A side above (u = w + 8);
+//  * each activation a becomes ua = a + 128 = 16 h + l with h, l in [0, 15]:
+//    the high codes h and the low codes l of BA activation rows are 2 BA code
+//    rows on the MMA N side (rows 0 .. BA-1 high, BA .. 2BA-1 low), in the
+//    same k order as the weight codes (within each 8 k the even k, then the odd
+//    k; in k block 1 the two 16-k halves of every 32 k swapped), so one MMA
+//    per 32 k of N = 2 BA yields S_h and S_l side by side;
+//  * C[m, n] = 16 S_h + S_l - 8 sum ua[m] - 128 sum u[n] + 1024 K, stored
+//    straight from the accumulator (a warp's store covers 32 consecutive n).
+//
+// Per 256-k chunk the producer loads the packed weights (one 128-byte box of
+// 128 rows, 128-byte swizzle) and the activations (two 128-byte boxes of BA
+// rows: k 0..127 and 128..255 of the chunk).
+template <int BA>
+struct SmallW4Cfg {
+    static constexpr int kBWarps = 8;                           // activation converters
+    static constexpr int kBRowsPerThread = BA / 16;             // 16 pieces of 16 bytes per activation row
+    static constexpr int kConvWarps = kSmallAWarps + kBWarps;
+    static constexpr int kWarpMma = kConvWarps, kWarpProd = kConvWarps + 1;
+    static constexpr int kThreads = 32 * (kConvWarps + 2);
+    static constexpr int kQRows = 2 * BA;                       // MMA N: high and low code rows
+    static constexpr int kBufs = 3;
+    static constexpr int kACols = 64;
+    static constexpr int kTmemUsed = kQRows + kBufs * kACols;
+    static constexpr int kTmemCols = kTmemUsed <= 256 ? 256 : 512;
+    static constexpr int kRawA = kSmallRowsA * 128;             // packed weights of one chunk
+    static constexpr int kRawHalf = BA * 128;                   // activations, one 128-k half of a chunk
+    static constexpr int kRawStage = kRawA + 2 * kRawHalf;
+    static constexpr int kBlockB = kQRows * 128;                // one 128-k block of activation codes
+    static constexpr int kCodeBuf = 2 * kBlockB;
+    static constexpr int kSmem = 1024 + kBufs * kCodeBuf + kSmallRaw * kRawStage + 4 * (2 * kSmallRowsA + BA) +
+                                 8 * (2 * kBufs + kSmallRaw) + 16;
+    static_assert(BA == 64, "activation rows per tile");
+    static_assert(kSmem <= 232448, "shared memory per CTA");
+};
+
+// 16 int8 activations (k 0..15 of a 16-k piece) -> 16 high codes and 16 low
+// codes of ua = a + 128, each as (even k of 0..7, odd k of 0..7, even k of
+// 8..15, odd k of 8..15); adds the sum of ua to `sum`.  An invalid piece gives
+// zeros.
+__device__ __forceinline__ void small_act_codes(const uint4 x, bool valid, uint4 &hc, uint4 &lc, int &sum)
+{
+    uint32_t w[4] = {__byte_perm(x.x, x.y, 0x6420), __byte_perm(x.x, x.y, 0x7531), __byte_perm(x.z, x.w, 0x6420),
+                     __byte_perm(x.z, x.w, 0x7531)};
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t ua = w[i] ^ 0x80808080u;  // a + 128 in each byte
+        h[i] = valid ? (ua >> 4) & 0x0F0F0F0Fu : 0u;
+        l[i] = valid ? ua & 0x0F0F0F0Fu : 0u;
+        if (valid) sum = static_cast<int>(__dp4a(ua, 0x01010101u, static_cast<uint32_t>(sum)));  // bytes unsigned
+    }
+    hc = make_uint4(h[0], h[1], h[2], h[3]);
+    lc = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+template <int BA>
+__global__ void __launch_bounds__(SmallW4Cfg<BA>::kThreads, 1)
+    igemm_small_w4a8_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapX,
+                            int32_t *__restrict__ C, int M, int N, int K, int *status, unsigned long long limit_ns)
+{
+    using Cfg = SmallW4Cfg<BA>;
+    constexpr int NB = Cfg::kBufs;
+    constexpr int QR = Cfg::kQRows;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint8_t *codes = smem;                                 // [NB][2 k blocks][2 BA rows][128]: activation codes
+    uint8_t *raw = smem + NB * Cfg::kCodeBuf;              // [kSmallRaw][weights | activations k 0..127 | 128..255]
+    int *sumW = reinterpret_cast<int *>(raw + kSmallRaw * Cfg::kRawStage);  // [2 k blocks][128]: sum u
+    int *sumX = sumW + 2 * kSmallRowsA;                                      // [BA]: sum (a + 128)
+    uint64_t *conv = reinterpret_cast<uint64_t *>(sumX + BA);
+    uint64_t *done = conv + NB;
+    uint64_t *full = done + NB;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(full + kSmallRaw);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool a_warp = warp < kSmallAWarps;
+    const bool b_warp = warp >= kSmallAWarps && warp < Cfg::kConvWarps;
+    const bool mma_thread = warp == Cfg::kWarpMma && lane == 0;
+    const bool producer = warp == Cfg::kWarpProd && lane == 0;
+    const int n0 = blockIdx.x * kSmallRowsA, m0 = blockIdx.y * BA;  // weight rows, activation rows
+    const int nchunks = (K + 255) / 256;
+
+    auto load = [&](int c) {
+        const int s = c % kSmallRaw;
+        uint8_t *dst = raw + s * Cfg::kRawStage;
+        mbar_arrive_expect_tx(&full[s], Cfg::kRawStage);
+        tma_load_2d(dst, &mapW, &full[s], c * 128, n0);
+        tma_load_2d(dst + Cfg::kRawA, &mapX, &full[s], c * 256, m0);
+        tma_load_2d(dst + Cfg::kRawA + Cfg::kRawHalf, &mapX, &full[s], c * 256 + 128, m0);
+    };
+    if (producer) {
+        tma_prefetch_map(&mapW);
+        tma_prefetch_map(&mapX);
+        for (int i = 0; i < NB; ++i) {
+            mbar_init(&conv[i], Cfg::kConvWarps);
+            mbar_init(&done[i], 1);
+        }
+        for (int i = 0; i < kSmallRaw; ++i) mbar_init(&full[i], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        for (int c = 0; c < kSmallRaw && c < nchunks; ++c) load(c);
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Watchdog wd{abort_flag, status, limit_ns};
+
+    bool ok = true;
+    uint32_t issued = 0;
+    int loads = producer ? min(kSmallRaw, nchunks) : 0;
+    const bool tile_full = n0 + kSmallRowsA <= N && m0 + BA <= M;
+    const int kh = K / 2;
+
+    if (a_warp || b_warp) {
+        // weights (A warps, as int4 x int4's A side): row ra, k block kba; TMEM
+        const int quad = warp & 3, kba = (warp >> 2) & 1;
+        const int ra = quad * 32 + lane;
+        const bool a_ok = n0 + ra < N;
+        const uint32_t a_tcol = tmem + (static_cast<uint32_t>(quad * 32) << 16) + QR + 32 * kba;
+        // activations (B warps): thread (g, p) takes 16-k piece p of rows g + 16 i;
+        // piece p lands in k block p / 8 at code chunk (p % 8) ^ (p / 8) (the
+        // halves of each 32 k swapped in k block 1), swizzled by row % 8
+        const int tb = tid - 32 * kSmallAWarps;
+        const int g = tb >> 4, p = tb & 15;
+        const int kb = p >> 3, pos = (p & 7) ^ kb;
+        bool x_ok[Cfg::kBRowsPerThread];
+        int sx[Cfg::kBRowsPerThread];
+#pragma unroll
+        for (int i = 0; i < Cfg::kBRowsPerThread; ++i) {
+            x_ok[i] = m0 + g + 16 * i < M;
+            sx[i] = 0;
+        }
+        int sa = 0;
+#pragma unroll 1
+        for (int c = 0; c < nchunks; ++c) {
+            const int s = c % kSmallRaw, use = c / NB, buf = c - use * NB;
+            ok = __all_sync(0xffffffffu, wait_bounded(&full[s], (c / kSmallRaw) & 1u, wd));
+            if (ok && use > 0) ok = __all_sync(0xffffffffu, wait_bounded(&done[buf], (use - 1) & 1u, wd));
+            if (!ok) break;  // the whole warp
+            const uint8_t *slot = raw + s * Cfg::kRawStage;
+            const int left = (kh - c * 128) >> 4;  // 32-k pieces of this chunk inside K (> 0)
+            auto convert = [&](auto full_tag) {
+                constexpr bool FULL = decltype(full_tag)::value;
+                if (a_warp) {
+                    tc_fence_after();  // the MMAs that read this TMEM buffer are done
+                    uint32_t code[32];
+                    const uint32_t vmask =
+                        FULL ? 0xFu : a_ok ? (left >= 8 ? 0xFFu : ((1u << left) - 1u)) >> (4 * kba) : 0u;
+                    if (kba == 0)
+                        small_a_codes<0>(slot + ra * 128, ra & 7, vmask, code, sa);
+                    else
+                        small_a_codes<1>(slot + ra * 128, ra & 7, vmask, code, sa);
+                    tmem_st_32x32b_x32(a_tcol + buf * Cfg::kACols, code);
+                    tmem_st_wait();
+                    tc_fence_before();
+                } else {
+                    // 16-k piece p is inside K iff its 32-k piece p / 2 is
+                    const bool in = FULL || (p >> 1) < left;
+                    uint8_t *bs = codes + buf * Cfg::kCodeBuf + kb * Cfg::kBlockB;
+                    const uint8_t *src = slot + Cfg::kRawA + kb * Cfg::kRawHalf + (p & 7) * 16;
+#pragma unroll
+                    for (int i = 0; i < Cfg::kBRowsPerThread; ++i) {
+                        const int r = g + 16 * i, sw = r & 7;
+                        const uint4 x = *reinterpret_cast<const uint4 *>(src + r * 128);
+                        uint4 hc, lc;
+                        small_act_codes(x, FULL || (in && x_ok[i]), hc, lc, sx[i]);
+                        *reinterpret_cast<uint4 *>(bs + r * 128 + ((pos ^ sw) << 4)) = hc;
+                        *reinterpret_cast<uint4 *>(bs + (BA + r) * 128 + ((pos ^ sw) << 4)) = lc;
+                    }
+                    fence_proxy_async_smem();  // generic writes, read next by the tensor core
+                }
+            };
+            if (tile_full && left >= 8)
+                convert(std::true_type{});
+            else
+                convert(std::false_type{});
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&conv[buf]);
+        }
+        if (a_warp) {
+            if (ok) {
+                const int c = nchunks - 1, use = c / NB;
+                ok = wait_bounded(&done[c - use * NB], use & 1u, wd);
+            }
+            sumW[kba * kSmallRowsA + ra] = sa;
+        } else {
+            // activation row sums: the sixteen lanes of a row hold one partial sum each
+#pragma unroll
+            for (int i = 0; i < Cfg::kBRowsPerThread; ++i) {
+                int v = sx[i];
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                if (p == 0) sumX[g + 16 * i] = v;
+            }
+        }
+    } else if (mma_thread) {
+        // ---------------------------------------------------------------- MMA thread
+        constexpr uint32_t idesc = idesc_e4m3_f32(kSmallRowsA, QR);
+        const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(codes));
+#pragma unroll 1
+        for (int c = 0; c < nchunks; ++c) {
+            const int use = c / NB, buf = c - use * NB;
+            ok = wait_spin_bounded(&conv[buf], use & 1u, wd);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t a0 = tmem + QR + buf * Cfg::kACols;
+            const uint64_t b0 = bdesc0 + static_cast<uint64_t>((buf * Cfg::kCodeBuf) >> 4);
+            const int nkb = min(2, (K - c * 256 + 127) / 128);
+            for (int b = 0; b < nkb; ++b) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f8f6f4_tmem_a(tmem, a0 + 32 * b + 8 * kk,
+                                      b0 + static_cast<uint64_t>((b * Cfg::kBlockB + 32 * kk) >> 4), idesc,
+                                      (c > 0 || b > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&done[buf]);
+            ++issued;
+        }
+    } else if (producer) {
+        // ---------------------------------------------------------------- TMA producer
+#pragma unroll 1
+        for (int c = 0; loads < nchunks; ++c) {
+            const int use = c / NB;
+            ok = wait_bounded(&conv[c - use * NB], use & 1u, wd);
+            if (!ok) break;
+            load(loads++);
+        }
+    }
+    tc_fence_after();
+    if (__syncthreads_and(ok) && a_warp) {
+        // ---------------------------------------------------------------- epilogue
+        // warp w: weight rows 32 (w % 4) .., activations half w / 4 of the tile;
+        // C[m, n] = 16 S_h[m] + S_l[m] - 8 sum ua[m] - 128 sum u[n] + 1024 K
+        constexpr int kHalf = BA / 2;
+        const int quad = warp & 3, mh = (warp >> 2) * kHalf;
+        const int r = quad * 32 + lane, n = n0 + r;
+        const int nterm = 1024 * K - 128 * (sumW[r] + sumW[kSmallRowsA + r]);
+        const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+#pragma unroll
+        for (int j = 0; j < kHalf; j += 16) {
+            uint32_t vh[16], vl[16];
+            tmem_ld_32x32b_x16(trow + mh + j, vh);
+            tmem_ld_32x32b_x16(trow + BA + mh + j, vl);
+            tmem_ld_wait_regs(vh, vl);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int mm = mh + j + e, m = m0 + mm;
+                const int v = 16 * __float2int_rn(__uint_as_float(vh[e]) * 262144.0f) +
+                              __float2int_rn(__uint_as_float(vl[e]) * 262144.0f) - 8 * sumX[mm] + nterm;
+                if (m < M && n < N) C[static_cast<int64_t>(m) * N + n] = v;
+            }
+        }
+    }
+    // ---------------------------------------------------------------- teardown
+    if (mma_thread && issued > 0) {
+        const uint64_t t0 = globaltimer_ns();
+        const uint32_t c = issued - 1, use = c / NB;
+        while (!mbar_try_wait(&done[c - use * NB], use & 1u) && globaltimer_ns() - t0 < limit_ns) {
+        }
+    }
+    if (producer) {
+        const uint64_t t0 = globaltimer_ns();
+        for (int c = loads - kSmallRaw < 0 ? 0 : loads - kSmallRaw; c < loads; ++c)
+            while (!mbar_try_wait(&full[c % kSmallRaw], (c / kSmallRaw) & 1u) && globaltimer_ns() - t0 < limit_ns) {
+            }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Cfg::kTmemCols);
+    }
+}
+
+int launch_w4a8_small(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
+{
+    constexpr int BA = 64;
+    using Cfg = SmallW4Cfg<BA>;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return kCudaError;
+    {
+        static std::mutex mu;  // first calls from several threads
+        static bool attr_set[64] = {};
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && !attr_set[dev]) {
+            if (cudaFuncSetAttribute(igemm_small_w4a8_kernel<BA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Cfg::kSmem) != cudaSuccess)
+                return kCudaError;
+            attr_set[dev] = true;
+        }
+    }
+    int *status = device_status_word();
+    if (!status) return kCudaError;
+    // packed weights: 128 bytes (one chunk) by 128 rows, 16-byte chunk j of row
+    // r stored at j ^ (r % 8); activations: 128 bytes (half a chunk) by BA rows
+    CUtensorMap mapW, mapX;
+    if (make_map(&mapW, CU_TENSOR_MAP_DATA_TYPE_UINT8, Bp, N, K / 2, kSmallRowsA, 128, CU_TENSOR_MAP_SWIZZLE_128B) !=
+            kOk ||
+        make_map(&mapX, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, M, K, BA, 128, CU_TENSOR_MAP_SWIZZLE_NONE) != kOk)
+        return kCudaError;
+    const dim3 grid((N + kSmallRowsA - 1) / kSmallRowsA, (M + BA - 1) / BA, 1);
+    const GemmEvents ev = take_gemm_events();
+    if (ev.start && cudaEventRecord(ev.start, stream) != cudaSuccess) return kCudaError;
+    igemm_small_w4a8_kernel<BA><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(mapW, mapX, C, M, N, K, status,
+                                                                              watchdog_limit_ns());
+    note_launch();
+    if (ev.stop && cudaEventRecord(ev.stop, stream) != cudaSuccess) return kCudaError;
+    return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
+}
+
 }  // namespace igemm

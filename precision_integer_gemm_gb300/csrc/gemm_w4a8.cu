@@ -2,8 +2,10 @@
 //
 // Skinny activation counts (M <= 64, decode) take igemm_skinny_kernel
 // (gemm_skinny_kernel.cuh): split K, each CTA's slice of the activations held
-// as codes in shared memory, the weights streamed once.  Large products
-// (M >= 768, M * N >= 4M) take the prepared-codes path: one pass writes weight
+// as codes in shared memory, the weights streamed once.  Small prefill
+// batches of about one wave of 128 x 64 tiles take igemm_small_w4a8_kernel
+// (gemm_small.cu).  Large products (M >= 768, M * N >= 4M, and every K past
+// 65536) take the prepared-codes path: one pass writes weight
 // code rows, activation
 // high/low code planes and the row sums (prep.cu), then igemm_ss_kernel
 // multiplies 128 weight rows by 128 activation rows (256 code rows) per tile
@@ -89,6 +91,23 @@ SkinnyPlan skinny_plan_w4a8(int M, int N, int K, int sms, int pairs, int quads)
     return skinny_plan_for<CfgW4A8Skinny64>(N, K, sms, pairs, quads);
 }
 
+// Small prefill batches (M > 64) whose tiles of 128 weight rows x 64
+// activations fill about one wave take igemm_small_w4a8_kernel (gemm_small.cu:
+// one launch, codes made per 256-k chunk, no workspace).  Measured on GB300
+// (call time, L2 flushed; the other paths in parentheses): 1024^3 10.9 us
+// (15.0), 128 x 4096 x 4096 19.1 (22.2), 512 x 4096 x 4096 33.4 (39.6, two
+// waves), 65 x 4100 x 1056 13.0 (19.1); it loses where the other paths split a
+// long K over few tiles or pack the tiles better: 300 x 777 x 4128 25.2 (21.2),
+// 96 x 11008 x 4096 37.5 (29.3), 256 x 28672 x 8192 154 (146).
+static bool use_small_w4a8(int M, int N, int K)
+{
+    if (M <= 64 || K > 4096) return false;
+    const int64_t sms = sm_count();
+    const int64_t tiles = int64_t((M + 63) / 64) * ((N + 127) / 128);
+    if (tiles <= sms && (K <= 2048 || 3 * tiles >= sms)) return true;
+    return tiles <= 2 * sms && M >= 256;
+}
+
 int launch_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
 {
     const uint8_t *a = reinterpret_cast<const uint8_t *>(A);
@@ -104,6 +123,7 @@ int launch_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, in
                                : launch_skinny<CfgW4A8Skinny64>(a, Bp, C, M, N, K, stream);
         if (rc != kUnsupportedShape) return rc;
     }
+    if (use_small_w4a8(M, N, K)) return launch_w4a8_small(A, Bp, C, M, N, K, stream);
     // the preparation pass writes N * K + 2 * M * K bytes of codes; measured on
     // GB300 it pays from about M = 768 with M * N >= 4M (1024 x 4096 x 4096: 48 vs
     // 52 us), not below (64 x 28672 x 8192: 130 vs 61 us; 1024^3: 28 vs 15 us)

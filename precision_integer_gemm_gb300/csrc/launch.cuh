@@ -528,6 +528,9 @@ int launch_i4i4(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, 
 // or 128), for small products.
 int launch_i4i4_small(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, int bn,
                       cudaStream_t stream);
+// igemm_small_w4a8_kernel (gemm_small.cu): one CTA per 128 weight rows x 64
+// activation rows, for small prefill batches.
+int launch_w4a8_small(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);
 // Skinny-path plans (M <= 64) of each variant, for the planning query.
 SkinnyPlan skinny_plan_i4i4(int M, int N, int K, int sms, int pairs, int quads);
 SkinnyPlan skinny_plan_w4a8(int M, int N, int K, int sms, int pairs, int quads);

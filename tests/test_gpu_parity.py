@@ -153,6 +153,34 @@ def test_i4i4_small_product_path(orc, M, N, K):
     assert np.array_equal(C, orc.i4i4_gemm(ap, bp, K))
 
 
+# W4A8 small-product path (M > 64, K <= 4096, about one wave of 128-weight x
+# 64-activation tiles, or two when M >= 256): M just above the skinny limit, K =
+# 32 and K tails inside a 256-k chunk, ragged M and N (N % 4 != 0), two waves.
+SMALL_PATH_W4A8 = [(65, 64, 32), (128, 128, 128), (129, 257, 96), (200, 130, 32), (300, 200, 1056),
+                   (520, 640, 1024), (1030, 1022, 1056), (65, 4100, 1056), (128, 4096, 4096), (512, 4096, 4096)]
+
+
+@pytest.mark.parametrize("M,N,K", SMALL_PATH_W4A8)
+def test_w4a8_small_product_path(orc, M, N, K):
+    a = si.int8_values(7400 + M + K, (M, K))
+    b = si.int4_values(7500 + N + K, (N, K))
+    C, bp = run_w4a8(a, b, orc)
+    assert np.array_equal(C, orc.w4a8_gemm(a, bp, K))
+
+
+# W4A8 shapes of the in-kernel unpack path (more tiles than a wave with few
+# rows, K past 4096 with few tiles).
+TC_W4A8 = [(96, 11008, 4096), (300, 777, 4128), (700, 1030, 4160)]
+
+
+@pytest.mark.parametrize("M,N,K", TC_W4A8)
+def test_w4a8_in_kernel_path(orc, M, N, K):
+    a = si.int8_values(7600 + M + K, (M, K))
+    b = si.int4_values(7700 + N + K, (N, K))
+    C, bp = run_w4a8(a, b, orc)
+    assert np.array_equal(C, orc.w4a8_gemm(a, bp, K))
+
+
 # Shapes that none of the other paths take (more tiles than the small-product
 # kernel runs in a wave, too few rows for the prepared codes; few tiles with a
 # K long enough to split): the in-kernel unpack path.
