@@ -33,8 +33,9 @@
 //    ahead of the MMAs;
 //  * the epilogue (the A warps) reads the accumulator (warp w: TMEM lanes
 //    32 (w % 4), half w / 4 of the columns), restores the signed result
-//    C = S - 8 sum uA - 8 sum uB + 64 K, stages the tile in shared memory and
-//    writes it out row by row (coalesced 16-byte stores).
+//    C = S - 8 sum uA - 8 sum uB + 64 K and stages the tile in shared memory as
+//    128-byte-swizzled boxes of 32 columns, which one thread stores with bulk
+//    tensor stores (N % 4 != 0: the warps store it row by row).
 //
 // Code order inside a piece of 32 k (16 packed bytes, words w0..w3): code
 // chunk X = (even k of w0, odd k of w0, even k of w1, odd k of w1), chunk Y the
@@ -141,7 +142,8 @@ __device__ __forceinline__ void small_a_codes(const uint8_t *raw_row, uint32_t s
 template <int BN>
 __global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1)
     igemm_small_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                       int32_t *__restrict__ C, int M, int N, int K, int *status, unsigned long long limit_ns)
+                       const __grid_constant__ CUtensorMap mapC, int tma_store, int32_t *__restrict__ C, int M, int N,
+                       int K, int *status, unsigned long long limit_ns)
 {
     using Cfg = SmallCfg<BN>;
     constexpr int NB = Cfg::kBufs;
@@ -329,7 +331,10 @@ __global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1)
         // ---------------------------------------------------------------- epilogue
         constexpr int kHalf = BN / 2;        // columns per warp
         constexpr int kRowChunks = BN / 4;   // 16-byte chunks of a C row
-        uint8_t *tile = codes;               // [128][BN] int32, chunk index swizzled by row % 8
+        // the int32 tile over the code buffers: [BN / 32 boxes][128 rows][32 values],
+        // the 16-byte chunk index within a row swizzled by row % 8 (the layout of a
+        // 128-byte-swizzled tensor box)
+        uint8_t *tile = codes;
         const int r = (warp & 3) * 32 + lane;
         const int col0 = (warp >> 2) * kHalf;
         const int base = 64 * K - 8 * (sumA[r] + sumA[kSmallRowsA + r]);
@@ -355,29 +360,42 @@ __global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1)
             o.y = __float2int_rn(__uint_as_float(v[4 * q + 1]) * 262144.0f) + base - 8 * sbv.y;
             o.z = __float2int_rn(__uint_as_float(v[4 * q + 2]) * 262144.0f) + base - 8 * sbv.z;
             o.w = __float2int_rn(__uint_as_float(v[4 * q + 3]) * 262144.0f) + base - 8 * sbv.w;
-            const int chunk = (n >> 2) ^ (r & 7);
-            *reinterpret_cast<int4 *>(tile + r * (BN * 4) + (chunk << 4)) = o;
+            const int chunk = ((n >> 2) & 7) ^ (r & 7);
+            *reinterpret_cast<int4 *>(tile + (n >> 5) * kSmallRowsA * 128 + r * 128 + (chunk << 4)) = o;
         }
+        fence_proxy_async_smem();  // generic writes, read next by the bulk tensor store
         named_barrier_sync(1, 32 * kSmallAWarps);
-        // write out: per instruction a warp covers 32 / kRowChunks whole rows
-        constexpr int kRowsPerInstr = 32 / kRowChunks;
-        const int q = lane % kRowChunks;
-        const int n = n0 + 4 * q;
-        const bool vec = (N & 3) == 0 && n + 4 <= N;
-        constexpr int kRowsPerWarp = kSmallRowsA / kSmallAWarps;
+        if (tma_store) {
+            // N % 4 == 0: one bulk tensor store per 32 columns (rows past M and
+            // columns past N are clipped by the tensor map)
+            if (tid == 0) {
+                for (int b = 0; b < BN / 32; ++b)
+                    if (n0 + 32 * b < N) tma_store_2d(&mapC, tile + b * kSmallRowsA * 128, n0 + 32 * b, m0);
+                bulk_commit_group();
+                bulk_wait_group_all();  // the stores are complete before the CTA leaves
+            }
+        } else {
+            // write out: per instruction a warp covers 32 / kRowChunks whole rows
+            constexpr int kRowsPerInstr = 32 / kRowChunks;
+            const int q = lane % kRowChunks;
+            const int n = n0 + 4 * q;
+            const bool vec = (N & 3) == 0 && n + 4 <= N;
+            constexpr int kRowsPerWarp = kSmallRowsA / kSmallAWarps;
 #pragma unroll 1
-        for (int rr = warp * kRowsPerWarp; rr < (warp + 1) * kRowsPerWarp; rr += kRowsPerInstr) {
-            const int row = rr + lane / kRowChunks, m = m0 + row;
-            const int4 o = *reinterpret_cast<const int4 *>(tile + row * (BN * 4) + ((q ^ (row & 7)) << 4));
-            if (m < M) {
-                int32_t *dst = C + static_cast<int64_t>(m) * N + n;
-                if (vec) {
-                    *reinterpret_cast<int4 *>(dst) = o;
-                } else {
-                    if (n + 0 < N) dst[0] = o.x;
-                    if (n + 1 < N) dst[1] = o.y;
-                    if (n + 2 < N) dst[2] = o.z;
-                    if (n + 3 < N) dst[3] = o.w;
+            for (int rr = warp * kRowsPerWarp; rr < (warp + 1) * kRowsPerWarp; rr += kRowsPerInstr) {
+                const int row = rr + lane / kRowChunks, m = m0 + row;
+                const int4 o = *reinterpret_cast<const int4 *>(tile + (q >> 3) * kSmallRowsA * 128 + row * 128 +
+                                                               (((q & 7) ^ (row & 7)) << 4));
+                if (m < M) {
+                    int32_t *dst = C + static_cast<int64_t>(m) * N + n;
+                    if (vec) {
+                        *reinterpret_cast<int4 *>(dst) = o;
+                    } else {
+                        if (n + 0 < N) dst[0] = o.x;
+                        if (n + 1 < N) dst[1] = o.y;
+                        if (n + 2 < N) dst[2] = o.z;
+                        if (n + 3 < N) dst[3] = o.w;
+                    }
                 }
             }
         }
@@ -431,11 +449,17 @@ static int launch_small(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M,
             kOk ||
         make_map(&mapB, CU_TENSOR_MAP_DATA_TYPE_UINT8, Bp, N, K / 2, BN, 128, CU_TENSOR_MAP_SWIZZLE_NONE) != kOk)
         return kCudaError;
+    // C (N % 4 == 0: a 16-byte row pitch): boxes of 32 values by 128 rows
+    CUtensorMap mapC = {};
+    const bool tma_store = (N % 4) == 0;
+    if (tma_store && make_map(&mapC, CU_TENSOR_MAP_DATA_TYPE_INT32, C, M, N, kSmallRowsA, 32,
+                              CU_TENSOR_MAP_SWIZZLE_128B) != kOk)
+        return kCudaError;
     const dim3 grid((N + BN - 1) / BN, (M + kSmallRowsA - 1) / kSmallRowsA, 1);
     const GemmEvents ev = take_gemm_events();
     if (ev.start && cudaEventRecord(ev.start, stream) != cudaSuccess) return kCudaError;
-    igemm_small_kernel<BN><<<grid, SmallCfg<BN>::kThreads, SmallCfg<BN>::kSmem, stream>>>(mapA, mapB, C, M, N, K, status,
-                                                                                 watchdog_limit_ns());
+    igemm_small_kernel<BN><<<grid, SmallCfg<BN>::kThreads, SmallCfg<BN>::kSmem, stream>>>(
+        mapA, mapB, mapC, tma_store ? 1 : 0, C, M, N, K, status, watchdog_limit_ns());
     note_launch();
     if (ev.stop && cudaEventRecord(ev.stop, stream) != cudaSuccess) return kCudaError;
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
