@@ -48,6 +48,10 @@ static bool use_codes_i4i4(int M, int N)
 // 256 x 8192 x 8192 31.4 (41.6); it loses at 2048 x 2048 x 4096 (35.5 vs
 // 31.5), 4096 x 4096 x 1024 (49.8 vs 44.8), 640 x 640 x 8192 (27.3 vs 22.4)
 // and 1024 x 1024 x 16384 (45.7 vs 41.6), where the other paths split K.
+// 256-wide tiles pay off only where 97..128 rows leave the in-kernel path's
+// 96-row tiles half empty and 128-wide tiles overflow a wave: 128 x 28672 x
+// 8192 54.0 us (72.4); with 96 rows or fewer columns they lose (96 x 28672 x
+// 8192 58.0 vs 47.8; 128 x 16384 x 4096 31.4 vs 21.1).
 static int small_tile_width(int M, int N, int K)
 {
     const int64_t sms = sm_count();
@@ -55,6 +59,8 @@ static int small_tile_width(int M, int N, int K)
     const int64_t t64 = rows * ((N + 63) / 64), t128 = rows * ((N + 127) / 128);
     if (t64 <= sms && (K <= 4096 || (K <= 8192 && 2 * t64 >= sms))) return 64;
     if (t128 <= sms && (K <= 4096 || (K <= 8192 && 2 * t128 >= sms))) return 128;
+    const int64_t t256 = rows * ((N + 255) / 256);
+    if (M > 96 && M <= 128 && t256 <= sms && K <= 8192) return 256;
     if (t128 <= 4 * sms && K <= 2048) return 128;
     return 0;
 }

@@ -59,7 +59,8 @@ struct SmallCfg {
     static constexpr int kConvWarps = kSmallAWarps + kBWarps;
     static constexpr int kWarpMma = kConvWarps, kWarpProd = kConvWarps + 1;
     static constexpr int kThreads = 32 * (kConvWarps + 2);
-    static constexpr int kBufs = 3;                            // code buffers
+    static constexpr int kBufs = BN == 256 ? 2 : 3;            // code buffers
+    static constexpr int kRaw = BN == 256 ? 2 : kSmallRaw;     // raw slots (shared memory for 256-wide tiles)
     static constexpr int kACols = 64;                          // TMEM columns of one chunk of A codes
     static constexpr int kTmemUsed = BN + kBufs * kACols;      // accumulator, then the A code buffers
     static constexpr int kTmemCols = kTmemUsed <= 256 ? 256 : 512;
@@ -69,8 +70,8 @@ struct SmallCfg {
     static constexpr int kCodeBuf = 2 * kBlockB;
     static constexpr int kStage = kSmallRowsA * BN * 4;         // the int32 tile, over the code buffers
     static_assert(kStage <= kBufs * kCodeBuf, "epilogue tile fits over the code buffers");
-    static constexpr int kSmem = 1024 + kBufs * kCodeBuf + kSmallRaw * kRawStage + 4 * (2 * kSmallRowsA + BN) +
-                                 8 * (2 * kBufs + kSmallRaw) + 16;
+    static constexpr int kSmem = 1024 + kBufs * kCodeBuf + kRaw * kRawStage + 4 * (kSmallRowsA + BN) +
+                                 8 * (2 * kBufs + kRaw) + 16;
     static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
@@ -150,13 +151,14 @@ __global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t *codes = smem;                                       // [NB][2 k blocks][BN rows][128]: B codes
-    uint8_t *raw = smem + NB * Cfg::kCodeBuf;                    // [kSmallRaw][A rows | B rows], 128 bytes a row
-    int *sumA = reinterpret_cast<int *>(raw + kSmallRaw * Cfg::kRawStage);  // [2 k blocks][128]
-    int *sumB = sumA + 2 * kSmallRowsA;                                      // [BN]
+    constexpr int NR = Cfg::kRaw;
+    uint8_t *raw = smem + NB * Cfg::kCodeBuf;                    // [NR][A rows | B rows], 128 bytes a row
+    int *sumA = reinterpret_cast<int *>(raw + NR * Cfg::kRawStage);  // [128], both k blocks' warps add in
+    int *sumB = sumA + kSmallRowsA;                                   // [BN]
     uint64_t *conv = reinterpret_cast<uint64_t *>(sumB + BN);    // [NB] code buffer written
     uint64_t *done = conv + NB;                                  // [NB] code buffer read by the MMAs
-    uint64_t *full = done + NB;                                  // [kSmallRaw] raw slot loaded
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(full + kSmallRaw);
+    uint64_t *full = done + NB;                                  // [NR] raw slot loaded
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(full + NR);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -168,9 +170,9 @@ __global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1)
     const int kh = K / 2;  // packed bytes per row (a multiple of 16)
     const int nchunks = (K + 255) / 256;
 
-    // chunk c's packed rows into raw slot c % kSmallRaw (producer)
+    // chunk c's packed rows into raw slot c % NR (producer)
     auto load = [&](int c) {
-        const int s = c % kSmallRaw;
+        const int s = c % NR;
         uint8_t *dst = raw + s * Cfg::kRawStage;
         mbar_arrive_expect_tx(&full[s], Cfg::kRawStage);
         tma_load_2d(dst, &mapA, &full[s], c * 128, m0);
@@ -183,11 +185,12 @@ __global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1)
             mbar_init(&conv[i], Cfg::kConvWarps);
             mbar_init(&done[i], 1);
         }
-        for (int i = 0; i < kSmallRaw; ++i) mbar_init(&full[i], 1);
+        for (int i = 0; i < NR; ++i) mbar_init(&full[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
-        for (int c = 0; c < kSmallRaw && c < nchunks; ++c) load(c);
+        for (int c = 0; c < NR && c < nchunks; ++c) load(c);
     }
+    if (tid < kSmallRowsA) sumA[tid] = 0;
     if (warp == 0) {
         tmem_alloc(tmem_slot, Cfg::kTmemCols);
         tmem_relinquish();
@@ -200,7 +203,7 @@ __global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1)
 
     bool ok = true;
     uint32_t issued = 0;  // commits issued (MMA thread)
-    int loads = producer ? min(kSmallRaw, nchunks) : 0;  // chunks whose loads were issued (producer)
+    int loads = producer ? min(NR, nchunks) : 0;  // chunks whose loads were issued (producer)
     const bool tile_full = m0 + kSmallRowsA <= M && n0 + BN <= N;
 
     if (a_warp || b_warp) {
@@ -228,8 +231,8 @@ __global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1)
         }
 #pragma unroll 1
         for (int c = 0; c < nchunks; ++c) {
-            const int s = c % kSmallRaw, use = c / NB, buf = c - use * NB;
-            ok = __all_sync(0xffffffffu, wait_bounded(&full[s], (c / kSmallRaw) & 1u, wd));
+            const int s = c % NR, use = c / NB, buf = c - use * NB;
+            ok = __all_sync(0xffffffffu, wait_bounded(&full[s], (c / NR) & 1u, wd));
             // the MMAs of chunk c - NB read this code buffer
             if (ok && use > 0) ok = __all_sync(0xffffffffu, wait_bounded(&done[buf], (use - 1) & 1u, wd));
             if (!ok) break;  // the whole warp
@@ -279,7 +282,7 @@ __global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1)
                 const int c = nchunks - 1, use = c / NB;
                 ok = wait_bounded(&done[c - use * NB], use & 1u, wd);
             }
-            sumA[kba * kSmallRowsA + ra] = sa;
+            atomicAdd(&sumA[ra], sa);
         } else {
             // B row sums: the eight lanes of a row hold one partial sum each
 #pragma unroll
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1)
         }
     } else if (producer) {
         // ---------------------------------------------------------------- TMA producer
-        // chunk c converted: its raw slot takes chunk c + kSmallRaw
+        // chunk c converted: its raw slot takes chunk c + NR
 #pragma unroll 1
         for (int c = 0; loads < nchunks; ++c) {
             const int use = c / NB;
@@ -337,31 +340,36 @@ __global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1)
         uint8_t *tile = codes;
         const int r = (warp & 3) * 32 + lane;
         const int col0 = (warp >> 2) * kHalf;
-        const int base = 64 * K - 8 * (sumA[r] + sumA[kSmallRowsA + r]);
+        const int base = 64 * K - 8 * sumA[r];
         const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-        uint32_t v[kHalf];
-        if constexpr (kHalf == 64) {
-            uint32_t (&v0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[0]);
-            uint32_t (&v1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[32]);
-            tmem_ld_32x32b_x32(trow + col0, v0);
-            tmem_ld_32x32b_x32(trow + col0 + 32, v1);
-            tmem_ld_wait_regs(v0, v1);
-        } else {
-            uint32_t (&v0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[0]);
-            tmem_ld_32x32b_x32(trow + col0, v0);
-            tmem_ld_wait_regs(v0);
-        }
+        // 64 columns per round: two TMEM loads, one wait
+        constexpr int kRound = kHalf < 64 ? kHalf : 64;
 #pragma unroll
-        for (int q = 0; q < kHalf / 4; ++q) {
-            const int n = col0 + 4 * q;
-            const int4 sbv = *reinterpret_cast<const int4 *>(sumB + n);
-            int4 o;
-            o.x = __float2int_rn(__uint_as_float(v[4 * q + 0]) * 262144.0f) + base - 8 * sbv.x;
-            o.y = __float2int_rn(__uint_as_float(v[4 * q + 1]) * 262144.0f) + base - 8 * sbv.y;
-            o.z = __float2int_rn(__uint_as_float(v[4 * q + 2]) * 262144.0f) + base - 8 * sbv.z;
-            o.w = __float2int_rn(__uint_as_float(v[4 * q + 3]) * 262144.0f) + base - 8 * sbv.w;
-            const int chunk = ((n >> 2) & 7) ^ (r & 7);
-            *reinterpret_cast<int4 *>(tile + (n >> 5) * kSmallRowsA * 128 + r * 128 + (chunk << 4)) = o;
+        for (int c0 = 0; c0 < kHalf; c0 += kRound) {
+            uint32_t v[kRound];
+            if constexpr (kRound == 64) {
+                uint32_t (&v0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[0]);
+                uint32_t (&v1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[32]);
+                tmem_ld_32x32b_x32(trow + col0 + c0, v0);
+                tmem_ld_32x32b_x32(trow + col0 + c0 + 32, v1);
+                tmem_ld_wait_regs(v0, v1);
+            } else {
+                uint32_t (&v0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[0]);
+                tmem_ld_32x32b_x32(trow + col0 + c0, v0);
+                tmem_ld_wait_regs(v0);
+            }
+#pragma unroll
+            for (int q = 0; q < kRound / 4; ++q) {
+                const int n = col0 + c0 + 4 * q;
+                const int4 sbv = *reinterpret_cast<const int4 *>(sumB + n);
+                int4 o;
+                o.x = __float2int_rn(__uint_as_float(v[4 * q + 0]) * 262144.0f) + base - 8 * sbv.x;
+                o.y = __float2int_rn(__uint_as_float(v[4 * q + 1]) * 262144.0f) + base - 8 * sbv.y;
+                o.z = __float2int_rn(__uint_as_float(v[4 * q + 2]) * 262144.0f) + base - 8 * sbv.z;
+                o.w = __float2int_rn(__uint_as_float(v[4 * q + 3]) * 262144.0f) + base - 8 * sbv.w;
+                const int chunk = ((n >> 2) & 7) ^ (r & 7);
+                *reinterpret_cast<int4 *>(tile + (n >> 5) * kSmallRowsA * 128 + r * 128 + (chunk << 4)) = o;
+            }
         }
         fence_proxy_async_smem();  // generic writes, read next by the bulk tensor store
         named_barrier_sync(1, 32 * kSmallAWarps);
@@ -375,22 +383,20 @@ __global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1)
                 bulk_wait_group_all();  // the stores are complete before the CTA leaves
             }
         } else {
-            // write out: per instruction a warp covers 32 / kRowChunks whole rows
-            constexpr int kRowsPerInstr = 32 / kRowChunks;
-            const int q = lane % kRowChunks;
-            const int n = n0 + 4 * q;
-            const bool vec = (N & 3) == 0 && n + 4 <= N;
+            // write out row by row: kLanes lanes per row, 32 / kLanes rows per instruction
+            constexpr int kLanes = kRowChunks < 32 ? kRowChunks : 32;
+            constexpr int kRowsPerInstr = 32 / kLanes;
             constexpr int kRowsPerWarp = kSmallRowsA / kSmallAWarps;
 #pragma unroll 1
             for (int rr = warp * kRowsPerWarp; rr < (warp + 1) * kRowsPerWarp; rr += kRowsPerInstr) {
-                const int row = rr + lane / kRowChunks, m = m0 + row;
-                const int4 o = *reinterpret_cast<const int4 *>(tile + (q >> 3) * kSmallRowsA * 128 + row * 128 +
-                                                               (((q & 7) ^ (row & 7)) << 4));
-                if (m < M) {
-                    int32_t *dst = C + static_cast<int64_t>(m) * N + n;
-                    if (vec) {
-                        *reinterpret_cast<int4 *>(dst) = o;
-                    } else {
+                const int row = rr + lane / kLanes, m = m0 + row;
+#pragma unroll
+                for (int q = lane % kLanes; q < kRowChunks; q += kLanes) {
+                    const int n = n0 + 4 * q;
+                    const int4 o = *reinterpret_cast<const int4 *>(tile + (q >> 3) * kSmallRowsA * 128 + row * 128 +
+                                                                   (((q & 7) ^ (row & 7)) << 4));
+                    if (m < M) {
+                        int32_t *dst = C + static_cast<int64_t>(m) * N + n;
                         if (n + 0 < N) dst[0] = o.x;
                         if (n + 1 < N) dst[1] = o.y;
                         if (n + 2 < N) dst[2] = o.z;
@@ -412,8 +418,8 @@ __global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1)
     }
     if (producer) {
         const uint64_t t0 = globaltimer_ns();
-        for (int c = loads - kSmallRaw < 0 ? 0 : loads - kSmallRaw; c < loads; ++c)
-            while (!mbar_try_wait(&full[c % kSmallRaw], (c / kSmallRaw) & 1u) && globaltimer_ns() - t0 < limit_ns) {
+        for (int c = loads - NR < 0 ? 0 : loads - NR; c < loads; ++c)
+            while (!mbar_try_wait(&full[c % NR], (c / NR) & 1u) && globaltimer_ns() - t0 < limit_ns) {
             }
     }
     tc_fence_before();
@@ -468,7 +474,9 @@ static int launch_small(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M,
 int launch_i4i4_small(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, int bn,
                       cudaStream_t stream)
 {
-    return bn == 64 ? launch_small<64>(Ap, Bp, C, M, N, K, stream) : launch_small<128>(Ap, Bp, C, M, N, K, stream);
+    return bn == 64    ? launch_small<64>(Ap, Bp, C, M, N, K, stream)
+           : bn == 128 ? launch_small<128>(Ap, Bp, C, M, N, K, stream)
+                       : launch_small<256>(Ap, Bp, C, M, N, K, stream);
 }
 
 

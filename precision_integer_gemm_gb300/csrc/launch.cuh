@@ -524,8 +524,8 @@ int launch_skinny(const uint8_t *A, const uint8_t *Bp, int32_t *C, int M, int N,
 }
 
 int launch_i4i4(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);
-// igemm_small_kernel (gemm_small.cu): one CTA per 128 x bn output tile (bn = 64
-// or 128), for small products.
+// igemm_small_kernel (gemm_small.cu): one CTA per 128 x bn output tile (bn = 64,
+// 128 or 256), for small products.
 int launch_i4i4_small(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, int bn,
                       cudaStream_t stream);
 // igemm_small_w4a8_kernel (gemm_small.cu): one CTA per 128 weight rows x 64

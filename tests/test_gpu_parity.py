@@ -142,7 +142,9 @@ SMALL_PATH_I4I4 = [(65, 64, 32), (128, 64, 256), (129, 257, 96), (200, 130, 32),
                    (130, 1000, 160), (512, 512, 512), (1024, 2048, 1024), (1536, 1536, 1536), (2048, 2048, 512),
                    (1024, 1024, 8192), (640, 1030, 4128),
                    # 128-wide tiles in up to four waves, and one wave with a long K
-                   (2560, 2560, 1024), (1030, 8190, 544), (256, 8192, 8192)]
+                   (2560, 2560, 1024), (1030, 8190, 544), (256, 8192, 8192),
+                   # 256-wide tiles (97..128 rows, a wave of them): K tail, N % 4 != 0
+                   (128, 28672, 1024), (120, 19462, 4128)]
 
 
 @pytest.mark.parametrize("M,N,K", SMALL_PATH_I4I4)
