@@ -98,12 +98,16 @@ SkinnyPlan skinny_plan_w4a8(int M, int N, int K, int sms, int pairs, int quads)
 // (15.0), 128 x 4096 x 4096 19.1 (22.2), 512 x 4096 x 4096 33.4 (39.6, two
 // waves), 65 x 4100 x 1056 13.0 (19.1); it loses where the other paths split a
 // long K over few tiles or pack the tiles better: 300 x 777 x 4128 25.2 (21.2),
-// 96 x 11008 x 4096 37.5 (29.3), 256 x 28672 x 8192 154 (146).
+// 96 x 11008 x 4096 37.5 (29.3), 256 x 28672 x 8192 154 (146).  With 97..128
+// rows the in-kernel path's 96-activation tiles are half empty and this kernel
+// wins even over several waves: 128 x 28672 x 8192 82.6 (94.9).
 static bool use_small_w4a8(int M, int N, int K)
 {
-    if (M <= 64 || K > 4096) return false;
+    if (M <= 64 || K > 8192) return false;
     const int64_t sms = sm_count();
     const int64_t tiles = int64_t((M + 63) / 64) * ((N + 127) / 128);
+    if (M > 96 && M <= 128 && tiles >= sms) return true;
+    if (K > 4096) return false;
     if (tiles <= sms && (K <= 2048 || 3 * tiles >= sms)) return true;
     return tiles <= 2 * sms && M >= 256;
 }

@@ -159,7 +159,9 @@ def test_i4i4_small_product_path(orc, M, N, K):
 # 64-activation tiles, or two when M >= 256): M just above the skinny limit, K =
 # 32 and K tails inside a 256-k chunk, ragged M and N (N % 4 != 0), two waves.
 SMALL_PATH_W4A8 = [(65, 64, 32), (128, 128, 128), (129, 257, 96), (200, 130, 32), (300, 200, 1056),
-                   (520, 640, 1024), (1030, 1022, 1056), (65, 4100, 1056), (128, 4096, 4096), (512, 4096, 4096)]
+                   (520, 640, 1024), (1030, 1022, 1056), (65, 4100, 1056), (128, 4096, 4096), (512, 4096, 4096),
+                   # 97..128 rows over several waves, K past 4096
+                   (120, 10002, 4160)]
 
 
 @pytest.mark.parametrize("M,N,K", SMALL_PATH_W4A8)
