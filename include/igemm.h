@@ -295,6 +295,24 @@ IGEMM_API uint64_t igemm_kernels_launched(void);
 IGEMM_API int igemm_skinny_plan(int variant, int M, int N, int K, int sms, int pairs, int quads, int *out);
 
 /*
+ * Planning query, host only: the work plan of the prepared-codes kernel (the
+ * path of large products) for i4i4_gemm (variant 0) or w4a8_gemm (variant 1)
+ * on a GPU where `clusters` CTA pairs of it fit at once, checked on the host by
+ * enumerating every pair's units the way the kernel does.  Tiles run whole,
+ * round robin over the pairs, except the last partial wave, whose k blocks are
+ * dealt out evenly (stream-K): each pair takes one range of them, cut where a
+ * tile ends, and the pieces add into C.  Writes out[0] = k splits of every tile
+ * (K past 65536), out[1] = k blocks of 128 per split, out[2] = whole units,
+ * out[3] = tiles of the stream-K tail (0: none), out[4] = k blocks per pair
+ * range of the tail, out[5] = pairs launched, out[6] = 1 when every k block of
+ * every tile is covered exactly once with one unit per tile starting at k 0,
+ * else 0.  The pages have no counterpart; the plan is this library's.
+ * IGEMM_INVALID_ARGUMENT for a variant other than 0 or 1, M or N < 1, K < 32,
+ * K % 32 != 0, K past the variant's bound, clusters < 1 or a null `out`.
+ */
+IGEMM_API int igemm_ss_plan(int variant, int M, int N, int K, int clusters, int *out);
+
+/*
  * Measurement hook: arms two caller-created CUDA events for the next GEMM call
  * (any of the GEMM entry points) made by this host thread.  That call records
  * `start` on its stream right before it launches its GEMM kernel and `stop`

@@ -23,7 +23,7 @@ __all__ = [
     "fp8_blockscaled_gemm_host", "fp8_blockscaled_gemm_e5m2_host", "unpack_int4",
     "igemm_strerror",
     "igemm_last_status", "igemm_watchdog_selftest", "igemm_kernels_launched", "igemm_time_next_gemm",
-    "igemm_skinny_plan",
+    "igemm_skinny_plan", "igemm_ss_plan",
     "EXPORTED_SYMBOLS", "LIB_PATH", "build_library",
 ]
 
@@ -31,7 +31,7 @@ EXPORTED_SYMBOLS = ("i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "i4i4_gemm_ho
                     "fp8_gemm_e5m2", "fp8_blockscaled_gemm", "fp8_blockscaled_gemm_e5m2", "fp8_gemm_host",
                     "fp8_gemm_e5m2_host", "fp8_blockscaled_gemm_host", "fp8_blockscaled_gemm_e5m2_host", "pack_int4", "unpack_int4", "igemm_strerror", "igemm_last_status",
                     "igemm_watchdog_selftest", "igemm_kernels_launched",
-                    "igemm_time_next_gemm", "igemm_skinny_plan")
+                    "igemm_time_next_gemm", "igemm_skinny_plan", "igemm_ss_plan")
 
 IGEMM_OK = 0
 IGEMM_INVALID_ARGUMENT = 1
@@ -98,6 +98,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.igemm_time_next_gemm.restype = i
     lib.igemm_skinny_plan.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
     lib.igemm_skinny_plan.restype = i
+    lib.igemm_ss_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
+    lib.igemm_ss_plan.restype = i
     lib.igemm_kernels_launched.argtypes = []
     lib.igemm_kernels_launched.restype = ctypes.c_uint64
     lib.igemm_watchdog_selftest.argtypes = [ctypes.c_uint32, p]
@@ -296,6 +298,16 @@ def igemm_skinny_plan(variant: str, M: int, N: int, K: int, sms: int, pairs: int
     v = {"i4i4": 0, "w4a8": 1}[variant]
     _check(load().igemm_skinny_plan(v, M, N, K, sms, pairs, quads, out), "igemm_skinny_plan")
     return {"split": out[0], "slice_k": out[1], "ctas": out[2], "cluster": out[3]}
+
+
+def igemm_ss_plan(variant: str, M: int, N: int, K: int, clusters: int) -> dict:
+    """The prepared-codes kernel's plan for an i4i4_gemm / w4a8_gemm call on a GPU
+    where `clusters` CTA pairs fit, with the host check of its coverage (host only)."""
+    out = (ctypes.c_int * 7)()
+    v = {"i4i4": 0, "w4a8": 1}[variant]
+    _check(load().igemm_ss_plan(v, M, N, K, clusters, out), "igemm_ss_plan")
+    return {"split": out[0], "kb_per_split": out[1], "units": out[2], "tail_tiles": out[3],
+            "tail_kb": out[4], "clusters": out[5], "covered": bool(out[6])}
 
 
 def igemm_kernels_launched() -> int:

@@ -493,6 +493,14 @@ extern "C" int igemm_skinny_plan(int variant, int M, int N, int K, int sms, int 
     return kOk;
 }
 
+extern "C" int igemm_ss_plan(int variant, int M, int N, int K, int clusters, int *out)
+{
+    if ((variant != 0 && variant != 1) || M < 1 || N < 1 || K < 32 || K % 32 != 0 ||
+        K > (variant == 0 ? kMaxKI4I4 : kMaxKW4A8) || clusters < 1 || !out)
+        return kInvalidArgument;
+    return variant == 0 ? ss_plan_report_i4i4(M, N, K, clusters, out) : ss_plan_report_w4a8(M, N, K, clusters, out);
+}
+
 extern "C" const char *igemm_strerror(int code)
 {
     switch (code) {

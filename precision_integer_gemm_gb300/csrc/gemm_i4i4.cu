@@ -104,6 +104,11 @@ SkinnyPlan skinny_plan_i4i4(int M, int N, int K, int sms, int pairs, int quads)
     return skinny_plan_for<CfgI4I4Skinny64>(N, K, sms, pairs, quads);
 }
 
+int ss_plan_report_i4i4(int M, int N, int K, int clusters, int *out)
+{
+    return ss_plan_report<CfgI4I4Ss>(clusters, M, N, K, M, N, (int64_t(M) + N) * K, out);
+}
+
 int launch_i4i4(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
 {
     // K past one exact f32 accumulation: the prepared-codes path, whose plan

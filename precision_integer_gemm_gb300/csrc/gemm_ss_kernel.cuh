@@ -89,7 +89,9 @@ struct SsCfg {
     static constexpr int kCStage = 32 * 32 * 4;
     static constexpr int kOffStages = 0;
     static constexpr int kOffCStage = kOffStages + ST * kStage;
-    static constexpr int kOffBars = kOffCStage + 4 * kCStage;
+    // two staging buffers per epilogue warp: a chunk is written while the bulk
+    // store of the one before still reads the other
+    static constexpr int kOffBars = kOffCStage + 8 * kCStage;
     static constexpr int kNumBars = 3 * ST + 4 + 1;
     static constexpr int kOffMisc = ((kOffBars + 8 * kNumBars + 127) / 128) * 128;
     static constexpr int kSmemBytes = kOffMisc + 128 + 1024;  // + alignment slack
@@ -117,10 +119,12 @@ struct SsParams {
     int p_rows, q_rows;   // rows of the P and Q operands
     int p_tiles, q_tiles;
     int group_p;          // tiles run in groups of group_p P-tile slots (slot fastest)
-    int kb_total, kb_per_split, split, num_units;
-    // tail split: units from tail_from on are pieces of the last tiles, tail_split
-    // pieces of kb_per_piece k blocks per tile (split == 1), added into C
-    int tail_from, tail_split, kb_per_piece;
+    int kb_total, kb_per_split, split;
+    int num_units;        // data-parallel units (whole tiles, or k ranges of a split K), round robin
+    // stream-K tail (split == 1): the k blocks of tiles tail_from .. tail_from +
+    // tail_tiles - 1, laid end to end, go to the clusters in ranges of tail_kb
+    // (0: no tail), each range cut where a tile ends; the pieces add into C
+    int tail_from, tail_tiles, tail_kb;
     int tma_store;
     int *status;
     unsigned long long limit_ns;
@@ -128,24 +132,53 @@ struct SsParams {
 
 struct SsUnit {
     int p0, q0, kb0, nkb;
+    bool reduce;  // adds into C (zeroed before this grid) instead of storing
 };
 
-// Unit u of the cluster; a P-tile slot holds Cfg::CL P tiles, one per CTA rank.
+// Data-parallel units of cluster cid: cid, cid + ncl, ... below num_units.
+__host__ __device__ __forceinline__ int ss_dp_units(const SsParams &prm, int cid, int ncl)
+{
+    return cid < prm.num_units ? (prm.num_units - 1 - cid) / ncl + 1 : 0;
+}
+
+// Units of cluster cid: its data-parallel units, then the pieces of its tail
+// range (one per tile that the range touches).
+__host__ __device__ __forceinline__ int ss_units(const SsParams &prm, int cid, int ncl)
+{
+    int n = ss_dp_units(prm, cid, ncl);
+    if (prm.tail_kb > 0) {
+        const int a = cid * prm.tail_kb;
+        const int b = min(a + prm.tail_kb, prm.tail_tiles * prm.kb_total);
+        if (a < b) n += (b - 1) / prm.kb_total - a / prm.kb_total + 1;
+    }
+    return n;
+}
+
+// Unit i of cluster cid (n_dp = ss_dp_units of it) on CTA `rank` of the
+// cluster; a P-tile slot holds Cfg::CL P tiles, one per CTA rank.
 template <class Cfg>
-__device__ __forceinline__ SsUnit ss_unit(const SsParams &prm, int u, int rank)
+__host__ __device__ __forceinline__ SsUnit ss_unit(const SsParams &prm, int cid, int ncl, int n_dp, int i, int rank)
 {
     const int p_slots = (prm.p_tiles + Cfg::CL - 1) / Cfg::CL;
-    int tile, s, kb_per;
-    if (u < prm.tail_from) {
+    int tile, kb0, nkb;
+    bool reduce;
+    if (i < n_dp) {
+        const int u = cid + i * ncl;
         tile = u / prm.split;
-        s = u - tile * prm.split;
-        kb_per = prm.kb_per_split;
+        kb0 = (u - tile * prm.split) * prm.kb_per_split;
+        nkb = min(prm.kb_total - kb0, prm.kb_per_split);
+        reduce = prm.split > 1;
     } else {
-        // a piece of one of the last tiles (split == 1, so unit tail_from is tile tail_from)
-        const int j = u - prm.tail_from;
-        tile = prm.tail_from + j / prm.tail_split;
-        s = j % prm.tail_split;
-        kb_per = prm.kb_per_piece;
+        // piece j of the range [a, b) of the tail's k blocks
+        const int j = i - n_dp;
+        const int a = cid * prm.tail_kb;
+        const int b = min(a + prm.tail_kb, prm.tail_tiles * prm.kb_total);
+        const int t = a / prm.kb_total + j;  // tail tile
+        kb0 = j == 0 ? a - t * prm.kb_total : 0;
+        const int kend = t == (b - 1) / prm.kb_total ? b - t * prm.kb_total : prm.kb_total;
+        nkb = kend - kb0;
+        tile = prm.tail_from + t;
+        reduce = true;
     }
     // Grouped order: group_p P tiles times every Q tile, P fastest.  The CTAs
     // of one wave share a few Q tiles through L2 and the group's P tiles
@@ -161,8 +194,9 @@ __device__ __forceinline__ SsUnit ss_unit(const SsParams &prm, int u, int rank)
     SsUnit x;
     x.p0 = pt * Cfg::kPRows;
     x.q0 = qt * Cfg::QA;
-    x.kb0 = s * kb_per;
-    x.nkb = min(prm.kb_total - x.kb0, kb_per);
+    x.kb0 = kb0;
+    x.nkb = nkb;
+    x.reduce = reduce;
     return x;
 }
 
@@ -264,8 +298,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             uint32_t g = 0;  // stages (k blocks) over all units of this CTA
             uint32_t issued_mask = 0, last_phase = 0;
             bool ok = true;
-            for (int u = cid; ok && u < prm.num_units; u += ncl) {
-                const SsUnit x = ss_unit<Cfg>(prm, u, rank);
+            const int n_dp = ss_dp_units(prm, cid, ncl), n_units = ss_units(prm, cid, ncl);
+            for (int i = 0; ok && i < n_units; ++i) {
+                const SsUnit x = ss_unit<Cfg>(prm, cid, ncl, n_dp, i, rank);
                 const int nst = (x.nkb + Cfg::kKB - 1) / Cfg::kKB;
                 for (int j = 0; j < nst; ++j, ++g) {
                     const int s = static_cast<int>(g % ST);
@@ -319,8 +354,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             constexpr uint32_t idesc = idesc_f8_f32(Cfg::kMmaM, Cfg::kQRows, Cfg::kFmt);
             uint32_t g = 0, nacc = 0;
             bool ok = true;
-            for (int u = cid; ok && u < prm.num_units; u += ncl, ++nacc) {
-                const SsUnit x = ss_unit<Cfg>(prm, u, rank);
+            const int n_dp = ss_dp_units(prm, cid, ncl), n_units = ss_units(prm, cid, ncl);
+            for (int i = 0; ok && i < n_units; ++i, ++nacc) {
+                const SsUnit x = ss_unit<Cfg>(prm, cid, ncl, n_dp, i, rank);
                 const uint32_t ab = nacc % Cfg::kAccBufs;
                 const uint32_t aph = (nacc / Cfg::kAccBufs) & 1u;
                 const uint32_t d_tmem = tmem + ab * Cfg::kAccCols;
@@ -375,8 +411,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const uint32_t pfull_remote = cluster_map(smem_u32(pfull), 0u);
             uint32_t g = 0;
             bool ok = true;
-            for (int u = cid; ok && u < prm.num_units; u += ncl) {
-                const SsUnit x = ss_unit<Cfg>(prm, u, rank);
+            const int n_dp = ss_dp_units(prm, cid, ncl), n_units = ss_units(prm, cid, ncl);
+            for (int i = 0; ok && i < n_units; ++i) {
+                const SsUnit x = ss_unit<Cfg>(prm, cid, ncl, n_dp, i, rank);
                 const int nst = (x.nkb + Cfg::kKB - 1) / Cfg::kKB;
                 for (int j = 0; j < nst; ++j, ++g) {
                     const int s = static_cast<int>(g % ST);
@@ -394,24 +431,40 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         const int quad = warp;
         const int p = quad * 32 + lane;
         const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-        uint8_t *stg = cstage + quad * Cfg::kCStage;
+        uint8_t *const stg2 = cstage + 2 * quad * Cfg::kCStage;  // this warp's two staging buffers
+        uint32_t nstg = 0;                                       // chunks this warp staged so far
         const uint64_t out_policy = l2_policy_evict_first();  // C is not read again
         // where this warp releases an accumulator: the even CTA's barrier
         const uint32_t acc_empty_leader = kPair ? cluster_map(smem_u32(acc_empty), 0u) : 0u;
         uint32_t nacc = 0;
-        for (int u = cid; u < prm.num_units; u += ncl, ++nacc) {
-            const SsUnit x = ss_unit<Cfg>(prm, u, rank);
+        const int n_dp = ss_dp_units(prm, cid, ncl), n_units = ss_units(prm, cid, ncl);
+        for (int i = 0; i < n_units; ++i, ++nacc) {
+            const SsUnit x = ss_unit<Cfg>(prm, cid, ncl, n_dp, i, rank);
             // the k ranges of a split tile add into C (zeroed before this grid)
-            const bool reduce = prm.split > 1 || u >= prm.tail_from;
+            const bool reduce = x.reduce;
+            const bool magic = x.nkb * Cfg::kBK <= 16384;  // every code sum below 2^22
+            const bool first = x.kb0 == 0;                  // the split that adds the row-sum terms
+            // The unit's row sums, fetched before its accumulator is ready (a global
+            // load waits about a microsecond behind the operand stream; one per
+            // chunk serialised the epilogue): this thread's P row sum, and the Q
+            // tile's sums spread over the lanes (lane l holds entries kQPer * l ..),
+            // read back by shuffles.
+            constexpr int kQPer = Cfg::QA / 32;  // 8 (int4 x int4) or 4 (W4A8)
+            int sp = 0;
+            int4 qs0 = make_int4(0, 0, 0, 0), qs1 = qs0;
+            if constexpr (!Cfg::kFloat) {
+                if (first) {
+                    sp = __ldg(prm.sumP + min(x.p0 + p, prm.p_rows - 1));
+                    // (the sums arrays are padded past the last row by more than a tile)
+                    const int4 *sq = reinterpret_cast<const int4 *>(prm.sumQ + x.q0) + (kQPer / 4) * lane;
+                    qs0 = __ldg(sq);
+                    if constexpr (kQPer == 8) qs1 = __ldg(sq + 1);
+                }
+            }
             const uint32_t ab = nacc % Cfg::kAccBufs;
             if (!ss_warp_wait(&acc_full[ab], (nacc / Cfg::kAccBufs) & 1u, wd)) break;
             tc_fence_after();
             const uint32_t tacc = trow + ab * Cfg::kAccCols;
-            const bool magic = x.nkb * Cfg::kBK <= 16384;  // every code sum below 2^22
-            const bool first = x.kb0 == 0;                  // the split that adds the row-sum terms
-            const int prow = min(x.p0 + p, prm.p_rows - 1);
-            int sp = 0;
-            if constexpr (!Cfg::kFloat) sp = first ? __ldg(prm.sumP + prow) : 0;
             if constexpr (!Cfg::kW4A8) {
                 // C[m, n] = S - 8 sum uA[m] - 8 sum uB[n] + 64 K   (first split adds the terms)
                 const int m = x.p0 + p;
@@ -427,13 +480,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     tmem_ld_wait_regs(v);
                     const int n0 = x.q0 + c0;
                     if constexpr (!Cfg::kFloat) {
-                        // -8 sum uB of the chunk's 32 columns (the sums array is padded
-                        // past the last row, so whole chunks are readable)
-                        const int4 *sq = reinterpret_cast<const int4 *>(prm.sumQ + n0);
+                        // -8 sum uB of the chunk's 32 columns: columns c0 + 4 j .. + 3
+                        // are the first or second four entries of lane (c0 + 4 j) / 8
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
-                            const int4 q = first ? __ldg(sq + j) : make_int4(0, 0, 0, 0);
-                            const int qq[4] = {q.x, q.y, q.z, q.w};
+                            const int src = (c0 >> 3) + (j >> 1);
+                            const int4 mine = (j & 1) ? qs1 : qs0;
+                            const int qq[4] = {__shfl_sync(0xffffffffu, mine.x, src), __shfl_sync(0xffffffffu, mine.y, src),
+                                               __shfl_sync(0xffffffffu, mine.z, src),
+                                               __shfl_sync(0xffffffffu, mine.w, src)};
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const int i = 4 * j + e;
@@ -443,7 +498,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                         }
                     }  // else: v holds the float32 sums, stored as they are
                     if (prm.tma_store) {
-                        if (lane == 0) bulk_wait_group_read<0>();
+                        // one bulk group per chunk (empty when nothing is stored): at most
+                        // one pending group means the store from this buffer two chunks ago
+                        // has read it
+                        uint8_t *stg = stg2 + (nstg++ & 1u) * Cfg::kCStage;
+                        if (lane == 0) bulk_wait_group_read<1>();
                         __syncwarp();
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
@@ -452,11 +511,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                         const int y = x.p0 + quad * 32;
-                        if (lane == 0 && y < prm.M && n0 < prm.N) {
-                            if (reduce)
-                                tma_reduce_add_2d_hint(&mapC, stg, n0, y, out_policy);
-                            else
-                                tma_store_2d_hint(&mapC, stg, n0, y, out_policy);
+                        if (lane == 0) {
+                            if (y < prm.M && n0 < prm.N) {
+                                if (reduce)
+                                    tma_reduce_add_2d_hint(&mapC, stg, n0, y, out_policy);
+                                else
+                                    tma_store_2d_hint(&mapC, stg, n0, y, out_policy);
+                            }
                             bulk_commit_group();
                         }
                     } else if (m < prm.M) {
@@ -480,11 +541,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 const int n = x.p0 + p;
                 const uint32_t colterm = 0u - 128u * static_cast<uint32_t>(sp) - (magic ? 17u * kSsMagic : 0u);
                 constexpr int kChunk = Cfg::kStageRows;
-                int *sbi = reinterpret_cast<int *>(stg);
 #pragma unroll 1
                 for (int j0 = 0; j0 < QA; j0 += kChunk) {
+                    // one bulk group per chunk, as above
+                    uint8_t *stg = stg2 + (nstg & 1u) * Cfg::kCStage;
+                    int *sbi = reinterpret_cast<int *>(stg);
                     if (prm.tma_store) {
-                        if (lane == 0) bulk_wait_group_read<0>();
+                        ++nstg;
+                        if (lane == 0) bulk_wait_group_read<1>();
                         __syncwarp();
                     }
 #pragma unroll
@@ -493,11 +557,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                         tmem_ld_32x32b_x16(tacc + j0 + h, vh);
                         tmem_ld_32x32b_x16(tacc + QA + j0 + h, vl);
                         tmem_ld_wait_regs(vh, vl);
-                        const int4 *sq = reinterpret_cast<const int4 *>(prm.sumQ + x.q0 + j0 + h);
 #pragma unroll
                         for (int jj = 0; jj < 4; ++jj) {
-                            const int4 q = first ? __ldg(sq + jj) : make_int4(0, 0, 0, 0);
-                            const int qq[4] = {q.x, q.y, q.z, q.w};
+                            // sums of activation rows j0 + h + 4 jj .. + 3: lane (j0 + h) / 4 + jj
+                            const int src = ((j0 + h) >> 2) + jj;
+                            const int qq[4] = {__shfl_sync(0xffffffffu, qs0.x, src), __shfl_sync(0xffffffffu, qs0.y, src),
+                                               __shfl_sync(0xffffffffu, qs0.z, src),
+                                               __shfl_sync(0xffffffffu, qs0.w, src)};
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const int i = 4 * jj + e;
@@ -526,11 +592,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                         const int m0 = x.q0 + j0, nx = x.p0 + quad * 32;
-                        if (lane == 0 && m0 < prm.M && nx < prm.N) {
-                            if (reduce)
-                                tma_reduce_add_2d_hint(&mapC, stg, nx, m0, out_policy);
-                            else
-                                tma_store_2d_hint(&mapC, stg, nx, m0, out_policy);
+                        if (lane == 0) {
+                            if (m0 < prm.M && nx < prm.N) {
+                                if (reduce)
+                                    tma_reduce_add_2d_hint(&mapC, stg, nx, m0, out_policy);
+                                else
+                                    tma_store_2d_hint(&mapC, stg, nx, m0, out_policy);
+                            }
                             bulk_commit_group();
                         }
                     }

@@ -84,6 +84,11 @@ static int run_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N
                             stream);
 }
 
+int ss_plan_report_w4a8(int M, int N, int K, int clusters, int *out)
+{
+    return ss_plan_report<CfgW4A8Ss>(clusters, M, N, K, N, M, int64_t(N) * K + 2 * int64_t(M) * K, out);
+}
+
 SkinnyPlan skinny_plan_w4a8(int M, int N, int K, int sms, int pairs, int quads)
 {
     if (M <= 16) return skinny_plan_for<CfgW4A8Skinny16, CfgW4A8Skinny16C2, CfgW4A8Skinny16C4>(N, K, sms, pairs, quads);

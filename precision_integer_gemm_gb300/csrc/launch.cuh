@@ -2,6 +2,7 @@
 #pragma once
 #include <algorithm>
 #include <mutex>
+#include <vector>
 #include <type_traits>
 #include <cstdint>
 #include <cuda.h>
@@ -170,8 +171,8 @@ int ss_resident_ctas(Kernel k)
 struct SsPlan {
     int p_tiles, q_tiles, p_slots, group_p, kb_total;
     int split, kb_per_split;                  // every tile in `split` k ranges (split K)
-    int tail_from, tail_split, kb_per_piece;  // tiles from tail_from on: tail_split pieces each
-    int num_units, clusters;
+    int tail_from, tail_tiles, tail_kb;       // stream-K tail: ranges of tail_kb k blocks (0: none)
+    int num_units, clusters;                  // data-parallel units; clusters launched
 };
 
 // The kernel's shared-memory attribute (once per device) and the clusters that
@@ -196,16 +197,18 @@ int ss_clusters()
     return ss_resident_ctas<Cfg>(kernel) / Cfg::CL;
 }
 
-// Tail split: with T tiles on W clusters, the first (T / W) * W tiles run whole
-// and the last r = T mod W tiles run as S pieces of their k range each, S
-// chosen to minimise the time of that last partial wave (ceil(r S / W) waves of
-// 1/S of a tile); the pieces add into C, which the preparation pass zeroes for
-// those tiles.  `allow_tail` false: no tail split.
+// Stream-K tail: with T tiles on W clusters, the first (T / W) * W tiles run
+// whole (round robin) and the k blocks of the last r = T mod W tiles, laid end
+// to end, are cut into W ranges of L = ceil(r kb_total / W) blocks (whole
+// pipeline stages, at least eight of them), one per cluster; a range that
+// crosses a tile's end runs as two pieces.  Every piece adds into C, which the
+// preparation pass zeroes for those tiles.  So the last partial wave takes L
+// k blocks instead of kb_total.  `allow_tail` false (float output, whose sums
+// would depend on the order of the pieces): no tail.
 template <class Cfg>
-int ss_plan(int M, int N, int K, int p_rows, int q_rows, int64_t operand_bytes, bool allow_tail, SsPlan *pl)
+void ss_plan_for(int W, int M, int N, int K, int p_rows, int q_rows, int64_t operand_bytes, bool allow_tail,
+                 SsPlan *pl)
 {
-    const int W = ss_clusters<Cfg>();
-    if (W < 1) return kCudaError;
     pl->p_tiles = (p_rows + Cfg::kPRows - 1) / Cfg::kPRows;
     pl->q_tiles = (q_rows + Cfg::QA - 1) / Cfg::QA;
     pl->p_slots = (pl->p_tiles + Cfg::CL - 1) / Cfg::CL;
@@ -232,36 +235,90 @@ int ss_plan(int M, int N, int K, int p_rows, int q_rows, int64_t operand_bytes, 
     pl->kb_per_split = plan.kb_per_split;
     pl->num_units = tiles * plan.split;
     pl->tail_from = pl->num_units;
-    pl->tail_split = 1;
-    pl->kb_per_piece = pl->kb_total;
+    pl->tail_tiles = 0;
+    pl->tail_kb = 0;
     const int r = tiles % W;
-    if (allow_tail && plan.split == 1 && tiles > W && r > 0 && pl->kb_total >= 2 * Cfg::kKB) {
-        int best_s = 1;
-        double best = 1.0;  // the last partial wave, in tiles of time
-        for (int S = 2; S <= 8; ++S) {
-            // pieces of eight stages at least: each piece ends with an epilogue
-            // that adds its tile into C (measured: pieces of four stages made W4A8
-            // 4096^3 slower, their epilogues outlasting their main loops)
-            if ((pl->kb_total + S - 1) / S < 8 * Cfg::kKB) break;
-            const double waves = static_cast<double>((r * S + W - 1) / W) / S;
-            if (waves < best - 0.02) {
-                best = waves;
-                best_s = S;
-            }
-        }
-        if (best_s > 1) {
-            // pieces of whole pipeline stages
-            const int kbpp = ((pl->kb_total + best_s - 1) / best_s + Cfg::kKB - 1) / Cfg::kKB * Cfg::kKB;
-            const int S = (pl->kb_total + kbpp - 1) / kbpp;
-            if (S >= 2) {
-                pl->tail_from = tiles - r;
-                pl->tail_split = S;
-                pl->kb_per_piece = kbpp;
-                pl->num_units = tiles - r + r * S;
-            }
+    if (allow_tail && plan.split == 1 && tiles > W && r > 0) {
+        const int64_t blocks = int64_t(r) * pl->kb_total;
+        int L = static_cast<int>((blocks + W - 1) / W);
+        L = std::max((L + Cfg::kKB - 1) / Cfg::kKB * Cfg::kKB, 8 * Cfg::kKB);
+        // (pieces of fewer than eight stages measured slower at W4A8 4096^3:
+        // their epilogues outlast their main loops)
+        if (L + 2 * Cfg::kKB <= pl->kb_total) {
+            pl->tail_from = tiles - r;
+            pl->tail_tiles = r;
+            pl->tail_kb = L;
+            pl->num_units = tiles - r;
         }
     }
-    pl->clusters = std::min(pl->num_units, W);
+    pl->clusters = std::min(pl->tail_kb > 0 ? W : pl->num_units, W);
+}
+
+// The plan for this device: W = the clusters of igemm_ss_kernel<Cfg> that fit at once.
+template <class Cfg>
+int ss_plan(int M, int N, int K, int p_rows, int q_rows, int64_t operand_bytes, bool allow_tail, SsPlan *pl)
+{
+    const int W = ss_clusters<Cfg>();
+    if (W < 1) return kCudaError;
+    ss_plan_for<Cfg>(W, M, N, K, p_rows, q_rows, operand_bytes, allow_tail, pl);
+    return kOk;
+}
+
+// Host check of a plan on W clusters (the planning query): enumerates every
+// cluster's units as the kernel does and reports in out[0..6] split,
+// kb_per_split, data-parallel units, tail tiles, tail_kb, clusters launched,
+// and 1 when every k block of every tile is covered exactly once, each tile
+// has exactly one unit starting at k block 0 (the one that adds the row-sum
+// terms) and every unit that shares its tile with another adds into C.
+template <class Cfg>
+int ss_plan_report(int W, int M, int N, int K, int p_rows, int q_rows, int64_t operand_bytes, int *out)
+{
+    SsPlan pl;
+    ss_plan_for<Cfg>(W, M, N, K, p_rows, q_rows, operand_bytes, true, &pl);
+    SsParams prm{};
+    prm.p_tiles = pl.p_tiles;
+    prm.q_tiles = pl.q_tiles;
+    prm.group_p = pl.group_p;
+    prm.kb_total = pl.kb_total;
+    prm.kb_per_split = pl.kb_per_split;
+    prm.split = pl.split;
+    prm.num_units = pl.num_units;
+    prm.tail_from = pl.tail_from;
+    prm.tail_tiles = pl.tail_tiles;
+    prm.tail_kb = pl.tail_kb;
+    const int64_t cells = int64_t(pl.p_slots) * pl.q_tiles * pl.kb_total;
+    bool ok = cells <= (int64_t(1) << 26);
+    std::vector<uint8_t> hits(ok ? static_cast<size_t>(cells) : 0), firsts(ok ? size_t(pl.p_slots) * pl.q_tiles : 0),
+        pieces(firsts.size()), reduced(firsts.size());
+    const int ncl = pl.clusters;
+    for (int c = 0; ok && c < ncl; ++c) {
+        const int n_dp = ss_dp_units(prm, c, ncl), n = ss_units(prm, c, ncl);
+        for (int i = 0; ok && i < n; ++i) {
+            const SsUnit x = ss_unit<Cfg>(prm, c, ncl, n_dp, i, 0);
+            const int slot = x.p0 / (Cfg::kPRows * Cfg::CL), qt = x.q0 / Cfg::QA;
+            if (x.p0 % (Cfg::kPRows * Cfg::CL) || slot >= pl.p_slots || qt >= pl.q_tiles || x.nkb < 1 ||
+                x.kb0 < 0 || x.kb0 + x.nkb > pl.kb_total) {
+                ok = false;
+                break;
+            }
+            const size_t t = size_t(qt) * pl.p_slots + slot;
+            for (int k = x.kb0; k < x.kb0 + x.nkb; ++k) ok = ok && hits[t * pl.kb_total + k]++ == 0;
+            firsts[t] += x.kb0 == 0 ? 1 : 0;
+            pieces[t] += 1;
+            reduced[t] += x.reduce ? 1 : 0;
+        }
+    }
+    for (size_t t = 0; ok && t < firsts.size(); ++t) {
+        ok = firsts[t] == 1 && (pieces[t] == 1 || reduced[t] == pieces[t]);
+        for (int k = 0; ok && k < pl.kb_total; ++k) ok = hits[t * pl.kb_total + k] == 1;
+    }
+    out[0] = pl.split;
+    out[1] = pl.kb_per_split;
+    out[2] = pl.num_units;
+    out[3] = pl.tail_tiles;
+    out[4] = pl.tail_kb;
+    out[5] = pl.clusters;
+    out[6] = ok ? 1 : 0;
     return kOk;
 }
 
@@ -273,7 +330,7 @@ TailZero ss_tail_zero(const SsPlan &pl, int32_t *C, int M, int N)
     z.C = C;
     z.M = M;
     z.N = N;
-    z.tiles = pl.split == 1 ? (pl.num_units - pl.tail_from) / pl.tail_split : 0;
+    z.tiles = pl.tail_tiles;
     z.first_tile = pl.tail_from;
     z.group_p = pl.group_p;
     z.p_slots = pl.p_slots;
@@ -306,8 +363,8 @@ int launch_ss(const CUtensorMap &mapP, const CUtensorMap &mapQ, const CUtensorMa
     prm.kb_per_split = pl.kb_per_split;
     prm.split = pl.split;
     prm.tail_from = pl.tail_from;
-    prm.tail_split = pl.tail_split;
-    prm.kb_per_piece = pl.kb_per_piece;
+    prm.tail_tiles = pl.tail_tiles;
+    prm.tail_kb = pl.tail_kb;
     prm.num_units = pl.num_units;
     prm.tma_store = tma_store ? 1 : 0;
     prm.status = device_status_word();
@@ -534,6 +591,10 @@ int launch_w4a8_small(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int
 // Skinny-path plans (M <= 64) of each variant, for the planning query.
 SkinnyPlan skinny_plan_i4i4(int M, int N, int K, int sms, int pairs, int quads);
 SkinnyPlan skinny_plan_w4a8(int M, int N, int K, int sms, int pairs, int quads);
+// Prepared-codes plans of each variant on `clusters` CTA pairs, checked on the
+// host (ss_plan_report), for the planning query.
+int ss_plan_report_i4i4(int M, int N, int K, int clusters, int *out);
+int ss_plan_report_w4a8(int M, int N, int K, int clusters, int *out);
 
 // Fixed workspace of i4i4_gemm_noalloc (a file-scope device array).
 constexpr size_t kNoAllocWorkspaceBytes = size_t(32) << 20;

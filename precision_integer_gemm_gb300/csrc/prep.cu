@@ -32,23 +32,10 @@ __device__ __forceinline__ void int4_codes(uint4 w, uint4 &o0, uint4 &o1, int &s
     o1 = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-__device__ __forceinline__ int block_sum(int v, int *red)
-{
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    int t = 0;
-    if (threadIdx.x == 0)
-        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += red[w];
-    return t;
-}
-
-// Zeros in part `part` (of kZeroParts row bands) of the C region of tail tile
+// Zeros in part `part` (of `parts` row bands) of the C region of tail tile
 // `t` of the GEMM that follows (its tiles in igemm_ss_kernel's grouped order:
 // group_p P-tile slots times every Q tile, slot fastest).
-constexpr int kZeroParts = 8;
-__device__ void zero_tail_tile(const TailZero &z, int t, int part)
+__device__ void zero_tail_tile(const TailZero &z, int t, int part, int parts)
 {
     const int tile = z.first_tile + t;
     const int per_group = z.group_p * z.q_tiles;
@@ -60,7 +47,7 @@ __device__ void zero_tail_tile(const TailZero &z, int t, int part)
     const int row0 = z.q_is_row ? q0 : p0, col0 = z.q_is_row ? p0 : q0;
     const int rows = min(z.q_is_row ? z.q_cols : z.p_rows, z.M - row0);
     const int cols = min(z.q_is_row ? z.p_rows : z.q_cols, z.N - col0);
-    const int band = (rows + kZeroParts - 1) / kZeroParts;
+    const int band = (rows + parts - 1) / parts;
     const int r0 = part * band, r1 = min(rows, r0 + band);
     if (z.N % 4 == 0 && col0 % 4 == 0 && cols % 4 == 0) {
         // 16-byte stores (C is 16-byte aligned, rows a multiple of 16 bytes)
@@ -80,70 +67,115 @@ __device__ void zero_tail_tile(const TailZero &z, int t, int part)
 // First kZeroParts CTAs per tail tile of `zero` (they run among the first CTAs,
 // not after the rows); then one CTA per row: rows [0, p_rows) of the packed
 // int4 operand P, then rows [p_rows, p_rows + q_rows) of Q (packed int4, or
-// int8 when kQInt8).
+// int8 when kQInt8).  Each thread issues up to kLoads 16-byte loads before it
+// converts any of them.  Measured on GB300 (pass time at the sizes of the
+// benchmarks): W4A8 rows want more bytes in flight (64 threads x 4 loads: 2 us
+// less than 256 x 1 at 4096^3), int4 x int4 rows do not (256 x 1: 7 us less
+// than 64 x 4 at 8192^3, whose pass writes twice what it reads).
 template <bool kQInt8>
-__global__ void __launch_bounds__(256) prep_codes_kernel(const uint8_t *__restrict__ P, int p_rows,
-                                                         const uint8_t *__restrict__ Q, int q_rows, int K,
-                                                         uint8_t *__restrict__ p_codes, uint8_t *__restrict__ q_codes,
-                                                         int32_t *__restrict__ p_sums, int32_t *__restrict__ q_sums,
-                                                         const TailZero zero)
+struct PrepShape {
+    static constexpr int kThreads = kQInt8 ? 64 : 256;
+    static constexpr int kLoads = kQInt8 ? 4 : 1;
+    static constexpr int kZeroParts = 2048 / kThreads;  // CTAs per tail tile zeroed
+};
+template <bool kQInt8>
+__global__ void __launch_bounds__(PrepShape<kQInt8>::kThreads) prep_codes_kernel(
+    const uint8_t *__restrict__ P, int p_rows, const uint8_t *__restrict__ Q, int q_rows, int K,
+    uint8_t *__restrict__ p_codes, uint8_t *__restrict__ q_codes, int32_t *__restrict__ p_sums,
+    int32_t *__restrict__ q_sums, const TailZero zero)
 {
-    __shared__ int red[8];
+    constexpr int kPrepThreads = PrepShape<kQInt8>::kThreads, kPrepLoads = PrepShape<kQInt8>::kLoads;
+    constexpr int kZeroParts = PrepShape<kQInt8>::kZeroParts;
+    __shared__ int red[kPrepThreads / 32];
     // the GEMM that follows may launch now; it waits for this grid before it
     // reads any code or sum, or touches C
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int zero_ctas = kZeroParts * zero.tiles;
     if (static_cast<int>(blockIdx.x) < zero_ctas) {
-        zero_tail_tile(zero, blockIdx.x / kZeroParts, blockIdx.x % kZeroParts);
+        zero_tail_tile(zero, blockIdx.x / kZeroParts, blockIdx.x % kZeroParts, kZeroParts);
         return;
     }
+    const int t = threadIdx.x;
     const int row = blockIdx.x - zero_ctas;
     int sum = 0;
     const bool is_p = row < p_rows;
     const int r = is_p ? row : row - p_rows;
+    constexpr int kStep = kPrepThreads * kPrepLoads;
     if (is_p || !kQInt8) {
+        // 16 packed bytes -> 32 codes
+        const int n = K / 32;
         const uint4 *src = reinterpret_cast<const uint4 *>((is_p ? P : Q) + static_cast<size_t>(r) * (K / 2));
         uint4 *dst = reinterpret_cast<uint4 *>((is_p ? p_codes : q_codes) + static_cast<size_t>(r) * K);
-        for (int c = threadIdx.x; c < K / 32; c += blockDim.x) {
-            uint4 o0, o1;
-            int4_codes(src[c], o0, o1, sum);
-            dst[2 * c] = o0;
-            dst[2 * c + 1] = o1;
+        for (int c0 = t; c0 < n; c0 += kStep) {
+            uint4 w[kPrepLoads];
+#pragma unroll
+            for (int i = 0; i < kPrepLoads; ++i)
+                if (c0 + kPrepThreads * i < n) w[i] = __ldg(src + c0 + kPrepThreads * i);
+#pragma unroll
+            for (int i = 0; i < kPrepLoads; ++i) {
+                const int c = c0 + kPrepThreads * i;
+                if (c < n) {
+                    uint4 o0, o1;
+                    int4_codes(w[i], o0, o1, sum);
+                    dst[2 * c] = o0;
+                    dst[2 * c + 1] = o1;
+                }
+            }
         }
     } else {
+        // 16 int8 values -> 16 high codes and 16 low codes
+        const int n = K / 16;
         const uint4 *src = reinterpret_cast<const uint4 *>(Q + static_cast<size_t>(r) * K);
         uint4 *dh = reinterpret_cast<uint4 *>(q_codes + static_cast<size_t>(r) * K);
         uint4 *dl = reinterpret_cast<uint4 *>(q_codes + (static_cast<size_t>(q_rows) + r) * K);
-        for (int c = threadIdx.x; c < K / 16; c += blockDim.x) {
-            const uint4 w = src[c];
-            const uint32_t x[4] = {w.x, w.y, w.z, w.w};
-            uint32_t h[4], l[4];
+        for (int c0 = t; c0 < n; c0 += kStep) {
+            uint4 w[kPrepLoads];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                // (a + 128) >> 4 = ((a >> 4) & 15) ^ 8 ;  (a + 128) & 15 = a & 15
-                h[i] = ((x[i] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
-                l[i] = x[i] & 0x0F0F0F0Fu;
-                sum = __dp4a(static_cast<int>(x[i]), 0x01010101, sum);
+            for (int i = 0; i < kPrepLoads; ++i)
+                if (c0 + kPrepThreads * i < n) w[i] = __ldg(src + c0 + kPrepThreads * i);
+#pragma unroll
+            for (int i = 0; i < kPrepLoads; ++i) {
+                const int c = c0 + kPrepThreads * i;
+                if (c < n) {
+                    const uint32_t x[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+                    uint32_t h[4], l[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        // (a + 128) >> 4 = ((a >> 4) & 15) ^ 8 ;  (a + 128) & 15 = a & 15
+                        h[j] = ((x[j] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+                        l[j] = x[j] & 0x0F0F0F0Fu;
+                        sum = __dp4a(static_cast<int>(x[j]), 0x01010101, sum);
+                    }
+                    dh[c] = make_uint4(h[0], h[1], h[2], h[3]);
+                    dl[c] = make_uint4(l[0], l[1], l[2], l[3]);
+                }
             }
-            dh[c] = make_uint4(h[0], h[1], h[2], h[3]);
-            dl[c] = make_uint4(l[0], l[1], l[2], l[3]);
         }
     }
-    const int t = block_sum(sum, red);
-    if (threadIdx.x == 0) (is_p ? p_sums : q_sums)[r] = t;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
+    if ((t & 31) == 0) red[t >> 5] = sum;
+    __syncthreads();
+    if (t == 0) {
+        int total = 0;
+#pragma unroll
+        for (int w = 0; w < kPrepThreads / 32; ++w) total += red[w];
+        (is_p ? p_sums : q_sums)[r] = total;
+    }
 }
 
 int launch_prep(const uint8_t *P, int p_rows, const uint8_t *Q, int q_rows, bool q_int8, int K, uint8_t *p_codes,
                 uint8_t *q_codes, int32_t *p_sums, int32_t *q_sums, const TailZero &zero, cudaStream_t stream)
 {
-    const unsigned grid = static_cast<unsigned>(p_rows) + static_cast<unsigned>(q_rows) +
-                          static_cast<unsigned>(kZeroParts * zero.tiles);
+    const unsigned rows = static_cast<unsigned>(p_rows) + static_cast<unsigned>(q_rows);
     if (q_int8)
-        prep_codes_kernel<true><<<grid, 256, 0, stream>>>(P, p_rows, Q, q_rows, K, p_codes, q_codes, p_sums, q_sums,
-                                                          zero);
+        prep_codes_kernel<true>
+            <<<rows + PrepShape<true>::kZeroParts * zero.tiles, PrepShape<true>::kThreads, 0, stream>>>(
+                P, p_rows, Q, q_rows, K, p_codes, q_codes, p_sums, q_sums, zero);
     else
-        prep_codes_kernel<false><<<grid, 256, 0, stream>>>(P, p_rows, Q, q_rows, K, p_codes, q_codes, p_sums, q_sums,
-                                                           zero);
+        prep_codes_kernel<false>
+            <<<rows + PrepShape<false>::kZeroParts * zero.tiles, PrepShape<false>::kThreads, 0, stream>>>(
+                P, p_rows, Q, q_rows, K, p_codes, q_codes, p_sums, q_sums, zero);
     note_launch();
     return cudaGetLastError() == cudaSuccess ? kOk : kCudaError;
 }

@@ -35,6 +35,13 @@ int main(void)
     EXPECT(plan[0] >= 1 && plan[1] > 0 && plan[1] % 256 == 0 && plan[2] >= 1 && plan[2] <= 152);
     EXPECT(plan[3] == 1 || plan[3] == 2 || plan[3] == 4);
     EXPECT(igemm_skinny_plan(1, 65, 28672, 8192, 152, 76, 36, plan) == IGEMM_INVALID_ARGUMENT);
+    {
+        int ss[7] = {0};
+        /* W4A8 4096^3 on 76 pairs: 512 tiles, the last 56 dealt out as ranges of k blocks */
+        EXPECT(igemm_ss_plan(1, 4096, 4096, 4096, 76, ss) == IGEMM_OK);
+        EXPECT(ss[0] == 1 && ss[3] == 56 && ss[4] > 0 && ss[4] < 32 && ss[5] == 76 && ss[6] == 1);
+        EXPECT(igemm_ss_plan(2, 4096, 4096, 4096, 76, ss) == IGEMM_INVALID_ARGUMENT);
+    }
     printf("c abi ok: split %d, slice %d, ctas %d, cluster %d\n", plan[0], plan[1], plan[2], plan[3]);
     return 0;
 }

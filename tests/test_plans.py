@@ -76,3 +76,52 @@ def test_plan_argument_validation(lib):
     assert f(1, 16, 128, 256, 0, 0, 0, out) == pig.IGEMM_INVALID_ARGUMENT
     assert f(1, 16, 128, 256, 152, 0, 0, None) == pig.IGEMM_INVALID_ARGUMENT
     assert f(1, 16, 128, 256, 152, 0, 0, out) == pig.IGEMM_OK
+
+
+# ---------------------------------------------------------------- prepared-codes plan
+# The large-product kernel runs whole tiles round robin over the CTA pairs and
+# deals the k blocks of the last partial wave out evenly (stream-K).  The query
+# enumerates every pair's units with the kernel's own unit function and checks
+# that each k block of each tile is computed exactly once.
+
+def ss_plan(variant, M, N, K, clusters=76):
+    return pig.igemm_ss_plan(variant, M, N, K, clusters)
+
+
+def test_ss_plan_of_the_benchmark_shapes(lib):
+    # W4A8 4096^3: 16 pair slots of weights x 32 activation tiles = 512 tiles,
+    # 6 whole waves of 76 and 56 tiles of 32 k blocks dealt out as 24-block ranges
+    p = ss_plan("w4a8", 4096, 4096, 4096)
+    assert p == {"split": 1, "kb_per_split": 32, "units": 456, "tail_tiles": 56, "tail_kb": 24,
+                 "clusters": 76, "covered": True}
+    # int4 x int4 8192^3: 1024 tiles, 36 left over; 36 * 64 / 76 -> 32 blocks: two pieces a tile
+    p = ss_plan("i4i4", 8192, 8192, 8192)
+    assert (p["tail_tiles"], p["tail_kb"], p["units"], p["covered"]) == (36, 32, 988, True)
+    # ragged W4A8 4000 x 12288 x 5120: 48 x 32 tiles, 16 left over; ranges of at
+    # least eight stages (16 blocks) over 40 pairs
+    p = ss_plan("w4a8", 4000, 12288, 5120)
+    assert (p["tail_tiles"], p["tail_kb"], p["covered"]) == (16, 16, True)
+    # fewer tiles than pairs (32): K split in two, one unit per pair, no tail
+    p = ss_plan("i4i4", 1024, 2048, 4096)
+    assert (p["split"], p["tail_tiles"], p["units"], p["clusters"], p["covered"]) == (2, 0, 64, 64, True)
+
+
+@pytest.mark.parametrize("variant", ["i4i4", "w4a8"])
+def test_ss_plan_invariants(lib, variant):
+    Ms = [512, 768, 1000, 2048, 4000, 8192]
+    Ns = [512, 1000, 4096, 12288]
+    Ks = [32, 256, 1056, 4096, 5120, 8192, 65536, 70016]
+    for M, N, K, W in itertools.product(Ms, Ns, Ks, [76, 74, 13, 1]):
+        p = ss_plan(variant, M, N, K, W)
+        assert p["covered"], (variant, M, N, K, W, p)
+        kb_total = -(-K // 128)
+        assert 1 <= p["clusters"] <= W
+        assert p["split"] * p["kb_per_split"] >= kb_total
+        # one exact f32 accumulation covers at most 512 k blocks
+        assert p["kb_per_split"] <= 512
+        if p["tail_tiles"]:
+            assert p["split"] == 1 and p["clusters"] == W
+            assert p["units"] % W == 0 and 0 < p["tail_tiles"] < W
+            assert p["tail_kb"] % 2 == 0 and 16 <= p["tail_kb"] <= kb_total - 4
+            # the ranges cover the tail: no pair takes two
+            assert p["tail_kb"] * W >= p["tail_tiles"] * kb_total
