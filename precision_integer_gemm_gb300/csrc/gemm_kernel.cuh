@@ -754,7 +754,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 mbar_arrive(&sum_empty[rs.idx]);
             }
         }
-        if (lane == 0) bulk_wait_group_all();
+        if (lane == 0) bulk_wait_group_read<0>();  // the staging is read before the CTA leaves
     }
 
     // ---------------------------------------------------------------- teardown

@@ -380,7 +380,9 @@ __global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1)
                 for (int b = 0; b < BN / 32; ++b)
                     if (n0 + 32 * b < N) tma_store_2d(&mapC, tile + b * kSmallRowsA * 128, n0 + 32 * b, m0);
                 bulk_commit_group();
-                bulk_wait_group_all();  // the stores are complete before the CTA leaves
+                // the stores have read the tile before the CTA leaves (their writes
+                // complete on their own; the grid boundary makes them visible)
+                bulk_wait_group_read<0>();
             }
         } else {
             // write out row by row: kLanes lanes per row, 32 / kLanes rows per instruction

@@ -529,7 +529,6 @@ __device__ __forceinline__ void bulk_wait_group_read()
 }
 
 // Wait until every committed bulk group has fully completed.
-__device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Shared-memory matrix descriptor for a K-major operand in the 128-byte
 // swizzled canonical layout: rows of 128 bytes, groups of 8 rows 1024 bytes
