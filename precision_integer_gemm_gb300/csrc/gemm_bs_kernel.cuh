@@ -49,12 +49,12 @@ struct BsParams {
     unsigned long long limit_ns;
 };
 
-template <int ST_, int SS_, int EPQ_ = 2, int PB_ = 4, int CL_ = 1, int FMT_ = 0>
+template <int ST_, int SS_, int EPQ_ = 2, int PB_ = 4, int CL_ = 1, int FMT_ = 0, int CW_ = 64>
 struct BsCfg {
     static constexpr int ST = ST_;          // operand stages (A + B of one 128-k block)
     static constexpr int SS = SS_;          // scale stages
     static constexpr int EPQ = EPQ_;        // epilogue warps per TMEM lane quadrant
-    static constexpr int CW = 64;           // partial-tile columns per epilogue warp
+    static constexpr int CW = CW_;          // partial-tile columns per epilogue warp
     static constexpr int BN = CW * EPQ;     // tile width (B rows)
     // partial-tile buffers in TMEM: the MMAs run up to PB - 1 blocks ahead of the
     // promotion
@@ -78,7 +78,8 @@ struct BsCfg {
     static_assert(SS % kScaleIssuers == 0, "each scale lane owns fixed stages");
     static constexpr int kWarpProd = kEpiWarps, kWarpMma = kEpiWarps + 1;
     static constexpr int kThreads = 32 * (kEpiWarps + 2);
-    static_assert(EPQ >= 2 && EPQ <= 3, "epilogue warps per quadrant (the totals' registers)");
+    static_assert(EPQ >= 2 && EPQ <= 5, "epilogue warps per quadrant");
+    static_assert(CW % 16 == 0 && CW <= 64, "columns per epilogue warp: whole 16-column TMEM loads");
     static_assert(CL == 1 || CL == 2, "cluster size");
     static_assert(FMT_ == 0 || FMT_ == 1, "fp8 format");
     static constexpr int kTmemCols = PB * BN <= 256 ? 256 : 512;  // PB partial buffers of BN columns
@@ -317,9 +318,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         const int r = quad * 32 + lane;  // tile row = TMEM lane
         const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) + part * CW;
         // block G (counted over all tiles of the CTA): partial buffer G % PB, its
-        // use G / PB; scale stage G % SS, its use G / SS.  The 64 columns go
-        // through registers 32 at a time (the totals take 64 registers already;
-        // 16 at a time measured 2.5 % slower).
+        // use G / PB; scale stage G % SS, its use G / SS.  The CW columns go
+        // through registers 16 at a time in two alternating register sets: the
+        // TMEM load of the next 16 columns is in flight while the current ones
+        // are scaled (one exposed load latency per block instead of one per
+        // chunk; the totals take CW registers already).
         auto block = [&](float (&tot)[CW], uint32_t G) -> bool {
             const uint32_t pb = G % Cfg::PB;
             const int ss = static_cast<int>(G % SS);
@@ -328,19 +331,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             tc_fence_after();
             const float *sc = scales + ss * (Cfg::kScaleStage / 4);
             const float sa = sc[r];
-#pragma unroll
-            for (int c = 0; c < CW; c += 32) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tbase + pb * Cfg::BN + c, v);
-                tmem_ld_wait_regs(v);
-                if (c + 32 == CW) {  // the partial buffer may be rewritten
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&p_empty[pb]);
-                }
+            const uint32_t tb = tbase + pb * Cfg::BN;
+            // columns c .. c + 15 of this warp's part, scaled and added into the totals
+            auto scale16 = [&](const uint32_t (&v)[16], int c) {
                 const float4 *sb4 = reinterpret_cast<const float4 *>(sc + 128 + part * CW + c);
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
+                for (int j4 = 0; j4 < 4; ++j4) {
                     const float4 b = sb4[j4];
                     float *t = tot + c + 4 * j4;
                     fma2_scaled(t[0], t[1], __uint_as_float(v[4 * j4 + 0]), __uint_as_float(v[4 * j4 + 1]), b.x, b.y,
@@ -348,6 +344,22 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     fma2_scaled(t[2], t[3], __uint_as_float(v[4 * j4 + 2]), __uint_as_float(v[4 * j4 + 3]), b.z, b.w,
                                 sa);
                 }
+            };
+            constexpr int kChunks = CW / 16;
+            uint32_t v[2][16];
+            tmem_ld_32x32b_x16(tb, v[0]);
+            tmem_ld_wait_regs(v[0]);
+#pragma unroll
+            for (int i = 0; i < kChunks; ++i) {
+                if (i + 1 < kChunks) {
+                    tmem_ld_32x32b_x16(tb + 16 * (i + 1), v[(i + 1) & 1]);  // in flight while chunk i is scaled
+                } else {  // every column of the partial is in registers: it may be rewritten
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&p_empty[pb]);
+                }
+                scale16(v[i & 1], 16 * i);
+                if (i + 1 < kChunks) tmem_ld_wait_regs(v[(i + 1) & 1]);
             }
             fence_proxy_async_smem();  // generic reads before the bulk copy refills the stage
             __syncwarp();

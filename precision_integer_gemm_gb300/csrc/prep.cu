@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(PrepShape<kQInt8>::kThreads) prep_codes_kernel
     constexpr int kPrepThreads = PrepShape<kQInt8>::kThreads, kPrepLoads = PrepShape<kQInt8>::kLoads;
     constexpr int kZeroParts = PrepShape<kQInt8>::kZeroParts;
     __shared__ int red[kPrepThreads / 32];
+    __shared__ uint4 xpose[kPrepThreads / 32][64];  // per warp: its 64 output chunks
     // the GEMM that follows may launch now; it waits for this grid before it
     // reads any code or sum, or touches C
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -106,20 +107,29 @@ __global__ void __launch_bounds__(PrepShape<kQInt8>::kThreads) prep_codes_kernel
         const int n = K / 32;
         const uint4 *src = reinterpret_cast<const uint4 *>((is_p ? P : Q) + static_cast<size_t>(r) * (K / 2));
         uint4 *dst = reinterpret_cast<uint4 *>((is_p ? p_codes : q_codes) + static_cast<size_t>(r) * K);
-        for (int c0 = t; c0 < n; c0 += kStep) {
+        // Thread c makes output chunks 2 c and 2 c + 1; stored as they come, a warp's
+        // store would write 16 bytes of every other 16 (half sectors).  The warp
+        // passes its 64 chunks through shared memory instead and stores them as two
+        // contiguous 512-byte runs.  (The loop runs warp by warp: every lane of a
+        // warp takes the same iterations.)
+        const int lane = t & 31;
+        uint4 *xp = xpose[t >> 5];
+        for (int base = t - lane; base < n; base += kStep) {
             uint4 w[kPrepLoads];
 #pragma unroll
             for (int i = 0; i < kPrepLoads; ++i)
-                if (c0 + kPrepThreads * i < n) w[i] = __ldg(src + c0 + kPrepThreads * i);
+                if (base + lane + kPrepThreads * i < n) w[i] = __ldg(src + base + lane + kPrepThreads * i);
 #pragma unroll
             for (int i = 0; i < kPrepLoads; ++i) {
-                const int c = c0 + kPrepThreads * i;
-                if (c < n) {
-                    uint4 o0, o1;
-                    int4_codes(w[i], o0, o1, sum);
-                    dst[2 * c] = o0;
-                    dst[2 * c + 1] = o1;
-                }
+                const int cw = base + kPrepThreads * i;  // the warp's first chunk
+                uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+                if (cw + lane < n) int4_codes(w[i], o0, o1, sum);
+                __syncwarp();
+                xp[2 * lane] = o0;
+                xp[2 * lane + 1] = o1;
+                __syncwarp();
+                if (2 * cw + lane < 2 * n) dst[2 * cw + lane] = xp[lane];
+                if (2 * cw + 32 + lane < 2 * n) dst[2 * cw + 32 + lane] = xp[32 + lane];
             }
         }
     } else {
