@@ -221,7 +221,10 @@ CODES_I4I4 = [(8192, 2048, 32), (8200, 2056, 96), (2049, 2050, 4128), (8192, 205
               (1024, 4100, 8224),
               # more tiles than CTA pairs: the last tiles run as k pieces added into C
               # (N % 4 != 0: scalar atomic adds)
-              (2560, 2050, 4096), (4096, 4096, 4096)]
+              (2560, 2050, 4096), (4096, 4096, 4096),
+              # stream-K ranges of 28 k blocks that cross tile ends (on 76 pairs), with
+              # bulk reduce-adds, and with a K tail, ragged M and N and scalar atomics
+              (2304, 3072, 8192), (2300, 3070, 8160)]
 
 
 @pytest.mark.parametrize("M,N,K", CODES_I4I4)
@@ -233,7 +236,10 @@ def test_i4i4_prepared_codes_path(orc, M, N, K):
 
 
 CODES_W4A8 = [(1024, 4096, 32), (1030, 4100, 4160), (2000, 2100, 1056), (1024, 4096, 65536), (1024, 4098, 384),
-              (1030, 4102, 4160)]
+              (1030, 4102, 4160),
+              # stream-K ranges that cross tile ends (on 76 pairs) over a K tail, with bulk
+              # reduce-adds and with scalar atomics (N % 4 != 0)
+              (1000, 4100, 4160), (1000, 4098, 4160)]
 
 
 @pytest.mark.parametrize("M,N,K", CODES_W4A8)

@@ -125,3 +125,13 @@ def test_ss_plan_invariants(lib, variant):
             assert p["tail_kb"] % 2 == 0 and 16 <= p["tail_kb"] <= kb_total - 4
             # the ranges cover the tail: no pair takes two
             assert p["tail_kb"] * W >= p["tail_tiles"] * kb_total
+
+
+def test_ss_plan_parity_shapes_cross_tile_ends(lib):
+    # the GPU parity cases for the stream-K tail: on 76 pairs their ranges of 28 k
+    # blocks do not divide the tiles' k blocks, so ranges cross tile ends
+    for variant, M, N, K in [("i4i4", 2304, 3072, 8192), ("i4i4", 2300, 3070, 8160),
+                             ("w4a8", 1000, 4100, 4160), ("w4a8", 1000, 4098, 4160)]:
+        p = ss_plan(variant, M, N, K)
+        kb_total = -(-K // 128)
+        assert p["covered"] and p["tail_tiles"] > 1 and kb_total % p["tail_kb"] != 0, (variant, M, N, K, p)
