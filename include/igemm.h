@@ -313,6 +313,21 @@ IGEMM_API int igemm_skinny_plan(int variant, int M, int N, int K, int sms, int p
 IGEMM_API int igemm_ss_plan(int variant, int M, int N, int K, int clusters, int *out);
 
 /*
+ * Routing query, host only: the path an i4i4_gemm (variant 0) or w4a8_gemm
+ * (variant 1) call of this shape takes on a GPU with `sms` SMs where `pairs`
+ * clusters of two and `quads` clusters of four of the skinny kernel fit (the
+ * calls use the same decisions, with the device's own counts).  Writes *route:
+ * 0 = skinny kernel (M <= 64: split K, activation codes resident), 1 =
+ * small-product kernel (one CTA per output tile), 2 = prepared codes (a pass
+ * writes both operands' codes, then the CTA-pair kernel), 3 = in-kernel
+ * unpacking kernel, 4 = prepared activation codes with the weights expanded in
+ * the CTA-pair kernel (W4A8 only).  IGEMM_INVALID_ARGUMENT for a variant other
+ * than 0 or 1, M or N < 1, K < 32, K % 32 != 0, K past the variant's bound,
+ * sms < 1, negative cluster counts or a null `route`.
+ */
+IGEMM_API int igemm_route(int variant, int M, int N, int K, int sms, int pairs, int quads, int *route);
+
+/*
  * Measurement hook: arms two caller-created CUDA events for the next GEMM call
  * (any of the GEMM entry points) made by this host thread.  That call records
  * `start` on its stream right before it launches its GEMM kernel and `stop`

@@ -23,7 +23,7 @@ __all__ = [
     "fp8_blockscaled_gemm_host", "fp8_blockscaled_gemm_e5m2_host", "unpack_int4",
     "igemm_strerror",
     "igemm_last_status", "igemm_watchdog_selftest", "igemm_kernels_launched", "igemm_time_next_gemm",
-    "igemm_skinny_plan", "igemm_ss_plan",
+    "igemm_skinny_plan", "igemm_ss_plan", "igemm_route",
     "EXPORTED_SYMBOLS", "LIB_PATH", "build_library",
 ]
 
@@ -31,7 +31,7 @@ EXPORTED_SYMBOLS = ("i4i4_gemm", "i4i4_gemm_noalloc", "w4a8_gemm", "i4i4_gemm_ho
                     "fp8_gemm_e5m2", "fp8_blockscaled_gemm", "fp8_blockscaled_gemm_e5m2", "fp8_gemm_host",
                     "fp8_gemm_e5m2_host", "fp8_blockscaled_gemm_host", "fp8_blockscaled_gemm_e5m2_host", "pack_int4", "unpack_int4", "igemm_strerror", "igemm_last_status",
                     "igemm_watchdog_selftest", "igemm_kernels_launched",
-                    "igemm_time_next_gemm", "igemm_skinny_plan", "igemm_ss_plan")
+                    "igemm_time_next_gemm", "igemm_skinny_plan", "igemm_ss_plan", "igemm_route")
 
 IGEMM_OK = 0
 IGEMM_INVALID_ARGUMENT = 1
@@ -100,6 +100,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.igemm_skinny_plan.restype = i
     lib.igemm_ss_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
     lib.igemm_ss_plan.restype = i
+    lib.igemm_route.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
+    lib.igemm_route.restype = i
     lib.igemm_kernels_launched.argtypes = []
     lib.igemm_kernels_launched.restype = ctypes.c_uint64
     lib.igemm_watchdog_selftest.argtypes = [ctypes.c_uint32, p]
@@ -298,6 +300,18 @@ def igemm_skinny_plan(variant: str, M: int, N: int, K: int, sms: int, pairs: int
     v = {"i4i4": 0, "w4a8": 1}[variant]
     _check(load().igemm_skinny_plan(v, M, N, K, sms, pairs, quads, out), "igemm_skinny_plan")
     return {"split": out[0], "slice_k": out[1], "ctas": out[2], "cluster": out[3]}
+
+
+ROUTES = ("skinny", "small", "codes", "in-kernel", "packed")
+
+
+def igemm_route(variant: str, M: int, N: int, K: int, sms: int = 152, pairs: int = 76, quads: int = 36) -> str:
+    """The path an i4i4_gemm / w4a8_gemm call of this shape takes on a GPU with `sms`
+    SMs and room for `pairs` / `quads` skinny clusters (host only)."""
+    out = ctypes.c_int()
+    v = {"i4i4": 0, "w4a8": 1}[variant]
+    _check(load().igemm_route(v, M, N, K, sms, pairs, quads, ctypes.byref(out)), "igemm_route")
+    return ROUTES[out.value]
 
 
 def igemm_ss_plan(variant: str, M: int, N: int, K: int, clusters: int) -> dict:

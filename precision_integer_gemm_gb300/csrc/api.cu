@@ -493,6 +493,15 @@ extern "C" int igemm_skinny_plan(int variant, int M, int N, int K, int sms, int 
     return kOk;
 }
 
+extern "C" int igemm_route(int variant, int M, int N, int K, int sms, int pairs, int quads, int *route)
+{
+    if ((variant != 0 && variant != 1) || M < 1 || N < 1 || K < 32 || K % 32 != 0 ||
+        K > (variant == 0 ? kMaxKI4I4 : kMaxKW4A8) || sms < 1 || pairs < 0 || quads < 0 || !route)
+        return kInvalidArgument;
+    *route = variant == 0 ? route_i4i4(M, N, K, sms, pairs, quads) : route_w4a8(M, N, K, sms, pairs, quads);
+    return kOk;
+}
+
 extern "C" int igemm_ss_plan(int variant, int M, int N, int K, int clusters, int *out)
 {
     if ((variant != 0 && variant != 1) || M < 1 || N < 1 || K < 32 || K % 32 != 0 ||

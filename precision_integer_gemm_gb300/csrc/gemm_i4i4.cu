@@ -52,9 +52,8 @@ static bool use_codes_i4i4(int M, int N)
 // 96-row tiles half empty and 128-wide tiles overflow a wave: 128 x 28672 x
 // 8192 54.0 us (72.4); with 96 rows or fewer columns they lose (96 x 28672 x
 // 8192 58.0 vs 47.8; 128 x 16384 x 4096 31.4 vs 21.1).
-static int small_tile_width(int M, int N, int K)
+static int small_tile_width(int M, int N, int K, int64_t sms)
 {
-    const int64_t sms = sm_count();
     const int64_t rows = (M + 127) / 128;
     const int64_t t64 = rows * ((N + 63) / 64), t128 = rows * ((N + 127) / 128);
     if (t64 <= sms && (K <= 4096 || (K <= 8192 && 2 * t64 >= sms))) return 64;
@@ -104,6 +103,15 @@ SkinnyPlan skinny_plan_i4i4(int M, int N, int K, int sms, int pairs, int quads)
     return skinny_plan_for<CfgI4I4Skinny64>(N, K, sms, pairs, quads);
 }
 
+int route_i4i4(int M, int N, int K, int sms, int pairs, int quads)
+{
+    if (K > kMaxK) return kRouteCodes;
+    if (M <= 64 && skinny_plan_i4i4(M, N, K, sms, pairs, quads).ctas >= 1) return kRouteSkinny;
+    if (small_tile_width(M, N, K, sms)) return kRouteSmall;
+    if (use_codes_i4i4(M, N)) return kRouteCodes;
+    return kRouteInKernel;
+}
+
 int ss_plan_report_i4i4(int M, int N, int K, int clusters, int *out)
 {
     return ss_plan_report<CfgI4I4Ss>(clusters, M, N, K, M, N, (int64_t(M) + N) * K, out);
@@ -124,7 +132,7 @@ int launch_i4i4(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, int N, 
                                : launch_skinny<CfgI4I4Skinny64>(Ap, Bp, C, M, N, K, stream);
         if (rc != kUnsupportedShape) return rc;
     }
-    if (const int bn = small_tile_width(M, N, K)) return launch_i4i4_small(Ap, Bp, C, M, N, K, bn, stream);
+    if (const int bn = small_tile_width(M, N, K, sm_count())) return launch_i4i4_small(Ap, Bp, C, M, N, K, bn, stream);
     if (use_codes_i4i4(M, N)) return run_i4i4_codes(Ap, Bp, C, M, N, K, stream);
     using Cfg = CfgI4I4;
     CUtensorMap mapA, mapB, mapC32 = {}, mapC31 = {};

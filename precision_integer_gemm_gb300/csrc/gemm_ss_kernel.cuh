@@ -51,9 +51,16 @@
 
 namespace igemm {
 
-template <bool W4A8, int BN_, int ST_, int CL_ = 1, bool FLOAT_ = false, int FMT_ = 0, int KB_ = 1>
+template <bool W4A8, int BN_, int ST_, int CL_ = 1, bool FLOAT_ = false, int FMT_ = 0, int KB_ = 1,
+          bool PACKED_P_ = false>
 struct SsCfg {
     static constexpr bool kW4A8 = W4A8;
+    // kPackedP: the P operand arrives as packed int4 rows, 64 bytes a row per k
+    // block, and four converter warps expand it in place into e4m3 codes, summing
+    // each row's codes over the unit (no preparation pass over P).  The packed
+    // rows of converter warp w (P rows 32 w ..) land in the upper half of the
+    // 4 KB that its rows' codes take, so a warp overwrites only its own input.
+    static constexpr bool kPackedP = PACKED_P_;
     // kFloat: plain fp8 operands (the fp8 GEMM), C = the float32 accumulator;
     // kFmt: their format, 0 = E4M3 (also the integer codes), 1 = E5M2
     static constexpr bool kFloat = FLOAT_;
@@ -92,10 +99,16 @@ struct SsCfg {
     // two staging buffers per epilogue warp: a chunk is written while the bulk
     // store of the one before still reads the other
     static constexpr int kOffBars = kOffCStage + 8 * kCStage;
-    static constexpr int kNumBars = 3 * ST + 4 + 1;
+    // full, pfull, empty [ST]; acc_full, acc_empty [2]; mma_drain; packed P: conv
+    // [ST], psum_full, psum_free [2]
+    static constexpr int kNumBars = 3 * ST + 4 + 1 + (kPackedP ? ST + 4 : 0);
     static constexpr int kOffMisc = ((kOffBars + 8 * kNumBars + 127) / 128) * 128;
-    static constexpr int kSmemBytes = kOffMisc + 128 + 1024;  // + alignment slack
-    static constexpr int kThreads = 6 * 32;
+    static constexpr int kOffPSum = kOffMisc + 128;  // packed P: [2][128] row sums of a unit's codes
+    static constexpr int kSmemBytes = kOffPSum + (kPackedP ? 2 * 128 * 4 : 0) + 1024;  // + alignment slack
+    static constexpr int kWarpConv = 6;  // packed P: warps 6-9 convert (one P row per thread)
+    static constexpr int kThreads = (kPackedP ? 10 : 6) * 32;
+    static constexpr int kRawA = kPRows * kBK / 2;   // packed bytes of one k block of P
+    static_assert(!kPackedP || (W4A8 && !FLOAT_), "packed P: the W4A8 weights");
     static_assert(kQRows % 16 == 0 && kQRows <= 256, "MMA N");
     static_assert(CL == 1 || (kQRows % 32 == 0 && kQRows >= 64), "MMA N of an M = 256 pair MMA");
     static_assert(!W4A8 || QA % 8 == 0, "high and low blocks start on 1024-byte boundaries");
@@ -240,6 +253,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     uint64_t *acc_full = empty + ST;    // [2] accumulator complete (commit)
     uint64_t *acc_empty = acc_full + 2; // [2] accumulator drained (the epilogue warps of the pair)
     uint64_t *mma_drain = acc_empty + 2;
+    uint64_t *conv = mma_drain + 1;     // [ST] packed P: this CTA's P codes of a stage written (4 converter warps)
+    uint64_t *psum_full = conv + ST;    // [2] packed P: a unit's P row sums written (4 converter warps)
+    uint64_t *psum_free = psum_full + 2;  // [2] packed P: ... and read (this CTA's 4 epilogue warps)
+    int *psum = reinterpret_cast<int *>(smem + Cfg::kOffPSum);  // [2][128]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
 
@@ -261,6 +278,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             mbar_init(&acc_empty[b], 4 * Cfg::CL);  // 4 epilogue warps per CTA of the pair
         }
         mbar_init(mma_drain, 1);
+        if constexpr (Cfg::kPackedP) {
+            for (int s = 0; s < ST; ++s) mbar_init(&conv[s], 4);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&psum_full[b], 4);
+                mbar_init(&psum_free[b], 4);
+            }
+        }
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_map(&mapP);
@@ -313,13 +337,20 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     uint8_t *st = stages + s * Cfg::kStage;
                     // every box of the stage is loaded (a last stage with one k block of
                     // the unit loads the next block too, unused: zeros past K)
-                    mbar_arrive_expect_tx(&full[s], Cfg::kStage);
+                    mbar_arrive_expect_tx(&full[s], Cfg::kPackedP ? Cfg::kKB * (Cfg::kRawA + Cfg::kBoxB) : Cfg::kStage);
 #pragma unroll
                     for (int b = 0; b < Cfg::kKB; ++b) {
                         const int kx = (x.kb0 + j * Cfg::kKB + b) * Cfg::kBK;
                         uint8_t *sa = st + b * Cfg::kBoxA;
                         uint8_t *sb = st + Cfg::kStageA + b * Cfg::kBoxB;
-                        tma_load_2d_hint(sa, &mapP, &full[s], kx, x.p0, keep);
+                        if constexpr (Cfg::kPackedP) {
+                            // packed rows 32 w .. 32 w + 31 into the upper half of their codes' 4 KB
+#pragma unroll
+                            for (int w = 0; w < 4; ++w)
+                                tma_load_2d_hint(sa + w * 4096 + 2048, &mapP, &full[s], kx / 2, x.p0 + 32 * w, keep);
+                        } else {
+                            tma_load_2d_hint(sa, &mapP, &full[s], kx, x.p0, keep);
+                        }
                         if constexpr (kPair) {
                             // this CTA's half of the Q tile, into its own stage
                             const int qy = Cfg::kW4A8 ? (rank == 0 ? x.q0 : prm.q_rows + x.q0)
@@ -366,7 +397,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 for (int j = 0; j < nst; ++j, ++g) {
                     const int s = static_cast<int>(g % ST);
                     const uint32_t ph = (g / ST) & 1u;
-                    if (!wait_bounded(&full[s], ph, wd) || (kPair && !wait_bounded(&pfull[s], ph, wd))) {
+                    // this CTA's stage landed (packed P: and converted), and the odd CTA's
+                    if (!wait_bounded(Cfg::kPackedP ? &conv[s] : &full[s], ph, wd) ||
+                        (kPair && !wait_bounded(&pfull[s], ph, wd))) {
                         ok = false;
                         break;
                     }
@@ -417,13 +450,85 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 const int nst = (x.nkb + Cfg::kKB - 1) / Cfg::kKB;
                 for (int j = 0; j < nst; ++j, ++g) {
                     const int s = static_cast<int>(g % ST);
-                    if (!wait_bounded(&full[s], (g / ST) & 1u, wd)) {
+                    if (!wait_bounded(Cfg::kPackedP ? &conv[s] : &full[s], (g / ST) & 1u, wd)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_peer(pfull_remote + 8u * static_cast<uint32_t>(s));
                 }
             }
+        }
+    } else if (Cfg::kPackedP && warp >= Cfg::kWarpConv) {
+        // ------------------------------------------------------------ P converters (packed P)
+        // thread = P row r of this CTA: each k block's 64 packed bytes of the row
+        // (upper half of warp w's 4 KB) become 128 codes u = v + 8 in natural k
+        // order (the order the prepared Q codes have), at 16-byte chunk c ^ (r % 8)
+        // of the row (128-byte swizzle); codes past K are 0.  Each warp reads its
+        // rows' packed bytes before it writes their codes over them.
+        const int cw = warp - Cfg::kWarpConv;
+        const int r = cw * 32 + lane;
+        const int kh = prm.K / 2;  // packed bytes per row
+        uint32_t g = 0, nacc = 0;
+        bool ok = true;
+        const int n_dp = ss_dp_units(prm, cid, ncl), n_units = ss_units(prm, cid, ncl);
+        for (int i = 0; ok && i < n_units; ++i, ++nacc) {
+            const SsUnit x = ss_unit<Cfg>(prm, cid, ncl, n_dp, i, rank);
+            const int nst = (x.nkb + Cfg::kKB - 1) / Cfg::kKB;
+            int su = 0;  // sum of this row's codes over the unit's k blocks
+            for (int j = 0; j < nst; ++j, ++g) {
+                const int s = static_cast<int>(g % ST);
+                if (!ss_warp_wait(&full[s], (g / ST) & 1u, wd)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *st = stages + s * Cfg::kStage;
+                const int nb = min(Cfg::kKB, x.nkb - j * Cfg::kKB);  // the unit's k blocks in this stage
+#pragma unroll
+                for (int b = 0; b < Cfg::kKB; ++b) {
+                    if (b >= nb) continue;  // loaded, not used
+                    uint8_t *blk = st + b * Cfg::kBoxA;
+                    const uint8_t *raw = blk + cw * 4096 + 2048 + lane * 64;
+                    uint4 w[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint4 *>(raw + 16 * c);
+                    __syncwarp();  // the warp's packed rows are read before its codes overwrite them
+                    // packed bytes of this block inside K (k < K): 0..64
+                    const int valid = max(0, min(64, kh - (x.kb0 + j * Cfg::kKB + b) * (Cfg::kBK / 2)));
+                    uint8_t *row = blk + r * 128;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t q[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+                        uint32_t o[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int b0 = 16 * c + 4 * e;  // first packed byte of this word
+                            const uint32_t keep =
+                                b0 + 4 <= valid ? 0xFFFFFFFFu : (b0 >= valid ? 0u : (0xFFFFFFFFu >> (8 * (b0 + 4 - valid))));
+                            const uint32_t lo = ((q[e] & 0x0F0F0F0Fu) ^ 0x08080808u) & keep;         // even k
+                            const uint32_t hi = (((q[e] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u) & keep;  // odd k
+                            o[2 * e] = __byte_perm(lo, hi, 0x5140);
+                            o[2 * e + 1] = __byte_perm(lo, hi, 0x7362);
+                            su = __dp4a(static_cast<int>(lo), 0x01010101, su);
+                            su = __dp4a(static_cast<int>(hi), 0x01010101, su);
+                        }
+                        // 32 codes = code chunks 2 c and 2 c + 1 of the row
+                        *reinterpret_cast<uint4 *>(row + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4 *>(row + (((2 * c + 1) ^ (r & 7)) << 4)) =
+                            make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                }
+                fence_proxy_async_smem();  // generic writes, read next by the tensor core
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&conv[s]);
+            }
+            if (!ok) break;
+            // the unit's row sums into slot nacc % 2, once the epilogue has read what
+            // unit nacc - 2 left there
+            const uint32_t sb = nacc & 1u;
+            if (nacc >= 2 && !ss_warp_wait(&psum_free[sb], ((nacc >> 1) - 1u) & 1u, wd)) break;
+            psum[sb * 128 + r] = su;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&psum_full[sb]);
         }
     } else {
         // ------------------------------------------------------------ epilogue (warps 0-3)
@@ -454,7 +559,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             int4 qs0 = make_int4(0, 0, 0, 0), qs1 = qs0;
             if constexpr (!Cfg::kFloat) {
                 if (first) {
-                    sp = __ldg(prm.sumP + min(x.p0 + p, prm.p_rows - 1));
+                    if constexpr (!Cfg::kPackedP) sp = __ldg(prm.sumP + min(x.p0 + p, prm.p_rows - 1));
                     // (the sums arrays are padded past the last row by more than a tile)
                     const int4 *sq = reinterpret_cast<const int4 *>(prm.sumQ + x.q0) + (kQPer / 4) * lane;
                     qs0 = __ldg(sq);
@@ -464,6 +569,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const uint32_t ab = nacc % Cfg::kAccBufs;
             if (!ss_warp_wait(&acc_full[ab], (nacc / Cfg::kAccBufs) & 1u, wd)) break;
             tc_fence_after();
+            if constexpr (Cfg::kPackedP) {
+                // packed P: the sum of this row's codes over the unit's own k blocks,
+                // added by every piece of a split tile (the pieces' sums add up to the
+                // whole row's)
+                const uint32_t sb = nacc & 1u;
+                if (!ss_warp_wait(&psum_full[sb], (nacc >> 1) & 1u, wd)) break;
+                sp = psum[sb * 128 + p];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&psum_free[sb]);
+            }
             const uint32_t tacc = trow + ab * Cfg::kAccCols;
             if constexpr (!Cfg::kW4A8) {
                 // C[m, n] = S - 8 sum uA[m] - 8 sum uB[n] + 64 K   (first split adds the terms)

@@ -2,17 +2,20 @@
 //
 // Skinny activation counts (M <= 64, decode) take igemm_skinny_kernel
 // (gemm_skinny_kernel.cuh): split K, each CTA's slice of the activations held
-// as codes in shared memory, the weights streamed once.  Small prefill
-// batches of about one wave of 128 x 64 tiles take igemm_small_w4a8_kernel
-// (gemm_small.cu).  Large products (M >= 768, M * N >= 4M, and every K past
-// 65536) take the prepared-codes path: one pass writes weight
-// code rows, activation
-// high/low code planes and the row sums (prep.cu), then igemm_ss_kernel
-// multiplies 128 weight rows by 128 activation rows (256 code rows) per tile
-// from shared memory.  The rest takes igemm_tc_kernel below.  Swap-AB: the
-// MMA A side is the weights (128 rows per tile, codes in TMEM); the B side is
-// QA = 96 activation rows split into high and low code rows (N = 192, shared
-// memory).  C leaves through bulk tensor stores of [m][n] boxes.
+// as codes in shared memory, the weights streamed once.  128 to 640
+// activations against large weights take igemm_ss_kernel on packed weights
+// (below: a preparation pass writes only the activations' high/low code
+// planes; the kernel expands each weight tile in shared memory).  Small
+// prefill batches of about one wave of 128 x 64 tiles take
+// igemm_small_w4a8_kernel (gemm_small.cu).  Large products (M >= 768,
+// M * N >= 4M, and every K past 65536) take the prepared-codes path: one pass
+// writes weight code rows, activation high/low code planes and the row sums
+// (prep.cu), then igemm_ss_kernel multiplies 128 weight rows by 128
+// activation rows (256 code rows) per tile from shared memory.  The rest takes
+// igemm_tc_kernel below.  Swap-AB: the MMA A side is the weights (128 rows per
+// tile, codes in TMEM); the B side is QA = 96 activation rows split into high
+// and low code rows (N = 192, shared memory).  C leaves through bulk tensor
+// stores of [m][n] boxes.
 #include "launch.cuh"
 
 namespace igemm {
@@ -29,6 +32,8 @@ using CfgW4A8Skinny32 = SkinnyCfg<false, 32, 6, 4, 2, 2, 1>;
 using CfgW4A8Skinny64 = SkinnyCfg<false, 64, 6, 4, 2, 1, 1>;
 //                    W4A8  BN  stages CL  float out  format  k blocks per stage
 using CfgW4A8Ss = SsCfg<true, 256, 3, 2, false, 0, 2>;
+// the same kernel on packed weights, expanded into codes in the kernel
+using CfgW4A8SsPacked = SsCfg<true, 256, 3, 2, false, 0, 2, true>;
 
 static int run_w4a8_codes(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
 {
@@ -59,6 +64,56 @@ static int run_w4a8_codes(const int8_t *A, const uint8_t *Bp, int32_t *C, int M,
         rc = make_map(&mapC, CU_TENSOR_MAP_DATA_TYPE_INT32, C, M, N, Cfg::kStageRows, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc == kOk)
         rc = launch_ss<Cfg>(mapP, mapQ, mapC, tma_store, C, M, N, K, w_sums, a_sums, N, M, plan, stream, true);
+    const int rf = workspace_free(ws, stream);
+    return rc != kOk ? rc : rf;
+}
+
+// The prepared-codes kernel with the weights expanded in the kernel: the
+// preparation pass writes only the activations' code planes and sums (2 M K
+// bytes instead of 2 M K + N K), the kernel TMA-loads the packed weights.
+// Each weight tile is expanded once per 128-activation tile, so it pays where
+// the activations make few such tiles and the weights are large.  Measured on
+// GB300 (call time; the path taken until then in parentheses): 256 x 28672 x 8192
+// 106 us (144), 512 x 28672 x 8192 195 (253), 128 x 28672 x 8192 71 (80),
+// 384 x 11008 x 4096 46 (52), 512 x 12288 x 5120 67 (79); it loses with 96 or 192
+// rows (tiles a quarter empty), from 768 rows (the weight codes of the
+// preparation pass serve six tiles and more) and on 4096 x 4096 weights.
+static bool use_packed_w4a8(int M, int N, int K)
+{
+    const int q_tiles = (M + 127) / 128;
+    if (M < 128 || M > 640 || 5 * M <= 4 * 128 * q_tiles) return false;  // 128..640 rows, tiles more than 4/5 full
+    const int64_t nk = int64_t(N) * K;
+    return nk >= (q_tiles >= 3 ? (int64_t(40) << 20) : (int64_t(100) << 20));
+}
+
+static int run_w4a8_packed(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
+{
+    using Cfg = CfgW4A8SsPacked;
+    CodesLayout lay;
+    codes_layout(0, 2 * M, M, K, &lay);
+    void *ws = nullptr;
+    if (workspace_alloc(&ws, lay.total, stream) != kOk) return kCudaError;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    uint8_t *a_codes = base + lay.q_codes;
+    int32_t *a_sums = reinterpret_cast<int32_t *>(base + lay.q_sums);
+    SsPlan plan;
+    int rc = ss_plan<Cfg>(M, N, K, N, M, int64_t(N) * K / 2 + 2 * int64_t(M) * K, true, &plan);
+    if (rc == kOk)
+        rc = launch_prep(nullptr, 0, reinterpret_cast<const uint8_t *>(A), M, true, K, nullptr, a_codes, nullptr,
+                         a_sums, ss_tail_zero<Cfg>(plan, C, M, N), stream);
+    CUtensorMap mapP, mapQ, mapC = {};
+    // packed weights: 64 bytes (128 k) by 32 rows per box, four boxes per k block
+    if (rc == kOk)
+        rc = make_map(&mapP, CU_TENSOR_MAP_DATA_TYPE_UINT8, Bp, N, K / 2, 32, Cfg::kBK / 2,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc == kOk)
+        rc = make_map(&mapQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, 2 * uint64_t(M), K, Cfg::kQBoxRows, Cfg::kBK,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    const bool tma_store = (N % 4) == 0;
+    if (rc == kOk && tma_store)
+        rc = make_map(&mapC, CU_TENSOR_MAP_DATA_TYPE_INT32, C, M, N, Cfg::kStageRows, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc == kOk)
+        rc = launch_ss<Cfg>(mapP, mapQ, mapC, tma_store, C, M, N, K, nullptr, a_sums, N, M, plan, stream, true);
     const int rf = workspace_free(ws, stream);
     return rc != kOk ? rc : rf;
 }
@@ -106,15 +161,26 @@ SkinnyPlan skinny_plan_w4a8(int M, int N, int K, int sms, int pairs, int quads)
 // 96 x 11008 x 4096 37.5 (29.3), 256 x 28672 x 8192 154 (146).  With 97..128
 // rows the in-kernel path's 96-activation tiles are half empty and this kernel
 // wins even over several waves: 128 x 28672 x 8192 82.6 (94.9).
-static bool use_small_w4a8(int M, int N, int K)
+static bool use_small_w4a8(int M, int N, int K, int64_t sms)
 {
     if (M <= 64 || K > 8192) return false;
-    const int64_t sms = sm_count();
     const int64_t tiles = int64_t((M + 63) / 64) * ((N + 127) / 128);
     if (M > 96 && M <= 128 && tiles >= sms) return true;
     if (K > 4096) return false;
     if (tiles <= sms && (K <= 2048 || 3 * tiles >= sms)) return true;
     return tiles <= 2 * sms && M >= 256;
+}
+
+// Path of a call that the skinny kernel does not take (K <= 65536).
+static int large_route_w4a8(int M, int N, int K, int64_t sms)
+{
+    if (use_packed_w4a8(M, N, K)) return kRoutePacked;
+    if (use_small_w4a8(M, N, K, sms)) return kRouteSmall;
+    // the preparation pass writes N * K + 2 * M * K bytes of codes; measured on
+    // GB300 it pays from about M = 768 with M * N >= 4M (1024 x 4096 x 4096: 48 vs
+    // 52 us), not below (64 x 28672 x 8192: 130 vs 61 us; 1024^3: 28 vs 15 us)
+    if (M >= 768 && N >= 256 && int64_t(M) * N >= (int64_t(1) << 22)) return kRouteCodes;
+    return kRouteInKernel;
 }
 
 int launch_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
@@ -132,13 +198,19 @@ int launch_w4a8(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, in
                                : launch_skinny<CfgW4A8Skinny64>(a, Bp, C, M, N, K, stream);
         if (rc != kUnsupportedShape) return rc;
     }
-    if (use_small_w4a8(M, N, K)) return launch_w4a8_small(A, Bp, C, M, N, K, stream);
-    // the preparation pass writes N * K + 2 * M * K bytes of codes; measured on
-    // GB300 it pays from about M = 768 with M * N >= 4M (1024 x 4096 x 4096: 48 vs
-    // 52 us), not below (64 x 28672 x 8192: 130 vs 61 us; 1024^3: 28 vs 15 us)
-    if (M >= 768 && N >= 256 && int64_t(M) * N >= (int64_t(1) << 22))
-        return run_w4a8_codes(A, Bp, C, M, N, K, stream);
-    return run_w4a8<CfgW4A8>(A, Bp, C, M, N, K, stream);
+    switch (large_route_w4a8(M, N, K, sm_count())) {
+    case kRoutePacked: return run_w4a8_packed(A, Bp, C, M, N, K, stream);
+    case kRouteSmall: return launch_w4a8_small(A, Bp, C, M, N, K, stream);
+    case kRouteCodes: return run_w4a8_codes(A, Bp, C, M, N, K, stream);
+    default: return run_w4a8<CfgW4A8>(A, Bp, C, M, N, K, stream);
+    }
+}
+
+int route_w4a8(int M, int N, int K, int sms, int pairs, int quads)
+{
+    if (K > kMaxK) return kRouteCodes;
+    if (M <= 64 && skinny_plan_w4a8(M, N, K, sms, pairs, quads).ctas >= 1) return kRouteSkinny;
+    return large_route_w4a8(M, N, K, sms);
 }
 
 }  // namespace igemm

@@ -588,6 +588,12 @@ int launch_i4i4_small(const uint8_t *Ap, const uint8_t *Bp, int32_t *C, int M, i
 // igemm_small_w4a8_kernel (gemm_small.cu): one CTA per 128 weight rows x 64
 // activation rows, for small prefill batches.
 int launch_w4a8_small(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream);
+// The path a GEMM call takes (the launchers and the routing query share these).
+enum Route { kRouteSkinny = 0, kRouteSmall = 1, kRouteCodes = 2, kRouteInKernel = 3, kRoutePacked = 4 };
+// Path of an M x N x K call on a GPU with `sms` SMs where `pairs` / `quads`
+// clusters of two / four of the skinny kernel fit (host only).
+int route_i4i4(int M, int N, int K, int sms, int pairs, int quads);
+int route_w4a8(int M, int N, int K, int sms, int pairs, int quads);
 // Skinny-path plans (M <= 64) of each variant, for the planning query.
 SkinnyPlan skinny_plan_i4i4(int M, int N, int K, int sms, int pairs, int quads);
 SkinnyPlan skinny_plan_w4a8(int M, int N, int K, int sms, int pairs, int quads);

@@ -41,6 +41,11 @@ int main(void)
         EXPECT(igemm_ss_plan(1, 4096, 4096, 4096, 76, ss) == IGEMM_OK);
         EXPECT(ss[0] == 1 && ss[3] == 56 && ss[4] > 0 && ss[4] < 32 && ss[5] == 76 && ss[6] == 1);
         EXPECT(igemm_ss_plan(2, 4096, 4096, 4096, 76, ss) == IGEMM_INVALID_ARGUMENT);
+        /* W4A8 decode: skinny; 256 activations against 28672 x 8192 weights: packed weights */
+        EXPECT(igemm_route(1, 16, 28672, 8192, 152, 76, 36, ss) == IGEMM_OK && ss[0] == 0);
+        EXPECT(igemm_route(1, 256, 28672, 8192, 152, 76, 36, ss) == IGEMM_OK && ss[0] == 4);
+        EXPECT(igemm_route(0, 8192, 8192, 8192, 152, 76, 36, ss) == IGEMM_OK && ss[0] == 2);
+        EXPECT(igemm_route(0, 8, 8, 48, 152, 76, 36, ss) == IGEMM_INVALID_ARGUMENT);
     }
     printf("c abi ok: split %d, slice %d, ctas %d, cluster %d\n", plan[0], plan[1], plan[2], plan[3]);
     return 0;

@@ -250,6 +250,23 @@ def test_w4a8_prepared_codes_path(orc, M, N, K):
     assert np.array_equal(C, orc.w4a8_gemm(a, bp, K))
 
 
+# W4A8 on packed weights (128..640 activations against large weights: the
+# weights are expanded into codes inside the prepared-codes kernel, only the
+# activations go through the preparation pass): one activation tile with a K
+# tail; two tiles with N % 4 != 0 (direct stores); ragged activations with a K
+# tail and N % 4 != 0; four tiles; three tiles over more tiles than CTA pairs,
+# whose stream-K ranges cross tile ends.  Whole C, element by element.
+PACKED_W4A8 = [(128, 12800, 8224), (256, 16386, 6400), (350, 10102, 4160), (512, 8192, 5120), (384, 12288, 5120)]
+
+
+@pytest.mark.parametrize("M,N,K", PACKED_W4A8)
+def test_w4a8_packed_weights_path(orc, M, N, K):
+    a = si.int8_values(7300 + M + K, (M, K))
+    b = si.int4_values(8300 + N + K, (N, K))
+    C, bp = run_w4a8(a, b, orc)
+    assert np.array_equal(C, orc.w4a8_gemm(a, bp, K))
+
+
 # ---------------------------------------------------------------- W4A8 with per-channel dequantisation
 
 @pytest.mark.parametrize("M,N,K", [(16, 28672, 1024), (130, 300, 512), (257, 1000, 2048), (3, 13, 64)])

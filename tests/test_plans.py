@@ -135,3 +135,32 @@ def test_ss_plan_parity_shapes_cross_tile_ends(lib):
         p = ss_plan(variant, M, N, K)
         kb_total = -(-K // 128)
         assert p["covered"] and p["tail_tiles"] > 1 and kb_total % p["tail_kb"] != 0, (variant, M, N, K, p)
+
+
+def test_packed_w4a8_parity_shapes_plan(lib):
+    # (384, 12288, 5120) on 76 pairs: 48 weight slots x 3 activation tiles = 144
+    # tiles, the last 68 dealt out as ranges of 36 k blocks (of 40 per tile)
+    p = ss_plan("w4a8", 384, 12288, 5120)
+    assert (p["tail_tiles"], p["tail_kb"], p["covered"]) == (68, 36, True)
+
+
+# ---------------------------------------------------------------- routing
+# The path each kind of GPU parity case is meant to cover, on a 152-SM part
+# (the calls take the same decisions with the device's own SM count).
+ROUTED = [
+    ("w4a8", 16, 28672, 8192, "skinny"), ("w4a8", 64, 28672, 8192, "skinny"), ("i4i4", 16, 28672, 8192, "skinny"),
+    ("i4i4", 1024, 1024, 1024, "small"), ("i4i4", 256, 256, 256, "small"), ("w4a8", 1024, 1024, 1024, "small"),
+    ("i4i4", 8192, 8192, 8192, "codes"), ("w4a8", 4096, 4096, 4096, "codes"), ("w4a8", 4000, 12288, 5120, "codes"),
+    ("i4i4", 64, 100, 131104, "codes"),
+    # the packed-weights parity cases
+    ("w4a8", 128, 12800, 8224, "packed"), ("w4a8", 256, 16386, 6400, "packed"), ("w4a8", 350, 10102, 4160, "packed"),
+    ("w4a8", 512, 8192, 5120, "packed"), ("w4a8", 384, 12288, 5120, "packed"), ("w4a8", 256, 28672, 8192, "packed"),
+    # just outside the packed-weights rule: too few rows, tiles a quarter empty, too many rows, small weights
+    ("w4a8", 96, 28672, 8192, "in-kernel"), ("w4a8", 192, 28672, 8192, "in-kernel"), ("w4a8", 768, 28672, 8192, "codes"),
+    ("w4a8", 512, 4096, 4096, "small"),
+]
+
+
+@pytest.mark.parametrize("variant,M,N,K,route", ROUTED)
+def test_route(lib, variant, M, N, K, route):
+    assert pig.igemm_route(variant, M, N, K) == route
