@@ -103,10 +103,13 @@ struct SsCfg {
     // [ST], psum_full, psum_free [2]
     static constexpr int kNumBars = 3 * ST + 4 + 1 + (kPackedP ? ST + 4 : 0);
     static constexpr int kOffMisc = ((kOffBars + 8 * kNumBars + 127) / 128) * 128;
+    // packed P: one set of four converter warps per k block of a stage (set b
+    // converts block b of every stage, one P row per thread)
+    static constexpr int kConvSets = kPackedP ? kKB : 0;
     static constexpr int kOffPSum = kOffMisc + 128;  // packed P: [2][128] row sums of a unit's codes
     static constexpr int kSmemBytes = kOffPSum + (kPackedP ? 2 * 128 * 4 : 0) + 1024;  // + alignment slack
-    static constexpr int kWarpConv = 6;  // packed P: warps 6-9 convert (one P row per thread)
-    static constexpr int kThreads = (kPackedP ? 10 : 6) * 32;
+    static constexpr int kWarpConv = 6;  // packed P: converter warps 6 ..
+    static constexpr int kThreads = (6 + 4 * kConvSets) * 32;
     static constexpr int kRawA = kPRows * kBK / 2;   // packed bytes of one k block of P
     static_assert(!kPackedP || (W4A8 && !FLOAT_), "packed P: the W4A8 weights");
     static_assert(kQRows % 16 == 0 && kQRows <= 256, "MMA N");
@@ -253,10 +256,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     uint64_t *acc_full = empty + ST;    // [2] accumulator complete (commit)
     uint64_t *acc_empty = acc_full + 2; // [2] accumulator drained (the epilogue warps of the pair)
     uint64_t *mma_drain = acc_empty + 2;
-    uint64_t *conv = mma_drain + 1;     // [ST] packed P: this CTA's P codes of a stage written (4 converter warps)
-    uint64_t *psum_full = conv + ST;    // [2] packed P: a unit's P row sums written (4 converter warps)
+    uint64_t *conv = mma_drain + 1;     // [ST] packed P: this CTA's P codes of a stage written (converter warps)
+    uint64_t *psum_full = conv + ST;    // [2] packed P: a unit's P row sums written (converter warps)
     uint64_t *psum_free = psum_full + 2;  // [2] packed P: ... and read (this CTA's 4 epilogue warps)
-    int *psum = reinterpret_cast<int *>(smem + Cfg::kOffPSum);  // [2][128]
+    // [2][128]: the converter sets add their rows' sums in, the epilogue reads
+    // and clears them
+    int *psum = reinterpret_cast<int *>(smem + Cfg::kOffPSum);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
 
@@ -279,9 +284,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
         mbar_init(mma_drain, 1);
         if constexpr (Cfg::kPackedP) {
-            for (int s = 0; s < ST; ++s) mbar_init(&conv[s], 4);
+            for (int s = 0; s < ST; ++s) mbar_init(&conv[s], 4 * Cfg::kConvSets);
             for (int b = 0; b < 2; ++b) {
-                mbar_init(&psum_full[b], 4);
+                mbar_init(&psum_full[b], 4 * Cfg::kConvSets);
                 mbar_init(&psum_free[b], 4);
             }
         }
@@ -290,6 +295,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         tma_prefetch_map(&mapP);
         tma_prefetch_map(&mapQ);
         if (prm.tma_store) tma_prefetch_map(&mapC);
+    }
+    if constexpr (Cfg::kPackedP) {
+        if (threadIdx.x < 2 * 128) psum[threadIdx.x] = 0;  // (before the barrier below)
     }
     if (warp == 4) {
         // a pair allocates together: warp 4 of both CTAs, the same slot offset
@@ -460,12 +468,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
     } else if (Cfg::kPackedP && warp >= Cfg::kWarpConv) {
         // ------------------------------------------------------------ P converters (packed P)
-        // thread = P row r of this CTA: each k block's 64 packed bytes of the row
-        // (upper half of warp w's 4 KB) become 128 codes u = v + 8 in natural k
-        // order (the order the prepared Q codes have), at 16-byte chunk c ^ (r % 8)
-        // of the row (128-byte swizzle); codes past K are 0.  Each warp reads its
-        // rows' packed bytes before it writes their codes over them.
-        const int cw = warp - Cfg::kWarpConv;
+        // thread = P row r of this CTA; set `cset` converts k block cset of every
+        // stage: the block's 64 packed bytes of the row (upper half of warp cw's
+        // 4 KB) become 128 codes u = v + 8 in natural k order (the order the
+        // prepared Q codes have), at 16-byte chunk c ^ (r % 8) of the row
+        // (128-byte swizzle); codes past K are 0.  Each warp reads its rows'
+        // packed bytes before it writes their codes over them.
+        const int cset = (warp - Cfg::kWarpConv) >> 2, cw = (warp - Cfg::kWarpConv) & 3;
         const int r = cw * 32 + lane;
         const int kh = prm.K / 2;  // packed bytes per row
         uint32_t g = 0, nacc = 0;
@@ -483,17 +492,18 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 }
                 uint8_t *st = stages + s * Cfg::kStage;
                 const int nb = min(Cfg::kKB, x.nkb - j * Cfg::kKB);  // the unit's k blocks in this stage
-#pragma unroll
-                for (int b = 0; b < Cfg::kKB; ++b) {
-                    if (b >= nb) continue;  // loaded, not used
+                {
+                    const int b = cset;
                     uint8_t *blk = st + b * Cfg::kBoxA;
                     const uint8_t *raw = blk + cw * 4096 + 2048 + lane * 64;
                     uint4 w[4];
+                    // (a block past the unit's k blocks is loaded, not used: its bytes
+                    // count as past K, so it gets zero codes and adds nothing)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint4 *>(raw + 16 * c);
                     __syncwarp();  // the warp's packed rows are read before its codes overwrite them
-                    // packed bytes of this block inside K (k < K): 0..64
-                    const int valid = max(0, min(64, kh - (x.kb0 + j * Cfg::kKB + b) * (Cfg::kBK / 2)));
+                    // packed bytes of this block inside K (k < K) and the unit: 0..64
+                    const int valid = b < nb ? max(0, min(64, kh - (x.kb0 + j * Cfg::kKB + b) * (Cfg::kBK / 2))) : 0;
                     uint8_t *row = blk + r * 128;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -526,7 +536,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             // unit nacc - 2 left there
             const uint32_t sb = nacc & 1u;
             if (nacc >= 2 && !ss_warp_wait(&psum_free[sb], ((nacc >> 1) - 1u) & 1u, wd)) break;
-            psum[sb * 128 + r] = su;
+            atomicAdd(&psum[sb * 128 + r], su);
             __syncwarp();
             if (lane == 0) mbar_arrive(&psum_full[sb]);
         }
@@ -576,6 +586,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 const uint32_t sb = nacc & 1u;
                 if (!ss_warp_wait(&psum_full[sb], (nacc >> 1) & 1u, wd)) break;
                 sp = psum[sb * 128 + p];
+                psum[sb * 128 + p] = 0;  // for the slot's next unit
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&psum_free[sb]);
             }
