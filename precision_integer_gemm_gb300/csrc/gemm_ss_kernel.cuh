@@ -43,6 +43,8 @@
 //   warp 4      TMEM allocation (both CTAs of a pair), MMA issue (one thread;
 //               the even CTA of a pair), relay (one thread; the odd CTA)
 //   warp 5      TMA producer (one lane)
+//   warps 6..   packed P only: converters (a set of four per k block of a
+//               stage, one P row per thread)
 // Every wait is bounded (ptx.cuh wait_bounded).
 #pragma once
 #include <cstdint>
@@ -56,10 +58,11 @@ template <bool W4A8, int BN_, int ST_, int CL_ = 1, bool FLOAT_ = false, int FMT
 struct SsCfg {
     static constexpr bool kW4A8 = W4A8;
     // kPackedP: the P operand arrives as packed int4 rows, 64 bytes a row per k
-    // block, and four converter warps expand it in place into e4m3 codes, summing
-    // each row's codes over the unit (no preparation pass over P).  The packed
-    // rows of converter warp w (P rows 32 w ..) land in the upper half of the
-    // 4 KB that its rows' codes take, so a warp overwrites only its own input.
+    // block, and converter warps (a set of four per k block of a stage) expand
+    // it in place into e4m3 codes, summing each row's codes over the unit (no
+    // preparation pass over P).  The packed rows of converter warp w of a set (P
+    // rows 32 w ..) land in the upper half of the 4 KB that those rows' codes
+    // take, so a warp overwrites only its own input.
     static constexpr bool kPackedP = PACKED_P_;
     // kFloat: plain fp8 operands (the fp8 GEMM), C = the float32 accumulator;
     // kFmt: their format, 0 = E4M3 (also the integer codes), 1 = E5M2
