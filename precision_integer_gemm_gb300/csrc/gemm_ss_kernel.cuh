@@ -58,7 +58,7 @@ template <bool W4A8, int BN_, int ST_, int CL_ = 1, bool FLOAT_ = false, int FMT
 struct SsCfg {
     static constexpr bool kW4A8 = W4A8;
     // kPackedP: the P operand arrives as packed int4 rows, 64 bytes a row per k
-    // block, and converter warps (a set of four per k block of a stage) expand
+    // block (64-byte swizzled boxes), and converter warps (a set of four per k block of a stage) expand
     // it in place into e4m3 codes, summing each row's codes over the unit (no
     // preparation pass over P).  The packed rows of converter warp w of a set (P
     // rows 32 w ..) land in the upper half of the 4 KB that those rows' codes
@@ -501,9 +501,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     const uint8_t *raw = blk + cw * 4096 + 2048 + lane * 64;
                     uint4 w[4];
                     // (a block past the unit's k blocks is loaded, not used: its bytes
-                    // count as past K, so it gets zero codes and adds nothing)
+                    // count as past K, so it gets zero codes and adds nothing.)  The
+                    // packed rows land 64-byte swizzled: 16-byte chunk c of row l at
+                    // chunk c ^ ((l / 2) % 4), so eight lanes' reads of a chunk hit
+                    // eight different bank groups (unswizzled rows 64 bytes apart put
+                    // four lanes on each)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint4 *>(raw + 16 * c);
+                    for (int c = 0; c < 4; ++c)
+                        w[c] = *reinterpret_cast<const uint4 *>(raw + 16 * (c ^ ((lane >> 1) & 3)));
                     __syncwarp();  // the warp's packed rows are read before its codes overwrite them
                     // packed bytes of this block inside K (k < K) and the unit: 0..64
                     const int valid = b < nb ? max(0, min(64, kh - (x.kb0 + j * Cfg::kKB + b) * (Cfg::kBK / 2))) : 0;

@@ -102,10 +102,11 @@ static int run_w4a8_packed(const int8_t *A, const uint8_t *Bp, int32_t *C, int M
         rc = launch_prep(nullptr, 0, reinterpret_cast<const uint8_t *>(A), M, true, K, nullptr, a_codes, nullptr,
                          a_sums, ss_tail_zero<Cfg>(plan, C, M, N), stream);
     CUtensorMap mapP, mapQ, mapC = {};
-    // packed weights: 64 bytes (128 k) by 32 rows per box, four boxes per k block
+    // packed weights: 64 bytes (128 k) by 32 rows per box, four boxes per k block,
+    // 64-byte swizzle (the converter warps' reads are then free of bank conflicts)
     if (rc == kOk)
         rc = make_map(&mapP, CU_TENSOR_MAP_DATA_TYPE_UINT8, Bp, N, K / 2, 32, Cfg::kBK / 2,
-                      CU_TENSOR_MAP_SWIZZLE_NONE);
+                      CU_TENSOR_MAP_SWIZZLE_64B);
     if (rc == kOk)
         rc = make_map(&mapQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, 2 * uint64_t(M), K, Cfg::kQBoxRows, Cfg::kBK,
                       CU_TENSOR_MAP_SWIZZLE_128B);
