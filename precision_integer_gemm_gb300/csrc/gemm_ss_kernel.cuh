@@ -48,6 +48,7 @@
 // Every wait is bounded (ptx.cuh wait_bounded).
 #pragma once
 #include <cstdint>
+#include <type_traits>
 #include <cuda.h>
 #include "ptx.cuh"
 
@@ -513,27 +514,43 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     // packed bytes of this block inside K (k < K) and the unit: 0..64
                     const int valid = b < nb ? max(0, min(64, kh - (x.kb0 + j * Cfg::kKB + b) * (Cfg::kBK / 2))) : 0;
                     uint8_t *row = blk + r * 128;
+                    // FULL: every byte of the block inside K (no masking; the same for the
+                    // whole warp)
+                    auto expand = [&](auto full_tag) {
+                        constexpr bool FULL = decltype(full_tag)::value;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint32_t q[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
-                        uint32_t o[8];
+                        for (int c = 0; c < 4; ++c) {
+                            const uint32_t q[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+                            uint32_t o[8];
+                            uint32_t bytesum = 0;  // per byte: the chunk's codes there, <= 8 x 15
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int b0 = 16 * c + 4 * e;  // first packed byte of this word
-                            const uint32_t keep =
-                                b0 + 4 <= valid ? 0xFFFFFFFFu : (b0 >= valid ? 0u : (0xFFFFFFFFu >> (8 * (b0 + 4 - valid))));
-                            const uint32_t lo = ((q[e] & 0x0F0F0F0Fu) ^ 0x08080808u) & keep;         // even k
-                            const uint32_t hi = (((q[e] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u) & keep;  // odd k
-                            o[2 * e] = __byte_perm(lo, hi, 0x5140);
-                            o[2 * e + 1] = __byte_perm(lo, hi, 0x7362);
-                            su = __dp4a(static_cast<int>(lo), 0x01010101, su);
-                            su = __dp4a(static_cast<int>(hi), 0x01010101, su);
+                            for (int e = 0; e < 4; ++e) {
+                                uint32_t lo = (q[e] & 0x0F0F0F0Fu) ^ 0x08080808u;         // even k
+                                uint32_t hi = ((q[e] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;  // odd k
+                                if constexpr (!FULL) {
+                                    const int b0 = 16 * c + 4 * e;  // first packed byte of this word
+                                    const uint32_t keep =
+                                        b0 + 4 <= valid ? 0xFFFFFFFFu
+                                                        : (b0 >= valid ? 0u : (0xFFFFFFFFu >> (8 * (b0 + 4 - valid))));
+                                    lo &= keep;
+                                    hi &= keep;
+                                }
+                                o[2 * e] = __byte_perm(lo, hi, 0x5140);
+                                o[2 * e + 1] = __byte_perm(lo, hi, 0x7362);
+                                bytesum += lo + hi;  // no byte carries: each byte stays <= 120
+                            }
+                            su = __dp4a(static_cast<int>(bytesum), 0x01010101, su);
+                            // 32 codes = code chunks 2 c and 2 c + 1 of the row
+                            *reinterpret_cast<uint4 *>(row + (((2 * c) ^ (r & 7)) << 4)) =
+                                make_uint4(o[0], o[1], o[2], o[3]);
+                            *reinterpret_cast<uint4 *>(row + (((2 * c + 1) ^ (r & 7)) << 4)) =
+                                make_uint4(o[4], o[5], o[6], o[7]);
                         }
-                        // 32 codes = code chunks 2 c and 2 c + 1 of the row
-                        *reinterpret_cast<uint4 *>(row + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                        *reinterpret_cast<uint4 *>(row + (((2 * c + 1) ^ (r & 7)) << 4)) =
-                            make_uint4(o[4], o[5], o[6], o[7]);
-                    }
+                    };
+                    if (valid == 64)
+                        expand(std::true_type{});
+                    else
+                        expand(std::false_type{});
                 }
                 fence_proxy_async_smem();  // generic writes, read next by the tensor core
                 __syncwarp();
