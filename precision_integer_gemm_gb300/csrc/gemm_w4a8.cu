@@ -2,7 +2,7 @@
 //
 // Skinny activation counts (M <= 64, decode) take igemm_skinny_kernel
 // (gemm_skinny_kernel.cuh): split K, each CTA's slice of the activations held
-// as codes in shared memory, the weights streamed once.  128 to 640
+// as codes in shared memory, the weights streamed once.  128 to 896
 // activations against large weights take igemm_ss_kernel on packed weights
 // (below: a preparation pass writes only the activations' high/low code
 // planes; the kernel expands each weight tile in shared memory).  Small
@@ -73,17 +73,20 @@ static int run_w4a8_codes(const int8_t *A, const uint8_t *Bp, int32_t *C, int M,
 // bytes instead of 2 M K + N K), the kernel TMA-loads the packed weights.
 // Each weight tile is expanded once per 128-activation tile, so it pays where
 // the activations make few such tiles and the weights are large.  Measured on
-// GB300 (call time; the path taken until then in parentheses): 256 x 28672 x 8192
-// 106 us (144), 512 x 28672 x 8192 195 (253), 128 x 28672 x 8192 71 (80),
-// 384 x 11008 x 4096 46 (52), 512 x 12288 x 5120 67 (79); it loses with 96 or 192
-// rows (tiles a quarter empty), from 768 rows (the weight codes of the
-// preparation pass serve six tiles and more) and on 4096 x 4096 weights.
+// GB300 (call time; the path taken otherwise in parentheses): 256 x 28672 x 8192
+// 87 us (144), 512 x 28672 x 8192 155 (253), 128 x 28672 x 8192 63 (78),
+// 768 x 28672 x 8192 221 (236), 192 x 12288 x 5120 39 (46), 512 x 4096 x 4096
+// 28 (32); even with 1024 rows (the prepared weight codes then serve eight
+// tiles); it loses with 96 rows, with one activation tile on weights below about
+// 60M values (128 x 11008 x 4096: 34 vs 31) and with two or three on weights
+// below 40M (256 x 8192 x 2048: 22 vs 21).
 static bool use_packed_w4a8(int M, int N, int K)
 {
     const int q_tiles = (M + 127) / 128;
-    if (M < 128 || M > 640 || 5 * M <= 4 * 128 * q_tiles) return false;  // 128..640 rows, tiles more than 4/5 full
+    if (M < 128 || M > 896 || 10 * M < 7 * 128 * q_tiles) return false;  // 128..896 rows, tiles at least 70 % full
     const int64_t nk = int64_t(N) * K;
-    return nk >= (q_tiles >= 3 ? (int64_t(40) << 20) : (int64_t(100) << 20));
+    const int64_t mi = int64_t(1) << 20;
+    return nk >= (q_tiles == 1 ? 60 * mi : q_tiles <= 3 ? 40 * mi : 16 * mi);
 }
 
 static int run_w4a8_packed(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)

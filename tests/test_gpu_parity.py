@@ -250,13 +250,15 @@ def test_w4a8_prepared_codes_path(orc, M, N, K):
     assert np.array_equal(C, orc.w4a8_gemm(a, bp, K))
 
 
-# W4A8 on packed weights (128..640 activations against large weights: the
+# W4A8 on packed weights (128..896 activations against large weights: the
 # weights are expanded into codes inside the prepared-codes kernel, only the
 # activations go through the preparation pass): one activation tile with a K
 # tail; two tiles with N % 4 != 0 (direct stores); ragged activations with a K
 # tail and N % 4 != 0; four tiles; three tiles over more tiles than CTA pairs,
-# whose stream-K ranges cross tile ends.  Whole C, element by element.
-PACKED_W4A8 = [(128, 12800, 8224), (256, 16386, 6400), (350, 10102, 4160), (512, 8192, 5120), (384, 12288, 5120)]
+# whose stream-K ranges cross tile ends; six tiles (the last ragged) with a K
+# tail and N % 4 != 0.  Whole C, element by element.
+PACKED_W4A8 = [(128, 12800, 8224), (256, 16386, 6400), (350, 10102, 4160), (512, 8192, 5120), (384, 12288, 5120),
+               (700, 6002, 2848)]
 
 
 @pytest.mark.parametrize("M,N,K", PACKED_W4A8)

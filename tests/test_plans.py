@@ -154,10 +154,12 @@ ROUTED = [
     ("i4i4", 64, 100, 131104, "codes"),
     # the packed-weights parity cases
     ("w4a8", 128, 12800, 8224, "packed"), ("w4a8", 256, 16386, 6400, "packed"), ("w4a8", 350, 10102, 4160, "packed"),
-    ("w4a8", 512, 8192, 5120, "packed"), ("w4a8", 384, 12288, 5120, "packed"), ("w4a8", 256, 28672, 8192, "packed"),
-    # just outside the packed-weights rule: too few rows, tiles a quarter empty, too many rows, small weights
-    ("w4a8", 96, 28672, 8192, "in-kernel"), ("w4a8", 192, 28672, 8192, "in-kernel"), ("w4a8", 768, 28672, 8192, "codes"),
-    ("w4a8", 512, 4096, 4096, "small"),
+    ("w4a8", 512, 8192, 5120, "packed"), ("w4a8", 384, 12288, 5120, "packed"), ("w4a8", 700, 6002, 2848, "packed"),
+    ("w4a8", 256, 28672, 8192, "packed"),
+    ("w4a8", 192, 28672, 8192, "packed"), ("w4a8", 768, 28672, 8192, "packed"), ("w4a8", 512, 4096, 4096, "packed"),
+    # just outside the packed-weights rule: too few rows, too many, small weights for one or two tiles
+    ("w4a8", 96, 28672, 8192, "in-kernel"), ("w4a8", 1024, 28672, 8192, "codes"), ("w4a8", 128, 11008, 4096, "small"),
+    ("w4a8", 256, 8192, 2048, "small"),
 ]
 
 
