@@ -20,7 +20,7 @@ namespace igemm {
 //                      W4A8   QA  SP  SO  NB  A stages  A sets  ones row  staging
 using CfgI4I4 = KernelCfg<false, 192, 2, 4, 8, 4, 1, true, 1>;
 //                    W4A8   BN  stages CL  float out  format  k blocks per stage
-using CfgI4I4Ss = SsCfg<false, 256, 3, 2, false, 0, 2>;
+using CfgI4I4Ss = SsCfg<false, 256, 6, 2, false, 0, 1>;
 //                          int4 act  QA  stages  TMEM stages  unpack sets  MMA issuers  cluster
 using CfgI4I4Skinny16 = SkinnyCfg<true, 16, 8, 6, 2, 2, 1>;
 using CfgI4I4Skinny16C2 = SkinnyCfg<true, 16, 8, 6, 2, 2, 2>;

@@ -43,7 +43,9 @@
 //   warp 4      TMEM allocation (both CTAs of a pair), MMA issue (one thread;
 //               the even CTA of a pair), relay (one thread; the odd CTA)
 //   warp 5      TMA producer (one lane)
-//   warps 6..   packed P only: converters (a set of four per k block of a
+//   warp 6      integer GEMMs: the second MMA issuer (one thread; the even CTA
+//               of a pair), taking the stages of every other ring slot
+//   warps 6/7.. packed P only: converters (a set of four per k block of a
 //               stage, one P row per thread)
 // Every wait is bounded (ptx.cuh wait_bounded).
 #pragma once
@@ -78,9 +80,10 @@ struct SsCfg {
     // loads both blocks with two boxes)
     static constexpr int kQBoxRows = W4A8 ? QA : QA / CL;
     static constexpr int kBK = 128;                    // k per k block (one TMA box of 128 bytes per row)
-    // k blocks per pipeline stage: each stage costs the MMA thread two barrier
-    // waits, a fence and a commit while the tensor pipe drains; two blocks (8
-    // MMAs) per stage halve that per MMA
+    // k blocks per pipeline stage: each stage costs its MMA thread two barrier
+    // waits, a fence and a commit while the tensor pipe drains; with one issuer
+    // two blocks (8 MMAs) per stage halve that per MMA, with two issuers (one
+    // block per stage, six stages) the other issuer's MMAs cover it
     static constexpr int kKB = KB_;
     static constexpr int kPRows = 128;                 // P rows per CTA (MMA M = 128 * CL)
     static constexpr int kMmaM = kPRows * CL;
@@ -112,8 +115,20 @@ struct SsCfg {
     static constexpr int kConvSets = kPackedP ? kKB : 0;
     static constexpr int kOffPSum = kOffMisc + 128;  // packed P: [2][128] row sums of a unit's codes
     static constexpr int kSmemBytes = kOffPSum + (kPackedP ? 2 * 128 * 4 : 0) + 1024;  // + alignment slack
-    static constexpr int kWarpConv = 6;  // packed P: converter warps 6 ..
-    static constexpr int kThreads = (6 + 4 * kConvSets) * 32;
+    // MMA issuing threads (lane 0 of warp 4 and, for two, of warp 6), taking
+    // the stages of alternate ring slots.  An mbarrier wait by a thread that has MMAs in flight
+    // returns only once they are done, so one issuer leaves the tensor pipe
+    // idle for ~110 ns at every stage (8 MMAs of M = 128, N = 128: 262 ns back
+    // to back, 371 ns with a wait between stages); a second issuer's MMAs fill
+    // that gap.  Both add into the same accumulator, so every MMA accumulates
+    // and the epilogue zeroes the accumulator after reading it: the integer
+    // sums are exact in any order.  The float GEMM keeps one issuer (the order
+    // of its roundings stays fixed), and so does an odd number of ring slots
+    // (two issuers split them 2:1 and measured 1-2 % slower than one).
+    static constexpr int kMmaIssuers = (!FLOAT_ && ST_ % 2 == 0) ? 2 : 1;
+    static constexpr int kWarpMma2 = 6;                    // second issuer (kMmaIssuers == 2)
+    static constexpr int kWarpConv = 5 + kMmaIssuers;      // packed P: converter warps
+    static constexpr int kThreads = (kWarpConv + 4 * kConvSets) * 32;
     static constexpr int kRawA = kPRows * kBK / 2;   // packed bytes of one k block of P
     static_assert(!kPackedP || (W4A8 && !FLOAT_), "packed P: the W4A8 weights");
     static_assert(kQRows % 16 == 0 && kQRows <= 256, "MMA N");
@@ -242,6 +257,17 @@ __device__ __forceinline__ uint32_t ss_magic(uint32_t bits)
 constexpr uint32_t kSsMagic = 0x4B400000u;
 __device__ __forceinline__ int ss_exact(uint32_t bits) { return __float2int_rn(__uint_as_float(bits) * 262144.0f); }
 
+// Zero `cols` (a multiple of 32) accumulator columns of the calling warp's
+// lane quadrant, from TMEM address `taddr` (followed by tmem_st_wait).
+__device__ __forceinline__ void ss_zero_cols(uint32_t taddr, int cols)
+{
+    uint32_t z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0u;
+#pragma unroll 1
+    for (int c = 0; c < cols; c += 32) tmem_st_32x32b_x32(taddr + static_cast<uint32_t>(c), z);
+}
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::kThreads, 1)
     igemm_ss_kernel(const __grid_constant__ CUtensorMap mapP, const __grid_constant__ CUtensorMap mapQ,
@@ -283,10 +309,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             mbar_init(&empty[s], 1);  // the even CTA's MMA commit reaches both CTAs
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_full[b], Cfg::kMmaIssuers);  // a commit per issuer
             mbar_init(&acc_empty[b], 4 * Cfg::CL);  // 4 epilogue warps per CTA of the pair
         }
-        mbar_init(mma_drain, 1);
+        mbar_init(mma_drain, Cfg::kMmaIssuers);
         if constexpr (Cfg::kPackedP) {
             for (int s = 0; s < ST; ++s) mbar_init(&conv[s], 4 * Cfg::kConvSets);
             for (int b = 0; b < 2; ++b) {
@@ -316,9 +342,21 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // the peer's barriers are initialised before anything reaches them
-    if constexpr (kPair) cluster_sync_all();
     const uint32_t tmem = *tmem_slot;
+    if constexpr (Cfg::kMmaIssuers > 1) {
+        // every MMA accumulates: the epilogue warps zero both accumulators once
+        // here (their lane quadrant), and each again after reading it
+        if (warp < 4) {
+            ss_zero_cols(tmem + (static_cast<uint32_t>(warp * 32) << 16), Cfg::kAccBufs * Cfg::kAccCols);
+            tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    // the peer's barriers are initialised (and its accumulators zeroed) before
+    // anything reaches them
+    if constexpr (kPair) cluster_sync_all();
     const Watchdog wd{abort_flag, prm.status, prm.limit_ns};
 
     if (warp == 5) {
@@ -391,9 +429,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 }
             }
         }
-    } else if (warp == 4) {
+    } else if (warp == 4 || (Cfg::kMmaIssuers > 1 && warp == Cfg::kWarpMma2)) {
         if (leader && lane == 0) {
-            // -------------------------------------------------------- MMA issuer
+            // -------------------------------------------------------- MMA issuers
+            // issuer jm takes the stages in ring slots s with s % kMmaIssuers == jm:
+            // a slot's successive uses go to one issuer, as with a single one (an
+            // issuer that met a slot on alternate uses could wait on its barrier a
+            // phase too early and pass it)
+            const int jm = warp == 4 ? 0 : 1;
             constexpr uint32_t idesc = idesc_f8_f32(Cfg::kMmaM, Cfg::kQRows, Cfg::kFmt);
             uint32_t g = 0, nacc = 0;
             bool ok = true;
@@ -408,6 +451,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 const int nst = (x.nkb + Cfg::kKB - 1) / Cfg::kKB;
                 for (int j = 0; j < nst; ++j, ++g) {
                     const int s = static_cast<int>(g % ST);
+                    if (s % Cfg::kMmaIssuers != jm) continue;
                     const uint32_t ph = (g / ST) & 1u;
                     // this CTA's stage landed (packed P: and converted), and the odd CTA's
                     if (!wait_bounded(Cfg::kPackedP ? &conv[s] : &full[s], ph, wd) ||
@@ -426,7 +470,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                             for (int kk = 0; kk < Cfg::kBK / 32; ++kk) {
                                 const uint64_t ad = sdesc_kmajor_sw128(a_base + b * Cfg::kBoxA + 32 * kk);
                                 const uint64_t bd = sdesc_kmajor_sw128(b_base + b * Cfg::kBoxB + 32 * kk);
-                                const uint32_t acc = (j > 0 || b > 0 || kk > 0) ? 1u : 0u;
+                                // one issuer: the unit's first MMA starts the sum; two: the
+                                // accumulator was zeroed, every MMA adds
+                                const uint32_t acc =
+                                    (Cfg::kMmaIssuers > 1 || j > 0 || b > 0 || kk > 0) ? 1u : 0u;
                                 if constexpr (kPair)
                                     mma_f8f6f4_pair(d_tmem, ad, bd, idesc, acc);
                                 else
@@ -439,6 +486,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     else
                         mma_commit(&empty[s]);
                 }
+                // (every issuer commits, also one with no stage in this unit)
                 if (ok) {
                     if constexpr (kPair)
                         mma_commit_pair_multicast(&acc_full[ab], 0x3);
@@ -450,7 +498,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 mma_commit_pair(mma_drain);
             else
                 mma_commit(mma_drain);
-        } else if (kPair && !leader && lane == 0) {
+        } else if (kPair && !leader && warp == 4 && lane == 0) {
             // -------------------------------------------------------- relay (odd CTA of a pair)
             // each stage of this CTA that landed, in order, to the even CTA's MMA thread
             const uint32_t pfull_remote = cluster_map(smem_u32(pfull), 0u);
@@ -754,6 +802,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                         }
                     }
                 }
+            }
+            if constexpr (Cfg::kMmaIssuers > 1) {
+                // the next unit in this accumulator adds into zeros
+                ss_zero_cols(tacc, Cfg::kAccCols);
+                tmem_st_wait();
             }
             tc_fence_before();
             __syncwarp();

@@ -31,7 +31,7 @@ using CfgW4A8Skinny32 = SkinnyCfg<false, 32, 6, 4, 2, 2, 1>;
 // of 128 columns and four TMEM code stages fill the 512 columns)
 using CfgW4A8Skinny64 = SkinnyCfg<false, 64, 6, 4, 2, 1, 1>;
 //                    W4A8  BN  stages CL  float out  format  k blocks per stage
-using CfgW4A8Ss = SsCfg<true, 256, 3, 2, false, 0, 2>;
+using CfgW4A8Ss = SsCfg<true, 256, 6, 2, false, 0, 1>;
 // the same kernel on packed weights, expanded into codes in the kernel
 using CfgW4A8SsPacked = SsCfg<true, 256, 3, 2, false, 0, 2, true>;
 

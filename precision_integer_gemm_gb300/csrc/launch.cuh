@@ -200,7 +200,7 @@ int ss_clusters()
 // Stream-K tail: with T tiles on W clusters, the first (T / W) * W tiles run
 // whole (round robin) and the k blocks of the last r = T mod W tiles, laid end
 // to end, are cut into W ranges of L = ceil(r kb_total / W) blocks (whole
-// pipeline stages, at least eight of them), one per cluster; a range that
+// pipeline stages, at least 16 blocks), one per cluster; a range that
 // crosses a tile's end runs as two pieces.  Every piece adds into C, which the
 // preparation pass zeroes for those tiles.  So the last partial wave takes L
 // k blocks instead of kb_total.  `allow_tail` false (float output, whose sums
@@ -241,8 +241,8 @@ void ss_plan_for(int W, int M, int N, int K, int p_rows, int q_rows, int64_t ope
     if (allow_tail && plan.split == 1 && tiles > W && r > 0) {
         const int64_t blocks = int64_t(r) * pl->kb_total;
         int L = static_cast<int>((blocks + W - 1) / W);
-        L = std::max((L + Cfg::kKB - 1) / Cfg::kKB * Cfg::kKB, 8 * Cfg::kKB);
-        // (pieces of fewer than eight stages measured slower at W4A8 4096^3:
+        L = std::max((L + Cfg::kKB - 1) / Cfg::kKB * Cfg::kKB, 16);
+        // (pieces of fewer than 16 k blocks measured slower at W4A8 4096^3:
         // their epilogues outlast their main loops)
         if (L + 2 * Cfg::kKB <= pl->kb_total) {
             pl->tail_from = tiles - r;

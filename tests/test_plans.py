@@ -94,11 +94,12 @@ def test_ss_plan_of_the_benchmark_shapes(lib):
     p = ss_plan("w4a8", 4096, 4096, 4096)
     assert p == {"split": 1, "kb_per_split": 32, "units": 456, "tail_tiles": 56, "tail_kb": 24,
                  "clusters": 76, "covered": True}
-    # int4 x int4 8192^3: 1024 tiles, 36 left over; 36 * 64 / 76 -> 32 blocks: two pieces a tile
+    # int4 x int4 8192^3: 1024 tiles, 36 left over; 36 * 64 / 76 = 30.3 -> 31 blocks
+    # (stages of one block): two or three pieces a tile
     p = ss_plan("i4i4", 8192, 8192, 8192)
-    assert (p["tail_tiles"], p["tail_kb"], p["units"], p["covered"]) == (36, 32, 988, True)
+    assert (p["tail_tiles"], p["tail_kb"], p["units"], p["covered"]) == (36, 31, 988, True)
     # ragged W4A8 4000 x 12288 x 5120: 48 x 32 tiles, 16 left over; ranges of at
-    # least eight stages (16 blocks) over 40 pairs
+    # least 16 blocks over 40 pairs
     p = ss_plan("w4a8", 4000, 12288, 5120)
     assert (p["tail_tiles"], p["tail_kb"], p["covered"]) == (16, 16, True)
     # fewer tiles than pairs (32): K split in two, one unit per pair, no tail
@@ -122,7 +123,9 @@ def test_ss_plan_invariants(lib, variant):
         if p["tail_tiles"]:
             assert p["split"] == 1 and p["clusters"] == W
             assert p["units"] % W == 0 and 0 < p["tail_tiles"] < W
-            assert p["tail_kb"] % 2 == 0 and 16 <= p["tail_kb"] <= kb_total - 4
+            # (ranges of at least 16 blocks and two stages shorter than a tile;
+            # the prepared-codes stages are one k block)
+            assert 16 <= p["tail_kb"] <= kb_total - 2
             # the ranges cover the tail: no pair takes two
             assert p["tail_kb"] * W >= p["tail_tiles"] * kb_total
 
