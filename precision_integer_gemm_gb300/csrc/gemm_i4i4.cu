@@ -26,7 +26,7 @@ using CfgI4I4Skinny16 = SkinnyCfg<true, 16, 8, 6, 2, 2, 1>;
 using CfgI4I4Skinny16C2 = SkinnyCfg<true, 16, 8, 6, 2, 2, 2>;
 using CfgI4I4Skinny16C4 = SkinnyCfg<true, 16, 8, 6, 2, 2, 4>;
 using CfgI4I4Skinny32 = SkinnyCfg<true, 32, 8, 6, 2, 2, 1>;
-using CfgI4I4Skinny64 = SkinnyCfg<true, 64, 8, 4, 2, 1, 1>;
+using CfgI4I4Skinny64 = SkinnyCfg<true, 64, 8, 4, 2, 2, 1, true>;
 
 // The preparation pass costs (M + N) * K bytes of codes written and read again;
 // it pays once the product is large.  Measured crossovers on GB300: the

@@ -68,7 +68,7 @@ struct SkinnyParams {
     unsigned long long limit_ns;
 };
 
-template <bool ACT_I4, int QA_, int ST_, int TS_, int ASETS_, int ISSUERS_ = 2, int CS_ = 1>
+template <bool ACT_I4, int QA_, int ST_, int TS_, int ASETS_, int ISSUERS_ = 2, int CS_ = 1, bool SHARED_ACC_ = false>
 struct SkinnyCfg {
     static constexpr bool kActI4 = ACT_I4;
     static constexpr int QA = QA_;       // activation rows (M <= QA)
@@ -76,6 +76,12 @@ struct SkinnyCfg {
     static constexpr int TS = TS_;       // TMEM code stages
     static constexpr int kASets = ASETS_;
     static constexpr int kMmaIssuers = ISSUERS_;  // MMA threads, each on alternate stages
+    // kSharedAcc: the two issuers add into the same two accumulators (every MMA
+    // accumulates; the epilogue zeroes what it read), where the TMEM holds no
+    // second pair: an issuer that waits on a barrier with MMAs in flight resumes
+    // only once they are done, so one issuer alone leaves the tensor pipe idle
+    // at every stage
+    static constexpr bool kSharedAcc = SHARED_ACC_;
     // CS = 2 or 4: the k slices of a tile run on the CTAs of a cluster and are
     // summed through distributed shared memory (no zeroed C, no atomics);
     // CS = 1: slices add into a zeroed C with integer atomics
@@ -87,7 +93,8 @@ struct SkinnyCfg {
     static constexpr int kAccCols = kQRows < 32 ? 32 : kQRows;
     static constexpr int kTStageCols = kStageK / 4;      // 64 columns of four codes
     // two accumulators (tile parity) per MMA issuer, then the code ring
-    static constexpr int kACol0 = 2 * kMmaIssuers * kAccCols;
+    static constexpr int kAccSets = kSharedAcc ? 1 : kMmaIssuers;
+    static constexpr int kACol0 = 2 * kAccSets * kAccCols;
     static constexpr int kTmemCols = 512;
     static_assert(QA == 16 || QA == 32 || QA == 64, "activation rows");
     static_assert(kQRows % 16 == 0 && kQRows <= 256, "MMA N for M = 128");
@@ -95,6 +102,7 @@ struct SkinnyCfg {
     static_assert(TS % kASets == 0, "each unpack set owns fixed TMEM stages");
     static_assert(TS % kMmaIssuers == 0, "each MMA issuer owns fixed TMEM stages");
     static_assert(kMmaIssuers == 1 || kMmaIssuers == 2, "MMA issuers");
+    static_assert(!kSharedAcc || (kMmaIssuers == 2 && CS_ == 1), "shared accumulators: two issuers, no cluster");
     // a ring slot must always go to the same unpack set: a set that met a slot
     // on alternate rounds could wait on a parity two phases ahead and pass early
     static_assert(ST % kASets == 0, "each unpack set owns fixed ring slots");
@@ -170,6 +178,16 @@ __device__ __forceinline__ void sk_wait_drain(uint64_t *bar, uint32_t parity, un
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < limit_ns) {
     }
+}
+
+// Zero the 32 columns from `taddr` of the calling warp's lane quadrant
+// (followed by tmem_st_wait).
+__device__ __forceinline__ void sk_zero32(uint32_t taddr)
+{
+    uint32_t z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0u;
+    tmem_st_32x32b_x32(taddr, z);
 }
 
 // Build the activation codes of k slice [k0, k0 + nst * 256) into `act`
@@ -373,6 +391,24 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 if ((issued_mask >> s) & 1u) sk_wait_drain(&full[s], (last_phase >> s) & 1u, prm.limit_ns);
         }
     } else {
+        if constexpr (Cfg::kSharedAcc) {
+            // both accumulators start at zero: each epilogue warp zeroes the columns
+            // it reads (the sync below orders this before the first MMA)
+            if (warp < Cfg::kEpiWarps) {
+                const uint32_t tq = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+                const int me = (warp >> 2) * Cfg::kEpiCols;
+#pragma unroll
+                for (int a = 0; a < 2; ++a) {
+#pragma unroll
+                    for (int c = 0; c < Cfg::kEpiCols; c += 32) {
+                        sk_zero32(tq + a * Cfg::kAccCols + me + c);
+                        if constexpr (!Cfg::kActI4) sk_zero32(tq + a * Cfg::kAccCols + QA + me + c);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+            }
+        }
         // ------------------------------------------------------------ activation codes
         sk_build<Cfg>(prm, k0, nst, act, sums, threadIdx.x < 32 * Cfg::kWarpTma ? threadIdx.x : threadIdx.x - 32);
         fence_proxy_async_smem();  // generic writes, read next by the tensor core
@@ -381,6 +417,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         if (warp >= Cfg::kWarpMma) {
             // -------------------------------------------------------- MMA issuers
             // issuer j takes the stages g = j mod kMmaIssuers into its own accumulators
+            // (shared accumulators: into the same ones)
             const int j = warp - Cfg::kWarpMma;
             if (lane == 0) {
                 constexpr uint32_t idesc = idesc_e4m3_f32(128, Cfg::kQRows);
@@ -392,7 +429,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 for (int t = t0; ok && t < prm.n_tiles; t += tstep) {
                     if (!wait_bounded(&acc_empty[acc], acc_ph ^ 1u, wd)) break;
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem + (2 * j + acc) * Cfg::kAccCols;
+                    const uint32_t d_tmem = tmem + ((Cfg::kSharedAcc ? 0 : 2 * j) + acc) * Cfg::kAccCols;
                     bool first = true;  // this issuer's first stage of the tile starts its sum
                     for (int i = 0; i < nst; ++i, ++g) {
                         if (static_cast<int>(g % Cfg::kMmaIssuers) != j) continue;
@@ -410,7 +447,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                         for (int q = 0; q < Cfg::kStageK / 32; ++q)
                             mma_f8f6f4_tmem_a(d_tmem, a0 + 8 * q,
                                               b0 + static_cast<uint64_t>(((q >> 2) * Cfg::kChunk + 32 * (q & 3)) >> 4),
-                                              idesc, (first && q == 0) ? 0u : 1u);
+                                              idesc, (!Cfg::kSharedAcc && first && q == 0) ? 0u : 1u);
                         first = false;
                         mma_commit(&tempty[ts]);
                     }
@@ -498,10 +535,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 #pragma unroll
                 for (int m = 0; m < QE; ++m) val[m] = 0;
 #pragma unroll 1
-                for (int jj = 0; jj < Cfg::kMmaIssuers; ++jj) {
+                for (int jj = 0; jj < Cfg::kAccSets; ++jj) {
                     // an issuer with no stage in this tile (a one-stage tile) left its
                     // accumulator untouched
-                    if (nst < Cfg::kMmaIssuers && static_cast<int>(g0 % Cfg::kMmaIssuers) != jj) continue;
+                    if (!Cfg::kSharedAcc && nst < Cfg::kMmaIssuers && static_cast<int>(g0 % Cfg::kMmaIssuers) != jj)
+                        continue;
                     const uint32_t tacc = trow + (2 * jj + acc) * Cfg::kAccCols + me;
 #pragma unroll
                     for (int j = 0; j < QE; j += 16) {
@@ -522,6 +560,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                                 val[j + e] += __float2int_rn(__uint_as_float(v0[e]) * 262144.0f);
                         }
                     }
+                }
+                if constexpr (Cfg::kSharedAcc) {
+                    // the next tile in this accumulator adds into zeros
+                    const uint32_t tz = trow + acc * Cfg::kAccCols + me;
+#pragma unroll
+                    for (int c = 0; c < QE; c += 32) {
+                        sk_zero32(tz + c);
+                        if constexpr (!Cfg::kActI4) sk_zero32(tz + QA + c);
+                    }
+                    tmem_st_wait();
                 }
                 tc_fence_before();
                 __syncwarp();

@@ -562,8 +562,11 @@ def test_i4i4_extreme_constants(orc, K, av, bv):
 # cluster of two or four, atomics after the overlapped zeroing).
 SKINNY = [(1, 129, 8224), (7, 1000, 4128), (16, 2048, 65536), (17, 300, 2080), (32, 520, 8192), (24, 128, 256),
           (16, 28672, 512), (3, 1001, 6400), (16, 4096, 8192),
-          # the 64-row configuration: ragged M above 32, deep K (many slices), N tails
-          (33, 300, 2080), (48, 1000, 4128), (64, 28672, 512), (64, 520, 8192), (40, 129, 65536)]
+          # the 64-row configuration: ragged M above 32, deep K (many slices), N tails;
+          # tiles of one stage (one of its two MMA issuers has nothing to add) and of
+          # one partial stage
+          (33, 300, 2080), (48, 1000, 4128), (64, 28672, 512), (64, 520, 8192), (40, 129, 65536),
+          (64, 1000, 256), (57, 700, 96)]
 
 
 @pytest.mark.parametrize("M,N,K", SKINNY)
