@@ -44,10 +44,11 @@
 //   warps E .. E+4*ASETS-1    weight unpack, ASETS sets of four warps taking
 //                             alternate packed stages (quadrant = warp % 4)
 //   next warp                 TMA producer (several issuing lanes)
-//   next one or two warps     MMA issue (one thread each, alternate stages,
-//                             own accumulators: one thread alone spends about
-//                             80 cycles per N = 32 MMA, as long as 16 KB of
-//                             weights take to arrive); the first allocates TMEM
+//   next one or two warps     MMA issue (one thread each, alternate stages, own
+//                             accumulators, or shared ones for 64 activation
+//                             rows: a thread that waits on a barrier with MMAs
+//                             in flight resumes only once they are done); the
+//                             first allocates TMEM
 // All but the producer build the activation codes first.  Every wait is
 // bounded (ptx.cuh wait_bounded).
 #pragma once

@@ -27,8 +27,9 @@ using CfgW4A8Skinny16 = SkinnyCfg<false, 16, 8, 6, 2, 2, 1>;
 using CfgW4A8Skinny16C2 = SkinnyCfg<false, 16, 6, 6, 2, 2, 2>;
 using CfgW4A8Skinny16C4 = SkinnyCfg<false, 16, 8, 6, 2, 2, 4>;
 using CfgW4A8Skinny32 = SkinnyCfg<false, 32, 6, 4, 2, 2, 1>;
-// 64 rows: 128 code rows on the MMA N side, one MMA thread (its two accumulators
-// of 128 columns and four TMEM code stages fill the 512 columns)
+// 64 rows: 128 code rows on the MMA N side, two MMA threads adding into the same
+// two accumulators of 128 columns (with four TMEM code stages they fill the 512
+// columns; a second pair of accumulators would not fit)
 using CfgW4A8Skinny64 = SkinnyCfg<false, 64, 6, 4, 2, 2, 1, true>;
 //                    W4A8  BN  stages CL  float out  format  k blocks per stage
 using CfgW4A8Ss = SsCfg<true, 256, 6, 2, false, 0, 1>;
