@@ -110,9 +110,11 @@ struct SsCfg {
     // [ST], psum_full, psum_free [2]
     static constexpr int kNumBars = 3 * ST + 4 + 1 + (kPackedP ? ST + 4 : 0);
     static constexpr int kOffMisc = ((kOffBars + 8 * kNumBars + 127) / 128) * 128;
-    // packed P: one set of four converter warps per k block of a stage (set b
-    // converts block b of every stage, one P row per thread)
-    static constexpr int kConvSets = kPackedP ? kKB : 0;
+    // packed P: two sets of four converter warps, one P row per thread; with two
+    // k blocks a stage set b converts block b of every stage, with one set b
+    // converts the stages of the ring slots s with s % 2 == b (ST even)
+    static constexpr int kConvSets = kPackedP ? 2 : 0;
+    static constexpr int kConvPerStage = kKB;  // converter sets that arrive on a stage's conv barrier
     static constexpr int kOffPSum = kOffMisc + 128;  // packed P: [2][128] row sums of a unit's codes
     static constexpr int kSmemBytes = kOffPSum + (kPackedP ? 2 * 128 * 4 : 0) + 1024;  // + alignment slack
     // MMA issuing threads (lane 0 of warp 4 and, for two, of warp 6), taking
@@ -131,6 +133,7 @@ struct SsCfg {
     static constexpr int kThreads = (kWarpConv + 4 * kConvSets) * 32;
     static constexpr int kRawA = kPRows * kBK / 2;   // packed bytes of one k block of P
     static_assert(!kPackedP || (W4A8 && !FLOAT_), "packed P: the W4A8 weights");
+    static_assert(!kPackedP || kKB == 2 || ST % 2 == 0, "packed P, one-block stages: each converter set owns fixed slots");
     static_assert(kQRows % 16 == 0 && kQRows <= 256, "MMA N");
     static_assert(CL == 1 || (kQRows % 32 == 0 && kQRows >= 64), "MMA N of an M = 256 pair MMA");
     static_assert(!W4A8 || QA % 8 == 0, "high and low blocks start on 1024-byte boundaries");
@@ -314,7 +317,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
         mbar_init(mma_drain, Cfg::kMmaIssuers);
         if constexpr (Cfg::kPackedP) {
-            for (int s = 0; s < ST; ++s) mbar_init(&conv[s], 4 * Cfg::kConvSets);
+            for (int s = 0; s < ST; ++s) mbar_init(&conv[s], 4 * Cfg::kConvPerStage);
             for (int b = 0; b < 2; ++b) {
                 mbar_init(&psum_full[b], 4 * Cfg::kConvSets);
                 mbar_init(&psum_free[b], 4);
@@ -521,7 +524,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     } else if (Cfg::kPackedP && warp >= Cfg::kWarpConv) {
         // ------------------------------------------------------------ P converters (packed P)
         // thread = P row r of this CTA; set `cset` converts k block cset of every
-        // stage: the block's 64 packed bytes of the row (upper half of warp cw's
+        // stage (one-block stages: block 0 of the stages in its ring slots): the
+        // block's 64 packed bytes of the row (upper half of warp cw's
         // 4 KB) become 128 codes u = v + 8 in natural k order (the order the
         // prepared Q codes have), at 16-byte chunk c ^ (r % 8) of the row
         // (128-byte swizzle); codes past K are 0.  Each warp reads its rows'
@@ -538,6 +542,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             int su = 0;  // sum of this row's codes over the unit's k blocks
             for (int j = 0; j < nst; ++j, ++g) {
                 const int s = static_cast<int>(g % ST);
+                // one-block stages: a slot's successive uses go to one set (as for the
+                // MMA threads; a set meeting a slot on alternate uses could pass its
+                // barrier a phase early)
+                if (Cfg::kKB == 1 && s % Cfg::kConvSets != cset) continue;
                 if (!ss_warp_wait(&full[s], (g / ST) & 1u, wd)) {
                     ok = false;
                     break;
@@ -545,7 +553,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 uint8_t *st = stages + s * Cfg::kStage;
                 const int nb = min(Cfg::kKB, x.nkb - j * Cfg::kKB);  // the unit's k blocks in this stage
                 {
-                    const int b = cset;
+                    const int b = Cfg::kKB == 1 ? 0 : cset;
                     uint8_t *blk = st + b * Cfg::kBoxA;
                     const uint8_t *raw = blk + cw * 4096 + 2048 + lane * 64;
                     uint4 w[4];

@@ -34,7 +34,7 @@ using CfgW4A8Skinny64 = SkinnyCfg<false, 64, 6, 4, 2, 2, 1, true>;
 //                    W4A8  BN  stages CL  float out  format  k blocks per stage
 using CfgW4A8Ss = SsCfg<true, 256, 6, 2, false, 0, 1>;
 // the same kernel on packed weights, expanded into codes in the kernel
-using CfgW4A8SsPacked = SsCfg<true, 256, 3, 2, false, 0, 2, true>;
+using CfgW4A8SsPacked = SsCfg<true, 256, 6, 2, false, 0, 1, true>;
 
 static int run_w4a8_codes(const int8_t *A, const uint8_t *Bp, int32_t *C, int M, int N, int K, cudaStream_t stream)
 {

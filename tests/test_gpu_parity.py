@@ -224,7 +224,10 @@ CODES_I4I4 = [(8192, 2048, 32), (8200, 2056, 96), (2049, 2050, 4128), (8192, 205
               (2560, 2050, 4096), (4096, 4096, 4096),
               # stream-K ranges of 28 k blocks that cross tile ends (on 76 pairs), with
               # bulk reduce-adds, and with a K tail, ragged M and N and scalar atomics
-              (2304, 3072, 8192), (2300, 3070, 8160)]
+              (2304, 3072, 8192), (2300, 3070, 8160),
+              # the two MMA threads (alternate one-block stages into one accumulator):
+              # units of two stages (one each), and stream-K ranges of an odd 17 blocks
+              (4096, 4096, 256), (3072, 3072, 2432)]
 
 
 @pytest.mark.parametrize("M,N,K", CODES_I4I4)
@@ -239,7 +242,9 @@ CODES_W4A8 = [(1024, 4096, 32), (1030, 4100, 4160), (2000, 2100, 1056), (1024, 4
               (1030, 4102, 4160),
               # stream-K ranges that cross tile ends (on 76 pairs) over a K tail, with bulk
               # reduce-adds and with scalar atomics (N % 4 != 0)
-              (1000, 4100, 4160), (1000, 4098, 4160)]
+              (1000, 4100, 4160), (1000, 4098, 4160),
+              # the two MMA threads: units of two stages, stream-K ranges of 17 blocks
+              (1024, 4096, 256), (1536, 3072, 2432)]
 
 
 @pytest.mark.parametrize("M,N,K", CODES_W4A8)
