@@ -31,11 +31,14 @@
 // Its MMA thread learns that the odd CTA's half of a stage landed from a relay
 // thread there (an arrival on the even CTA's barrier), and the odd CTA's
 // epilogue warps release an accumulator with arrivals on the even CTA's
-// barrier too.  These hand-overs carry no data written by the arriving thread
-// (TMA wrote the stage, the tensor core the accumulator), so they arrive with
-// the default CTA-scope semantics: a cluster-scope release costs a fence that
-// measured about 0.8 us per stage with six stages of copies in flight.  Each CTA's accumulator (TMEM lanes 0-127) holds its own
-// P rows times the whole Q tile.
+// barrier too.  These hand-overs carry no data written to memory by the
+// arriving thread (TMA wrote the stage, the tensor core the accumulator; the
+// zeros an epilogue warp writes into its TMEM are complete, tcgen05.wait::st,
+// before it arrives, and the MMAs that add onto them are issued only after the
+// arrival is seen), so they arrive with the default CTA-scope semantics: a
+// cluster-scope release costs a fence that measured about 0.8 us per stage with
+// six stages of copies in flight.  Each CTA's accumulator (TMEM lanes 0-127)
+// holds its own P rows times the whole Q tile.
 //
 // Warp roles (persistent CTAs, one per SM, work units = (tile, k split)):
 //   warps 0-3   epilogue: TMEM -> registers -> int32 -> shared staging ->
@@ -43,10 +46,12 @@
 //   warp 4      TMEM allocation (both CTAs of a pair), MMA issue (one thread;
 //               the even CTA of a pair), relay (one thread; the odd CTA)
 //   warp 5      TMA producer (one lane)
-//   warp 6      integer GEMMs: the second MMA issuer (one thread; the even CTA
-//               of a pair), taking the stages of every other ring slot
-//   warps 6/7.. packed P only: converters (a set of four per k block of a
-//               stage, one P row per thread)
+//   warp 6      integer GEMMs on an even number of ring slots: the second MMA
+//               issuer (one thread; the even CTA of a pair), taking the stages
+//               of every other ring slot
+//   warps 6/7.. packed P only: converters, two sets of four (one per k block of
+//               a two-block stage, or alternate ring slots of one-block
+//               stages), one P row per thread
 // Every wait is bounded (ptx.cuh wait_bounded).
 #pragma once
 #include <cstdint>
